@@ -1,0 +1,551 @@
+/*
+ * oracle.c -- plain CPU definition of the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE.  This file is the checker the CUDA library is compared
+ * against.  Only the tests, the package smoke check and the benchmark's CPU
+ * baseline leg load it; no product code path calls it, and it shares no code,
+ * header, table or constant generator with the CUDA sources.
+ *
+ * Everything is single-threaded, in double precision, in the order the
+ * definition states: no blocking, no fusion, no reordering.  The steps and
+ * where they come from (pages cited by title and section):
+ *
+ *  - Target distribution (temperature, top-k, top-p, normalise): jianc99/sglang
+ *    PR #8, commit "build_speculative_verify_target_probs ..." -- top-k on the
+ *    raw logits commutes with a positive temperature, the tie choice at the
+ *    top-k boundary is deterministic, the probabilities are unchanged.
+ *  - Acceptance: local-inference-lab/rtx6kpro dspark-upstream-consolidation.md,
+ *    section "Identical rejection scheme" -- greedy accepts iff the draft equals
+ *    the target argmax, temperature > 0 runs the Leviathan ratio test.
+ *  - Residual resample / bonus from the last verified row: same page
+ *    ("residual-mass reweighting") and jianc99/sglang PR #8, the DFLASH
+ *    adaptive-verification commit ("The bonus comes from the last verified
+ *    row"; accept paths stop at the planned verify length).
+ *  - Planner: NVIDIA/TensorRT-LLM PR #17056, description section
+ *    "What is here / Scheduler" (cumulative product survival, global survival
+ *    rank, value-independent tie-break) and "Ragged (per-request)
+ *    verification" (qo_indptr, token bucket); review commit, section
+ *    "Cost model" (tokens submitted = bs * (verify_len + 1)).
+ *  - Ragged rejection: NVIDIA/TensorRT-LLM PR #17056, the
+ *    `_rejection_buffers_valid` commit (padding rows can never be accepted,
+ *    accepted count clamped to verify_lens).
+ *  - Uniforms: Philox4x32-10, Salmon, Moraes, Dror, Shaw, "Parallel random
+ *    numbers: as easy as 1, 2, 3", SC'11.
+ *
+ * Readings where the pages are silent are listed in the design doc; each is
+ * restated at the function that takes it.
+ */
+#include <math.h>
+#include <stdint.h>
+
+/* ORC_PLANT selects a deliberate mistake for the tests that show each pin
+ * catches one (0 = the oracle as defined; the tests build the others as
+ * separate libraries):
+ *   1 residual max(0, q - p) instead of max(0, p - q)
+ *   2 top-p keeps the prefix before the crossing token
+ *   3 argmax keeps the last occurrence of the maximum
+ *   4 planner tie-break by request before position
+ *   5 resample reuses the acceptance draw (draw 0)                          */
+#ifndef ORC_PLANT
+#define ORC_PLANT 0
+#endif
+#include <stdlib.h>
+#include <string.h>
+
+/* Row / position status bits.  Bits 0..4 and 6 make a request an error. */
+#define ORC_NONFINITE   1   /* NaN or +inf logit in a row that is read        */
+#define ORC_EMPTY       2   /* sampling row whose logits are all -inf         */
+#define ORC_BAD_TOKEN   4   /* draft token outside [0, vocab)                 */
+#define ORC_BAD_PARAM   8   /* T < 0 or not finite; top_p NaN or <= 0        */
+#define ORC_BAD_LAYOUT 16   /* ragged window inconsistent with the bucket     */
+#define ORC_Q_ZERO     32   /* q(d) == 0 at a tested position (informational) */
+#define ORC_RESID_ZERO 64   /* residual mass zero, sampled from p (informat.) */
+#define ORC_ERROR_MASK (ORC_NONFINITE | ORC_EMPTY | ORC_BAD_TOKEN | ORC_BAD_PARAM | ORC_BAD_LAYOUT)
+
+/* Near-tie flags per request: a decision whose margin is below the bound is
+ * reported, and everything downstream of it in that request goes unchecked. */
+#define ORC_FLAG_RATIO   1  /* |u - p/q| < 1e-6 (the bound the task states)   */
+#define ORC_FLAG_CUTOFF  2  /* top-p prefix mass within 1e-9*Z1 of top_p*Z1   */
+#define ORC_FLAG_INVCDF  4  /* u*W within 1e-9*W of a cumulative boundary     */
+#define ORC_FLAG_RESID   8  /* residual mass W below 1e-9                     */
+
+static const double RATIO_MARGIN = 1e-6;
+static const double CUTOFF_MARGIN = 1e-9;
+static const double INVCDF_MARGIN = 1e-9;
+static const double RESID_MIN = 1e-9;
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 (Salmon et al., SC'11): ten rounds of two 32x32->64 products */
+/* with the Weyl key schedule.                                               */
+/* ------------------------------------------------------------------------- */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr_in[0], x1 = ctr_in[1], x2 = ctr_in[2], x3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)x0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* Uniform for (request, position, draw): key = seed split in two 32-bit
+ * halves, counter = (request, position, draw, 0); u = (word0 >> 8) * 2^-24,
+ * which is exact in fp32.  draw 0 = acceptance test, draw 1 = resample/bonus. */
+double orc_uniform(uint64_t seed, uint32_t req, uint32_t pos, uint32_t draw)
+{
+    uint32_t ctr[4] = { req, pos, draw, 0u };
+    uint32_t key[2] = { (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32) };
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return (double)(out[0] >> 8) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------- */
+/* C1: decode a logit to double.  dtype 0 = bf16 (upper half of an fp32),    */
+/* dtype 1 = fp32.                                                           */
+/* ------------------------------------------------------------------------- */
+static double decode(const void* row, int dtype, int64_t i)
+{
+    if (dtype == 0) {
+        uint16_t h = ((const uint16_t*)row)[i];
+        uint32_t bits = (uint32_t)h << 16;
+        float f;
+        memcpy(&f, &bits, 4);
+        return (double)f;
+    }
+    return (double)((const float*)row)[i];
+}
+
+typedef struct {
+    double value;
+    int64_t index;
+} orc_entry_t;
+
+/* Order tokens by (logit desc, index asc).  Doubles compare -0 == +0. */
+static int cmp_entry(const void* a, const void* b)
+{
+    const orc_entry_t* x = (const orc_entry_t*)a;
+    const orc_entry_t* y = (const orc_entry_t*)b;
+    if (x->value > y->value) return -1;
+    if (x->value < y->value) return 1;
+    if (x->index < y->index) return -1;
+    if (x->index > y->index) return 1;
+    return 0;
+}
+
+typedef struct {
+    double max_logit;    /* m                                                */
+    double log_norm;     /* ln of sum over kept tokens of exp((l - m) / T)   */
+    double cutoff_logit; /* logit of the last kept token in sorted order     */
+    int32_t cutoff_ties; /* kept tokens whose logit equals cutoff_logit      */
+    int32_t kept;        /* number of kept tokens                            */
+    int32_t argmax;      /* smallest index holding m                         */
+    int32_t status;      /* ORC_* bits                                       */
+    double cut_margin;   /* top-p decision margin / Z1 (inf when top-p off)  */
+} orc_row_t;
+
+static int bad_params(float T, float top_p)
+{
+    if (!(T >= 0.0f) || isinf(T)) return 1;     /* NaN, negative or +inf     */
+    if (T == 0.0f) return 0;                    /* greedy ignores top-k/p    */
+    if (!(top_p > 0.0f)) return 1;              /* NaN or <= 0               */
+    return 0;
+}
+
+/*
+ * C2 / C3: one row's target distribution.
+ *   T == 0: greedy.  argmax = smallest index x with l_x = max; p is one-hot
+ *           there (the T -> 0 limit).
+ *   T  > 0: order tokens by (l desc, index asc); keep the first k if
+ *           0 < k < V; e_x = exp((l_x - m) / T) over the kept tokens; Z1 = sum;
+ *           if top_p < 1 keep the shortest prefix whose cumulative sum is
+ *           >= top_p * Z1 (the token that crosses is kept, at least one token);
+ *           p(x) = e_x / (sum over the final kept set).
+ * probs (nullable, length V) receives p.  Returns the status bits.
+ */
+int orc_row_transform(const void* row, int dtype, int64_t vocab, float T, int32_t top_k, float top_p,
+                      orc_row_t* out, double* probs)
+{
+    memset(out, 0, sizeof(*out));
+    out->cut_margin = INFINITY;
+    if (probs)
+        for (int64_t i = 0; i < vocab; ++i) probs[i] = 0.0;
+    if (bad_params(T, top_p)) {
+        out->status = ORC_BAD_PARAM;
+        return out->status;
+    }
+    /* C1: NaN / +inf make the row an error; -inf is probability zero. */
+    double m = -INFINITY;
+    int64_t amax = 0;
+    int found = 0;
+    for (int64_t i = 0; i < vocab; ++i) {
+        double l = decode(row, dtype, i);
+        if (isnan(l) || (isinf(l) && l > 0)) {
+            out->status |= ORC_NONFINITE;
+            return out->status;
+        }
+        if (!found || l > m || (ORC_PLANT == 3 && l == m)) {
+            m = l;
+            amax = i;
+            found = 1;
+        }
+    }
+    out->max_logit = m;
+    out->argmax = (int32_t)amax;
+    if (T == 0.0f) {
+        out->log_norm = 0.0;
+        out->cutoff_logit = m;
+        out->cutoff_ties = 1;
+        out->kept = 1;
+        if (probs) probs[amax] = 1.0;
+        return out->status;
+    }
+    if (isinf(m)) {                 /* every logit is -inf: no distribution */
+        out->status |= ORC_EMPTY;
+        return out->status;
+    }
+    orc_entry_t* ord = (orc_entry_t*)malloc((size_t)vocab * sizeof(orc_entry_t));
+    double* e = (double*)malloc((size_t)vocab * sizeof(double));
+    for (int64_t i = 0; i < vocab; ++i) {
+        ord[i].value = decode(row, dtype, i);
+        ord[i].index = i;
+    }
+    qsort(ord, (size_t)vocab, sizeof(orc_entry_t), cmp_entry);
+    int64_t kk = (top_k > 0 && (int64_t)top_k < vocab) ? (int64_t)top_k : vocab;
+    double Td = (double)T;
+    double z1 = 0.0;
+    for (int64_t i = 0; i < kk; ++i) {
+        e[i] = exp((ord[i].value - m) / Td);
+        z1 += e[i];
+    }
+    int64_t kept = kk;
+    if (top_p < 1.0f) {
+        double target = (double)top_p * z1;
+        double cum = 0.0, prev = 0.0;
+        for (int64_t i = 0; i < kk; ++i) {
+            prev = cum;
+            cum += e[i];
+            if (cum >= target) {
+                kept = (ORC_PLANT == 2 && i > 0) ? i : i + 1;
+                double below = target - prev;   /* > 0: prev did not reach  */
+                double above = cum - target;    /* >= 0: cum reached        */
+                out->cut_margin = (below < above ? below : above) / z1;
+                break;
+            }
+        }
+    }
+    double z = 0.0;
+    for (int64_t i = 0; i < kept; ++i) z += e[i];
+    out->log_norm = log(z);
+    out->kept = (int32_t)kept;
+    out->cutoff_logit = ord[kept - 1].value;
+    int32_t ties = 0;
+    for (int64_t i = 0; i < kept; ++i)
+        if (ord[i].value == out->cutoff_logit) ++ties;
+    out->cutoff_ties = ties;
+    if (probs)
+        for (int64_t i = 0; i < kept; ++i) probs[ord[i].index] = e[i] / z;
+    free(ord);
+    free(e);
+    return out->status;
+}
+
+/*
+ * C7: inverse CDF over weights w in index order.  W = sum of w in index
+ * order; the result is the smallest x with cumulative > u * W; if rounding
+ * leaves no such x, the largest x with w_x > 0.  *margin receives the
+ * distance of u * W to the nearest cumulative boundary, divided by W.
+ */
+static int64_t inv_cdf(const double* w, int64_t n, double u, double* margin)
+{
+    double W = 0.0;
+    int64_t last_pos = -1;
+    for (int64_t x = 0; x < n; ++x) {
+        W += w[x];
+        if (w[x] > 0.0) last_pos = x;
+    }
+    double target = u * W;
+    double cum = 0.0;
+    for (int64_t x = 0; x < n; ++x) {
+        double before = cum;
+        cum += w[x];
+        if (cum > target) {
+            double a = target - before, b = cum - target;
+            *margin = (a < b ? a : b) / W;
+            return x;
+        }
+    }
+    *margin = 0.0;
+    return last_pos;
+}
+
+/*
+ * One request's chain (C5, C6).  tgt_rows[j] (j <= v) and drf_rows[j]
+ * (j < v) point at the logits rows of the window; d[j] are the drafts.
+ * Outputs follow the library's layout: out_tokens has K+1 slots, -1 filled.
+ */
+static void verify_request(const void* const* tgt_rows, const void* const* drf_rows, int dtype, int64_t vocab,
+                           int v, int K, const int32_t* d, float T, int32_t top_k, float top_p,
+                           uint64_t seed, uint32_t req, int32_t layout_bad,
+                           int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                           int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+{
+    *flags = 0;
+    for (int j = 0; j <= K; ++j) {
+        out_tokens[j] = -1;
+        pos_status[j] = 0;
+        p_tok[j] = NAN;
+        q_tok[j] = NAN;
+    }
+    *accept_len = 0;
+    *num_emitted = 0;
+    if (layout_bad) {
+        pos_status[0] |= ORC_BAD_LAYOUT;
+        return;
+    }
+    const int greedy = (T == 0.0f);
+    int err = 0;
+    if (bad_params(T, top_p)) {
+        pos_status[0] |= ORC_BAD_PARAM;
+        return;
+    }
+    double** P = (double**)calloc((size_t)(v + 1), sizeof(double*));
+    double** Q = (double**)calloc((size_t)(v + 1), sizeof(double*));
+    orc_row_t* tr = (orc_row_t*)calloc((size_t)(v + 1), sizeof(orc_row_t));
+    orc_row_t qr;
+    for (int j = 0; j <= v; ++j) {
+        P[j] = (double*)malloc((size_t)vocab * sizeof(double));
+        pos_status[j] |= orc_row_transform(tgt_rows[j], dtype, vocab, T, top_k, top_p, &tr[j], P[j]);
+        if (!greedy && tr[j].cut_margin < CUTOFF_MARGIN) *flags |= ORC_FLAG_CUTOFF;
+        if (j < v) {
+            if (d[j] < 0 || (int64_t)d[j] >= vocab) pos_status[j] |= ORC_BAD_TOKEN;
+            if (!greedy) {
+                Q[j] = (double*)malloc((size_t)vocab * sizeof(double));
+                pos_status[j] |= orc_row_transform(drf_rows[j], dtype, vocab, T, top_k, top_p, &qr, Q[j]);
+                if (qr.cut_margin < CUTOFF_MARGIN) *flags |= ORC_FLAG_CUTOFF;
+            }
+        }
+        if (pos_status[j] & ORC_ERROR_MASK) err = 1;
+    }
+    if (!err) {
+        int a = v;
+        int64_t t = -1;
+        if (greedy) {
+            for (int j = 0; j < v; ++j)
+                if (d[j] != tr[j].argmax) { a = j; break; }
+            t = tr[a].argmax;
+        } else {
+            for (int j = 0; j < v; ++j) {
+                double p = P[j][d[j]], q = Q[j][d[j]];
+                p_tok[j] = p;
+                q_tok[j] = q;
+                double u = orc_uniform(seed, req, (uint32_t)j, 0u);
+                int accept;
+                if (q > 0.0) {
+                    double ratio = p / q;
+                    accept = (u < ratio);
+                    if (fabs(u - ratio) < RATIO_MARGIN) *flags |= ORC_FLAG_RATIO;
+                } else {
+                    /* q(d) == 0: the ratio is +inf when p > 0 and 0/0 when
+                     * p == 0 (reading: accept only in the first case). */
+                    pos_status[j] |= ORC_Q_ZERO;
+                    accept = (p > 0.0);
+                }
+                if (!accept) { a = j; break; }
+            }
+            double* w = (double*)malloc((size_t)vocab * sizeof(double));
+            if (a < v) {
+                double W = 0.0;
+                for (int64_t x = 0; x < vocab; ++x) {
+                    double r = ORC_PLANT == 1 ? Q[a][x] - P[a][x] : P[a][x] - Q[a][x];
+                    w[x] = r > 0.0 ? r : 0.0;
+                    W += w[x];
+                }
+                if (W < RESID_MIN) *flags |= ORC_FLAG_RESID;
+                if (!(W > 0.0)) {
+                    /* reading: an empty residual falls back to p itself */
+                    pos_status[a] |= ORC_RESID_ZERO;
+                    for (int64_t x = 0; x < vocab; ++x) w[x] = P[a][x];
+                }
+            } else {
+                for (int64_t x = 0; x < vocab; ++x) w[x] = P[a][x];
+            }
+            double margin;
+            t = inv_cdf(w, vocab, orc_uniform(seed, req, (uint32_t)a, ORC_PLANT == 5 ? 0u : 1u), &margin);
+            if (margin < INVCDF_MARGIN) *flags |= ORC_FLAG_INVCDF;
+            free(w);
+        }
+        for (int j = 0; j < a; ++j) out_tokens[j] = d[j];
+        out_tokens[a] = (int32_t)t;
+        *accept_len = a;
+        *num_emitted = a + 1;
+    }
+    for (int j = 0; j <= v; ++j) {
+        free(P[j]);
+        if (Q[j]) free(Q[j]);
+    }
+    free(P);
+    free(Q);
+    free(tr);
+}
+
+static const void* row_ptr(const void* base, int dtype, int64_t row, int64_t stride)
+{
+    size_t esz = dtype == 0 ? 2 : 4;
+    return (const void*)((const char*)base + (size_t)row * (size_t)stride * esz);
+}
+
+/*
+ * Uniform layout (C5-C7): target [n, K+1, V], draft [n, K, V], row stride
+ * = vocab.  verify_len (nullable => K) caps each request's window.
+ * p_tok / q_tok ([n, K+1]) receive p_j(d_j) and q_j(d_j) where tested.
+ */
+void orc_verify_chain(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
+                      const int32_t* draft_tokens, const int32_t* verify_len,
+                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed,
+                      int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+{
+    const void** tr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
+    const void** dr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
+    for (int r = 0; r < n; ++r) {
+        int v = verify_len ? verify_len[r] : K;
+        int bad = (v < 0 || v > K);
+        if (bad) v = 0;
+        for (int j = 0; j <= v; ++j) {
+            tr[j] = row_ptr(target, dtype, (int64_t)r * (K + 1) + j, vocab);
+            dr[j] = (j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K + j, vocab) : NULL;
+        }
+        verify_request(tr, dr, dtype, vocab, v, K, draft_tokens + (size_t)r * K, T[r],
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)r, bad,
+                       accept_len + r, out_tokens + (size_t)r * (K + 1), num_emitted + r,
+                       pos_status + (size_t)r * (K + 1), flags + r,
+                       p_tok + (size_t)r * (K + 1), q_tok + (size_t)r * (K + 1));
+    }
+    free(tr);
+    free(dr);
+}
+
+/*
+ * Ragged layout (C9): target rows packed on a flat token axis, request r's
+ * row j at qo_indptr[r] + j (j <= verify_lens[r]), rows past the last window
+ * up to the bucket are padding and never read.  Draft rows stay in the
+ * drafted block layout [n, K_max, V] (the block is drafted in full; only the
+ * verified positions change).  A window that is not qo_indptr[r+1] -
+ * qo_indptr[r] == verify_lens[r] + 1 wide, or leaves [0, bucket), is a
+ * layout error for that request.
+ */
+void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, int K_max, int64_t vocab,
+                       int64_t bucket, const int32_t* qo_indptr, const int32_t* verify_lens,
+                       const int32_t* draft_tokens, const float* T, const int32_t* top_k, const float* top_p,
+                       uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                       int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+{
+    const void** tr = (const void**)malloc((size_t)(K_max + 1) * sizeof(void*));
+    const void** dr = (const void**)malloc((size_t)(K_max + 1) * sizeof(void*));
+    for (int r = 0; r < n; ++r) {
+        int v = verify_lens[r];
+        int64_t start = qo_indptr[r], end = qo_indptr[r + 1];
+        int bad = (v < 0 || v > K_max || start < 0 || end - start != (int64_t)v + 1 || end > bucket);
+        if (bad) v = 0;
+        for (int j = 0; j <= v; ++j) {
+            tr[j] = bad ? NULL : row_ptr(target, dtype, start + j, vocab);
+            dr[j] = (!bad && j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K_max + j, vocab) : NULL;
+        }
+        verify_request(tr, dr, dtype, vocab, v, K_max, draft_tokens + (size_t)r * K_max, T[r],
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)r, bad,
+                       accept_len + r, out_tokens + (size_t)r * (K_max + 1), num_emitted + r,
+                       pos_status + (size_t)r * (K_max + 1), flags + r,
+                       p_tok + (size_t)r * (K_max + 1), q_tok + (size_t)r * (K_max + 1));
+    }
+    free(tr);
+    free(dr);
+}
+
+/* ------------------------------------------------------------------------- */
+/* C8: confidence-scheduled budget planner.                                  */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    float s;
+    int32_t i;
+    int32_t r;
+} orc_cand_t;
+
+/* Global survival rank: s desc, then position asc, then request asc.  The
+ * tie-break uses no values, and position before request keeps each
+ * request's selection a prefix even when c == 1 makes survivals tie. */
+static int cmp_cand(const void* a, const void* b)
+{
+    const orc_cand_t* x = (const orc_cand_t*)a;
+    const orc_cand_t* y = (const orc_cand_t*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+#if ORC_PLANT == 4
+    if (x->r != y->r) return x->r < y->r ? -1 : 1;
+#endif
+    if (x->i != y->i) return x->i < y->i ? -1 : 1;
+    if (x->r != y->r) return x->r < y->r ? -1 : 1;
+    return 0;
+}
+
+/*
+ * c_{r,i} = conf[r * ld + i], NaN -> 0, clamped to [0, 1].  Survival
+ * s_{r,i} = s_{r,i-1} * c_{r,i} in fp32, left to right, s_{r,-1} = 1 (fp32 so
+ * that the device planner can reach the same bits).  Candidates are (r, i)
+ * for i < K_r (K_r = draft_len[r], or K; outside [0, K] is clamped and
+ * reported in *status).  N_sel = min(budget - n, sum K_r) candidates are
+ * taken in rank order; v_r counts r's; each request submits v_r + 1 tokens
+ * (one anchor/bonus row), qo_indptr is the exclusive prefix sum of the
+ * windows and total = qo_indptr[n].  Returns 0, or -1 for bad arguments.
+ */
+int orc_plan_budget(const float* conf, int ld, const int32_t* draft_len, int n, int K,
+                    int budget, int bucket, int32_t* verify_lens, int32_t* qo_indptr,
+                    int32_t* total, int32_t* status)
+{
+    if (n <= 0 || K < 0 || ld < K || budget < n || bucket < budget) return -1;
+    *status = 0;
+    orc_cand_t* cand = (orc_cand_t*)malloc((size_t)n * (size_t)(K > 0 ? K : 1) * sizeof(orc_cand_t));
+    int64_t nc = 0;
+    for (int r = 0; r < n; ++r) {
+        int kr = draft_len ? draft_len[r] : K;
+        if (kr < 0 || kr > K) {
+            *status |= 1;
+            kr = kr < 0 ? 0 : K;
+        }
+        float s = 1.0f;
+        for (int i = 0; i < kr; ++i) {
+            float c = conf[(size_t)r * (size_t)ld + (size_t)i];
+            if (isnan(c)) c = 0.0f;
+            if (c < 0.0f) c = 0.0f;
+            if (c > 1.0f) c = 1.0f;
+            volatile float prod = s * c;   /* one fp32 rounding per step */
+            s = prod;
+            cand[nc].s = s;
+            cand[nc].i = i;
+            cand[nc].r = r;
+            ++nc;
+        }
+    }
+    int64_t nsel = (int64_t)budget - n;
+    if (nsel > nc) nsel = nc;
+    qsort(cand, (size_t)nc, sizeof(orc_cand_t), cmp_cand);
+    for (int r = 0; r < n; ++r) verify_lens[r] = 0;
+    for (int64_t t = 0; t < nsel; ++t) verify_lens[cand[t].r] += 1;
+    qo_indptr[0] = 0;
+    for (int r = 0; r < n; ++r) qo_indptr[r + 1] = qo_indptr[r] + verify_lens[r] + 1;
+    *total = qo_indptr[n];
+    free(cand);
+    return 0;
+}
