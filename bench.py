@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the verify step: verify rows/s and logits HBM GB/s.
+
+Workload (default): 128 requests x 8-token blocks = 1,024 target rows (+ 896
+draft rows) x 248,320 vocab, bf16, T = 0.6, top-k 20, top-p 0.95 -- the shape
+the pages quote for GB300.  One step = one sv_verify_chain call over the whole
+batch with inputs resident in HBM (target-distribution build, draft
+distribution, chain test, residual / bonus resample).
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (the
+reference arm of this repository: a plain single-threaded C definition),
+on a bounded sample of the same workload per step.
+
+Multi-GPU (torchrun): every rank runs its own independent batch on its own
+GPU (the requests of a verify step are independent: weak scaling, no
+collective on the data path); a barrier brackets the timed region and the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "verify rows/s and logits HBM GB/s (% of peak), 1024 rows x 248k vocab bf16"
+UNIT = "rows/s"
+L2_BYTES = 129 * 1024 * 1024
+DESCRIPTIONS = {
+    "large": "128 requests x 8-token blocks (1024 target rows + 896 draft rows) x 248,320 vocab bf16; "
+             "T=0.6, top-k 20, top-p 0.95",
+    "medium": "32 requests x (5+1) rows x 151,936 vocab bf16; T=1.0, top-p 0.95",
+    "greedy_wide": "512 requests x 8-token blocks (4096 rows) x 129,280 vocab bf16; greedy",
+    "ragged": "256 requests x 16 drafted, budget 2048 tokens, bucket 2048, 248,320 vocab bf16; "
+              "half greedy, half T~U[0.3,1.2] top-p 0.9; planner + ragged verify",
+    "tiny": "4 requests x (4+1) rows x 1024 vocab fp32",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="large", choices=sorted(DESCRIPTIONS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (barrier and max over ranks only)
+# ----------------------------------------------------------------------------
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the load window
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), sm_max=float(f[2]), hw=f[5], hw_thermal=f[6],
+                                 sw_thermal=f[7], sw_power=f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "window": "warm-up + timed region + end-to-end pass (continuous load)"}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("sv_fast.cu", "sv_internal.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_rows_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the row kernel from a committed ncu summary,
+    if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# the workload
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(w) -> tuple[int, int]:
+    """(bytes the row kernel must read, target rows) for one step: every target
+    row, plus the draft rows of sampling requests, read once."""
+    esz = 2 if w.dtype == torch.bfloat16 else 4
+    sampling = int((w.temperature > 0).sum())
+    if w.layout == "ragged":
+        rows_t = w.budget
+        rows_d = None   # depends on the plan; filled in by the caller
+        return rows_t * w.V * esz, rows_t
+    rows_t = w.n * (w.K + 1)
+    rows_d = sampling * w.K
+    return (rows_t + rows_d) * w.V * esz, rows_t
+
+
+def make_step(w, sv, dev):
+    """A closure running one verify step with preallocated outputs/workspace."""
+    ws = sv.Workspace(dev)
+    n, K = w.n, w.K
+    out = sv.VerifyOut(torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
+                                                                                 device=dev),
+                       torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
+                                                                                 device=dev))
+    if w.layout == "chain":
+        def step(tgt=w.target, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
+            return sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out)
+        return step, out, None
+    # ragged: planner then verify over target rows packed by the plan
+    from speculative_decoding_verification_rows_gb300 import workloads
+    ws_p = sv.Workspace(dev)
+    vl, qo, tot, _ = sv.plan_budget(w.conf, w.budget, w.bucket, ws=ws_p)
+    packed = workloads.pack_rows(w.target, qo.cpu(), vl.cpu(), w.bucket)
+    extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()))
+
+    def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
+        vl_, qo_, _, _ = sv.plan_budget(w.conf, w.budget, w.bucket, ws=ws_p)
+        return sv.verify_ragged(tgt, drf, qo_, vl_, toks, T, tk, tp, seed=w.seed, ws=ws, out=out)
+    return step, out, extra
+
+
+def run_ours(args, rank, world, local):
+    from speculative_decoding_verification_rows_gb300 import build as sv_build
+    from speculative_decoding_verification_rows_gb300 import sv, workloads
+    sv_build.build()
+    sv.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make(args.workload, device=dev)
+    step, out, extra = make_step(w, sv, dev)
+    alg_bytes, rows_t = algorithmic_bytes(w)
+    if extra is not None:
+        alg_bytes += extra["draft_rows"] * w.V * 2
+    launches_per_step = 6 + (1 if w.layout == "ragged" else 0)
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    # settle: about a second of steps before the warm-up (untimed)
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        step()
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        sv.set_timing_events(k0[i], k1[i])
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    sv.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    ms_worst = max_over_ranks(ms_per_step, world)
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    e2e = run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+
+    value = world * rows_t / (ms_worst / 1e3)
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / kern_avg_s / 1e9
+    logits_gbs_step = alg_bytes / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_worst, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "impl": "ours",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "rows_per_step": rows_t,
+                   "vocab": w.V, "logits_bytes_per_step": alg_bytes,
+                   "logits_gbs_step": round(logits_gbs_step, 1),
+                   "logits_frac_of_8tbs_step": round(logits_gbs_step / 8000.0, 4),
+                   "l2": f"no flush: inputs of {alg_bytes / 1e6:.1f} MB per step exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms)},
+        "roofline": {"bound": "hbm", "kernel": "fast_rows_kernel (one-pass top-k / argmax row select)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+                     "traffic": recorded_traffic(args.workload), "kernel_ms_mean": statistics.mean(kern_ms),
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(w, sv, dev, extra, steps):
+    """Same metric through the public API from pinned host buffers: H2D of the
+    step's inputs and D2H of its results inside the timed region."""
+    names = ["target", "draft", "draft_tokens", "temperature", "top_k", "top_p"]
+    dev_t = {k: (extra["packed"] if (k == "target" and extra) else getattr(w, k)) for k in names}
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in dev_t.items()}
+    dbuf = {k: (torch.empty_like(v) if v is not None else None) for k, v in dev_t.items()}
+    res_host = [torch.empty(w.n, dtype=torch.int32).pin_memory(),
+                torch.empty((w.n, w.K + 1), dtype=torch.int32).pin_memory(),
+                torch.empty(w.n, dtype=torch.int32).pin_memory()]
+    ws = sv.Workspace(dev)
+    ws_p = sv.Workspace(dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = sum(t.numel() * t.element_size() for t in res_host)
+    if extra is not None:
+        h2d += w.conf.numel() * 4
+        conf_h = w.conf.cpu().pin_memory()
+        conf_d = torch.empty_like(w.conf)
+
+    def one():
+        for k in names:
+            if host[k] is not None:
+                dbuf[k].copy_(host[k], non_blocking=True)
+        if extra is None:
+            o = sv.verify_chain(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["temperature"],
+                                dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws)
+        else:
+            conf_d.copy_(conf_h, non_blocking=True)
+            vl, qo, _, _ = sv.plan_budget(conf_d, w.budget, w.bucket, ws=ws_p)
+            o = sv.verify_ragged(dbuf["target"], dbuf["draft"], qo, vl, dbuf["draft_tokens"], dbuf["temperature"],
+                                 dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws)
+        res_host[0].copy_(o.accept_len, non_blocking=True)
+        res_host[1].copy_(o.out_tokens, non_blocking=True)
+        res_host[2].copy_(o.num_emitted, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    rows = w.budget if extra is not None else w.n * (w.K + 1)
+    return {"value": rows / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "inputs copied from pinned host memory and results read back inside the timed region"}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle (baseline leg and reference arm)
+# ----------------------------------------------------------------------------
+def _host_logits(t):
+    import numpy as np
+    t = t.detach().contiguous().cpu()
+    return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def oracle_sample(w, r0, r1):
+    """Run the oracle on requests r0..r1-1 of a chain workload; returns (target rows, seconds)."""
+    import oracle
+    tgt = _host_logits(w.target[r0:r1])
+    drf = None if w.draft is None else _host_logits(w.draft[r0:r1])
+    args = (w.draft_tokens[r0:r1].cpu().numpy(), w.temperature[r0:r1].cpu().numpy(), w.top_k[r0:r1].cpu().numpy(),
+            w.top_p[r0:r1].cpu().numpy())
+    t0 = time.perf_counter()
+    oracle.verify_chain(tgt, drf, *args, seed=w.seed, first_req=r0)
+    dt = time.perf_counter() - t0
+    return (r1 - r0) * (w.K + 1), dt
+
+
+def cpu_baseline(w, seconds):
+    import oracle
+    oracle.build()
+    if w.layout != "chain":
+        return None
+    rows, dt = oracle_sample(w, 0, 1)
+    per_req = max(dt, 1e-6)
+    n = int(max(1, min(w.n, seconds / per_req)))
+    rows, dt = oracle_sample(w, 0, n)
+    return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"requests 0..{n - 1} of the same workload ({rows} target rows), single thread, fp64",
+            "seconds": dt, "host_cores": os.cpu_count()}
+
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verification_rows_gb300 import workloads
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = workloads.make(args.workload, device=dev)
+    if w.layout != "chain":
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm times chain workloads only"}))
+        return
+    for i in range(max(args.warmup, 3)):
+        oracle_sample(w, i % w.n, i % w.n + 1)
+    times, rows = [], 0
+    for i in range(args.steps):
+        r = (i * 7) % w.n
+        n_rows, dt = oracle_sample(w, r, r + 1)
+        times.append(dt)
+        rows = n_rows
+    ms = 1e3 * sum(times) / len(times)
+    value = rows / (ms / 1e3)
+    sample = f"one request ({rows} target rows + its draft rows) of the workload per step, single thread, fp64"
+    print(json.dumps({
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+/*
+ * sv.h -- C ABI of the GB300 speculative-decoding verify library (libsv.so).
+ *
+ * The library computes the verify step of block speculative decoding on one
+ * GPU: the per-request target distribution (temperature, top-k, top-p), the
+ * chain rejection test against the draft distribution, the residual / bonus
+ * resample, and the confidence-scheduled verify-budget planner that lays the
+ * ragged windows out.  Pages cited by title and section:
+ *
+ *   [P2] jianc99/sglang PR #8 (adaptive verification for DFLASH), commit
+ *        "build_speculative_verify_target_probs ...": per-row temperature,
+ *        top-k and top-p on [rows, vocab] logits; top-k on the raw logits
+ *        commutes with a positive temperature; deterministic ties; and the
+ *        DFLASH adaptive-verification commit: accept paths stop at the
+ *        planned verify length, the bonus comes from the last verified row.
+ *   [P3] local-inference-lab/rtx6kpro, dspark-upstream-consolidation.md,
+ *        "Identical rejection scheme": greedy accepts iff draft == target
+ *        argmax; temperature > 0 runs the Leviathan ratio test; block
+ *        verification reweights the residual mass.
+ *   [P4] NVIDIA/TensorRT-LLM PR #17056: description, "Scheduler" (cumulative
+ *        product survival, global survival rank, value-independent
+ *        tie-break, sync-free) and "Ragged (per-request) verification"
+ *        (qo_indptr, token bucket); review commit "Cost model" (tokens
+ *        submitted = bs * (verify_len + 1)); the `_rejection_buffers_valid`
+ *        commit (padding rows never accepted, accept clamped to verify_lens).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers marked (device) are device memory owned by the caller; the
+ *    library allocates and frees nothing.  Scratch comes from the caller's
+ *    workspace `ws` of `ws_bytes` (>= sv_workspace_size(...)), 256-byte
+ *    aligned, which must not be shared by calls that run concurrently.
+ *  - Every call is asynchronous on `stream`: no host synchronisation and no
+ *    device-to-host copy, so every call can be captured in a CUDA graph.
+ *  - Argument errors the host can see (null pointers, sizes, dtype, small
+ *    workspace) return a status before any launch.  Data-dependent errors
+ *    (non-finite logits, bad tokens, bad per-request parameters, inconsistent
+ *    ragged windows) are reported per position in `row_status`; the affected
+ *    request gets accept_len = 0, num_emitted = 0 and out_tokens all -1.
+ *    Unsupported combinations are refused (status bit SV_ROW_UNSUPPORTED),
+ *    never silently degraded.
+ *  - A launch failure returns SV_ERR_CUDA (cudaGetLastError after launch).
+ *  - Logits rows are contiguous along the vocabulary; `row_stride` is in
+ *    elements.
+ *  - Sampling parameters are per request (device arrays of length n_req):
+ *      temperature == 0 -> greedy (argmax, lowest index wins ties);
+ *      top_k <= 0 or >= vocab -> top-k off (top_k may be NULL: off);
+ *      top_p >= 1 -> top-p off (top_p may be NULL: off);
+ *      temperature < 0 / NaN / inf, or top_p <= 0 / NaN -> SV_ROW_BAD_PARAM.
+ *  - Target distribution p of a row (T > 0): tokens ordered by (logit desc,
+ *    index asc), the first k kept (top-k), then the shortest prefix whose
+ *    mass exp((l - m) / T) reaches top_p times the top-k mass (the crossing
+ *    token is kept), p = mass / kept mass.  The draft distribution q is the
+ *    same transform of the draft logits with the same request parameters.
+ *  - Uniforms: Philox4x32-10 with key (seed low 32 bits, seed high 32 bits)
+ *    and counter (request, position, draw, 0); u = (word0 >> 8) * 2^-24.
+ *    draw 0 decides acceptance at a position, draw 1 samples the token
+ *    emitted at the first rejection (residual) or after full acceptance
+ *    (bonus).  request = the request's index in the call.
+ */
+#ifndef SV_H
+#define SV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is struct CUstream_st* */
+typedef struct CUstream_st* sv_stream_t;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* null pointer, negative/zero size, inconsistent sizes */
+    SV_ERR_WORKSPACE = 2,   /* ws NULL, misaligned or smaller than sv_workspace_size */
+    SV_ERR_CUDA = 3,        /* a kernel launch failed                                */
+    SV_ERR_UNSUPPORTED = 4  /* a size or layout this build does not handle           */
+} sv_status_t;
+
+typedef enum { SV_DTYPE_BF16 = 0, SV_DTYPE_F32 = 1 } sv_dtype_t;
+
+/* Per-position / per-row status bits. */
+enum {
+    SV_ROW_NONFINITE = 1,    /* NaN or +inf logit in a row that is read            */
+    SV_ROW_EMPTY = 2,        /* sampling row whose logits are all -inf             */
+    SV_ROW_BAD_TOKEN = 4,    /* draft token outside [0, vocab)                     */
+    SV_ROW_BAD_PARAM = 8,    /* invalid temperature / top_p for the request        */
+    SV_ROW_BAD_LAYOUT = 16,  /* ragged window does not match qo_indptr / bucket    */
+    SV_ROW_Q_ZERO = 32,      /* informational: q(d) == 0 at a tested position      */
+    SV_ROW_RESID_ZERO = 64,  /* informational: empty residual, sampled from p      */
+    SV_ROW_UNSUPPORTED = 128 /* combination this build refuses (see sv_verify_*)   */
+};
+#define SV_ROW_ERROR_MASK (SV_ROW_NONFINITE | SV_ROW_EMPTY | SV_ROW_BAD_TOKEN | SV_ROW_BAD_PARAM | \
+                           SV_ROW_BAD_LAYOUT | SV_ROW_UNSUPPORTED)
+
+typedef struct {
+    const float* temperature; /* (device) [n_req]; required                       */
+    const int32_t* top_k;     /* (device) [n_req] or NULL                         */
+    const float* top_p;       /* (device) [n_req] or NULL                         */
+} sv_sampling_t;
+
+/* Descriptor of one row's distribution (32 bytes).  With T = temperature,
+ * p(x) = exp((l_x - max_logit) / T - log_norm) if x is kept, else 0, where x
+ * is kept iff l_x > cutoff_logit, or l_x == cutoff_logit and fewer than
+ * cutoff_ties tokens with that logit precede x.  Greedy rows (T == 0) have
+ * kept = 1, cutoff = max_logit, p one-hot at argmax. */
+typedef struct {
+    float max_logit;     /* m = max logit                                     */
+    float log_norm;      /* ln of sum over kept tokens of exp((l - m) / T)    */
+    float cutoff_logit;  /* logit of the last kept token in sorted order      */
+    int32_t cutoff_ties; /* kept tokens whose logit equals cutoff_logit       */
+    int32_t kept;        /* number of kept tokens                             */
+    int32_t argmax;      /* lowest index holding m                            */
+    int32_t status;      /* SV_ROW_* bits of this row                         */
+    float temperature;   /* T the row was built with                          */
+} sv_row_desc_t;
+
+/* Workspace bytes for a verify call with n_req requests, at most k_max drafted
+ * positions each, and this vocabulary; for sv_build_target_probs pass
+ * (rows, 0, vocab); for sv_plan_budget pass (n_req, K, 0).  0 on overflow. */
+size_t sv_workspace_size(int n_req, int k_max, int vocab);
+
+/* Human-readable name of a status code (static string). */
+const char* sv_status_string(sv_status_t status);
+
+/*
+ * Confidence-scheduled verify-budget planner ([P4] "Scheduler", "Ragged").
+ *   conf        (device) fp32 [n_req, ld_conf]: c_{r,i} = chance that drafted
+ *               position i of request r survives verification; NaN -> 0,
+ *               clamped to [0, 1].
+ *   draft_len   (device) [n_req] drafted positions per request, or NULL (= K);
+ *               values outside [0, K] are clamped and reported in *status.
+ *   Survival s_{r,i} = prod_{l <= i} c_{r,l}, in fp32, left to right.  The
+ *   N_sel = min(budget_tokens - n_req, sum_r K_r) candidates (r, i) ranked
+ *   first by (s desc, i asc, r asc) are verified; verify_lens[r] counts r's
+ *   (a per-request prefix); each request submits verify_lens[r] + 1 tokens
+ *   (one anchor / bonus row).  qo_indptr [n_req + 1] is the exclusive prefix
+ *   sum of the windows, *total_tokens = qo_indptr[n_req] <= budget_tokens;
+ *   rows [total_tokens, bucket_tokens) are padding.
+ *   Outputs verify_lens [n_req], qo_indptr [n_req + 1], total_tokens [1],
+ *   status [1] (device; status may be NULL).
+ *   Errors: SV_ERR_INVALID_ARG if n_req < 1, K < 0, ld_conf < K,
+ *   budget_tokens < n_req or bucket_tokens < budget_tokens.
+ */
+sv_status_t sv_plan_budget(const float* conf, int ld_conf, const int32_t* draft_len, int n_req, int K,
+                           int budget_tokens, int bucket_tokens, int32_t* verify_lens, int32_t* qo_indptr,
+                           int32_t* total_tokens, int32_t* status, void* ws, size_t ws_bytes,
+                           sv_stream_t stream);
+
+/*
+ * Target-distribution build for `rows` logits rows ([P2]).
+ *   logits        (device) [rows, row_stride] of dtype `dt`.
+ *   row_to_req    (device) [rows] request of each row (index into the
+ *                 n_req-long sampling arrays), or NULL: row r uses request r
+ *                 (then n_req must be >= rows).  An index outside [0, n_req)
+ *                 gives the row SV_ROW_BAD_PARAM.
+ *   token_per_row (device) [rows] or NULL; prob_of_token (device) [rows] fp32
+ *                 receives p(token) for rows with a token (may be NULL).
+ *   desc          (device) [rows] descriptors (may be NULL).
+ *   dense_probs   (device) [rows, vocab] fp32 or NULL: the full distribution
+ *                 (a test aid; it writes rows * vocab floats).
+ */
+sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row_stride, int rows, int vocab,
+                                  const int32_t* row_to_req, int n_req, sv_sampling_t sp, const int32_t* token_per_row,
+                                  float* prob_of_token, sv_row_desc_t* desc, float* dense_probs, void* ws,
+                                  size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Verify in the uniform layout ([P3] acceptance, [P2] cap and bonus).
+ *   target_logits (device) [n_req, K + 1, vocab]; draft_logits (device)
+ *   [n_req, K, vocab] (may be NULL when every request is greedy); both row
+ *   stride = vocab.  draft_tokens (device) [n_req, K].  verify_len (device)
+ *   [n_req] or NULL (= K): request r tests positions j < v_r only (the
+ *   "cap-accept" mode: the dense window is read, acceptance stops at v_r).
+ *   For j < v_r: greedy accepts iff d_j == argmax_j; otherwise accepts iff
+ *   u(r, j, 0) < p_j(d_j) / q_j(d_j) (q == 0: accept iff p > 0).  a = first
+ *   rejection or v_r.  Emitted token t: greedy -> argmax_a; sampling, a < v_r
+ *   -> inverse CDF (index order) of max(0, p_a - q_a) with u(r, a, 1) (of p_a
+ *   if that mass is zero); a == v_r -> inverse CDF of p_{v_r} with u(r, a, 1).
+ *   Outputs (device): accept_len [n_req] = a; out_tokens [n_req, K + 1] =
+ *   d_0 .. d_{a-1}, t, then -1; num_emitted [n_req] = a + 1; row_status
+ *   [n_req, K + 1] or NULL: OR of the position's target row, draft row and
+ *   token bits.
+ *   fp32 logits support greedy requests and top-k <= 32; other fp32 requests
+ *   get SV_ROW_UNSUPPORTED.
+ */
+sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                            int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                            uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                            int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Verify in the ragged layout ([P4] "Ragged (per-request) verification",
+ * `_rejection_buffers_valid`).  Request r's target rows are rows
+ * qo_indptr[r] .. qo_indptr[r] + verify_lens[r] of target_logits (device,
+ * [bucket_tokens, vocab]); rows past the last window are padding and never
+ * read.  Draft logits stay in the drafted block layout (device, [n_req,
+ * K_max, vocab]; NULL if every request is greedy): the block is drafted in
+ * full and only the number of verified positions changes.  draft_tokens
+ * (device) [n_req, K_max].  A window that is not qo_indptr[r + 1] -
+ * qo_indptr[r] == verify_lens[r] + 1 rows wide, or leaves [0,
+ * bucket_tokens), gets SV_ROW_BAD_LAYOUT.  Everything else as
+ * sv_verify_chain with v_r = verify_lens[r]; outputs are [n_req, K_max + 1].
+ */
+sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req,
+                             int K_max, int vocab, int bucket_tokens, const int32_t* qo_indptr,
+                             const int32_t* verify_lens, const int32_t* draft_tokens, sv_sampling_t sp,
+                             uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                             int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Measurement aid (not part of the method): when both are non-NULL, every
+ * later sv_verify_chain / sv_verify_ragged / sv_build_target_probs call
+ * records start_event (a cudaEvent_t) on its stream immediately before the
+ * one-pass row-selection kernel and stop_event immediately after it, so a
+ * caller can time that kernel alone with cudaEventElapsedTime.  Pass NULLs to
+ * stop.  Process-wide; not for calls issued concurrently from several host
+ * threads.  Always returns SV_OK.
+ */
+sv_status_t sv_set_timing_events(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_H */

@@ -82,9 +82,9 @@ def lib():
                                            ctypes.c_float, ctypes.POINTER(RowOut), P]
         _lib.orc_row_transform.restype = ctypes.c_int
         _lib.orc_verify_chain.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                          P, P, P, P, P, ctypes.c_uint64, P, P, P, P, P, P, P]
+                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P]
         _lib.orc_verify_ragged.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                           ctypes.c_int64, P, P, P, P, P, P, ctypes.c_uint64,
+                                           ctypes.c_int64, P, P, P, P, P, P, ctypes.c_uint64, ctypes.c_int,
                                            P, P, P, P, P, P, P]
         _lib.orc_plan_budget.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, P, P, P, P]
@@ -135,8 +135,10 @@ def _verify_outputs(n, width):
                 q_tok=np.zeros((n, width), np.float64))
 
 
-def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=None, verify_len=None, seed=0):
-    """Uniform layout: target [n, K+1, V], draft [n, K, V] (None if all greedy)."""
+def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=None, verify_len=None, seed=0,
+                 first_req=0):
+    """Uniform layout: target [n, K+1, V], draft [n, K, V] (None if all greedy).
+    The requests are requests first_req.. of a larger batch (uniform keys)."""
     target, dt = _logits(target)
     n, k1, V = target.shape
     K = k1 - 1
@@ -150,14 +152,14 @@ def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=Non
     vl = None if verify_len is None else np.ascontiguousarray(verify_len, dtype=np.int32)
     o = _verify_outputs(n, K + 1)
     lib().orc_verify_chain(_ptr(target), _ptr(draft), dt, n, K, V, _ptr(tok), _ptr(vl), _ptr(T), _ptr(tk),
-                           _ptr(tp), seed, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
+                           _ptr(tp), seed, first_req, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
                            _ptr(o["num_emitted"]), _ptr(o["pos_status"]), _ptr(o["flags"]),
                            _ptr(o["p_tok"]), _ptr(o["q_tok"]))
     return o
 
 
 def verify_ragged(target, draft, qo_indptr, verify_lens, draft_tokens, temperature, top_k=None, top_p=None,
-                  seed=0):
+                  seed=0, first_req=0):
     """Packed target [bucket, V] by qo_indptr; draft in block layout [n, K_max, V]."""
     target, dt = _logits(target)
     bucket, V = target.shape
@@ -173,7 +175,7 @@ def verify_ragged(target, draft, qo_indptr, verify_lens, draft_tokens, temperatu
     tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
     o = _verify_outputs(n, K + 1)
     lib().orc_verify_ragged(_ptr(target), _ptr(draft), dt, n, K, V, bucket, _ptr(qo), _ptr(vl), _ptr(tok),
-                            _ptr(T), _ptr(tk), _ptr(tp), seed, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
+                            _ptr(T), _ptr(tk), _ptr(tp), seed, first_req, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
                             _ptr(o["num_emitted"]), _ptr(o["pos_status"]), _ptr(o["flags"]),
                             _ptr(o["p_tok"]), _ptr(o["q_tok"]))
     return o

@@ -409,12 +409,14 @@ static const void* row_ptr(const void* base, int dtype, int64_t row, int64_t str
 
 /*
  * Uniform layout (C5-C7): target [n, K+1, V], draft [n, K, V], row stride
- * = vocab.  verify_len (nullable => K) caps each request's window.
+ * = vocab.  verify_len (nullable => K) caps each request's window.  The
+ * requests are requests first_req .. first_req + n - 1 of a larger batch (their
+ * uniforms are keyed by that index).
  * p_tok / q_tok ([n, K+1]) receive p_j(d_j) and q_j(d_j) where tested.
  */
 void orc_verify_chain(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
                       const int32_t* draft_tokens, const int32_t* verify_len,
-                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed,
+                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
                       int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
                       int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
 {
@@ -429,7 +431,7 @@ void orc_verify_chain(const void* target, const void* draft, int dtype, int n, i
             dr[j] = (j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K + j, vocab) : NULL;
         }
         verify_request(tr, dr, dtype, vocab, v, K, draft_tokens + (size_t)r * K, T[r],
-                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)r, bad,
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad,
                        accept_len + r, out_tokens + (size_t)r * (K + 1), num_emitted + r,
                        pos_status + (size_t)r * (K + 1), flags + r,
                        p_tok + (size_t)r * (K + 1), q_tok + (size_t)r * (K + 1));
@@ -450,7 +452,7 @@ void orc_verify_chain(const void* target, const void* draft, int dtype, int n, i
 void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, int K_max, int64_t vocab,
                        int64_t bucket, const int32_t* qo_indptr, const int32_t* verify_lens,
                        const int32_t* draft_tokens, const float* T, const int32_t* top_k, const float* top_p,
-                       uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                       uint64_t seed, int first_req, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
                        int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
 {
     const void** tr = (const void**)malloc((size_t)(K_max + 1) * sizeof(void*));
@@ -465,7 +467,7 @@ void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, 
             dr[j] = (!bad && j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K_max + j, vocab) : NULL;
         }
         verify_request(tr, dr, dtype, vocab, v, K_max, draft_tokens + (size_t)r * K_max, T[r],
-                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)r, bad,
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad,
                        accept_len + r, out_tokens + (size_t)r * (K_max + 1), num_emitted + r,
                        pos_status + (size_t)r * (K_max + 1), flags + r,
                        p_tok + (size_t)r * (K_max + 1), q_tok + (size_t)r * (K_max + 1));

@@ -1,0 +1,237 @@
+// sv_api.cu -- the C ABI of libsv (declared in include/sv.h): argument checks,
+// workspace carving and the launch sequence of each entry point.
+#include <stdint.h>
+
+#include "sv_internal.cuh"
+
+using namespace sv;
+
+namespace {
+
+constexpr int kMaxVocab = kMaxCluster * kHistMaxSlice;   // 524,280: one cluster per row
+constexpr int kPlanMaxK = 4094;
+constexpr int kPlanMaxN = (1 << 20) - 1;
+
+int sm_count()
+{
+    static int cached[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+bool ws_ok(const void* ws, size_t bytes, size_t need)
+{
+    return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0u && bytes >= need;
+}
+
+template <typename T>
+T* at(void* ws, size_t off)
+{
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+sv_status_t to_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+
+cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;   // sv_set_timing_events
+
+// Row kernels + finalize for whatever tasks the prep kernel listed.
+sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s)
+{
+    const cudaEvent_t ev0 = g_ev_start, ev1 = g_ev_stop;
+    if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return SV_ERR_CUDA;
+    cudaError_t e = launch_fast_rows(ra, s);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SV_ERR_CUDA;
+    e = launch_fast_finalize(ra, s);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    if (ra.dtype == 0) {   // fp32 rows never take the histogram path (refused in prep)
+        e = launch_hist_rows(ra, s);
+        if (e != cudaSuccess) return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+struct Carved {
+    RowsArgs ra;
+    ChainArgs ca;
+};
+
+Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* tgt, const void* drf,
+             int64_t stride_t, int64_t stride_d)
+{
+    const WsLayout L = ws_layout(n_req, k_max, vocab);
+    Carved c{};
+    RowsArgs& ra = c.ra;
+    ra.tgt = tgt;
+    ra.drf = drf;
+    ra.stride_t = stride_t;
+    ra.stride_d = stride_d;
+    ra.vocab = vocab;
+    ra.dtype = dtype;
+    ra.nchunks = L.nchunks;
+    ra.fast_tasks = at<RowTask>(ws, L.fast_tasks);
+    ra.slow_tasks = at<RowTask>(ws, L.slow_tasks);
+    ra.counters = at<Counters>(ws, L.counters);
+    ra.info = at<RowInfo>(ws, L.info);
+    ra.partials = at<Partial>(ws, L.partials);
+    ra.max_tasks = L.max_tasks;
+    ra.num_sms = sm_count();
+    ChainArgs& ca = c.ca;
+    ca.n_req = n_req;
+    ca.n_params = n_req;
+    ca.K = k_max;
+    ca.vocab = vocab;
+    ca.dtype = dtype;
+    ca.tgt = tgt;
+    ca.drf = drf;
+    ca.stride_t = stride_t;
+    ca.stride_d = stride_d;
+    ca.counters = ra.counters;
+    ca.fast_tasks = ra.fast_tasks;
+    ca.slow_tasks = ra.slow_tasks;
+    ca.info = ra.info;
+    ca.req = at<ReqState>(ws, L.req);
+    ca.jobs = at<ResampleJob>(ws, L.jobs);
+    ca.num_sms = ra.num_sms;
+    return c;
+}
+
+bool dtype_ok(sv_dtype_t dt) { return dt == SV_DTYPE_BF16 || dt == SV_DTYPE_F32; }
+
+sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t dt, int n, int K, int V, int bucket,
+                       const int32_t* qo, const int32_t* vl, const int32_t* toks, sv_sampling_t sp, uint64_t seed,
+                       int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted, int32_t* row_status, void* ws,
+                       size_t ws_bytes, cudaStream_t s)
+{
+    if (!tgt || n < 1 || K < 0 || V < 1 || !sp.temperature || !accept_len || !out_tokens || !num_emitted)
+        return SV_ERR_INVALID_ARG;
+    if (K > 0 && !toks) return SV_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
+    if (layout == 1 && (!qo || !vl || bucket < 1)) return SV_ERR_INVALID_ARG;
+    if (K > kMaxK || V > kMaxVocab || n > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const size_t need = sv_workspace_size(n, K, V);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, n, K, V, (int)dt, tgt, drf, V, V);
+    ChainArgs& ca = c.ca;
+    ca.layout = layout;
+    ca.bucket = bucket;
+    ca.qo_indptr = qo;
+    ca.verify_len = vl;
+    ca.draft_tokens = toks;
+    ca.sp = sp;
+    ca.seed = seed;
+    ca.accept_len = accept_len;
+    ca.out_tokens = out_tokens;
+    ca.num_emitted = num_emitted;
+    ca.row_status = row_status;
+    if (launch_prep(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+    sv_status_t st = run_rows(c.ra, s);
+    if (st != SV_OK) return st;
+    if (launch_chain(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (dt == SV_DTYPE_BF16 && launch_resample(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sv_workspace_size(int n_req, int k_max, int vocab)
+{
+    if (n_req < 0 || k_max < 0 || vocab < 0) return 0;
+    if (vocab == 0) {   // the planner: its rank keys only
+        if (n_req > kPlanMaxN || k_max > kPlanMaxK) return 0;
+        return align256(sizeof(unsigned long long) * (size_t)n_req * (size_t)(k_max > 0 ? k_max : 1));
+    }
+    if (n_req > (1 << 22) || k_max > kMaxK || vocab > kMaxVocab) return 0;
+    if ((long long)n_req * (2LL * k_max + 1) > (1LL << 30)) return 0;
+    return ws_layout(n_req, k_max, vocab).total;
+}
+
+const char* sv_status_string(sv_status_t status)
+{
+    switch (status) {
+        case SV_OK: return "SV_OK";
+        case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG";
+        case SV_ERR_WORKSPACE: return "SV_ERR_WORKSPACE";
+        case SV_ERR_CUDA: return "SV_ERR_CUDA";
+        case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED";
+    }
+    return "SV_ERR_UNKNOWN";
+}
+
+sv_status_t sv_plan_budget(const float* conf, int ld_conf, const int32_t* draft_len, int n_req, int K,
+                           int budget_tokens, int bucket_tokens, int32_t* verify_lens, int32_t* qo_indptr,
+                           int32_t* total_tokens, int32_t* status, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    if (n_req < 1 || K < 0 || ld_conf < K || budget_tokens < n_req || bucket_tokens < budget_tokens)
+        return SV_ERR_INVALID_ARG;
+    if ((K > 0 && !conf) || !verify_lens || !qo_indptr || !total_tokens) return SV_ERR_INVALID_ARG;
+    if (K > kPlanMaxK || n_req > kPlanMaxN) return SV_ERR_UNSUPPORTED;
+    const size_t need = sv_workspace_size(n_req, K, 0);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    return to_status(launch_plan(conf, ld_conf, draft_len, n_req, K, budget_tokens, verify_lens, qo_indptr,
+                                 total_tokens, status, static_cast<unsigned long long*>(ws), stream));
+}
+
+sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row_stride, int rows, int vocab,
+                                  const int32_t* row_to_req, int n_req, sv_sampling_t sp, const int32_t* token_per_row,
+                                  float* prob_of_token, sv_row_desc_t* desc, float* dense_probs, void* ws,
+                                  size_t ws_bytes, sv_stream_t stream)
+{
+    if (!logits || rows < 1 || vocab < 1 || row_stride < vocab || n_req < 1 || !sp.temperature)
+        return SV_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
+    if (!row_to_req && n_req < rows) return SV_ERR_INVALID_ARG;
+    if (vocab > kMaxVocab || rows > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const size_t need = sv_workspace_size(rows, 0, vocab);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, rows, 0, vocab, (int)dt, logits, nullptr, row_stride, row_stride);
+    ChainArgs& ca = c.ca;
+    ca.layout = 2;
+    ca.n_params = n_req;
+    ca.row_to_req = row_to_req;
+    ca.token_per_row = token_per_row;
+    ca.sp = sp;
+    if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
+    sv_status_t st = run_rows(c.ra, stream);
+    if (st != SV_OK) return st;
+    return to_status(launch_rows_out(ca, prob_of_token, desc, dense_probs, stream));
+}
+
+sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                            int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                            uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                            int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    return run_verify(0, target_logits, draft_logits, dt, n_req, K, vocab, 0, nullptr, verify_len, draft_tokens, sp,
+                      seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream);
+}
+
+sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req,
+                             int K_max, int vocab, int bucket_tokens, const int32_t* qo_indptr,
+                             const int32_t* verify_lens, const int32_t* draft_tokens, sv_sampling_t sp,
+                             uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                             int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    return run_verify(1, target_logits, draft_logits, dt, n_req, K_max, vocab, bucket_tokens, qo_indptr, verify_lens,
+                      draft_tokens, sp, seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream);
+}
+
+sv_status_t sv_set_timing_events(void* start_event, void* stop_event)
+{
+    g_ev_start = static_cast<cudaEvent_t>(start_event);
+    g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+    return SV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,778 @@
+// sv_chain.cu -- task lists, the chain rejection walk and the resample.
+//
+//  * prep: one CTA turns (requests, sampling parameters, windows) into the
+//    row task lists of the two row kernels, checks parameters, draft tokens
+//    and ragged windows ([P4] `_rejection_buffers_valid`: a window that does
+//    not match qo_indptr is refused, padding rows are never read).
+//  * chain: one warp per request walks its window ([P3] "Identical rejection
+//    scheme"): greedy accepts iff d_j == argmax_j, otherwise accepts iff
+//    u(r, j, 0) < p_j(d_j) / q_j(d_j); stops at the first rejection or at the
+//    planned window ([P2] accept paths stop at the planned verify length).
+//    When the rows' kept sets are listed (<= 32 tokens) it also draws the
+//    emitted token in fp64: inverse CDF in index order of max(0, p_a - q_a)
+//    ([P3] residual-mass reweighting) or of p_a after full acceptance ([P2]
+//    the bonus comes from the last verified row).
+//  * resample: one CTA per request whose kept set is too large to list draws
+//    the same token from the full rows with exact 62-bit fixed-point weights
+//    (fp64 per distinct logit value, integer prefix sums in index order).
+//  [P2] jianc99/sglang PR #8; [P3] local-inference-lab/rtx6kpro
+//  dspark-upstream-consolidation.md; [P4] NVIDIA/TensorRT-LLM PR #17056.
+#include <math.h>
+
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kPrepThreads = 1024;
+
+__device__ __forceinline__ int slot_target(int r, int K, int j) { return r * (2 * K + 1) + j; }
+__device__ __forceinline__ int slot_draft(int r, int K, int j) { return r * (2 * K + 1) + K + 1 + j; }
+
+__device__ __forceinline__ int bad_params(float T, float top_p)
+{
+    if (!(T >= 0.0f) || isinf(T)) return 1;
+    if (T == 0.0f) return 0;
+    if (!(top_p > 0.0f)) return 1;
+    return 0;
+}
+
+// Block-wide exclusive scan of two counters (blockDim = kPrepThreads).
+__device__ void block_scan2(int a, int b, int* ea, int* eb, int* ta, int* tb, int* sa, int* sb)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(0xFFFFFFFFu, ia, o), yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        if (lane >= o) {
+            ia += ya;
+            ib += yb;
+        }
+    }
+    if (lane == 31) {
+        sa[warp] = ia;
+        sb[warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int wa = sa[lane], wb = sb[lane];
+        int xa = wa, xb = wb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xFFFFFFFFu, xa, o), yb = __shfl_up_sync(0xFFFFFFFFu, xb, o);
+            if (lane >= o) {
+                xa += ya;
+                xb += yb;
+            }
+        }
+        sa[lane] = xa - wa;
+        sb[lane] = xb - wb;
+        if (lane == 31) {
+            *ta = xa;
+            *tb = xb;
+        }
+    }
+    __syncthreads();
+    *ea = sa[warp] + ia - a;
+    *eb = sb[warp] + ib - b;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
+{
+    __shared__ int s_wa[32], s_wb[32];
+    __shared__ int s_tot_a, s_tot_b;
+    int base_fast = 0, base_slow = 0;
+    const int n_units = a.n_req;   // requests, or rows for the plain row layout
+    const int K = a.K;
+    for (int u0 = 0; u0 < n_units; u0 += kPrepThreads) {
+        const int u = u0 + threadIdx.x;
+        const bool active = u < n_units;
+        int nf = 0, ns = 0;
+        int err = 0, v = 0, greedy = 0, k_eff = 1, req = u, start = 0;
+        uint64_t tok_bad = 0ull;
+        float T = 0.0f, tp = 1.0f;
+        if (active) {
+            if (a.layout == 2) req = a.row_to_req ? a.row_to_req[u] : u;
+            const bool req_ok = req >= 0 && req < a.n_params;
+            T = req_ok ? a.sp.temperature[req] : 0.0f;
+            const int tk = (req_ok && a.sp.top_k) ? a.sp.top_k[req] : 0;
+            tp = (req_ok && a.sp.top_p) ? a.sp.top_p[req] : 1.0f;
+            if (!req_ok || bad_params(T, tp)) err |= kBadParam;
+            greedy = T == 0.0f;
+            if (!greedy && a.layout != 2 && !a.drf) err |= kBadParam;   // q needs the draft logits
+            k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
+            const bool fast = greedy || k_eff <= kFastK;
+            if (!err && !fast && a.dtype != 0) err |= kUnsupported;
+            if (a.layout == 0) {
+                v = a.verify_len ? a.verify_len[u] : K;
+                if (v < 0 || v > K) {
+                    err |= kBadLayout;
+                    v = 0;
+                }
+                start = u * (K + 1);
+            } else if (a.layout == 1) {
+                v = a.verify_len[u];
+                const long long s = a.qo_indptr[u], e = a.qo_indptr[u + 1];
+                if (v < 0 || v > K || s < 0 || e - s != (long long)v + 1 || e > (long long)a.bucket) {
+                    err |= kBadLayout;
+                    v = 0;
+                }
+                start = (int)s;
+            }
+            if (a.layout != 2) {
+                // one request-level error: a bad window first, then bad parameters
+                if (err & kBadLayout) err = kBadLayout;
+                else if (err & kBadParam) err = kBadParam;
+                for (int j = 0; j < v; ++j) {
+                    const int d = a.draft_tokens[(size_t)u * K + j];
+                    if (d < 0 || d >= a.vocab) tok_bad |= 1ull << j;
+                }
+            }
+            if (!err) {
+                const int n_rows = a.layout == 2 ? 1 : (v + 1) + (greedy ? 0 : v);
+                if (fast) nf = n_rows; else ns = n_rows;
+            }
+        }
+        int off_f, off_s;
+        block_scan2(nf, ns, &off_f, &off_s, &s_tot_a, &s_tot_b, s_wa, s_wb);
+        if (active) {
+            RowTask* list = nf ? a.fast_tasks : a.slow_tasks;
+            int pos = base_fast + off_f;
+            if (!nf) pos = base_slow + off_s;
+            const int n_rows = nf + ns;
+            for (int i = 0; i < n_rows; ++i) {
+                RowTask t;
+                t.req = req;
+                t.k_eff = k_eff;
+                t.temp = T;
+                t.top_p = tp;
+                t.pad = 0;
+                if (a.layout == 2) {
+                    t.row = u;
+                    t.slot = u;
+                    t.is_draft = 0;
+                    const int d = a.token_per_row ? a.token_per_row[u] : -1;
+                    t.token = (d >= 0 && d < a.vocab) ? d : -1;
+                } else {
+                    const bool draft_row = i > v;
+                    const int j = draft_row ? i - v - 1 : i;
+                    t.is_draft = draft_row;
+                    t.row = draft_row ? (int64_t)u * K + j : (int64_t)start + j;
+                    t.slot = draft_row ? slot_draft(u, K, j) : slot_target(u, K, j);
+                    const bool has_tok = j < v && !((tok_bad >> j) & 1);
+                    t.token = has_tok ? a.draft_tokens[(size_t)u * K + j] : -1;
+                }
+                list[pos + i] = t;
+            }
+            if (a.layout == 2) {
+                if (err) {
+                    RowInfo* info = a.info + u;
+                    info->desc.max_logit = 0.0f;
+                    info->desc.log_norm = 0.0f;
+                    info->desc.cutoff_logit = 0.0f;
+                    info->desc.cutoff_ties = 0;
+                    info->desc.kept = 0;
+                    info->desc.argmax = -1;
+                    info->desc.status = err;
+                    info->desc.temperature = T;
+                    info->p_token = nan("");
+                    info->z = 0.0;
+                    info->n_list = -1;
+                    info->cut_count = 0;
+                }
+            } else {
+                ReqState st;
+                st.v = v;
+                st.greedy = greedy;
+                st.err = err;
+                st.pad = 0;
+                st.tok_bad = tok_bad;
+                a.req[u] = st;
+            }
+        }
+        base_fast += s_tot_a;
+        base_slow += s_tot_b;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        a.counters->n_fast = base_fast;
+        a.counters->n_slow = base_slow;
+        a.counters->n_jobs = 0;
+    }
+}
+
+// Inverse CDF in index order over a listed distribution (fp64, sequential):
+// the smallest listed index whose cumulative weight exceeds u * W; if rounding
+// leaves none, the last one with positive weight.
+__device__ int invcdf_list(const int* idx, const double* w, int n, double u, double W)
+{
+    const double target = u * W;
+    double cum = 0.0;
+    int last = -1;
+    for (int i = 0; i < n; ++i) {
+        cum += w[i];
+        if (w[i] > 0.0) last = idx[i];
+        if (cum > target) return idx[i];
+    }
+    return last;
+}
+
+constexpr int kChainWarps = 8;
+
+__global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
+{
+    __shared__ double s_w[kChainWarps][kFastK];
+    __shared__ int s_i[kChainWarps][kFastK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * kChainWarps + warp;
+    if (r >= a.n_req) return;
+    const int K = a.K, width = K + 1;
+    const ReqState st = a.req[r];
+    const int v = st.v;
+    int32_t* out = a.out_tokens + (size_t)r * width;
+    const int32_t* d = a.draft_tokens + (size_t)r * K;
+
+    // position status: target row j, draft row j, token j
+    int any_err = st.err;
+    for (int j = lane; j <= K; j += 32) {
+        int ps = 0;
+        if (!st.err && j <= v) {
+            ps |= a.info[slot_target(r, K, j)].desc.status;
+            if (j < v && !st.greedy) ps |= a.info[slot_draft(r, K, j)].desc.status;
+            if (j < v && ((st.tok_bad >> j) & 1)) ps |= kBadToken;
+        }
+        if (j == 0) ps |= st.err;
+        any_err |= ps & kErrorMask;
+        if (a.row_status) a.row_status[(size_t)r * width + j] = ps;
+        out[j] = -1;
+    }
+    any_err = __reduce_or_sync(0xFFFFFFFFu, any_err);
+    if (any_err) {
+        if (lane == 0) {
+            a.accept_len[r] = 0;
+            a.num_emitted[r] = 0;
+        }
+        return;
+    }
+    __syncwarp();
+    if (lane != 0) return;
+
+    int acc_len = v;
+    int extra_bits_pos = -1, extra_bits = 0;
+    uint64_t q_zero_mask = 0ull;
+    int t = -1;
+    if (st.greedy) {
+        for (int j = 0; j < v; ++j) {
+            if (d[j] != a.info[slot_target(r, K, j)].desc.argmax) {
+                acc_len = j;
+                break;
+            }
+        }
+        t = a.info[slot_target(r, K, acc_len)].desc.argmax;
+    } else {
+        for (int j = 0; j < v; ++j) {
+            const double p = a.info[slot_target(r, K, j)].p_token;
+            const double q = a.info[slot_draft(r, K, j)].p_token;
+            const double u = uniform_f64(a.seed, (uint32_t)r, (uint32_t)j, 0u);
+            bool accept;
+            if (q > 0.0) {
+                accept = u < p / q;
+            } else {
+                q_zero_mask |= 1ull << j;
+                accept = p > 0.0;
+            }
+            if (!accept) {
+                acc_len = j;
+                break;
+            }
+        }
+        const RowInfo& P = a.info[slot_target(r, K, acc_len)];
+        const bool residual = acc_len < v;
+        const double u1 = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u);
+        if (!residual && P.n_list >= 0) {
+            double W = 0.0;
+            for (int i = 0; i < P.n_list; ++i) W += P.list_p[i];
+            t = invcdf_list(P.list_idx, P.list_p, P.n_list, u1, W);
+        } else if (residual && P.n_list >= 0 && a.info[slot_draft(r, K, acc_len)].n_list >= 0) {
+            const RowInfo& Q = a.info[slot_draft(r, K, acc_len)];
+            double W = 0.0;
+            int qi = 0;
+            for (int i = 0; i < P.n_list; ++i) {
+                const int x = P.list_idx[i];
+                while (qi < Q.n_list && Q.list_idx[qi] < x) ++qi;
+                const double qx = (qi < Q.n_list && Q.list_idx[qi] == x) ? Q.list_p[qi] : 0.0;
+                const double w = P.list_p[i] - qx;
+                s_w[warp][i] = w > 0.0 ? w : 0.0;
+                s_i[warp][i] = x;
+                W += s_w[warp][i];
+            }
+            if (W > 0.0) {
+                t = invcdf_list(s_i[warp], s_w[warp], P.n_list, u1, W);
+            } else {
+                extra_bits_pos = acc_len;
+                extra_bits = kResidZero;
+                double Wp = 0.0;
+                for (int i = 0; i < P.n_list; ++i) Wp += P.list_p[i];
+                t = invcdf_list(P.list_idx, P.list_p, P.n_list, u1, Wp);
+            }
+        } else {
+            // kept set too large to list: the resample kernel draws the token
+            const int slot = atomicAdd(&a.counters->n_jobs, 1);
+            ResampleJob job;
+            job.req = r;
+            job.a = acc_len;
+            job.residual = residual ? 1 : 0;
+            job.pad = 0;
+            a.jobs[slot] = job;
+            t = -2;
+        }
+    }
+    for (int j = 0; j < acc_len; ++j) out[j] = d[j];
+    if (t != -2) out[acc_len] = t;
+    a.accept_len[r] = acc_len;
+    a.num_emitted[r] = acc_len + 1;
+    if (a.row_status) {
+        for (int j = 0; j < v; ++j)
+            if ((q_zero_mask >> j) & 1) a.row_status[(size_t)r * width + j] |= kQZero;
+        if (extra_bits_pos >= 0) a.row_status[(size_t)r * width + extra_bits_pos] |= extra_bits;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Full-row resample with exact fixed-point weights.
+// ----------------------------------------------------------------------------
+constexpr int kTableEntries = kTableBinades * 128;
+constexpr double kFix = 4611686018427387904.0;   // 2^62
+
+struct Dist {                 // one row's distribution, as the weight pass needs it
+    const uint16_t* row;
+    double m, T, z;
+    uint32_t cut_key;
+    int ties;                 // kept ties at the cutoff
+    int partial;              // ties < tokens at the cutoff: ranks are needed
+    int16_t* map;             // binade -> table slot, -1 = none
+    unsigned long long* tab;
+};
+
+struct ResampleSmem {
+    unsigned long long tab[kTableEntries];
+    int16_t map[2][512];
+    unsigned long long wsum_res[32], wsum_p[32];
+    int last_res[32], last_p[32];
+    int tie_p[32], tie_q[32];
+    int n_slots;
+    int fail;
+};
+
+// A binade is "tiny" when its values are below 2^-40 in magnitude: their
+// masses differ from exp(-m / T) by less than one part in 2^40 / T and are
+// computed per element instead of tabulated.
+__device__ __forceinline__ bool tiny_binade(int b) { return (b >= 256 && b < 256 + 87) || (b >= 169 && b <= 255); }
+
+__device__ __forceinline__ unsigned long long fix_of(double p)
+{
+    const double x = floor(p * kFix);
+    return x <= 0.0 ? 0ull : (x >= kFix ? (unsigned long long)kFix : (unsigned long long)x);
+}
+
+// 62-bit fixed-point probability of a key under a distribution (kept test
+// done by the caller).
+__device__ __forceinline__ unsigned long long fixp(const Dist& D, uint32_t key)
+{
+    const int b = (int)(key >> 7);
+    const int s = D.map[b];
+    if (s >= 0) return D.tab[s * 128 + (key & 127u)];
+    return fix_of(exp((key_value(key) - D.m) / D.T) / D.z);
+}
+
+__device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_rank)
+{
+    return key > D.cut_key || (key == D.cut_key && tie_rank < D.ties);
+}
+
+__global__ void __launch_bounds__(kResampleThreads, 1) resample_kernel(ChainArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ResampleSmem& sm = *reinterpret_cast<ResampleSmem*>(smem_raw);
+    if ((int)blockIdx.x >= a.counters->n_jobs) return;
+    const ResampleJob job = a.jobs[blockIdx.x];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = job.req, pa = job.a, K = a.K, V = a.vocab;
+    const RowInfo& IP = a.info[slot_target(r, K, pa)];
+    const RowInfo& IQ = a.info[slot_draft(r, K, pa)];
+    const bool residual = job.residual != 0;
+    const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (K + 1) + pa;
+    Dist P, Q;
+    P.row = (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
+    P.m = IP.desc.max_logit;
+    P.T = IP.desc.temperature;
+    P.z = IP.z;
+    P.cut_key = key16_of_bf16(__float_as_uint(IP.desc.cutoff_logit) >> 16);
+    P.ties = IP.desc.cutoff_ties;
+    P.partial = IP.desc.cutoff_ties < IP.cut_count;
+    P.map = sm.map[0];
+    P.tab = sm.tab;
+    Q = P;
+    if (residual) {
+        Q.row = (const uint16_t*)a.drf + ((size_t)r * K + pa) * (size_t)a.stride_d;
+        Q.m = IQ.desc.max_logit;
+        Q.T = IQ.desc.temperature;
+        Q.z = IQ.z;
+        Q.cut_key = key16_of_bf16(__float_as_uint(IQ.desc.cutoff_logit) >> 16);
+        Q.ties = IQ.desc.cutoff_ties;
+        Q.partial = IQ.desc.cutoff_ties < IQ.cut_count;
+        Q.map = sm.map[1];
+    }
+
+    // 1. binade -> slot maps over each kept key range [cutoff, max]
+    if (tid == 0) {
+        int n = 0;
+        sm.fail = 0;
+        for (int dd = 0; dd < 2; ++dd) {
+            const Dist& D = dd == 0 ? P : Q;
+            int16_t* map = sm.map[dd];
+            for (int b = 0; b < 512; ++b) map[b] = -1;
+            if (dd == 1 && !residual) continue;
+            const int lo = (int)(D.cut_key >> 7);
+            const int hi = (int)(key16_of_bf16(__float_as_uint((float)D.m) >> 16) >> 7);
+            for (int b = lo; b <= hi; ++b) {
+                if (b == 0 || tiny_binade(b)) continue;
+                if (n < kTableBinades) map[b] = (int16_t)n;
+                ++n;
+            }
+        }
+        if (n > kTableBinades) sm.fail = 1;
+        sm.n_slots = n < kTableBinades ? n : kTableBinades;
+    }
+    __syncthreads();
+    if (sm.fail) {
+        if (tid == 0) {
+            int32_t* out = a.out_tokens + (size_t)r * (K + 1);
+            for (int j = 0; j <= K; ++j) out[j] = -1;
+            a.accept_len[r] = 0;
+            a.num_emitted[r] = 0;
+            if (a.row_status) a.row_status[(size_t)r * (K + 1) + pa] |= kUnsupported;
+        }
+        return;
+    }
+    // 2. fill the tables: thread -> (slot, 8 keys)
+    for (int dd = 0; dd < (residual ? 2 : 1); ++dd) {
+        const Dist& D = dd == 0 ? P : Q;
+        const int16_t* map = sm.map[dd];
+        for (int item = tid; item < 512 * 16; item += kResampleThreads) {
+            const int b = item >> 4, g = item & 15;
+            const int s = map[b];
+            if (s < 0) continue;
+            double e[8];
+            binade_masses(b, g, D.m, D.T, e);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sm.tab[s * 128 + 8 * g + j] = fix_of(e[j] / D.z);
+        }
+    }
+    __syncthreads();
+
+    // Contiguous range of each warp, in 256-element tiles (32 lanes x 8).
+    const int tiles = (V + 255) / 256;
+    const int tiles_per_warp = (tiles + 31) / 32;
+    const int w_begin = warp * tiles_per_warp * 256;
+    const int w_end = min(V, w_begin + tiles_per_warp * 256);
+    const bool need_ranks = P.partial || (residual && Q.partial);
+
+    // Weights of one lane's 8 elements starting at e0 (tie ranks advanced in order).
+    auto lane_weights = [&](int e0, int& rank_p, int& rank_q, unsigned long long wr[8], unsigned long long wp[8]) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            wr[s] = 0ull;
+            wp[s] = 0ull;
+            const int x = e0 + s;
+            if (x >= w_end) continue;
+            const uint32_t kp = key16_of_bf16(P.row[x]);
+            const bool inp = kept_key(P, kp, rank_p);
+            if (kp == P.cut_key) ++rank_p;
+            const unsigned long long fp_ = inp ? fixp(P, kp) : 0ull;
+            wp[s] = fp_;
+            if (residual) {
+                const uint32_t kq = key16_of_bf16(Q.row[x]);
+                const bool inq = kept_key(Q, kq, rank_q);
+                if (kq == Q.cut_key) ++rank_q;
+                const unsigned long long fq = inq ? fixp(Q, kq) : 0ull;
+                wr[s] = fp_ > fq ? fp_ - fq : 0ull;
+            } else {
+                wr[s] = fp_;
+            }
+        }
+    };
+    // Tie counts of one lane's 8 elements.
+    auto lane_ties = [&](int e0, int& tp_, int& tq_) {
+        tp_ = 0;
+        tq_ = 0;
+        if (!need_ranks) return;
+        for (int s = 0; s < 8; ++s) {
+            const int x = e0 + s;
+            if (x >= w_end) break;
+            tp_ += key16_of_bf16(P.row[x]) == P.cut_key;
+            if (residual) tq_ += key16_of_bf16(Q.row[x]) == Q.cut_key;
+        }
+    };
+    auto warp_excl_scan = [&](int v_) {
+        int incl = v_;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        return incl - v_;
+    };
+
+    // 3. tie bases of each warp range (only with partial tie groups)
+    {
+        int tp_tot = 0, tq_tot = 0;
+        if (need_ranks) {
+            for (int e = w_begin + lane * 8; e < w_end; e += 256) {
+                int tp_, tq_;
+                lane_ties(e, tp_, tq_);
+                tp_tot += tp_;
+                tq_tot += tq_;
+            }
+            tp_tot = __reduce_add_sync(0xFFFFFFFFu, tp_tot);
+            tq_tot = __reduce_add_sync(0xFFFFFFFFu, tq_tot);
+        }
+        if (lane == 0) {
+            sm.tie_p[warp] = tp_tot;
+            sm.tie_q[warp] = tq_tot;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int cp = 0, cq = 0;
+            for (int w = 0; w < 32; ++w) {
+                const int xp = sm.tie_p[w], xq = sm.tie_q[w];
+                sm.tie_p[w] = cp;
+                sm.tie_q[w] = cq;
+                cp += xp;
+                cq += xq;
+            }
+        }
+        __syncthreads();
+    }
+
+    // 4. pass A: exact weight sums per warp range (residual and p alone)
+    {
+        unsigned long long sr = 0ull, sp_ = 0ull;
+        int last_r = -1, last_p = -1;
+        int run_p = sm.tie_p[warp], run_q = sm.tie_q[warp];
+        for (int e = w_begin; e < w_end; e += 256) {
+            const int e0 = e + lane * 8;
+            int tp_, tq_;
+            lane_ties(e0, tp_, tq_);
+            int rp = run_p + warp_excl_scan(tp_), rq = run_q + warp_excl_scan(tq_);
+            run_p += __reduce_add_sync(0xFFFFFFFFu, tp_);
+            run_q += __reduce_add_sync(0xFFFFFFFFu, tq_);
+            unsigned long long wr[8], wp[8];
+            lane_weights(e0, rp, rq, wr, wp);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                sr += wr[s];
+                sp_ += wp[s];
+                if (wr[s]) last_r = e0 + s;
+                if (wp[s]) last_p = e0 + s;
+            }
+        }
+        sr = warp_sum_u64(sr);
+        sp_ = warp_sum_u64(sp_);
+        last_r = __reduce_max_sync(0xFFFFFFFFu, last_r);
+        last_p = __reduce_max_sync(0xFFFFFFFFu, last_p);
+        if (lane == 0) {
+            sm.wsum_res[warp] = sr;
+            sm.wsum_p[warp] = sp_;
+            sm.last_res[warp] = last_r;
+            sm.last_p[warp] = last_p;
+        }
+    }
+    __syncthreads();
+
+    // 5. the target, the warp range that holds it, and pass B inside it
+    unsigned long long W = 0ull, Wp = 0ull;
+    int last_r = -1, last_p = -1;
+    for (int w = 0; w < 32; ++w) {
+        W += sm.wsum_res[w];
+        Wp += sm.wsum_p[w];
+        last_r = max(last_r, sm.last_res[w]);
+        last_p = max(last_p, sm.last_p[w]);
+    }
+    bool use_p = !residual;
+    int resid_zero = 0;
+    if (residual && W == 0ull) {
+        use_p = true;
+        resid_zero = 1;
+    }
+    const unsigned long long Wuse = use_p ? Wp : W;
+    const unsigned long long* wsum = use_p ? sm.wsum_p : sm.wsum_res;
+    const unsigned long long u24 = uniform24(a.seed, (uint32_t)r, (uint32_t)pa, 1u);
+    const unsigned long long hi = __umul64hi(Wuse, u24), lo = Wuse * u24;
+    const unsigned long long target = (hi << 40) | (lo >> 24);   // floor(W * u)
+    int wstar = -1;
+    unsigned long long before = 0ull;
+    for (int w = 0; w < 32; ++w) {
+        if (before + wsum[w] > target) {
+            wstar = w;
+            break;
+        }
+        before += wsum[w];
+    }
+    __shared__ int s_x;
+    if (tid == 0) s_x = -1;
+    __syncthreads();
+    if (warp == wstar) {
+        unsigned long long cum = before;
+        int run_p = sm.tie_p[warp], run_q = sm.tie_q[warp];
+        for (int e = w_begin; e < w_end; e += 256) {
+            const int e0 = e + lane * 8;
+            int tp_, tq_;
+            lane_ties(e0, tp_, tq_);
+            int rp = run_p + warp_excl_scan(tp_), rq = run_q + warp_excl_scan(tq_);
+            run_p += __reduce_add_sync(0xFFFFFFFFu, tp_);
+            run_q += __reduce_add_sync(0xFFFFFFFFu, tq_);
+            unsigned long long wr[8], wp[8];
+            lane_weights(e0, rp, rq, wr, wp);
+            unsigned long long ls = 0ull;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) ls += use_p ? wp[s] : wr[s];
+            unsigned long long incl = ls;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned long long tile = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (cum + tile > target) {
+                const unsigned hitmask = __ballot_sync(0xFFFFFFFFu, cum + incl > target);
+                const int L = __ffs(hitmask) - 1;
+                if (lane == L) {
+                    unsigned long long c = cum + incl - ls;
+                    for (int s = 0; s < 8; ++s) {
+                        c += use_p ? wp[s] : wr[s];
+                        if (c > target) {
+                            s_x = e0 + s;
+                            break;
+                        }
+                    }
+                }
+                break;
+            }
+            cum += tile;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int x = s_x;
+        if (x < 0) x = use_p ? last_p : last_r;
+        a.out_tokens[(size_t)r * (K + 1) + pa] = x;
+        if (resid_zero && a.row_status) a.row_status[(size_t)r * (K + 1) + pa] |= kResidZero;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// sv_build_target_probs outputs
+// ----------------------------------------------------------------------------
+__global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t* desc)
+{
+    const int rows = a.n_req;
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
+        const RowInfo& I = a.info[r];
+        if (desc) desc[r] = I.desc;
+        if (prob_of_token) prob_of_token[r] = (float)I.p_token;
+    }
+}
+
+// Dense p of every row, in fp64 then rounded to fp32 (a test aid): one CTA
+// per row, tiles of blockDim elements in index order for the tie ranks.
+__global__ void __launch_bounds__(1024) dense_kernel(ChainArgs a, float* dense)
+{
+    __shared__ int s_w[32];
+    const int row = blockIdx.x;
+    const RowInfo& I = a.info[row];
+    const int V = a.vocab;
+    float* out = dense + (size_t)row * V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (I.desc.status & kErrorMask) {
+        for (int x = tid; x < V; x += blockDim.x) out[x] = 0.0f;
+        return;
+    }
+    if (I.n_list >= 0) {
+        for (int x = tid; x < V; x += blockDim.x) out[x] = 0.0f;
+        __syncthreads();
+        if (tid < I.n_list) out[I.list_idx[tid]] = (float)I.list_p[tid];
+        return;
+    }
+    const double m = I.desc.max_logit, T = I.desc.temperature, z = I.z;
+    const float cut = I.desc.cutoff_logit;
+    const int ties = I.desc.cutoff_ties;
+    const char* base = (const char*)a.tgt + (size_t)row * (size_t)a.stride_t * (a.dtype == 0 ? 2 : 4);
+    int run = 0;
+    for (int x0 = 0; x0 < V; x0 += blockDim.x) {
+        const int x = x0 + tid;
+        float l = -INFINITY;
+        if (x < V) l = a.dtype == 0 ? load_logit<0>(base, x) : load_logit<1>(base, x);
+        const int is_tie = (x < V && l == cut) ? 1 : 0;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, is_tie);
+        if (lane == 0) s_w[warp] = __popc(bal);
+        __syncthreads();
+        int before = run;
+        for (int w = 0; w < warp; ++w) before += s_w[w];
+        before += __popc(bal & ((1u << lane) - 1u));
+        int tot = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_w[w];
+        __syncthreads();
+        run += tot;
+        if (x < V) {
+            const bool keep = l > cut || (is_tie && before < ties);
+            out[x] = keep ? (float)(exp(((double)l - m) / T) / z) : 0.0f;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s)
+{
+    prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s)
+{
+    const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
+    chain_kernel<<<grid, kChainWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
+{
+    const size_t smem = sizeof(ResampleSmem);
+    static int attr_set[128] = {0};   // once per device, before any graph capture
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(resample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        if (dev >= 0 && dev < 128) attr_set[dev] = 1;
+    }
+    resample_kernel<<<a.n_req, kResampleThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
+                            cudaStream_t s)
+{
+    int grid = (a.n_req + 255) / 256;
+    if (grid < 1) grid = 1;
+    rows_out_kernel<<<grid, 256, 0, s>>>(a, prob_of_token, desc);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || !dense) return err;
+    dense_kernel<<<a.n_req, 1024, 0, s>>>(a, dense);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,325 @@
+// sv_internal.cuh -- device-side types and helpers shared by the libsv kernels.
+//
+// Workspace records, the order-preserving integer keys of logits, Philox4x32-10,
+// warp reductions and the launchers each translation unit exports.  Nothing
+// here is visible through the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+// ----------------------------------------------------------------------------
+// Sizes
+// ----------------------------------------------------------------------------
+constexpr int kFastK = 32;          // largest top-k served by the one-pass select kernel
+constexpr int kFastThreads = 256;   // threads of the one-pass select kernel
+constexpr int kFastVecs = 8;        // 16-byte vectors per thread per chunk
+constexpr int kCandCap = 256;       // candidate buffer of one chunk
+constexpr int kMinChunk = kFastThreads * kFastVecs * 4;   // fp32 chunk (bf16 chunks are twice as long)
+constexpr int kHistThreads = 512;   // threads of the exact-histogram kernel
+constexpr int kHistWords = 32768;   // 65536 16-bit counters, two per 32-bit word
+constexpr int kHistMaxSlice = 65535;// elements per CTA so a 16-bit counter cannot wrap
+constexpr int kMaxCluster = 8;      // portable cluster size limit
+constexpr int kResampleThreads = 1024;
+constexpr int kTableBinades = 96;   // binades of fixed-point p / q a resample table holds
+
+// Row / position status bits (the public SV_ROW_* values).
+constexpr int kNonfinite = SV_ROW_NONFINITE, kEmpty = SV_ROW_EMPTY, kBadToken = SV_ROW_BAD_TOKEN,
+              kBadParam = SV_ROW_BAD_PARAM, kBadLayout = SV_ROW_BAD_LAYOUT, kQZero = SV_ROW_Q_ZERO,
+              kResidZero = SV_ROW_RESID_ZERO, kUnsupported = SV_ROW_UNSUPPORTED;
+constexpr int kErrorMask = SV_ROW_ERROR_MASK;
+
+// ----------------------------------------------------------------------------
+// Workspace records
+// ----------------------------------------------------------------------------
+// One logits row to process.
+struct RowTask {
+    int64_t row;      // row index in its logits tensor
+    int32_t slot;     // RowInfo slot the result goes to
+    int32_t req;      // request (index into the sampling parameters)
+    int32_t token;    // token whose probability is reported, -1 for none
+    int32_t k_eff;    // kept count of the top-k stage (1 for greedy rows)
+    float temp;       // 0 = greedy
+    float top_p;      // >= 1 = top-p off
+    int32_t is_draft; // 1: row of the draft logits
+    int32_t pad;
+};
+
+// Result of one row (its distribution, enough to sample from it).
+struct RowInfo {
+    sv_row_desc_t desc;         // 32 B, the public descriptor
+    double p_token;             // probability of the task's token (NaN if none)
+    double z;                   // normaliser: sum over kept of exp((l - m) / T)
+    int32_t n_list;             // kept tokens listed below (ascending index), -1 if not listed
+    int32_t cut_count;          // tokens whose logit equals the cutoff (all of them, kept or not)
+    int32_t list_idx[kFastK];
+    double list_p[kFastK];
+};
+
+// Top candidates of one chunk of one row: composite keys, descending.
+struct Partial {
+    uint32_t status;
+    uint32_t count;
+    unsigned long long keys[kFastK];
+};
+
+// Per-request state written by the prep kernel.
+struct ReqState {
+    int32_t v;        // verified drafts (window = v + 1 target rows)
+    int32_t greedy;   // temperature == 0
+    int32_t err;      // request-level error bits (params, layout)
+    int32_t pad;
+    uint64_t tok_bad; // bit j: draft token j out of range
+};
+
+constexpr int kMaxK = 63;           // drafted positions per request (bit masks above)
+
+// A request whose emitted token needs a full-row resample.
+struct ResampleJob {
+    int32_t req;
+    int32_t a;        // position of the emitted token
+    int32_t residual; // 1: max(0, p_a - q_a); 0: p_a (bonus)
+    int32_t pad;
+};
+
+// Counters at the head of the workspace.
+struct Counters {
+    int32_t n_fast;
+    int32_t n_slow;
+    int32_t n_jobs;
+    int32_t pad[13];
+};
+
+// Carving of the caller's workspace.
+struct WsLayout {
+    size_t counters, fast_tasks, slow_tasks, info, partials, req, jobs, total;
+    int slots, max_tasks, nchunks;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// slots: target positions 0..K and draft positions 0..K-1 of every request.
+inline WsLayout ws_layout(int n_req, int k_max, int vocab)
+{
+    WsLayout L{};
+    L.slots = n_req * (2 * k_max + 1);
+    L.max_tasks = L.slots;
+    L.nchunks = vocab > 0 ? (vocab + kMinChunk - 1) / kMinChunk : 1;
+    size_t off = 0;
+    L.counters = off;   off = align256(off + sizeof(Counters));
+    L.fast_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
+    L.slow_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
+    L.info = off;       off = align256(off + sizeof(RowInfo) * (size_t)L.slots);
+    L.partials = off;   off = align256(off + sizeof(Partial) * (size_t)L.max_tasks * (size_t)L.nchunks);
+    L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
+    L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
+    L.total = off;
+    return L;
+}
+
+// ----------------------------------------------------------------------------
+// Order-preserving keys.  Larger key <=> larger logit; -0 and +0 share a key.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key_of_f32_bits(uint32_t b)
+{
+    if ((b & 0x7FFFFFFFu) == 0u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float f32_of_key(uint32_t k)
+{
+    uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(b);
+}
+// 16-bit key of a bf16 pattern, and back.
+__device__ __forceinline__ uint32_t key16_of_bf16(uint32_t h)
+{
+    h &= 0xFFFFu;
+    if ((h & 0x7FFFu) == 0u) h = 0u;
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+__device__ __forceinline__ float f32_of_key16(uint32_t k)
+{
+    uint32_t h = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(h << 16);
+}
+// Composite key: logit key above, inverted index below, so that a larger
+// composite means (larger logit, or equal logit and smaller index).
+__device__ __forceinline__ unsigned long long ckey(float v, uint32_t idx)
+{
+    return ((unsigned long long)key_of_f32_bits(__float_as_uint(v)) << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ float ckey_value(unsigned long long c) { return f32_of_key((uint32_t)(c >> 32)); }
+__device__ __forceinline__ int ckey_index(unsigned long long c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
+
+// Exact value of a 16-bit key as a double.
+__device__ __forceinline__ double key_value(uint32_t k16) { return (double)f32_of_key16(k16); }
+
+// x^n for a small non-negative integer n (binary powering).
+__device__ __forceinline__ double powi(double x, int n)
+{
+    double r = 1.0;
+    while (n) {
+        if (n & 1) r *= x;
+        x *= x;
+        n >>= 1;
+    }
+    return r;
+}
+
+// exp((v - m) / T) in fp64 for the 8 keys b*128 + 8g .. + 7 of binade b (the
+// 128 keys sharing a sign and exponent; the mantissa step is constant along
+// it).  Binade 0 holds -inf (mass 0).  Where the step is small against T the
+// masses follow a geometric recurrence from two exps per binade; otherwise
+// each key gets its own exp.
+__device__ __forceinline__ void binade_masses(int b, int g, double m, double T, double e[8])
+{
+    if (b == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = 0.0;
+        return;
+    }
+    const uint32_t kb = (uint32_t)b * 128u;
+    const double v_first = key_value(kb);
+    const double step = key_value(kb + 1u) - v_first;
+    const double x = step / T;
+    if (x <= 1.0) {
+        const double R = exp(x);
+        const double base = exp((v_first - m) / T);
+        double cur = base * powi(R, 8 * g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            e[j] = cur;
+            cur *= R;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = exp((key_value(kb + 8u * g + j) - m) / T);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): counter (req, pos, draw, 0),
+// key (seed low, seed high); u = (word0 >> 8) * 2^-24.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t philox_word0(unsigned long long seed, uint32_t req, uint32_t pos, uint32_t draw)
+{
+    uint32_t c0 = req, c1 = pos, c2 = draw, c3 = 0u;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    return c0;
+}
+__device__ __forceinline__ uint32_t uniform24(unsigned long long seed, uint32_t req, uint32_t pos, uint32_t draw)
+{
+    return philox_word0(seed, req, pos, draw) >> 8;
+}
+__device__ __forceinline__ double uniform_f64(unsigned long long seed, uint32_t req, uint32_t pos, uint32_t draw)
+{
+    return (double)uniform24(seed, req, pos, draw) * (1.0 / 16777216.0);
+}
+
+// ----------------------------------------------------------------------------
+// Warp helpers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x, o);
+        x = y > x ? y : x;
+    }
+    return x;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
+// Value of a row element, by dtype (0 = bf16, 1 = fp32).
+template <int DT>
+__device__ __forceinline__ float load_logit(const void* row, int64_t i)
+{
+    if (DT == 0) return __uint_as_float((uint32_t)(((const uint16_t*)row)[i]) << 16);
+    return ((const float*)row)[i];
+}
+
+// ----------------------------------------------------------------------------
+// Launchers (host), one per kernel family.
+// ----------------------------------------------------------------------------
+struct RowsArgs {
+    const void* tgt;
+    const void* drf;
+    int64_t stride_t, stride_d;
+    int vocab;
+    int dtype;
+    int nchunks;
+    RowTask* fast_tasks;
+    RowTask* slow_tasks;
+    Counters* counters;
+    RowInfo* info;
+    Partial* partials;
+    int max_tasks;
+    int num_sms;
+};
+
+cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_fast_finalize(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
+
+struct ChainArgs {
+    int n_req, K;          // K = k_max: slots per request = 2K + 1 (layout 2: n_req = rows)
+    int n_params;          // length of the sampling-parameter arrays
+    int vocab, dtype;
+    int layout;            // 0 uniform, 1 ragged, 2 plain rows (build_target_probs)
+    const void* tgt;
+    const void* drf;
+    int64_t stride_t, stride_d;
+    int bucket;
+    const int32_t* qo_indptr;
+    const int32_t* verify_len;   // nullable in the uniform layout
+    const int32_t* draft_tokens; // [n, K]
+    const int32_t* row_to_req;   // layout 2
+    const int32_t* token_per_row;// layout 2
+    sv_sampling_t sp;
+    unsigned long long seed;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    int32_t* num_emitted;
+    int32_t* row_status;
+    Counters* counters;
+    RowTask* fast_tasks;
+    RowTask* slow_tasks;
+    RowInfo* info;
+    ReqState* req;
+    ResampleJob* jobs;
+    int num_sms;
+};
+
+cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
+                            cudaStream_t s);
+
+cudaError_t launch_plan(const float* conf, int ld, const int32_t* draft_len, int n, int K, int budget,
+                        int32_t* verify_lens, int32_t* qo_indptr, int32_t* total, int32_t* status,
+                        unsigned long long* keys, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace sv

@@ -1,0 +1,252 @@
+"""Thin Python binding of libsv (include/sv.h): argument marshalling only.
+
+Every step of the verify path runs in the CUDA library; this module passes
+tensor data pointers, sizes and the current CUDA stream through ctypes and
+allocates the output and workspace tensors with PyTorch.  There is no CPU
+fallback: if the library is missing or no GPU is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+DTYPE_BF16, DTYPE_F32 = 0, 1
+ROW_NONFINITE, ROW_EMPTY, ROW_BAD_TOKEN, ROW_BAD_PARAM, ROW_BAD_LAYOUT = 1, 2, 4, 8, 16
+ROW_Q_ZERO, ROW_RESID_ZERO, ROW_UNSUPPORTED = 32, 64, 128
+ROW_ERROR_MASK = ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | ROW_BAD_LAYOUT | ROW_UNSUPPORTED
+
+EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
+            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events")
+
+
+class SVError(RuntimeError):
+    pass
+
+
+class Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p)]
+
+
+class RowDesc(ctypes.Structure):
+    _fields_ = [("max_logit", ctypes.c_float), ("log_norm", ctypes.c_float), ("cutoff_logit", ctypes.c_float),
+                ("cutoff_ties", ctypes.c_int32), ("kept", ctypes.c_int32), ("argmax", ctypes.c_int32),
+                ("status", ctypes.c_int32), ("temperature", ctypes.c_float)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libsv.so (building it first only if asked)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB_PATH):
+        if not build_if_missing:
+            raise SVError(f"CUDA library not built: {_build.LIB_PATH} is missing (run build())")
+        _build.build()
+    L = ctypes.CDLL(_build.LIB_PATH)
+    P, I, I64, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+    L.sv_workspace_size.argtypes = [I, I, I]
+    L.sv_workspace_size.restype = SZ
+    L.sv_status_string.argtypes = [I]
+    L.sv_status_string.restype = ctypes.c_char_p
+    L.sv_plan_budget.argtypes = [P, I, P, I, I, I, I, P, P, P, P, P, SZ, P]
+    L.sv_plan_budget.restype = I
+    L.sv_build_target_probs.argtypes = [P, I, I64, I, I, P, I, Sampling, P, P, P, P, P, SZ, P]
+    L.sv_build_target_probs.restype = I
+    L.sv_verify_chain.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
+    L.sv_verify_chain.restype = I
+    L.sv_verify_ragged.argtypes = [P, P, I, I, I, I, I, P, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
+    L.sv_verify_ragged.restype = I
+    L.sv_set_timing_events.argtypes = [P, P]
+    L.sv_set_timing_events.restype = I
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != SV_OK:
+        raise SVError(load().sv_status_string(rc).decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise SVError(f"logits must be bf16 or fp32, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor, dtype=None) -> torch.Tensor:
+    if not t.is_cuda:
+        raise SVError("tensors must live on the GPU (the library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise SVError(f"expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise SVError("tensors must be contiguous")
+    return t
+
+
+def _sampling(temperature, top_k, top_p) -> Sampling:
+    return Sampling(temperature.data_ptr(), None if top_k is None else top_k.data_ptr(),
+                    None if top_p is None else top_p.data_ptr())
+
+
+def set_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["torch.cuda.Event"]):
+    """Have later calls record these events around the one-pass row kernel."""
+    if start is None or stop is None:
+        load().sv_set_timing_events(None, None)
+    else:
+        load().sv_set_timing_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
+
+
+def workspace_size(n_req: int, k_max: int, vocab: int) -> int:
+    size = load().sv_workspace_size(n_req, k_max, vocab)
+    if size == 0:
+        raise SVError("sizes beyond what this build supports")
+    return size
+
+
+class Workspace:
+    """A reusable device workspace (grows on demand, 256-byte aligned)."""
+
+    def __init__(self, device="cuda"):
+        self.device = torch.device(device)
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.buf.data_ptr()) % 256
+        return self.buf[off:off + nbytes]
+
+
+def _ws(ws: Optional[Workspace], device, nbytes) -> torch.Tensor:
+    if ws is None:
+        ws = Workspace(device)
+    return ws.get(nbytes)
+
+
+@dataclass
+class VerifyOut:
+    accept_len: torch.Tensor     # [n] int32
+    out_tokens: torch.Tensor     # [n, K+1] int32, -1 filled
+    num_emitted: torch.Tensor    # [n] int32
+    row_status: torch.Tensor     # [n, K+1] int32
+
+
+def plan_budget(conf: torch.Tensor, budget: int, bucket: int, draft_len: Optional[torch.Tensor] = None,
+                ws: Optional[Workspace] = None):
+    """sv_plan_budget: (verify_lens [n], qo_indptr [n+1], total [1], status [1]) on the device."""
+    conf = _dev(conf, torch.float32)
+    n, K = conf.shape
+    dev = conf.device
+    vl = torch.empty(n, dtype=torch.int32, device=dev)
+    qo = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    tot = torch.empty(1, dtype=torch.int32, device=dev)
+    st = torch.empty(1, dtype=torch.int32, device=dev)
+    w = _ws(ws, dev, workspace_size(n, K, 0))
+    _check(load().sv_plan_budget(_ptr(conf), K, _ptr(draft_len), n, K, budget, bucket, _ptr(vl), _ptr(qo),
+                                 _ptr(tot), _ptr(st), _ptr(w), w.numel(), _stream(dev)))
+    return vl, qo, tot, st
+
+
+def build_target_probs(logits: torch.Tensor, temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
+                       top_p: Optional[torch.Tensor] = None, row_to_req: Optional[torch.Tensor] = None,
+                       tokens: Optional[torch.Tensor] = None, dense: bool = False,
+                       ws: Optional[Workspace] = None):
+    """sv_build_target_probs over [rows, vocab] logits.
+
+    Returns (desc [rows, 8] int32 view of sv_row_desc_t, prob_of_token [rows]
+    or None, dense [rows, vocab] or None)."""
+    logits = _dev(logits)
+    rows, V = logits.shape
+    dev = logits.device
+    n_req = temperature.numel()
+    desc = torch.empty((rows, 8), dtype=torch.int32, device=dev)
+    ptok = torch.empty(rows, dtype=torch.float32, device=dev) if tokens is not None else None
+    dn = torch.empty((rows, V), dtype=torch.float32, device=dev) if dense else None
+    w = _ws(ws, dev, workspace_size(rows, 0, V))
+    _check(load().sv_build_target_probs(_ptr(logits), _dtype_code(logits), V, rows, V, _ptr(row_to_req), n_req,
+                                        _sampling(temperature, top_k, top_p), _ptr(tokens), _ptr(ptok),
+                                        _ptr(desc), _ptr(dn), _ptr(w), w.numel(), _stream(dev)))
+    return desc, ptok, dn
+
+
+def desc_fields(desc: torch.Tensor) -> dict:
+    """Split the [rows, 8] int32 descriptor view into named host arrays."""
+    d = desc.cpu()
+    f = d.view(torch.float32)
+    return dict(max_logit=f[:, 0].numpy(), log_norm=f[:, 1].numpy(), cutoff_logit=f[:, 2].numpy(),
+                cutoff_ties=d[:, 3].numpy(), kept=d[:, 4].numpy(), argmax=d[:, 5].numpy(),
+                status=d[:, 6].numpy(), temperature=f[:, 7].numpy())
+
+
+def _outs(n, K, dev):
+    return VerifyOut(torch.empty(n, dtype=torch.int32, device=dev),
+                     torch.empty((n, K + 1), dtype=torch.int32, device=dev),
+                     torch.empty(n, dtype=torch.int32, device=dev),
+                     torch.empty((n, K + 1), dtype=torch.int32, device=dev))
+
+
+def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                 temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
+                 top_p: Optional[torch.Tensor] = None, verify_len: Optional[torch.Tensor] = None, seed: int = 0,
+                 ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None) -> VerifyOut:
+    """sv_verify_chain: target [n, K+1, V], draft [n, K, V] (or None if all greedy)."""
+    target = _dev(target)
+    n, k1, V = target.shape
+    K = k1 - 1
+    dev = target.device
+    if draft is not None:
+        _dev(draft, target.dtype)
+        assert draft.shape == (n, K, V)
+    o = out or _outs(n, K, dev)
+    w = _ws(ws, dev, workspace_size(n, K, V))
+    _check(load().sv_verify_chain(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens),
+                                  _ptr(verify_len), _sampling(temperature, top_k, top_p), seed,
+                                  _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status),
+                                  _ptr(w), w.numel(), _stream(dev)))
+    return o
+
+
+def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], qo_indptr: torch.Tensor,
+                  verify_lens: torch.Tensor, draft_tokens: torch.Tensor, temperature: torch.Tensor,
+                  top_k: Optional[torch.Tensor] = None, top_p: Optional[torch.Tensor] = None, seed: int = 0,
+                  ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None) -> VerifyOut:
+    """sv_verify_ragged: packed target [bucket, V], draft [n, K_max, V] block layout."""
+    target = _dev(target)
+    bucket, V = target.shape
+    n, K = draft_tokens.shape
+    dev = target.device
+    if draft is not None:
+        _dev(draft, target.dtype)
+        assert draft.shape == (n, K, V)
+    o = out or _outs(n, K, dev)
+    w = _ws(ws, dev, workspace_size(n, K, V))
+    _check(load().sv_verify_ragged(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, bucket,
+                                   _ptr(qo_indptr), _ptr(verify_lens), _ptr(draft_tokens),
+                                   _sampling(temperature, top_k, top_p), seed, _ptr(o.accept_len),
+                                   _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status), _ptr(w),
+                                   w.numel(), _stream(dev)))
+    return o
