@@ -90,10 +90,12 @@ enum {
     SV_ROW_BAD_LAYOUT = 16,  /* ragged window does not match qo_indptr / bucket    */
     SV_ROW_Q_ZERO = 32,      /* informational: q(d) == 0 at a tested position      */
     SV_ROW_RESID_ZERO = 64,  /* informational: empty residual, sampled from p      */
-    SV_ROW_UNSUPPORTED = 128 /* combination this build refuses (see sv_verify_*)   */
+    SV_ROW_UNSUPPORTED = 128, /* combination this build refuses (see sv_verify_*)  */
+    SV_ROW_TIMEOUT = 256      /* a bounded wait on a bulk copy gave up: rows of the
+                                 call were not processed (never seen in practice) */
 };
 #define SV_ROW_ERROR_MASK (SV_ROW_NONFINITE | SV_ROW_EMPTY | SV_ROW_BAD_TOKEN | SV_ROW_BAD_PARAM | \
-                           SV_ROW_BAD_LAYOUT | SV_ROW_UNSUPPORTED)
+                           SV_ROW_BAD_LAYOUT | SV_ROW_UNSUPPORTED | SV_ROW_TIMEOUT)
 
 typedef struct {
     const float* temperature; /* (device) [n_req]; required                       */

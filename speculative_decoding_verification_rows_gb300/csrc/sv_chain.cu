@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         a.counters->n_fast = base_fast;
         a.counters->n_slow = base_slow;
         a.counters->n_jobs = 0;
+        a.counters->timeout = 0;
     }
 }
 
@@ -235,7 +236,8 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
     const int32_t* d = a.draft_tokens + (size_t)r * K;
 
     // position status: target row j, draft row j, token j
-    int any_err = st.err;
+    const int timed_out = a.counters->timeout ? kTimeout : 0;
+    int any_err = st.err | timed_out;
     for (int j = lane; j <= K; j += 32) {
         int ps = 0;
         if (!st.err && j <= v) {
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
             if (j < v && !st.greedy) ps |= a.info[slot_draft(r, K, j)].desc.status;
             if (j < v && ((st.tok_bad >> j) & 1)) ps |= kBadToken;
         }
-        if (j == 0) ps |= st.err;
+        if (j == 0) ps |= st.err | timed_out;
         any_err |= ps & kErrorMask;
         if (a.row_status) a.row_status[(size_t)r * width + j] = ps;
         out[j] = -1;
@@ -681,7 +683,11 @@ __global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t
     const int rows = a.n_req;
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
         const RowInfo& I = a.info[r];
-        if (desc) desc[r] = I.desc;
+        if (desc) {
+            sv_row_desc_t d = I.desc;
+            if (a.counters->timeout) d.status |= kTimeout;
+            desc[r] = d;
+        }
         if (prob_of_token) prob_of_token[r] = (float)I.p_token;
     }
 }

@@ -47,6 +47,68 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
     return r;
 }
 
+// ---- shared-memory ring fed by bulk async copies (TMA, cp.async.bulk) ----
+constexpr int kStages = 3;                                  // chunks in flight per CTA
+constexpr int kChunkBytes = kFastThreads * kFastVecs * 16;  // 32 KB: one chunk of either dtype
+constexpr long long kWaitPolls = 1ll << 26;                 // try_wait polls before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+// Bounded wait: false when the phase did not complete within kWaitPolls polls.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
+{
+    for (long long i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// Global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned)
+// completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
+
 // Element s (0..EPV-1) of a 16-byte vector, as fp32.
 template <int DT>
 __device__ __forceinline__ float vec_elem(const uint4& v, int s)
@@ -139,12 +201,36 @@ __device__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t*
     return prefix;
 }
 
+// Where unit u (row task t, chunk c) starts, and how many bytes of it the bulk
+// copy moves (a 16-byte-aligned multiple of 16; the rest, if any, is loaded
+// element by element).
 template <int DT>
-__global__ void __launch_bounds__(kFastThreads) fast_rows_kernel(RowsArgs a)
+__device__ __forceinline__ const char* unit_source(const RowsArgs& a, long long u, int nchunks, int& c0,
+                                                   uint32_t& bytes, RowTask& task)
+{
+    constexpr int ESZ = DT == 0 ? 2 : 4;
+    constexpr int CHUNK = kChunkBytes / ESZ;
+    const int t = (int)(u / nchunks);
+    const int c = (int)(u - (long long)t * nchunks);
+    task = a.fast_tasks[t];
+    const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
+    const char* row = (const char*)(task.is_draft ? a.drf : a.tgt) + (size_t)task.row * (size_t)stride * ESZ;
+    c0 = c * CHUNK;
+    const int n_here = min(CHUNK, a.vocab - c0);
+    const char* src = row + (size_t)c0 * ESZ;
+    bytes = ((uintptr_t)src & 15u) ? 0u : (uint32_t)(n_here * ESZ) & ~15u;
+    return row;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
 {
     constexpr int EPV = DT == 0 ? 8 : 4;
     constexpr int ESZ = DT == 0 ? 2 : 4;
     constexpr int CHUNK = kFastThreads * kFastVecs * EPV;
+    static_assert(CHUNK * ESZ == kChunkBytes, "one chunk fills one ring stage");
+    extern __shared__ __align__(128) unsigned char ring[];   // kStages x 32 KB
+    __shared__ __align__(8) unsigned long long full_bar[kStages];
     __shared__ unsigned long long s_cand[kCandCap];
     __shared__ uint32_t s_hist[256];
     __shared__ float s_redf[kFastThreads / 32];
@@ -157,22 +243,63 @@ __global__ void __launch_bounds__(kFastThreads) fast_rows_kernel(RowsArgs a)
     const int n_tasks = a.counters->n_fast;
     const int nchunks = (a.vocab + CHUNK - 1) / CHUNK;
     const long long n_units = (long long)n_tasks * nchunks;
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+    if ((long long)blockIdx.x >= n_units) return;
+
+    // Thread 0 feeds the ring: unit i of this CTA goes to stage i % kStages.
+    auto issue = [&](long long i) {
+        const long long uu = (long long)blockIdx.x + i * gridDim.x;
+        if (uu >= n_units) return;
+        int cc0;
+        uint32_t bytes;
+        RowTask tk;
+        const char* row = unit_source<DT>(a, uu, nchunks, cc0, bytes, tk);
+        unsigned long long* bar = &full_bar[i % kStages];
+        if (bytes) {
+            mbar_expect_tx(bar, bytes);
+            bulk_g2s(ring + (i % kStages) * kChunkBytes, row + (size_t)cc0 * ESZ, bytes, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], 1u);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int i = 0; i < kStages; ++i) issue(i);
+
+    long long it = 0;
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
         __syncthreads();   // shared memory of the previous unit is free
-        const int t = (int)(u / nchunks);
-        const int c = (int)(u - (long long)t * nchunks);
-        const RowTask task = a.fast_tasks[t];
-        const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
-        const char* row = (const char*)(task.is_draft ? a.drf : a.tgt) + (size_t)task.row * (size_t)stride * ESZ;
-        const int c0 = c * CHUNK;
-        const bool aligned = (((uintptr_t)row + (size_t)c0 * ESZ) & 15u) == 0u;
+        int c0;
+        uint32_t bytes;
+        RowTask task;
+        const char* row = unit_source<DT>(a, u, nchunks, c0, bytes, task);
+        const int stage = (int)(it % kStages);
+        const bool arrived = mbar_wait(&full_bar[stage], (uint32_t)((it / kStages) & 1));
+        if (!__syncthreads_and(arrived)) {
+            // A bulk copy never completed: report it, let the copies already
+            // issued land (bounded), and leave the remaining rows unprocessed.
+            if (tid == 0) {
+                atomicOr(&a.counters->timeout, 1);
+                for (long long j = it; j < it + kStages; ++j) {
+                    if ((long long)blockIdx.x + j * gridDim.x >= n_units) break;
+                    mbar_wait(&full_bar[j % kStages], (uint32_t)((j / kStages) & 1));
+                }
+            }
+            __syncthreads();
+            return;
+        }
+        const unsigned char* st = ring + stage * kChunkBytes;
 
         uint4 v[kFastVecs];
 #pragma unroll
         for (int i = 0; i < kFastVecs; ++i) {
+            const int off = (i * kFastThreads + tid) * 16;
             const int e0 = c0 + (i * kFastThreads + tid) * EPV;
-            if (aligned && e0 + EPV <= a.vocab)
-                v[i] = ld_stream(row + (size_t)e0 * ESZ);
+            if ((uint32_t)(off + 16) <= bytes)
+                v[i] = ld_shared_v4(st + off);
             else
                 v[i] = load_edge<DT>(row, e0, a.vocab);
         }
@@ -199,7 +326,13 @@ __global__ void __launch_bounds__(kFastThreads) fast_rows_kernel(RowsArgs a)
             }
         }
         Partial* out = a.partials + u;
-        if (__syncthreads_or(isnan(tmax) || tmax == INFINITY)) {
+        const int any_bad = __syncthreads_or(isnan(tmax) || tmax == INFINITY);
+        // every thread holds its data in registers: refill this stage
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(it + kStages);
+        }
+        if (any_bad) {
             if (tid == 0) {
                 out->status = kNonfinite;
                 out->count = 0u;
@@ -253,17 +386,19 @@ __global__ void __launch_bounds__(kFastThreads) fast_rows_kernel(RowsArgs a)
         } else {
             // Many elements tie at theta (or one thread holds most of the
             // top): exact k rounds of a block max over keys below the last.
+            // The values are re-read from the row (L2) so that the registers
+            // of the common path stay free.
             unsigned long long last = ~0ull;
             int n_out = 0;
             for (int r = 0; r < k; ++r) {
                 unsigned long long best = 0ull;
-#pragma unroll
                 for (int i = 0; i < kFastVecs; ++i) {
                     const int e0 = c0 + (i * kFastThreads + tid) * EPV;
+                    const uint4 w = load_edge<DT>(row, e0, a.vocab);
 #pragma unroll
                     for (int s = 0; s < EPV; ++s) {
                         if (e0 + s < a.vocab) {
-                            const unsigned long long ck = ckey(vec_elem<DT>(v[i], s), (uint32_t)(e0 + s));
+                            const unsigned long long ck = ckey(vec_elem<DT>(w, s), (uint32_t)(e0 + s));
                             if (ck < last && ck > best) best = ck;
                         }
                     }
@@ -437,15 +572,29 @@ __global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(Rows
 
 }  // namespace
 
+template <int DT>
+cudaError_t launch_fast_rows_t(const RowsArgs& a, cudaStream_t s)
+{
+    // Persistent grid: exactly the CTAs that fit at once, each with its ring.
+    const size_t smem = (size_t)kStages * kChunkBytes;
+    static int blocks_per_sm[128] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& nb = blocks_per_sm[(dev >= 0 && dev < 128) ? dev : 0];
+    if (nb == 0) {
+        cudaError_t e = cudaFuncSetAttribute(fast_rows_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fast_rows_kernel<DT>, kFastThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (nb < 1) nb = 1;
+    }
+    fast_rows_kernel<DT><<<a.num_sms * nb, kFastThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s)
 {
-    // Persistent grid: a few resident CTAs per SM walk the (row, chunk) units.
-    const int grid = a.num_sms * 6;
-    if (a.dtype == 0)
-        fast_rows_kernel<0><<<grid, kFastThreads, 0, s>>>(a);
-    else
-        fast_rows_kernel<1><<<grid, kFastThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return a.dtype == 0 ? launch_fast_rows_t<0>(a, s) : launch_fast_rows_t<1>(a, s);
 }
 
 cudaError_t launch_fast_finalize(const RowsArgs& a, cudaStream_t s)

@@ -259,11 +259,13 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mass += (double)c[j] * e[j];
             }
-            // fixed-order reduction over the 16 threads of this binade
+            // fixed-order reduction over the 16 threads of this binade: the two
+            // half-warps walk different binade lists, so each names only itself
+            const unsigned half = (lane < 16) ? 0x0000FFFFu : 0xFFFF0000u;
 #pragma unroll
             for (int o = 8; o; o >>= 1) {
-                mass += __shfl_xor_sync(0xFFFFFFFFu, mass, o, 16);
-                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 16);
+                mass += __shfl_xor_sync(half, mass, o, 16);
+                csum += __shfl_xor_sync(half, csum, o, 16);
             }
             if (g == 0) {
                 sums0[b].mass = mass;

@@ -30,7 +30,8 @@ constexpr int kTableBinades = 96;   // binades of fixed-point p / q a resample t
 // Row / position status bits (the public SV_ROW_* values).
 constexpr int kNonfinite = SV_ROW_NONFINITE, kEmpty = SV_ROW_EMPTY, kBadToken = SV_ROW_BAD_TOKEN,
               kBadParam = SV_ROW_BAD_PARAM, kBadLayout = SV_ROW_BAD_LAYOUT, kQZero = SV_ROW_Q_ZERO,
-              kResidZero = SV_ROW_RESID_ZERO, kUnsupported = SV_ROW_UNSUPPORTED;
+              kResidZero = SV_ROW_RESID_ZERO, kUnsupported = SV_ROW_UNSUPPORTED,
+              kTimeout = SV_ROW_TIMEOUT;
 constexpr int kErrorMask = SV_ROW_ERROR_MASK;
 
 // ----------------------------------------------------------------------------
@@ -91,7 +92,8 @@ struct Counters {
     int32_t n_fast;
     int32_t n_slow;
     int32_t n_jobs;
-    int32_t pad[13];
+    int32_t timeout;   // set by a row kernel whose bounded wait gave up
+    int32_t pad[12];
 };
 
 // Carving of the caller's workspace.

@@ -19,8 +19,9 @@ from . import build as _build
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
 DTYPE_BF16, DTYPE_F32 = 0, 1
 ROW_NONFINITE, ROW_EMPTY, ROW_BAD_TOKEN, ROW_BAD_PARAM, ROW_BAD_LAYOUT = 1, 2, 4, 8, 16
-ROW_Q_ZERO, ROW_RESID_ZERO, ROW_UNSUPPORTED = 32, 64, 128
-ROW_ERROR_MASK = ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | ROW_BAD_LAYOUT | ROW_UNSUPPORTED
+ROW_Q_ZERO, ROW_RESID_ZERO, ROW_UNSUPPORTED, ROW_TIMEOUT = 32, 64, 128, 256
+ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | ROW_BAD_LAYOUT | ROW_UNSUPPORTED
+                  | ROW_TIMEOUT)
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
             "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events")

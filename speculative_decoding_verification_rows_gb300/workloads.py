@@ -90,6 +90,8 @@ def _correlated(target32, g, rho=0.8, std=3.0):
 
 def _rank_drafts(draft32, g, n, K):
     """Drafter stand-in: the token at rank rho of each draft row."""
+    if n * K == 0:
+        return torch.zeros((n, K), dtype=torch.int32, device=draft32.device)
     top4 = torch.topk(draft32.reshape(n * K, -1), 4, dim=-1).indices
     probs = torch.tensor(RANK_PROBS, device=draft32.device)
     rho = torch.multinomial(probs.expand(n * K, 4), 1, generator=g)

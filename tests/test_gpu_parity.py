@@ -292,3 +292,17 @@ def test_repeated_runs_are_bitwise_identical():
         o = run_chain(w, seed=3)
         for a, b in zip(ref, (o.accept_len, o.out_tokens, o.num_emitted, o.row_status)):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 5])
+def test_tiny_vocabularies(V):
+    n, K = 6, 3
+    g = torch.Generator(device=DEV).manual_seed(V)
+    tgt = (torch.randn((n, K + 1, V), generator=g, device=DEV) * 2).to(torch.bfloat16)
+    drf = (torch.randn((n, K, V), generator=g, device=DEV) * 2).to(torch.bfloat16)
+    toks = torch.randint(0, V, (n, K), generator=g, device=DEV, dtype=torch.int32)
+    T = torch.tensor([0.0, 0.5, 1.0, 2.0, 0.5, 1.0], device=DEV)
+    tk = torch.tensor([0, 0, 1, 2, 5, 0], device=DEV, dtype=torch.int32)
+    tp = torch.tensor([1.0, 0.5, 1.0, 0.9, 1.0, 0.2], device=DEV)
+    w = workloads.Workload(f"vocab{V}", "chain", n, K, V, torch.bfloat16, tgt, drf, toks, T, tk, tp)
+    check(w, seed=V)
