@@ -56,6 +56,9 @@ def parse():
     p.add_argument("--workload", default="large", choices=sorted(DESCRIPTIONS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    p.add_argument("--quick", action="store_true",
+                   help="profiling runs: no settle loop, no end-to-end pass, no CPU baseline")
+    p.add_argument("--requests", type=int, default=0, help="scale the batch to this many requests (profiling)")
     return p.parse_args()
 
 
@@ -226,7 +229,7 @@ def run_ours(args, rank, world, local):
     sv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workloads.make(args.workload, device=dev)
+    w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
     step, out, extra = make_step(w, sv, dev)
     alg_bytes, rows_t = algorithmic_bytes(w)
     if extra is not None:
@@ -234,13 +237,14 @@ def run_ours(args, rank, world, local):
     launches_per_step = 6 + (1 if w.layout == "ragged" else 0)
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
-    clocks.start()
-    time.sleep(0.3)
-    # settle: about a second of steps before the warm-up (untimed)
-    t_end = time.time() + 1.0
-    while time.time() < t_end:
-        step()
-    torch.cuda.synchronize()
+    if not args.quick:
+        clocks.start()
+        time.sleep(0.3)
+        # settle: about a second of steps before the warm-up (untimed)
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            step()
+        torch.cuda.synchronize()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -250,6 +254,8 @@ def run_ours(args, rank, world, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for ev in k0 + k1:      # torch creates the CUDA event on its first record
+        ev.record(stream)
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
@@ -266,7 +272,7 @@ def run_ours(args, rank, world, local):
     ms_worst = max_over_ranks(ms_per_step, world)
 
     # end to end through the public API: pinned host inputs in, results out, every step
-    e2e = run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)))
+    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)))
     torch.cuda.synchronize()
     clk = clocks.stop()
 
@@ -296,7 +302,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             tp = (req_ok && a.sp.top_p) ? a.sp.top_p[req] : 1.0f;
             if (!req_ok || bad_params(T, tp)) err |= kBadParam;
             greedy = T == 0.0f;
-            if (!greedy && a.layout != 2 && !a.drf) err |= kBadParam;   // q needs the draft logits
             k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
             const bool fast = greedy || k_eff <= kFastK;
             if (!err && !fast && a.dtype != 0) err |= kUnsupported;
@@ -121,6 +120,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 }
                 start = (int)s;
             }
+            if (a.layout != 2 && !greedy && v > 0 && !a.drf) err |= kBadParam;   // q needs draft logits
             if (a.layout != 2) {
                 // one request-level error: a bad window first, then bad parameters
                 if (err & kBadLayout) err = kBadLayout;
