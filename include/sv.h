@@ -213,6 +213,28 @@ sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits
                              int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * sv_verify_chain without a workspace argument.  The pages have no
+ * counterpart: this is for callers that cannot allocate device memory where
+ * they verify -- code running while a CUDA graph is captured (cudaMalloc is
+ * refused in a global-mode capture), serving runtimes whose device memory is
+ * one pool reserved at start-up with no allocation allowed on the decode path,
+ * and plugins inside a host engine that owns all memory.  Arguments, outputs
+ * and results are those of sv_verify_chain; the scratch is a static 32 MiB
+ * device array in the library, resident on each GPU that loads it until the
+ * process exits.  Sizes whose sv_workspace_size(n_req, K, vocab) exceeds
+ * 32 MiB return SV_ERR_UNSUPPORTED before any launch (the benchmark's
+ * 128 x 8 x 248,320 batch needs about 17 MiB).  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU race, so serialise them.  Nothing
+ * is allocated or freed.
+ */
+sv_status_t sv_verify_chain_noalloc(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req,
+                                    int K, int vocab, const int32_t* draft_tokens, const int32_t* verify_len,
+                                    sv_sampling_t sp, uint64_t seed, int32_t* accept_len, int32_t* out_tokens,
+                                    int32_t* num_emitted, int32_t* row_status, sv_stream_t stream);
+
+/*
  * Measurement aid (not part of the method): when both are non-NULL, every
  * later sv_verify_chain / sv_verify_ragged / sv_build_target_probs call
  * records start_event (a cudaEvent_t) on its stream immediately before the

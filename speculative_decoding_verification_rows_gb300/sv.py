@@ -24,7 +24,7 @@ ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | RO
                   | ROW_TIMEOUT)
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
-            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events")
+            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc")
 
 
 class SVError(RuntimeError):
@@ -71,6 +71,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_verify_chain.restype = I
     L.sv_verify_ragged.argtypes = [P, P, I, I, I, I, I, P, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
     L.sv_verify_ragged.restype = I
+    L.sv_verify_chain_noalloc.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P]
+    L.sv_verify_chain_noalloc.restype = I
     L.sv_set_timing_events.argtypes = [P, P]
     L.sv_set_timing_events.restype = I
     _lib = L
@@ -228,6 +230,27 @@ def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_toke
                                   _ptr(verify_len), _sampling(temperature, top_k, top_p), seed,
                                   _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status),
                                   _ptr(w), w.numel(), _stream(dev)))
+    return o
+
+
+def verify_chain_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                         temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
+                         top_p: Optional[torch.Tensor] = None, verify_len: Optional[torch.Tensor] = None,
+                         seed: int = 0, out: Optional[VerifyOut] = None) -> VerifyOut:
+    """sv_verify_chain_noalloc: sv_verify_chain with the library's static scratch
+    (no workspace).  The outputs are allocated here unless `out` is given."""
+    target = _dev(target)
+    n, k1, V = target.shape
+    K = k1 - 1
+    dev = target.device
+    if draft is not None:
+        _dev(draft, target.dtype)
+        assert draft.shape == (n, K, V)
+    o = out or _outs(n, K, dev)
+    _check(load().sv_verify_chain_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V,
+                                          _ptr(draft_tokens), _ptr(verify_len), _sampling(temperature, top_k, top_p),
+                                          seed, _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted),
+                                          _ptr(o.row_status), _stream(dev)))
     return o
 
 
