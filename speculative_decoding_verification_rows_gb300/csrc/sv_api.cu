@@ -152,6 +152,8 @@ size_t sv_workspace_size(int n_req, int k_max, int vocab)
     }
     if (n_req > (1 << 22) || k_max > kMaxK || vocab > kMaxVocab) return 0;
     if ((long long)n_req * (2LL * k_max + 1) > (1LL << 30)) return 0;
+    // (row, segment) units of the row kernel are indexed in 32 bits
+    if ((long long)n_req * (2LL * k_max + 1) * ((vocab + kMinChunk - 1) / kMinChunk) > 0x7FFFFFFFLL) return 0;
     return ws_layout(n_req, k_max, vocab).total;
 }
 

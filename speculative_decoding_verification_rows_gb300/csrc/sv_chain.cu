@@ -222,10 +222,17 @@ __device__ int invcdf_list(const int* idx, const double* w, int n, double u, dou
 
 constexpr int kChainWarps = 8;
 
+// One warp per request.  Every lane takes its own positions j (lane, lane + 32):
+// it loads the rows' results, draws u(r, j, 0) and decides acceptance; a ballot
+// gives the first rejection, which is where the sequential walk would stop.
+// The emitted token's kept lists are staged in shared memory and lane 0 draws
+// from them in fp64, in index order.
 __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
 {
     __shared__ double s_w[kChainWarps][kFastK];
     __shared__ int s_i[kChainWarps][kFastK];
+    __shared__ double s_qp[kChainWarps][kFastK];
+    __shared__ int s_qi[kChainWarps][kFastK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = blockIdx.x * kChainWarps + warp;
     if (r >= a.n_req) return;
@@ -235,15 +242,35 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
     int32_t* out = a.out_tokens + (size_t)r * width;
     const int32_t* d = a.draft_tokens + (size_t)r * K;
 
-    // position status: target row j, draft row j, token j
+    // position status (target row j, draft row j, token j) and, for j < v,
+    // the acceptance decision
     const int timed_out = a.counters->timeout ? kTimeout : 0;
     int any_err = st.err | timed_out;
+    unsigned long long rejects = 0ull, qzero = 0ull;
     for (int j = lane; j <= K; j += 32) {
         int ps = 0;
         if (!st.err && j <= v) {
-            ps |= a.info[slot_target(r, K, j)].desc.status;
-            if (j < v && !st.greedy) ps |= a.info[slot_draft(r, K, j)].desc.status;
+            const RowInfo& T = a.info[slot_target(r, K, j)];
+            ps |= T.desc.status;
             if (j < v && ((st.tok_bad >> j) & 1)) ps |= kBadToken;
+            if (j < v) {
+                bool accept;
+                if (st.greedy) {
+                    accept = d[j] == T.desc.argmax;
+                } else {
+                    const RowInfo& Q = a.info[slot_draft(r, K, j)];
+                    ps |= Q.desc.status;
+                    const double p = T.p_token, q = Q.p_token;
+                    const double u = uniform_f64(a.seed, (uint32_t)r, (uint32_t)j, 0u);
+                    if (q > 0.0) {
+                        accept = u < p / q;
+                    } else {
+                        qzero |= 1ull << j;
+                        accept = p > 0.0;
+                    }
+                }
+                if (!accept) rejects |= 1ull << j;
+            }
         }
         if (j == 0) ps |= st.err | timed_out;
         any_err |= ps & kErrorMask;
@@ -251,6 +278,11 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
         out[j] = -1;
     }
     any_err = __reduce_or_sync(0xFFFFFFFFu, any_err);
+    // combine the lanes' 64-bit masks
+    rejects |= ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)rejects)) |
+               ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(rejects >> 32)) << 32);
+    qzero |= ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)qzero)) |
+             ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(qzero >> 32)) << 32);
     if (any_err) {
         if (lane == 0) {
             a.accept_len[r] = 0;
@@ -258,68 +290,59 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
         }
         return;
     }
+    const int acc_len = rejects ? (__ffsll((long long)rejects) - 1) : v;
+    const uint64_t tested = acc_len < 63 ? ((2ull << acc_len) - 1ull) : ~0ull;   // positions 0..acc_len
     __syncwarp();
-    if (lane != 0) return;
+    for (int j = lane; j < acc_len; j += 32) out[j] = d[j];
 
-    int acc_len = v;
-    int extra_bits_pos = -1, extra_bits = 0;
-    uint64_t q_zero_mask = 0ull;
     int t = -1;
+    int extra_bits = 0;
+    const RowInfo& P = a.info[slot_target(r, K, acc_len)];
     if (st.greedy) {
-        for (int j = 0; j < v; ++j) {
-            if (d[j] != a.info[slot_target(r, K, j)].desc.argmax) {
-                acc_len = j;
-                break;
-            }
-        }
-        t = a.info[slot_target(r, K, acc_len)].desc.argmax;
+        t = P.desc.argmax;
     } else {
-        for (int j = 0; j < v; ++j) {
-            const double p = a.info[slot_target(r, K, j)].p_token;
-            const double q = a.info[slot_draft(r, K, j)].p_token;
-            const double u = uniform_f64(a.seed, (uint32_t)r, (uint32_t)j, 0u);
-            bool accept;
-            if (q > 0.0) {
-                accept = u < p / q;
-            } else {
-                q_zero_mask |= 1ull << j;
-                accept = p > 0.0;
-            }
-            if (!accept) {
-                acc_len = j;
-                break;
-            }
-        }
-        const RowInfo& P = a.info[slot_target(r, K, acc_len)];
         const bool residual = acc_len < v;
-        const double u1 = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u);
-        if (!residual && P.n_list >= 0) {
-            double W = 0.0;
-            for (int i = 0; i < P.n_list; ++i) W += P.list_p[i];
-            t = invcdf_list(P.list_idx, P.list_p, P.n_list, u1, W);
-        } else if (residual && P.n_list >= 0 && a.info[slot_draft(r, K, acc_len)].n_list >= 0) {
-            const RowInfo& Q = a.info[slot_draft(r, K, acc_len)];
-            double W = 0.0;
-            int qi = 0;
-            for (int i = 0; i < P.n_list; ++i) {
-                const int x = P.list_idx[i];
-                while (qi < Q.n_list && Q.list_idx[qi] < x) ++qi;
-                const double qx = (qi < Q.n_list && Q.list_idx[qi] == x) ? Q.list_p[qi] : 0.0;
-                const double w = P.list_p[i] - qx;
-                s_w[warp][i] = w > 0.0 ? w : 0.0;
-                s_i[warp][i] = x;
-                W += s_w[warp][i];
+        const int np = P.n_list;
+        const RowInfo* Qp = residual ? &a.info[slot_draft(r, K, acc_len)] : nullptr;
+        const int nq = residual ? Qp->n_list : 0;
+        if (np >= 0 && nq >= 0) {
+            if (lane < np) {
+                s_i[warp][lane] = P.list_idx[lane];
+                s_w[warp][lane] = P.list_p[lane];
             }
-            if (W > 0.0) {
-                t = invcdf_list(s_i[warp], s_w[warp], P.n_list, u1, W);
-            } else {
-                extra_bits_pos = acc_len;
-                extra_bits = kResidZero;
-                double Wp = 0.0;
-                for (int i = 0; i < P.n_list; ++i) Wp += P.list_p[i];
-                t = invcdf_list(P.list_idx, P.list_p, P.n_list, u1, Wp);
+            if (residual && lane < nq) {
+                s_qi[warp][lane] = Qp->list_idx[lane];
+                s_qp[warp][lane] = Qp->list_p[lane];
             }
-        } else {
+            __syncwarp();
+            if (lane == 0) {
+                const double u1 = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u);
+                double W = 0.0;
+                if (residual) {
+                    // w_x = max(0, p_x - q_x) over p's kept tokens (index order)
+                    double wl[kFastK];
+                    int qi = 0;
+                    for (int i = 0; i < np; ++i) {
+                        const int x = s_i[warp][i];
+                        while (qi < nq && s_qi[warp][qi] < x) ++qi;
+                        const double qx = (qi < nq && s_qi[warp][qi] == x) ? s_qp[warp][qi] : 0.0;
+                        const double w = s_w[warp][i] - qx;
+                        wl[i] = w > 0.0 ? w : 0.0;
+                        W += wl[i];
+                    }
+                    if (W > 0.0) {
+                        for (int i = 0; i < np; ++i) s_w[warp][i] = wl[i];
+                    } else {
+                        extra_bits = kResidZero;   // empty residual: draw from p itself
+                        W = 0.0;
+                        for (int i = 0; i < np; ++i) W += s_w[warp][i];
+                    }
+                } else {
+                    for (int i = 0; i < np; ++i) W += s_w[warp][i];
+                }
+                t = invcdf_list(s_i[warp], s_w[warp], np, u1, W);
+            }
+        } else if (lane == 0) {
             // kept set too large to list: the resample kernel draws the token
             const int slot = atomicAdd(&a.counters->n_jobs, 1);
             ResampleJob job;
@@ -331,14 +354,16 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
             t = -2;
         }
     }
-    for (int j = 0; j < acc_len; ++j) out[j] = d[j];
-    if (t != -2) out[acc_len] = t;
-    a.accept_len[r] = acc_len;
-    a.num_emitted[r] = acc_len + 1;
-    if (a.row_status) {
-        for (int j = 0; j < v; ++j)
-            if ((q_zero_mask >> j) & 1) a.row_status[(size_t)r * width + j] |= kQZero;
-        if (extra_bits_pos >= 0) a.row_status[(size_t)r * width + extra_bits_pos] |= extra_bits;
+    if (lane == 0) {
+        if (t != -2) out[acc_len] = t;
+        a.accept_len[r] = acc_len;
+        a.num_emitted[r] = acc_len + 1;
+        if (a.row_status) {
+            const uint64_t qz = qzero & tested;
+            for (int j = 0; j < v; ++j)
+                if ((qz >> j) & 1) a.row_status[(size_t)r * width + j] |= kQZero;
+            if (extra_bits) a.row_status[(size_t)r * width + acc_len] |= extra_bits;
+        }
     }
 }
 

@@ -4,21 +4,27 @@
 // target_probs"): the top-k is selected on the raw logits (a positive
 // temperature keeps their order) and only the k kept values are divided by the
 // temperature.  Here the selection streams each [rows, vocab] row from HBM
-// exactly once, in chunks of 16 K bf16 (8 K fp32) elements:
+// exactly once and keeps at most a few hundred (logit, index) candidates:
 //
-//   1. each thread loads 8 x 16 B with streaming (L1 no-allocate) loads and
-//      takes a NaN-propagating packed max (max.NaN.bf16x2);
-//   2. the CTA finds theta = the k-th largest of its 256 thread maxima by a
-//      byte-wise radix select -- at least k elements are >= theta;
-//   3. only threads whose maximum reaches theta rescan their registers and
-//      push (logit, index) composite keys >= theta into shared memory;
-//   4. a rank-by-counting pass writes the chunk's top-k, ordered by (logit
-//      desc, index asc), to the workspace.
-// A warp per row then merges the chunk lists (a k-round tournament) and builds
-// the row's distribution in fp64 from the <= 32 kept values: temperature,
-// top-p over the top-k mass, normaliser, the probability of the row's token,
-// and the kept list in index order for the resample.  Greedy rows are the
-// k = 1 case (argmax, lowest index wins ties).
+//  * A persistent CTA owns segments of rows (4 chunks of 32 KB).  Thread 0
+//    keeps a ring of 3 shared-memory stages filled with bulk asynchronous
+//    copies (cp.async.bulk, completion on mbarriers, bounded waits), so loads
+//    stay in flight while the CTA selects.
+//  * Each thread takes a NaN-propagating packed max (max.NaN.bf16x2) of its
+//    8 x 16 B of a chunk.  In a segment's first chunk theta = the k-th largest
+//    of the 256 thread maxima (a radix select with warp-aggregated shared
+//    atomics): at least k elements are >= theta, and few more.
+//  * Only threads whose maximum reaches theta push composite keys (logit,
+//    inverted index) into shared memory.  Once the candidates hold k entries,
+//    theta becomes the exact k-th best so far, and later elements must beat
+//    it strictly (their indices are higher, so a tie cannot win).
+//  * At the segment's end a rank-by-counting pass writes its top-k, ordered by
+//    (logit desc, index asc), to the workspace.
+// A warp per row then merges the segment lists (a k-round tournament) and
+// builds the row's distribution in fp64 from the <= 32 kept values:
+// temperature, top-p over the top-k mass, normaliser, the probability of the
+// row's token, and the kept list in index order for the resample.  Greedy rows
+// are the k = 1 case (argmax, lowest index wins ties).
 #include <math.h>
 
 #include "sv_internal.cuh"
@@ -38,19 +44,13 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
-__device__ __forceinline__ uint4 ld_stream(const void* p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
 
 // ---- shared-memory ring fed by bulk async copies (TMA, cp.async.bulk) ----
 constexpr int kStages = 3;                                  // chunks in flight per CTA
 constexpr int kChunkBytes = kFastThreads * kFastVecs * 16;  // 32 KB: one chunk of either dtype
-constexpr long long kWaitPolls = 1ll << 26;                 // try_wait polls before a wait gives up
+constexpr int kSegChunks = 4;                               // chunks per segment (one partial list)
+constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
+constexpr int kCandCapS = 512;                              // candidate buffer of a segment
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -91,8 +91,8 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t pari
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
-// Global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned)
-// completing on `bar`.
+// Global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
+// aligned) completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -143,18 +143,32 @@ __device__ __forceinline__ uint4 load_edge(const char* row, int e0, int vocab)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ float warp_max_f(float x)
+// Byte offset of a row and the bulk-copied bytes of one chunk of it.
+template <int DT>
+__device__ __forceinline__ const char* task_row(const RowsArgs& a, const RowTask& t)
 {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-    return x;
+    constexpr int ESZ = DT == 0 ? 2 : 4;
+    const int64_t stride = t.is_draft ? a.stride_d : a.stride_t;
+    return (const char*)(t.is_draft ? a.drf : a.tgt) + (size_t)t.row * (size_t)stride * ESZ;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t chunk_bytes(const char* row, int c0, int vocab)
+{
+    constexpr int ESZ = DT == 0 ? 2 : 4;
+    constexpr int CHUNK = kChunkBytes / ESZ;
+    const int n_here = min(CHUNK, vocab - c0);
+    const char* src = row + (size_t)c0 * ESZ;
+    return ((uintptr_t)src & 15u) ? 0u : ((uint32_t)(n_here * ESZ) & ~15u);
 }
 
-// k-th largest of one 32-bit key per thread (k <= blockDim), by a radix select
-// over the top `rounds` bytes.  Keys whose low bytes are not examined are
-// assumed equal (bf16-derived keys: 0x0000 below a positive value, 0xFFFF
-// below a negative one).
-__device__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t* hist, uint32_t* s_digit, int* s_kk)
+// k-th largest of one 32-bit key per thread (k <= blockDim) by a byte-wise
+// radix select over the top `rounds` bytes.  Lanes of a warp that share a
+// digit add their count through one leader (__match_any_sync), so the many
+// equal digits of similar keys do not serialise on one shared counter.  Keys
+// whose low bytes are not examined are equal below a given top (bf16-derived
+// keys: 0x0000 under a positive value, 0xFFFF under a negative one).
+__device__ __noinline__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t* hist, uint32_t* s_digit,
+                                                    int* s_kk)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, mask = 0u;
@@ -163,22 +177,24 @@ __device__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t*
         const int shift = 24 - 8 * r;
         for (int b = tid; b < 256; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        const uint32_t d = ((key & mask) == prefix) ? ((key >> shift) & 255u) : 0x100u;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
+        if (d != 0x100u && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
         __syncthreads();
         if (warp == 0) {
-            uint32_t c[8], s = 0u;
+            uint32_t c[8], sum = 0u;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 c[i] = hist[255 - 8 * lane - i];
-                s += c[i];
+                sum += c[i];
             }
-            uint32_t incl = s;
+            uint32_t incl = sum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                 if (lane >= o) incl += y;
             }
-            uint32_t excl = incl - s;
+            uint32_t excl = incl - sum;
             if (excl < (uint32_t)kk && (uint32_t)kk <= incl) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -195,31 +211,92 @@ __device__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t*
         prefix |= (*s_digit) << shift;
         mask |= 0xFFu << shift;
         kk = *s_kk;
-        __syncthreads();
     }
     if (rounds == 2) prefix |= (prefix & 0x80000000u) ? 0u : 0xFFFFu;
     return prefix;
 }
 
-// Where unit u (row task t, chunk c) starts, and how many bytes of it the bulk
-// copy moves (a 16-byte-aligned multiple of 16; the rest, if any, is loaded
-// element by element).
-template <int DT>
-__device__ __forceinline__ const char* unit_source(const RowsArgs& a, long long u, int nchunks, int& c0,
-                                                   uint32_t& bytes, RowTask& task)
+// Keep the top k of the candidate buffer (rank by counting; composite keys
+// are distinct).  Raises theta to the k-th best once k candidates exist.
+__device__ __noinline__ void compact_candidates(unsigned long long* cand, unsigned long long* tmp, int* s_cnt,
+                                                float* s_theta, int* s_strict, int k)
 {
-    constexpr int ESZ = DT == 0 ? 2 : 4;
-    constexpr int CHUNK = kChunkBytes / ESZ;
-    const int t = (int)(u / nchunks);
-    const int c = (int)(u - (long long)t * nchunks);
-    task = a.fast_tasks[t];
-    const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
-    const char* row = (const char*)(task.is_draft ? a.drf : a.tgt) + (size_t)task.row * (size_t)stride * ESZ;
-    c0 = c * CHUNK;
-    const int n_here = min(CHUNK, a.vocab - c0);
-    const char* src = row + (size_t)c0 * ESZ;
-    bytes = ((uintptr_t)src & 15u) ? 0u : (uint32_t)(n_here * ESZ) & ~15u;
-    return row;
+    __syncthreads();
+    const int n = min(*s_cnt, kCandCapS);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const unsigned long long ck = cand[i];
+        int r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // eight independent chains
+        int j = 0;
+        for (; j + 8 <= n; j += 8) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) r8[q] += (cand[j + q] > ck) ? 1 : 0;
+        }
+        for (; j < n; ++j) r8[0] += (cand[j] > ck) ? 1 : 0;
+        const int rank = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+        if (rank < k) tmp[rank] = ck;
+    }
+    __syncthreads();
+    const int m = min(n, k);
+    if ((int)threadIdx.x < m) cand[threadIdx.x] = tmp[threadIdx.x];
+    if (threadIdx.x == 0) {
+        *s_cnt = m;
+        if (m == k) {
+            *s_theta = ckey_value(tmp[k - 1]);
+            *s_strict = 1;
+        }
+    }
+    __syncthreads();
+}
+
+// Push the elements of one 16-byte vector that reach theta (rare: called only
+// for vectors whose maximum does).  Kept out of line so that the per-chunk
+// loop stays small in the instruction cache.
+template <int DT>
+__device__ __noinline__ void push_vector(uint4 v, int e0, int vocab, float theta, int strict,
+                                         unsigned long long* cand, int* s_cnt, int* s_overflow)
+{
+    constexpr int EPV = DT == 0 ? 8 : 4;
+    for (int s = 0; s < EPV; ++s) {
+        const float val = vec_elem<DT>(v, s);
+        if (e0 + s < vocab && (strict ? val > theta : val >= theta)) {
+            const int pos = atomicAdd(s_cnt, 1);
+            if (pos < kCandCapS)
+                cand[pos] = ckey(val, (uint32_t)(e0 + s));
+            else
+                *s_overflow = 1;
+        }
+    }
+}
+
+// Exact top-k of a segment by k rounds of a block max over keys below the last
+// (used when too many elements tie at theta).  Out of line: it is cold.
+template <int DT>
+__device__ __noinline__ int exact_segment_topk(const char* row, int seg0, int seg_end, int k,
+                                               unsigned long long* out_keys, unsigned long long* s_red64)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long last = ~0ull;
+    int n_out = 0;
+    for (int r = 0; r < k; ++r) {
+        unsigned long long best = 0ull;
+        for (int e = seg0 + tid; e < seg_end; e += kFastThreads) {
+            const float val = DT == 0 ? __uint_as_float((uint32_t)((const uint16_t*)row)[e] << 16)
+                                      : ((const float*)row)[e];
+            const unsigned long long ck = ckey(val, (uint32_t)e);
+            if (ck < last && ck > best) best = ck;
+        }
+        best = warp_max_u64(best);
+        if (lane == 0) s_red64[warp] = best;
+        __syncthreads();
+        best = s_red64[0];
+        for (int w = 1; w < kFastThreads / 32; ++w) best = s_red64[w] > best ? s_red64[w] : best;
+        __syncthreads();
+        if (best == 0ull) break;
+        if (tid == 0) out_keys[r] = best;
+        last = best;
+        ++n_out;
+    }
+    return n_out;
 }
 
 template <int DT>
@@ -231,107 +308,176 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     static_assert(CHUNK * ESZ == kChunkBytes, "one chunk fills one ring stage");
     extern __shared__ __align__(128) unsigned char ring[];   // kStages x 32 KB
     __shared__ __align__(8) unsigned long long full_bar[kStages];
-    __shared__ unsigned long long s_cand[kCandCap];
-    __shared__ uint32_t s_hist[256];
-    __shared__ float s_redf[kFastThreads / 32];
+    __shared__ unsigned long long s_cand[kCandCapS];
+    __shared__ unsigned long long s_tmp[kFastK];
     __shared__ unsigned long long s_red64[kFastThreads / 32];
+    __shared__ uint32_t s_hist[256];
     __shared__ uint32_t s_digit;
     __shared__ int s_kk;
-    __shared__ int s_cnt;
+    __shared__ float s_theta;
+    __shared__ int s_strict, s_cnt, s_overflow;
+    __shared__ int s_compact[2];
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int n_tasks = a.counters->n_fast;
     const int nchunks = (a.vocab + CHUNK - 1) / CHUNK;
-    const long long n_units = (long long)n_tasks * nchunks;
-    if ((long long)blockIdx.x >= n_units) return;
+    const int nseg = (nchunks + kSegChunks - 1) / kSegChunks;
+    const int n_units = n_tasks * nseg;   // the host keeps this below 2^31
+    const int G = gridDim.x;
+    if ((int)blockIdx.x >= n_units) return;
 
-    // Thread 0 feeds the ring: unit i of this CTA goes to stage i % kStages.
-    auto issue = [&](long long i) {
-        const long long uu = (long long)blockIdx.x + i * gridDim.x;
-        if (uu >= n_units) return;
-        int cc0;
-        uint32_t bytes;
-        RowTask tk;
-        const char* row = unit_source<DT>(a, uu, nchunks, cc0, bytes, tk);
-        unsigned long long* bar = &full_bar[i % kStages];
+    // Consumer tasks: the current unit's and the next one's (prefetched).
+    int u = blockIdx.x;
+    int cur_t = u / nseg;
+    RowTask task = a.fast_tasks[cur_t];
+    int next_t = (u + G < n_units) ? (u + G) / nseg : -1;
+    RowTask next_task = next_t >= 0 ? a.fast_tasks[next_t] : task;
+
+    // Producer state (thread 0): the next (unit, chunk) to copy, where it goes
+    // in the ring, and the row it reads.  It runs up to kStages chunks ahead,
+    // which can be more than one unit when segments are short; it reuses the
+    // consumer's tasks when it can and reads the task list otherwise.
+    int p_u = u, p_t = cur_t, p_chunk = (u - cur_t * nseg) * kSegChunks;
+    int p_end = min(nchunks, p_chunk + kSegChunks);
+    int p_slot = 0;
+    const char* p_row = task_row<DT>(a, task);
+    auto produce = [&]() {
+        if (p_u >= n_units) return;
+        const int c0 = p_chunk * CHUNK;
+        const uint32_t bytes = chunk_bytes<DT>(p_row, c0, a.vocab);
+        unsigned long long* bar = &full_bar[p_slot];
         if (bytes) {
             mbar_expect_tx(bar, bytes);
-            bulk_g2s(ring + (i % kStages) * kChunkBytes, row + (size_t)cc0 * ESZ, bytes, bar);
+            bulk_g2s(ring + p_slot * kChunkBytes, p_row + (size_t)c0 * ESZ, bytes, bar);
         } else {
             mbar_arrive(bar);
+        }
+        if (++p_slot == kStages) p_slot = 0;
+        if (++p_chunk == p_end) {
+            p_u += G;
+            if (p_u < n_units) {
+                const int t = p_u / nseg;
+                if (t != p_t) {
+                    p_row = (t == cur_t) ? task_row<DT>(a, task)
+                                         : (t == next_t ? task_row<DT>(a, next_task) : task_row<DT>(a, a.fast_tasks[t]));
+                    p_t = t;
+                }
+                p_chunk = (p_u - t * nseg) * kSegChunks;
+                p_end = min(nchunks, p_chunk + kSegChunks);
+            }
         }
     };
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], 1u);
         mbar_fence_init();
+        s_compact[0] = s_compact[1] = 0;
     }
     __syncthreads();
     if (tid == 0)
-        for (int i = 0; i < kStages; ++i) issue(i);
+        for (int i = 0; i < kStages; ++i) produce();
 
-    long long it = 0;
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-        __syncthreads();   // shared memory of the previous unit is free
-        int c0;
-        uint32_t bytes;
-        RowTask task;
-        const char* row = unit_source<DT>(a, u, nchunks, c0, bytes, task);
-        const int stage = (int)(it % kStages);
-        const bool arrived = mbar_wait(&full_bar[stage], (uint32_t)((it / kStages) & 1));
-        if (!__syncthreads_and(arrived)) {
-            // A bulk copy never completed: report it, let the copies already
-            // issued land (bounded), and leave the remaining rows unprocessed.
-            if (tid == 0) {
-                atomicOr(&a.counters->timeout, 1);
-                for (long long j = it; j < it + kStages; ++j) {
-                    if ((long long)blockIdx.x + j * gridDim.x >= n_units) break;
-                    mbar_wait(&full_bar[j % kStages], (uint32_t)((j / kStages) & 1));
+    int c_slot = 0;
+    uint32_t c_phase = 0u;
+    for (; u < n_units; u += G) {
+        if (u != (int)blockIdx.x) {
+            cur_t = next_t;
+            task = next_task;
+            next_t = (u + G < n_units) ? (u + G) / nseg : -1;
+            if (next_t >= 0) next_task = (next_t == cur_t) ? task : a.fast_tasks[next_t];
+        }
+        const char* row = task_row<DT>(a, task);
+        const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
+        const int compact_at = max(2 * k, 32);
+        const int chunk0 = (u - cur_t * nseg) * kSegChunks;
+        const int ns = min(kSegChunks, nchunks - chunk0);
+        __syncthreads();   // the previous segment's buffers are free
+        if (tid == 0) {
+            s_cnt = 0;
+            s_overflow = 0;
+            s_strict = 0;
+        }
+        int bad = 0;
+        for (int j = 0; j < ns; ++j) {
+            const int c0 = (chunk0 + j) * CHUNK;
+            const uint32_t bytes = chunk_bytes<DT>(row, c0, a.vocab);
+            const bool arrived = mbar_wait(&full_bar[c_slot], c_phase);
+            const unsigned char* st = ring + c_slot * kChunkBytes;
+            uint4 v[kFastVecs];
+#pragma unroll
+            for (int i = 0; i < kFastVecs; ++i) {
+                const int off = (i * kFastThreads + tid) * 16;
+                if ((uint32_t)(off + 16) <= bytes)
+                    v[i] = ld_shared_v4(st + off);
+                else
+                    v[i] = load_edge<DT>(row, c0 + (i * kFastThreads + tid) * EPV, a.vocab);
+            }
+            if (++c_slot == kStages) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
+            // Per-vector NaN-propagating maxima, then their tree max: the same
+            // operation count as one running max, with independent chains.
+            float vmax[kFastVecs];
+            if (DT == 0) {
+                uint32_t m2[kFastVecs];
+#pragma unroll
+                for (int i = 0; i < kFastVecs; ++i) {
+                    m2[i] = bmax2_nan(bmax2_nan(v[i].x, v[i].y), bmax2_nan(v[i].z, v[i].w));
+                    vmax[i] = fmax_nan(__uint_as_float(m2[i] << 16), __uint_as_float(m2[i] & 0xFFFF0000u));
                 }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kFastVecs; ++i)
+                    vmax[i] = fmax_nan(fmax_nan(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
+                                       fmax_nan(__uint_as_float(v[i].z), __uint_as_float(v[i].w)));
             }
-            __syncthreads();
-            return;
-        }
-        const unsigned char* st = ring + stage * kChunkBytes;
-
-        uint4 v[kFastVecs];
-#pragma unroll
-        for (int i = 0; i < kFastVecs; ++i) {
-            const int off = (i * kFastThreads + tid) * 16;
-            const int e0 = c0 + (i * kFastThreads + tid) * EPV;
-            if ((uint32_t)(off + 16) <= bytes)
-                v[i] = ld_shared_v4(st + off);
-            else
-                v[i] = load_edge<DT>(row, e0, a.vocab);
-        }
-
-        float tmax;
-        if (DT == 0) {
-            uint32_t m2 = 0xFF80FF80u;
-#pragma unroll
-            for (int i = 0; i < kFastVecs; ++i) {
-                m2 = bmax2_nan(m2, v[i].x);
-                m2 = bmax2_nan(m2, v[i].y);
-                m2 = bmax2_nan(m2, v[i].z);
-                m2 = bmax2_nan(m2, v[i].w);
+            const float tmax = fmax_nan(fmax_nan(fmax_nan(vmax[0], vmax[1]), fmax_nan(vmax[2], vmax[3])),
+                                        fmax_nan(fmax_nan(vmax[4], vmax[5]), fmax_nan(vmax[6], vmax[7])));
+            bad |= (isnan(tmax) || tmax == INFINITY) ? 1 : 0;
+            // Thread 0 decides whether to compact before this chunk's pushes (a
+            // slightly stale count is fine; the flag is double-buffered so the
+            // previous chunk's readers are not overtaken).
+            if (tid == 0) s_compact[j & 1] = (j > 0 && s_cnt > compact_at) ? 1 : 0;
+            // One barrier per chunk: every thread holds its data (the stage can
+            // be refilled), the compaction decision is published, and a bulk
+            // copy that never arrived stops the whole CTA.
+            if (__syncthreads_or(!arrived)) {
+                if (tid == 0) {
+                    atomicOr(&a.counters->timeout, 1);
+                    // let the copies already issued land (bounded), then leave
+                    for (int q = 0; q < kStages; ++q) mbar_wait(&full_bar[q], c_phase ^ (q < c_slot ? 1u : 0u));
+                }
+                __syncthreads();
+                return;
             }
-            tmax = fmax_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
-        } else {
-            tmax = -INFINITY;
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                produce();
+            }
+            float theta;
+            int strict;
+            if (j == 0) {   // exact k-th largest of the 256 thread maxima
+                const uint32_t key = key_of_f32_bits(__float_as_uint(tmax));
+                theta = f32_of_key(block_kth_largest(key, k, DT == 0 ? 2 : 4, s_hist, &s_digit, &s_kk));
+                strict = 0;
+                if (tid == 0) s_theta = theta;
+            } else {
+                if (s_compact[j & 1]) compact_candidates(s_cand, s_tmp, &s_cnt, &s_theta, &s_strict, k);
+                theta = s_theta;
+                strict = s_strict;
+            }
+            // Only vectors whose maximum reaches theta are scanned element-wise
+            // (typically one vector of one thread in a few).
+            if (strict ? (tmax > theta) : (tmax >= theta)) {
 #pragma unroll
-            for (int i = 0; i < kFastVecs; ++i) {
-                tmax = fmax_nan(tmax, __uint_as_float(v[i].x));
-                tmax = fmax_nan(tmax, __uint_as_float(v[i].y));
-                tmax = fmax_nan(tmax, __uint_as_float(v[i].z));
-                tmax = fmax_nan(tmax, __uint_as_float(v[i].w));
+                for (int i = 0; i < kFastVecs; ++i)
+                    if (strict ? (vmax[i] > theta) : (vmax[i] >= theta))
+                        push_vector<DT>(v[i], c0 + (i * kFastThreads + tid) * EPV, a.vocab, theta, strict, s_cand,
+                                        &s_cnt, &s_overflow);
             }
         }
         Partial* out = a.partials + u;
-        const int any_bad = __syncthreads_or(isnan(tmax) || tmax == INFINITY);
-        // every thread holds its data in registers: refill this stage
-        if (tid == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(it + kStages);
-        }
+        const int any_bad = __syncthreads_or(bad);
         if (any_bad) {
             if (tid == 0) {
                 out->status = kNonfinite;
@@ -339,92 +485,30 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             }
             continue;
         }
-
-        const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
-        float theta;
-        if (k == 1) {
-            const float wm = warp_max_f(tmax);
-            if (lane == 0) s_redf[warp] = wm;
-            __syncthreads();
-            theta = s_redf[0];
-#pragma unroll
-            for (int w = 1; w < kFastThreads / 32; ++w) theta = fmaxf(theta, s_redf[w]);
-        } else {
-            const uint32_t key = key_of_f32_bits(__float_as_uint(tmax));
-            theta = f32_of_key(block_kth_largest(key, k, DT == 0 ? 2 : 4, s_hist, &s_digit, &s_kk));
-        }
-
-        if (tid == 0) s_cnt = 0;
-        __syncthreads();
-        if (tmax >= theta) {
-#pragma unroll
-            for (int i = 0; i < kFastVecs; ++i) {
-                const int e0 = c0 + (i * kFastThreads + tid) * EPV;
-#pragma unroll
-                for (int s = 0; s < EPV; ++s) {
-                    const float val = vec_elem<DT>(v[i], s);
-                    if (e0 + s < a.vocab && val >= theta) {
-                        const int pos = atomicAdd(&s_cnt, 1);
-                        if (pos < kCandCap) s_cand[pos] = ckey(val, (uint32_t)(e0 + s));
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        const int cnt = s_cnt;
-        if (cnt <= kCandCap) {
-            if (tid < cnt) {
-                const unsigned long long ck = s_cand[tid];
-                int rank = 0;
-                for (int j = 0; j < cnt; ++j) rank += (s_cand[j] > ck) ? 1 : 0;
-                if (rank < k) out->keys[rank] = ck;
-            }
+        if (!s_overflow) {
+            compact_candidates(s_cand, s_tmp, &s_cnt, &s_theta, &s_strict, k);
+            const int m = s_cnt;
+            if (tid < m) out->keys[tid] = s_cand[tid];
             if (tid == 0) {
                 out->status = 0u;
-                out->count = (uint32_t)(cnt < k ? cnt : k);
+                out->count = (uint32_t)m;
             }
-        } else {
-            // Many elements tie at theta (or one thread holds most of the
-            // top): exact k rounds of a block max over keys below the last.
-            // The values are re-read from the row (L2) so that the registers
-            // of the common path stay free.
-            unsigned long long last = ~0ull;
-            int n_out = 0;
-            for (int r = 0; r < k; ++r) {
-                unsigned long long best = 0ull;
-                for (int i = 0; i < kFastVecs; ++i) {
-                    const int e0 = c0 + (i * kFastThreads + tid) * EPV;
-                    const uint4 w = load_edge<DT>(row, e0, a.vocab);
-#pragma unroll
-                    for (int s = 0; s < EPV; ++s) {
-                        if (e0 + s < a.vocab) {
-                            const unsigned long long ck = ckey(vec_elem<DT>(w, s), (uint32_t)(e0 + s));
-                            if (ck < last && ck > best) best = ck;
-                        }
-                    }
-                }
-                best = warp_max_u64(best);
-                if (lane == 0) s_red64[warp] = best;
-                __syncthreads();
-                best = s_red64[0];
-#pragma unroll
-                for (int w = 1; w < kFastThreads / 32; ++w) best = s_red64[w] > best ? s_red64[w] : best;
-                __syncthreads();
-                if (best == 0ull) break;
-                if (tid == 0) out->keys[r] = best;
-                last = best;
-                ++n_out;
-            }
-            if (tid == 0) {
-                out->status = 0u;
-                out->count = (uint32_t)n_out;
-            }
+            continue;
+        }
+        // Too many elements reached theta (heavy ties): exact k rounds of a
+        // block max over the segment, re-read from the row.
+        const int seg0 = chunk0 * CHUNK;
+        const int n_out = exact_segment_topk<DT>(row, seg0, min(a.vocab, seg0 + ns * CHUNK), k, out->keys, s_red64);
+        if (tid == 0) {
+            out->status = 0u;
+            out->count = (uint32_t)n_out;
         }
     }
 }
 
 constexpr int kFinalizeWarps = 8;
-constexpr int kMaxChunkSlots = 4;   // chunks per lane in the merge: up to 128 chunks per row
+constexpr int kMaxChunkSlots = 4;   // segment lists per lane in the merge: up to 128 per row
+constexpr int kStagedLists = 8;     // rows with at most this many lists merge in shared memory
 
 template <int DT>
 __global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(RowsArgs a)
@@ -432,13 +516,14 @@ __global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(Rows
     constexpr int EPV = DT == 0 ? 8 : 4;
     constexpr int CHUNK = kFastThreads * kFastVecs * EPV;
     __shared__ unsigned long long s_top[kFinalizeWarps][kFastK];
+    __shared__ unsigned long long s_lists[kFinalizeWarps][kStagedLists][kFastK];
     __shared__ double s_e[kFinalizeWarps][kFastK];
     __shared__ int s_kept[kFinalizeWarps];
     __shared__ double s_z[kFinalizeWarps];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
-    const int nchunks = (a.vocab + CHUNK - 1) / CHUNK;
+    const int nchunks = ((a.vocab + CHUNK - 1) / CHUNK + kSegChunks - 1) / kSegChunks;   // segment lists per row
     for (int t = blockIdx.x * kFinalizeWarps + warp; t < n_tasks; t += gridDim.x * kFinalizeWarps) {
         const RowTask task = a.fast_tasks[t];
         const Partial* P = a.partials + (size_t)t * nchunks;
@@ -450,30 +535,47 @@ __global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(Rows
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
         int n_top = 0;
         if (!(st & kNonfinite)) {
-            int head[kMaxChunkSlots];
+            if (nchunks <= kStagedLists) {
+                // Stage the lists in shared memory with independent loads, then
+                // merge: lane c holds the head of list c.
+                for (int c = 0; c < nchunks; ++c) s_lists[warp][c][lane] = P[c].keys[lane];
+                const int cnt = lane < nchunks ? (int)P[lane].count : 0;
+                __syncwarp();
+                int head = 0;
+                for (int r = 0; r < k; ++r) {
+                    const unsigned long long key = head < cnt ? s_lists[warp][lane][head] : 0ull;
+                    const unsigned long long wbest = warp_max_u64(key);
+                    if (wbest == 0ull) break;
+                    if (key == wbest) ++head;
+                    if (lane == 0) s_top[warp][r] = wbest;
+                    n_top = r + 1;
+                }
+            } else {
+                int head[kMaxChunkSlots];
 #pragma unroll
-            for (int j = 0; j < kMaxChunkSlots; ++j) head[j] = 0;
-            for (int r = 0; r < k; ++r) {
-                unsigned long long best = 0ull;
-                int bj = -1;
+                for (int j = 0; j < kMaxChunkSlots; ++j) head[j] = 0;
+                for (int r = 0; r < k; ++r) {
+                    unsigned long long best = 0ull;
+                    int bj = -1;
 #pragma unroll
-                for (int j = 0; j < kMaxChunkSlots; ++j) {
-                    const int c = lane + 32 * j;
-                    if (c < nchunks && head[j] < (int)P[c].count) {
-                        const unsigned long long key = P[c].keys[head[j]];
-                        if (key > best) {
-                            best = key;
-                            bj = j;
+                    for (int j = 0; j < kMaxChunkSlots; ++j) {
+                        const int c = lane + 32 * j;
+                        if (c < nchunks && head[j] < (int)P[c].count) {
+                            const unsigned long long key = P[c].keys[head[j]];
+                            if (key > best) {
+                                best = key;
+                                bj = j;
+                            }
                         }
                     }
-                }
-                const unsigned long long wbest = warp_max_u64(best);
-                if (wbest == 0ull) break;
+                    const unsigned long long wbest = warp_max_u64(best);
+                    if (wbest == 0ull) break;
 #pragma unroll
-                for (int j = 0; j < kMaxChunkSlots; ++j)
-                    if (best == wbest && bj == j) head[j] += 1;
-                if (lane == 0) s_top[warp][r] = wbest;
-                n_top = r + 1;
+                    for (int j = 0; j < kMaxChunkSlots; ++j)
+                        if (best == wbest && bj == j) head[j] += 1;
+                    if (lane == 0) s_top[warp][r] = wbest;
+                    n_top = r + 1;
+                }
             }
         }
         __syncwarp();
