@@ -48,9 +48,10 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
 // ---- shared-memory ring fed by bulk async copies (TMA, cp.async.bulk) ----
 constexpr int kStages = 3;                                  // chunks in flight per CTA
 constexpr int kChunkBytes = kFastThreads * kFastVecs * 16;  // 32 KB: one chunk of either dtype
-constexpr int kSegChunks = 4;                               // chunks per segment (one partial list)
+constexpr int kSegChunks = 8;                               // chunks per segment (one partial list)
 constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
-constexpr int kCandCapS = 512;                              // candidate buffer of a segment
+constexpr int kWarpCap = 64;                                // candidate slots per warp
+constexpr int kCandCapS = kWarpCap * (kFastThreads / 32);   // candidate buffer of a segment
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -216,56 +217,48 @@ __device__ __noinline__ uint32_t block_kth_largest(uint32_t key, int k, int roun
     return prefix;
 }
 
-// Keep the top k of the candidate buffer (rank by counting; composite keys
-// are distinct).  Raises theta to the k-th best once k candidates exist.
-__device__ __noinline__ void compact_candidates(unsigned long long* cand, unsigned long long* tmp, int* s_cnt,
-                                                float* s_theta, int* s_strict, int k)
+// Keep the top k of the candidates (rank by counting; composite keys are
+// distinct).  The candidates sit in per-warp regions of kWarpCap slots with
+// their counts in wcnt[]; they are gathered into `all`, ranked, and the top k
+// go back to warp 0's region (the other regions become empty).  Raises theta
+// to the k-th best once k candidates exist.
+__device__ __noinline__ void compact_candidates(unsigned long long* cand, int* wcnt, unsigned long long* all,
+                                                float* s_theta, int* s_strict, int* s_n, int k)
 {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncthreads();
-    const int n = min(*s_cnt, kCandCapS);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const unsigned long long ck = cand[i];
+    int off = 0, n = 0;
+    for (int w = 0; w < kFastThreads / 32; ++w) {
+        const int c = min(wcnt[w], kWarpCap);
+        if (w < warp) off += c;
+        n += c;
+    }
+    const int mine = min(wcnt[warp], kWarpCap);
+    for (int i = lane; i < mine; i += 32) all[off + i] = cand[warp * kWarpCap + i];
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+        const unsigned long long ck = all[i];
         int r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // eight independent chains
         int j = 0;
         for (; j + 8 <= n; j += 8) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) r8[q] += (cand[j + q] > ck) ? 1 : 0;
+            for (int q = 0; q < 8; ++q) r8[q] += (all[j + q] > ck) ? 1 : 0;
         }
-        for (; j < n; ++j) r8[0] += (cand[j] > ck) ? 1 : 0;
+        for (; j < n; ++j) r8[0] += (all[j] > ck) ? 1 : 0;
         const int rank = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-        if (rank < k) tmp[rank] = ck;
+        if (rank < k) cand[rank] = ck;   // warp 0's region, ordered
     }
-    __syncthreads();
     const int m = min(n, k);
-    if ((int)threadIdx.x < m) cand[threadIdx.x] = tmp[threadIdx.x];
-    if (threadIdx.x == 0) {
-        *s_cnt = m;
+    __syncthreads();
+    if (tid < kFastThreads / 32) wcnt[tid] = tid == 0 ? m : 0;
+    if (tid == 0) {
+        *s_n = m;
         if (m == k) {
-            *s_theta = ckey_value(tmp[k - 1]);
+            *s_theta = ckey_value(cand[k - 1]);
             *s_strict = 1;
         }
     }
     __syncthreads();
-}
-
-// Push the elements of one 16-byte vector that reach theta (rare: called only
-// for vectors whose maximum does).  Kept out of line so that the per-chunk
-// loop stays small in the instruction cache.
-template <int DT>
-__device__ __noinline__ void push_vector(uint4 v, int e0, int vocab, float theta, int strict,
-                                         unsigned long long* cand, int* s_cnt, int* s_overflow)
-{
-    constexpr int EPV = DT == 0 ? 8 : 4;
-    for (int s = 0; s < EPV; ++s) {
-        const float val = vec_elem<DT>(v, s);
-        if (e0 + s < vocab && (strict ? val > theta : val >= theta)) {
-            const int pos = atomicAdd(s_cnt, 1);
-            if (pos < kCandCapS)
-                cand[pos] = ckey(val, (uint32_t)(e0 + s));
-            else
-                *s_overflow = 1;
-        }
-    }
 }
 
 // Exact top-k of a segment by k rounds of a block max over keys below the last
@@ -308,17 +301,18 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     static_assert(CHUNK * ESZ == kChunkBytes, "one chunk fills one ring stage");
     extern __shared__ __align__(128) unsigned char ring[];   // kStages x 32 KB
     __shared__ __align__(8) unsigned long long full_bar[kStages];
-    __shared__ unsigned long long s_cand[kCandCapS];
-    __shared__ unsigned long long s_tmp[kFastK];
+    __shared__ unsigned long long s_cand[kCandCapS];      // per-warp candidate regions
+    __shared__ unsigned long long s_all[kCandCapS];       // gathered candidates (compaction)
+    __shared__ int s_wcnt[kFastThreads / 32];
     __shared__ unsigned long long s_red64[kFastThreads / 32];
     __shared__ uint32_t s_hist[256];
     __shared__ uint32_t s_digit;
     __shared__ int s_kk;
     __shared__ float s_theta;
-    __shared__ int s_strict, s_cnt, s_overflow;
+    __shared__ int s_strict, s_n, s_overflow;
     __shared__ int s_compact[2];
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_tasks = a.counters->n_fast;
     const int nchunks = (a.vocab + CHUNK - 1) / CHUNK;
     const int nseg = (nchunks + kSegChunks - 1) / kSegChunks;
@@ -387,15 +381,15 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         }
         const char* row = task_row<DT>(a, task);
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
-        const int compact_at = max(2 * k, 32);
+        const int compact_at = max(2 * k, 40);
         const int chunk0 = (u - cur_t * nseg) * kSegChunks;
         const int ns = min(kSegChunks, nchunks - chunk0);
         __syncthreads();   // the previous segment's buffers are free
         if (tid == 0) {
-            s_cnt = 0;
             s_overflow = 0;
             s_strict = 0;
         }
+        int wcnt = 0;   // this warp's candidates (same value in every lane)
         int bad = 0;
         for (int j = 0; j < ns; ++j) {
             const int c0 = (chunk0 + j) * CHUNK;
@@ -437,7 +431,12 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             // Thread 0 decides whether to compact before this chunk's pushes (a
             // slightly stale count is fine; the flag is double-buffered so the
             // previous chunk's readers are not overtaken).
-            if (tid == 0) s_compact[j & 1] = (j > 0 && s_cnt > compact_at) ? 1 : 0;
+            if (lane == 0) s_wcnt[warp] = wcnt;
+            if (tid == 0) {
+                int tot = 0;   // possibly a little stale: the decision only needs to be shared
+                for (int w = 0; w < kFastThreads / 32; ++w) tot += s_wcnt[w];
+                s_compact[j & 1] = (j > 0 && s_strict == 0 && tot > compact_at) ? 1 : 0;
+            }
             // One barrier per chunk: every thread holds its data (the stage can
             // be refilled), the compaction decision is published, and a bulk
             // copy that never arrived stops the whole CTA.
@@ -462,18 +461,43 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                 strict = 0;
                 if (tid == 0) s_theta = theta;
             } else {
-                if (s_compact[j & 1]) compact_candidates(s_cand, s_tmp, &s_cnt, &s_theta, &s_strict, k);
+                if (s_compact[j & 1]) {
+                    compact_candidates(s_cand, s_wcnt, s_all, &s_theta, &s_strict, &s_n, k);
+                    wcnt = s_wcnt[warp];
+                }
                 theta = s_theta;
                 strict = s_strict;
             }
-            // Only vectors whose maximum reaches theta are scanned element-wise
-            // (typically one vector of one thread in a few).
-            if (strict ? (tmax > theta) : (tmax >= theta)) {
+            // Warp-cooperative push: one ballot per vector slot; for each lane
+            // whose vector maximum reaches theta, the warp takes that vector
+            // (broadcast), EPV lanes test one element each, and one atomic
+            // reserves the slots.  Uniform control flow, no calls.
 #pragma unroll
-                for (int i = 0; i < kFastVecs; ++i)
-                    if (strict ? (vmax[i] > theta) : (vmax[i] >= theta))
-                        push_vector<DT>(v[i], c0 + (i * kFastThreads + tid) * EPV, a.vocab, theta, strict, s_cand,
-                                        &s_cnt, &s_overflow);
+            for (int i = 0; i < kFastVecs; ++i) {
+                unsigned bal = __ballot_sync(0xFFFFFFFFu, strict ? (vmax[i] > theta) : (vmax[i] >= theta));
+                while (bal) {
+                    const int src = __ffs(bal) - 1;
+                    bal &= bal - 1u;
+                    const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, v[i].x, src);
+                    const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, v[i].y, src);
+                    const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, v[i].z, src);
+                    const uint32_t w3 = __shfl_sync(0xFFFFFFFFu, v[i].w, src);
+                    const int q = DT == 0 ? (lane >> 1) : lane;
+                    const uint32_t word = q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
+                    const float val = DT == 0 ? __uint_as_float((lane & 1) ? (word & 0xFFFF0000u) : (word << 16))
+                                              : __uint_as_float(word);
+                    const int e = c0 + (i * kFastThreads + warp * 32 + src) * EPV + lane;
+                    const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
+                    const unsigned tb = __ballot_sync(0xFFFFFFFFu, take);
+                    if (take) {
+                        const int pos = wcnt + __popc(tb & ((1u << lane) - 1u));
+                        if (pos < kWarpCap)
+                            s_cand[warp * kWarpCap + pos] = ckey(val, (uint32_t)e);
+                        else
+                            s_overflow = 1;
+                    }
+                    wcnt += __popc(tb);
+                }
             }
         }
         Partial* out = a.partials + u;
@@ -485,9 +509,10 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             }
             continue;
         }
+        if (lane == 0) s_wcnt[warp] = wcnt;
         if (!s_overflow) {
-            compact_candidates(s_cand, s_tmp, &s_cnt, &s_theta, &s_strict, k);
-            const int m = s_cnt;
+            compact_candidates(s_cand, s_wcnt, s_all, &s_theta, &s_strict, &s_n, k);
+            const int m = s_n;
             if (tid < m) out->keys[tid] = s_cand[tid];
             if (tid == 0) {
                 out->status = 0u;
