@@ -234,7 +234,9 @@ def run_ours(args, rank, world, local):
     alg_bytes, rows_t = algorithmic_bytes(w)
     if extra is not None:
         alg_bytes += extra["draft_rows"] * w.V * 2
-    launches_per_step = 6 + (1 if w.layout == "ragged" else 0)
+    # prep, row select (with finalisation), cluster histogram, chain, resample
+    # (+ the planner for ragged batches)
+    launches_per_step = 5 + (1 if w.layout == "ragged" else 0)
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     if not args.quick:

@@ -40,7 +40,8 @@ sv_status_t to_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_
 
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;   // sv_set_timing_events
 
-// Row kernels + finalize for whatever tasks the prep kernel listed.
+// Row kernels for whatever tasks the prep kernel listed (the one-pass kernel
+// also finalises its rows).
 sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s)
 {
     const cudaEvent_t ev0 = g_ev_start, ev1 = g_ev_stop;
@@ -48,8 +49,6 @@ sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s)
     cudaError_t e = launch_fast_rows(ra, s);
     if (e != cudaSuccess) return SV_ERR_CUDA;
     if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SV_ERR_CUDA;
-    e = launch_fast_finalize(ra, s);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
     if (ra.dtype == 0) {   // fp32 rows never take the histogram path (refused in prep)
         e = launch_hist_rows(ra, s);
         if (e != cudaSuccess) return SV_ERR_CUDA;
@@ -74,12 +73,12 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ra.stride_d = stride_d;
     ra.vocab = vocab;
     ra.dtype = dtype;
-    ra.nchunks = L.nchunks;
     ra.fast_tasks = at<RowTask>(ws, L.fast_tasks);
     ra.slow_tasks = at<RowTask>(ws, L.slow_tasks);
     ra.counters = at<Counters>(ws, L.counters);
     ra.info = at<RowInfo>(ws, L.info);
     ra.partials = at<Partial>(ws, L.partials);
+    ra.row_done = at<int32_t>(ws, L.row_done);
     ra.max_tasks = L.max_tasks;
     ra.num_sms = sm_count();
     ChainArgs& ca = c.ca;
@@ -95,6 +94,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.counters = ra.counters;
     ca.fast_tasks = ra.fast_tasks;
     ca.slow_tasks = ra.slow_tasks;
+    ca.row_done = ra.row_done;
     ca.info = ra.info;
     ca.req = at<ReqState>(ws, L.req);
     ca.jobs = at<ResampleJob>(ws, L.jobs);
@@ -152,8 +152,6 @@ size_t sv_workspace_size(int n_req, int k_max, int vocab)
     }
     if (n_req > (1 << 22) || k_max > kMaxK || vocab > kMaxVocab) return 0;
     if ((long long)n_req * (2LL * k_max + 1) > (1LL << 30)) return 0;
-    // (row, segment) units of the row kernel are indexed in 32 bits
-    if ((long long)n_req * (2LL * k_max + 1) * ((vocab + kMinChunk - 1) / kMinChunk) > 0x7FFFFFFFLL) return 0;
     return ws_layout(n_req, k_max, vocab).total;
 }
 

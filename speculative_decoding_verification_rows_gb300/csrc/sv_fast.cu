@@ -4,27 +4,31 @@
 // target_probs"): the top-k is selected on the raw logits (a positive
 // temperature keeps their order) and only the k kept values are divided by the
 // temperature.  Here the selection streams each [rows, vocab] row from HBM
-// exactly once and keeps at most a few hundred (logit, index) candidates:
+// exactly once and keeps at most a few dozen (logit, index) candidates:
 //
-//  * A persistent CTA owns segments of rows (4 chunks of 32 KB).  Thread 0
-//    keeps a ring of 3 shared-memory stages filled with bulk asynchronous
-//    copies (cp.async.bulk, completion on mbarriers, bounded waits), so loads
-//    stay in flight while the CTA selects.
-//  * Each thread takes a NaN-propagating packed max (max.NaN.bf16x2) of its
-//    8 x 16 B of a chunk.  In a segment's first chunk theta = the k-th largest
-//    of the 256 thread maxima (a radix select with warp-aggregated shared
-//    atomics): at least k elements are >= theta, and few more.
-//  * Only threads whose maximum reaches theta push composite keys (logit,
-//    inverted index) into shared memory.  Once the candidates hold k entries,
-//    theta becomes the exact k-th best so far, and later elements must beat
-//    it strictly (their indices are higher, so a tie cannot win).
-//  * At the segment's end a rank-by-counting pass writes its top-k, ordered by
-//    (logit desc, index asc), to the workspace.
-// A warp per row then merges the segment lists (a k-round tournament) and
-// builds the row's distribution in fp64 from the <= 32 kept values:
-// temperature, top-p over the top-k mass, normaliser, the probability of the
-// row's token, and the kept list in index order for the resample.  Greedy rows
-// are the k = 1 case (argmax, lowest index wins ties).
+//  * The (row, 4 KB chunk) units of all rows are split into one contiguous,
+//    balanced range per warp of a persistent grid.  A range covers the tail of
+//    one row, whole rows and the head of another; each of its row parts gives
+//    one partial list.  Warps never wait for one another while streaming.
+//  * Lane 0 of each warp keeps a private ring of 3 shared-memory stages filled
+//    with bulk asynchronous copies (cp.async.bulk, completion on mbarriers,
+//    bounded waits).
+//  * Each lane takes a NaN-propagating packed max (max.NaN.bf16x2) of its
+//    8 x 16 B of a chunk.  In a part's first chunk theta = the k-th largest of
+//    the 32 lane maxima (bisection on the key bits with warp votes): at least
+//    k elements reach it.  Those are pushed as composite keys (logit, inverted
+//    index) into the warp's 64 shared-memory slots and cut to the exact top k;
+//    from then on theta is the k-th best so far and an element must beat it
+//    strictly (its index is higher, so a tie cannot win).  A chunk with no
+//    lane maximum above theta costs one vote; the slots are cut back to k
+//    whenever a push could overflow them.
+//  * At a part's end the warp writes its top k, ordered by (logit desc, index
+//    asc), and counts the part in the row's counter.  The warp that finishes a
+//    row's last part merges the row's lists (bitonic merges of sorted lists of
+//    32) and builds the row's distribution in fp64 from the <= 32 kept values:
+//    temperature, top-p over the top-k mass, normaliser, the probability of
+//    the row's token, and the kept list in index order for the resample.
+//    Greedy rows are the k = 1 case (argmax, lowest index wins ties).
 #include <math.h>
 
 #include "sv_internal.cuh"
@@ -44,14 +48,18 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
+// Larger of the two bf16 halves of a word, as fp32 (NaN-propagating).
+__device__ __forceinline__ float bf16x2_hmax(uint32_t w)
+{
+    return fmax_nan(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
 
-// ---- shared-memory ring fed by bulk async copies (TMA, cp.async.bulk) ----
-constexpr int kStages = 3;                                  // chunks in flight per CTA
-constexpr int kChunkBytes = kFastThreads * kFastVecs * 16;  // 32 KB: one chunk of either dtype
-constexpr int kSegChunks = 8;                               // chunks per segment (one partial list)
+// ---- per-warp shared-memory ring fed by bulk async copies (cp.async.bulk) ----
+constexpr int kCtaWarps = kFastThreads / 32;
+constexpr int kStages = 3;                                  // chunks in flight per warp
+constexpr int kWarpChunkBytes = 32 * kFastVecs * 16;        // 4 KB: one warp chunk of either dtype
 constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
 constexpr int kWarpCap = 64;                                // candidate slots per warp
-constexpr int kCandCapS = kWarpCap * (kFastThreads / 32);   // candidate buffer of a segment
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -110,18 +118,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void* p)
     return r;
 }
 
-// Element s (0..EPV-1) of a 16-byte vector, as fp32.
-template <int DT>
-__device__ __forceinline__ float vec_elem(const uint4& v, int s)
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if (DT == 0) {
-        const uint32_t word = w[s >> 1];
-        return __uint_as_float((s & 1) ? (word & 0xFFFF0000u) : (word << 16));
-    }
-    return __uint_as_float(w[s]);
-}
-
 // Ragged edge of a row (or a misaligned row): element loads, -inf past the end.
 template <int DT>
 __device__ __forceinline__ uint4 load_edge(const char* row, int e0, int vocab)
@@ -144,7 +140,7 @@ __device__ __forceinline__ uint4 load_edge(const char* row, int e0, int vocab)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Byte offset of a row and the bulk-copied bytes of one chunk of it.
+// Byte offset of a row and the bulk-copied bytes of one warp chunk of it.
 template <int DT>
 __device__ __forceinline__ const char* task_row(const RowsArgs& a, const RowTask& t)
 {
@@ -156,140 +152,198 @@ template <int DT>
 __device__ __forceinline__ uint32_t chunk_bytes(const char* row, int c0, int vocab)
 {
     constexpr int ESZ = DT == 0 ? 2 : 4;
-    constexpr int CHUNK = kChunkBytes / ESZ;
+    constexpr int CHUNK = kWarpChunkBytes / ESZ;
     const int n_here = min(CHUNK, vocab - c0);
     const char* src = row + (size_t)c0 * ESZ;
     return ((uintptr_t)src & 15u) ? 0u : ((uint32_t)(n_here * ESZ) & ~15u);
 }
 
-// k-th largest of one 32-bit key per thread (k <= blockDim) by a byte-wise
-// radix select over the top `rounds` bytes.  Lanes of a warp that share a
-// digit add their count through one leader (__match_any_sync), so the many
-// equal digits of similar keys do not serialise on one shared counter.  Keys
-// whose low bytes are not examined are equal below a given top (bf16-derived
-// keys: 0x0000 under a positive value, 0xFFFF under a negative one).
-__device__ __noinline__ uint32_t block_kth_largest(uint32_t key, int k, int rounds, uint32_t* hist, uint32_t* s_digit,
-                                                    int* s_kk)
+// Balanced split of U = tasks x chunks units over W warps: warp w takes
+// [w U / W, (w + 1) U / W).  With W <= U every warp has at least one unit,
+// and a warp's range touches at most Pw = ceil(ceil(U / W) / nc) + 1 rows, so
+// W * Pw <= tasks + 3 W part slots suffice.
+struct Split {
+    long long U, W;
+    int nc, Pw;
+};
+__device__ __forceinline__ long long split_lo(const Split& s, long long w) { return w * s.U / s.W; }
+// The warp whose range holds unit g: the largest w with split_lo(w) <= g.
+__device__ __forceinline__ long long split_owner(const Split& s, long long g) { return ((g + 1) * s.W + s.U - 1) / s.U - 1; }
+__device__ __forceinline__ size_t part_slot(const Split& s, long long w, int t)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t prefix = 0u, mask = 0u;
-    int kk = k;
-    for (int r = 0; r < rounds; ++r) {
-        const int shift = 24 - 8 * r;
-        for (int b = tid; b < 256; b += blockDim.x) hist[b] = 0u;
-        __syncthreads();
-        const uint32_t d = ((key & mask) == prefix) ? ((key >> shift) & 255u) : 0x100u;
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
-        if (d != 0x100u && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t c[8], sum = 0u;
+    return (size_t)(w * s.Pw + (t - split_lo(s, w) / s.nc));
+}
+
+// k-th largest (1 <= k <= 32) of one NB-bit key per lane: bisection on the
+// key bits, one warp vote per bit.
+template <int NB>
+__device__ __forceinline__ uint32_t warp_kth_key(uint32_t key, int k)
+{
+    uint32_t pre = 0u;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = hist[255 - 8 * lane - i];
-                sum += c[i];
-            }
-            uint32_t incl = sum;
+    for (int b = NB - 1; b >= 0; --b) {
+        const uint32_t tv = pre | (1u << b);
+        if (__popc(__ballot_sync(0xFFFFFFFFu, key >= tv)) >= k) pre = tv;
+    }
+    return pre;
+}
+
+// Keeps the top k (<= 32) of the n (<= kWarpCap) candidates in a warp's slots,
+// descending, in the first min(n, k) slots.  Composite keys are distinct, so a
+// candidate's rank is the number of larger ones.  Out of line: it is cold.
+__device__ __noinline__ int warp_compact(unsigned long long* cand, int n, int k)
+{
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    const unsigned long long a0 = lane < n ? cand[lane] : 0ull;
+    const unsigned long long a1 = lane + 32 < n ? cand[lane + 32] : 0ull;
+    int r0 = 0, r1 = 0, s0 = 0, s1 = 0;
+    int j = 0;
+    for (; j + 2 <= n; j += 2) {
+        const unsigned long long x = cand[j], y = cand[j + 1];
+        r0 += x > a0 ? 1 : 0;
+        r1 += x > a1 ? 1 : 0;
+        s0 += y > a0 ? 1 : 0;
+        s1 += y > a1 ? 1 : 0;
+    }
+    if (j < n) {
+        const unsigned long long x = cand[j];
+        r0 += x > a0 ? 1 : 0;
+        r1 += x > a1 ? 1 : 0;
+    }
+    r0 += s0;
+    r1 += s1;
+    __syncwarp();
+    if (lane < n && r0 < k) cand[r0] = a0;
+    if (lane + 32 < n && r1 < k) cand[r1] = a1;
+    __syncwarp();
+    return n < k ? n : k;
+}
+
+// Top 32 of two descending lists of 32 (lane i holds element i of each), as a
+// descending list: the elementwise max against the reversed second list is
+// bitonic and holds the top 32; five compare-exchange stages sort it.
+__device__ __forceinline__ unsigned long long merge_desc(unsigned long long acc, unsigned long long b)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned long long rb = __shfl_sync(0xFFFFFFFFu, b, 31 - lane);
+    unsigned long long c = acc > rb ? acc : rb;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            uint32_t excl = incl - sum;
-            if (excl < (uint32_t)kk && (uint32_t)kk <= incl) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (excl + c[i] >= (uint32_t)kk) {
-                        *s_digit = (uint32_t)(255 - 8 * lane - i);
-                        *s_kk = kk - (int)excl;
-                        break;
-                    }
-                    excl += c[i];
+    for (int j = 16; j; j >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xFFFFFFFFu, c, j);
+        c = (lane & j) ? (x < c ? x : c) : (x > c ? x : c);
+    }
+    return c;
+}
+
+// The distribution of fast task t from its parts' lists (one warp; s_e is 32
+// doubles of the warp's shared memory).  Out of line: it runs once per row.
+__device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, const Partial* parts, int t,
+                                          Split sp, double* s_e)
+{
+    const int lane = threadIdx.x & 31;
+    const RowTask task = tasks[t];
+    RowInfo* info = infos + task.slot;
+    const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
+    const long long g0 = (long long)t * sp.nc;
+    const long long w0 = split_owner(sp, g0), w1 = split_owner(sp, g0 + sp.nc - 1);
+    unsigned long long acc = 0ull;
+    uint32_t st = 0u;
+    for (long long w = w0; w <= w1; ++w) {
+        const Partial* P = parts + part_slot(sp, w, t);
+        const uint32_t cnt = __ldcg(&P->count);
+        st |= __ldcg(&P->status);
+        const unsigned long long key = lane < (int)cnt ? __ldcg(&P->keys[lane]) : 0ull;
+        acc = merge_desc(acc, key);
+    }
+    const unsigned long long ck = lane < k ? acc : 0ull;
+    const int n_top = __popc(__ballot_sync(0xFFFFFFFFu, ck != 0ull));
+    const float lv = ckey_value(ck);
+    const int li = ckey_index(ck);
+    const float m = __shfl_sync(0xFFFFFFFFu, lv, 0);
+    const int amax = __shfl_sync(0xFFFFFFFFu, li, 0);
+    const float T = task.temp;
+    int status = (int)st & kNonfinite;
+    if (status == 0 && T > 0.0f && m == -INFINITY) status = kEmpty;
+    if (lane == 0) {
+        info->desc.max_logit = m;
+        info->desc.argmax = amax;
+        info->desc.status = status;
+        info->desc.temperature = T;
+        info->cut_count = -1;
+    }
+    if (status != 0) {
+        if (lane == 0) {
+            info->desc.log_norm = 0.0f;
+            info->desc.cutoff_logit = m;
+            info->desc.cutoff_ties = 0;
+            info->desc.kept = 0;
+            info->p_token = nan("");
+            info->z = 0.0;
+            info->n_list = -1;
+        }
+        return;
+    }
+    if (T == 0.0f) {
+        if (lane == 0) {
+            info->desc.log_norm = 0.0f;
+            info->desc.cutoff_logit = m;
+            info->desc.cutoff_ties = 1;
+            info->desc.kept = 1;
+            info->p_token = task.token >= 0 ? (task.token == amax ? 1.0 : 0.0) : nan("");
+            info->z = 1.0;
+            info->n_list = 1;
+            info->list_idx[0] = amax;
+            info->list_p[0] = 1.0;
+        }
+        return;
+    }
+    // Sampling row: masses of the kept values in fp64, in sorted order.
+    const double e = lane < n_top ? exp(((double)lv - (double)m) / (double)T) : 0.0;
+    s_e[lane] = e;
+    __syncwarp();
+    int kept = n_top;
+    double z = 0.0;
+    if (lane == 0) {
+        double z1 = 0.0;
+        for (int i = 0; i < n_top; ++i) z1 += s_e[i];
+        if (task.top_p < 1.0f) {
+            const double target = (double)task.top_p * z1;
+            double cum = 0.0;
+            for (int i = 0; i < n_top; ++i) {
+                cum += s_e[i];
+                if (cum >= target) {
+                    kept = i + 1;
+                    break;
                 }
             }
         }
-        __syncthreads();
-        prefix |= (*s_digit) << shift;
-        mask |= 0xFFu << shift;
-        kk = *s_kk;
+        for (int i = 0; i < kept; ++i) z += s_e[i];
     }
-    if (rounds == 2) prefix |= (prefix & 0x80000000u) ? 0u : 0xFFFFu;
-    return prefix;
-}
-
-// Keep the top k of the candidates (rank by counting; composite keys are
-// distinct).  The candidates sit in per-warp regions of kWarpCap slots with
-// their counts in wcnt[]; they are gathered into `all`, ranked, and the top k
-// go back to warp 0's region (the other regions become empty).  Raises theta
-// to the k-th best once k candidates exist.
-__device__ __noinline__ void compact_candidates(unsigned long long* cand, int* wcnt, unsigned long long* all,
-                                                float* s_theta, int* s_strict, int* s_n, int k)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    __syncthreads();
-    int off = 0, n = 0;
-    for (int w = 0; w < kFastThreads / 32; ++w) {
-        const int c = min(wcnt[w], kWarpCap);
-        if (w < warp) off += c;
-        n += c;
+    kept = __shfl_sync(0xFFFFFFFFu, kept, 0);
+    z = __shfl_sync(0xFFFFFFFFu, z, 0);
+    __syncwarp();   // s_e is the warp's candidate space again after this
+    const bool in = lane < kept;
+    const double p = in ? e / z : 0.0;
+    const float cut = __shfl_sync(0xFFFFFFFFu, lv, kept - 1);
+    const int ties = __popc(__ballot_sync(0xFFFFFFFFu, in && lv == cut));
+    int rank = 0;
+    for (int j = 0; j < kept; ++j) rank += (__shfl_sync(0xFFFFFFFFu, li, j) < li) ? 1 : 0;
+    if (in) {
+        info->list_idx[rank] = li;
+        info->list_p[rank] = p;
     }
-    const int mine = min(wcnt[warp], kWarpCap);
-    for (int i = lane; i < mine; i += 32) all[off + i] = cand[warp * kWarpCap + i];
-    __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-        const unsigned long long ck = all[i];
-        int r8[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // eight independent chains
-        int j = 0;
-        for (; j + 8 <= n; j += 8) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) r8[q] += (all[j + q] > ck) ? 1 : 0;
-        }
-        for (; j < n; ++j) r8[0] += (all[j] > ck) ? 1 : 0;
-        const int rank = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-        if (rank < k) cand[rank] = ck;   // warp 0's region, ordered
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, in && li == task.token);
+    const double ptok = hit ? __shfl_sync(0xFFFFFFFFu, p, __ffs(hit) - 1) : 0.0;
+    if (lane == 0) {
+        info->desc.log_norm = (float)log(z);
+        info->desc.cutoff_logit = cut;
+        info->desc.cutoff_ties = ties;
+        info->desc.kept = kept;
+        info->p_token = task.token >= 0 ? ptok : nan("");
+        info->z = z;
+        info->n_list = kept;
     }
-    const int m = min(n, k);
-    __syncthreads();
-    if (tid < kFastThreads / 32) wcnt[tid] = tid == 0 ? m : 0;
-    if (tid == 0) {
-        *s_n = m;
-        if (m == k) {
-            *s_theta = ckey_value(cand[k - 1]);
-            *s_strict = 1;
-        }
-    }
-    __syncthreads();
-}
-
-// Exact top-k of a segment by k rounds of a block max over keys below the last
-// (used when too many elements tie at theta).  Out of line: it is cold.
-template <int DT>
-__device__ __noinline__ int exact_segment_topk(const char* row, int seg0, int seg_end, int k,
-                                               unsigned long long* out_keys, unsigned long long* s_red64)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    unsigned long long last = ~0ull;
-    int n_out = 0;
-    for (int r = 0; r < k; ++r) {
-        unsigned long long best = 0ull;
-        for (int e = seg0 + tid; e < seg_end; e += kFastThreads) {
-            const float val = DT == 0 ? __uint_as_float((uint32_t)((const uint16_t*)row)[e] << 16)
-                                      : ((const float*)row)[e];
-            const unsigned long long ck = ckey(val, (uint32_t)e);
-            if (ck < last && ck > best) best = ck;
-        }
-        best = warp_max_u64(best);
-        if (lane == 0) s_red64[warp] = best;
-        __syncthreads();
-        best = s_red64[0];
-        for (int w = 1; w < kFastThreads / 32; ++w) best = s_red64[w] > best ? s_red64[w] : best;
-        __syncthreads();
-        if (best == 0ull) break;
-        if (tid == 0) out_keys[r] = best;
-        last = best;
-        ++n_out;
-    }
-    return n_out;
 }
 
 template <int DT>
@@ -297,403 +351,211 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
 {
     constexpr int EPV = DT == 0 ? 8 : 4;
     constexpr int ESZ = DT == 0 ? 2 : 4;
-    constexpr int CHUNK = kFastThreads * kFastVecs * EPV;
-    static_assert(CHUNK * ESZ == kChunkBytes, "one chunk fills one ring stage");
-    extern __shared__ __align__(128) unsigned char ring[];   // kStages x 32 KB
-    __shared__ __align__(8) unsigned long long full_bar[kStages];
-    __shared__ unsigned long long s_cand[kCandCapS];      // per-warp candidate regions
-    __shared__ unsigned long long s_all[kCandCapS];       // gathered candidates (compaction)
-    __shared__ int s_wcnt[kFastThreads / 32];
-    __shared__ unsigned long long s_red64[kFastThreads / 32];
-    __shared__ uint32_t s_hist[256];
-    __shared__ uint32_t s_digit;
-    __shared__ int s_kk;
-    __shared__ float s_theta;
-    __shared__ int s_strict, s_n, s_overflow;
-    __shared__ int s_compact[2];
+    constexpr int CHUNK = 32 * kFastVecs * EPV;   // elements of a warp chunk
+    static_assert(CHUNK * ESZ == kWarpChunkBytes, "one warp chunk fills one ring stage");
+    constexpr unsigned FULL = 0xFFFFFFFFu;
+    extern __shared__ __align__(128) unsigned char ring[];   // warps x kStages x 4 KB
+    __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
+    __shared__ unsigned long long s_cand[kCtaWarps][kWarpCap];
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
-    const int nchunks = (a.vocab + CHUNK - 1) / CHUNK;
-    const int nseg = (nchunks + kSegChunks - 1) / kSegChunks;
-    const int n_units = n_tasks * nseg;   // the host keeps this below 2^31
-    const int G = gridDim.x;
-    if ((int)blockIdx.x >= n_units) return;
+    Split sp;
+    sp.nc = (a.vocab + CHUNK - 1) / CHUNK;
+    sp.U = (long long)n_tasks * sp.nc;
+    sp.W = min((long long)gridDim.x * kCtaWarps, sp.U);
+    const long long w = (long long)blockIdx.x * kCtaWarps + warp;
+    if (w >= sp.W) return;   // whole warps leave: nothing below waits on the block
+    sp.Pw = (int)(((sp.U + sp.W - 1) / sp.W + sp.nc - 1) / sp.nc) + 1;
+    const long long lo = split_lo(sp, w), hi = split_lo(sp, w + 1);
+    unsigned long long* bar = s_bar[warp];
+    unsigned char* wring = ring + (size_t)warp * (kStages * kWarpChunkBytes);
+    unsigned long long* cand = s_cand[warp];
 
-    // Consumer tasks: the current unit's and the next one's (prefetched).
-    int u = blockIdx.x;
-    int cur_t = u / nseg;
-    RowTask task = a.fast_tasks[cur_t];
-    int next_t = (u + G < n_units) ? (u + G) / nseg : -1;
-    RowTask next_task = next_t >= 0 ? a.fast_tasks[next_t] : task;
-
-    // Producer state (thread 0): the next (unit, chunk) to copy, where it goes
-    // in the ring, and the row it reads.  It runs up to kStages chunks ahead,
-    // which can be more than one unit when segments are short; it reuses the
-    // consumer's tasks when it can and reads the task list otherwise.
-    int p_u = u, p_t = cur_t, p_chunk = (u - cur_t * nseg) * kSegChunks;
-    int p_end = min(nchunks, p_chunk + kSegChunks);
+    // Producer (lane 0): the next unit to copy, its row and its ring stage.
+    long long p_g = lo;
+    int p_t = (int)(lo / sp.nc);
+    int p_c = (int)(lo - (long long)p_t * sp.nc);
     int p_slot = 0;
-    const char* p_row = task_row<DT>(a, task);
+    const char* p_row = nullptr;
     auto produce = [&]() {
-        if (p_u >= n_units) return;
-        const int c0 = p_chunk * CHUNK;
+        if (p_g >= hi) return;
+        const int c0 = p_c * CHUNK;
         const uint32_t bytes = chunk_bytes<DT>(p_row, c0, a.vocab);
-        unsigned long long* bar = &full_bar[p_slot];
+        unsigned long long* b = &bar[p_slot];
         if (bytes) {
-            mbar_expect_tx(bar, bytes);
-            bulk_g2s(ring + p_slot * kChunkBytes, p_row + (size_t)c0 * ESZ, bytes, bar);
+            mbar_expect_tx(b, bytes);
+            bulk_g2s(wring + p_slot * kWarpChunkBytes, p_row + (size_t)c0 * ESZ, bytes, b);
         } else {
-            mbar_arrive(bar);
+            mbar_arrive(b);
         }
         if (++p_slot == kStages) p_slot = 0;
-        if (++p_chunk == p_end) {
-            p_u += G;
-            if (p_u < n_units) {
-                const int t = p_u / nseg;
-                if (t != p_t) {
-                    p_row = (t == cur_t) ? task_row<DT>(a, task)
-                                         : (t == next_t ? task_row<DT>(a, next_task) : task_row<DT>(a, a.fast_tasks[t]));
-                    p_t = t;
-                }
-                p_chunk = (p_u - t * nseg) * kSegChunks;
-                p_end = min(nchunks, p_chunk + kSegChunks);
-            }
+        ++p_g;
+        if (++p_c == sp.nc) {
+            p_c = 0;
+            ++p_t;
+            if (p_g < hi) p_row = task_row<DT>(a, a.fast_tasks[p_t]);
         }
     };
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], 1u);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1u);
         mbar_fence_init();
-        s_compact[0] = s_compact[1] = 0;
+        p_row = task_row<DT>(a, a.fast_tasks[p_t]);
+        for (int s = 0; s < kStages; ++s) produce();
     }
-    __syncthreads();
-    if (tid == 0)
-        for (int i = 0; i < kStages; ++i) produce();
+    __syncwarp();
 
     int c_slot = 0;
     uint32_t c_phase = 0u;
-    for (; u < n_units; u += G) {
-        if (u != (int)blockIdx.x) {
-            cur_t = next_t;
-            task = next_task;
-            next_t = (u + G < n_units) ? (u + G) / nseg : -1;
-            if (next_t >= 0) next_task = (next_t == cur_t) ? task : a.fast_tasks[next_t];
-        }
+    long long g = lo;
+    int t = (int)(lo / sp.nc);
+    int c = (int)(lo - (long long)t * sp.nc);
+    while (g < hi) {
+        // One row part: chunks [c, c_end) of task t.
+        const RowTask task = a.fast_tasks[t];
         const char* row = task_row<DT>(a, task);
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
-        const int compact_at = max(2 * k, 40);
-        const int chunk0 = (u - cur_t * nseg) * kSegChunks;
-        const int ns = min(kSegChunks, nchunks - chunk0);
-        __syncthreads();   // the previous segment's buffers are free
-        if (tid == 0) {
-            s_overflow = 0;
-            s_strict = 0;
-        }
-        int wcnt = 0;   // this warp's candidates (same value in every lane)
-        int bad = 0;
-        for (int j = 0; j < ns; ++j) {
-            const int c0 = (chunk0 + j) * CHUNK;
+        const int c_end = (int)min((long long)sp.nc, (long long)c + (hi - g));
+        int wcnt = 0, strict = 0, bad = 0;
+        float theta = -INFINITY;
+        for (int cc = c; cc < c_end; ++cc) {
+            const int c0 = cc * CHUNK;
             const uint32_t bytes = chunk_bytes<DT>(row, c0, a.vocab);
-            const bool arrived = mbar_wait(&full_bar[c_slot], c_phase);
-            const unsigned char* st = ring + c_slot * kChunkBytes;
+            if (!__all_sync(FULL, mbar_wait(&bar[c_slot], c_phase))) {
+                // A bulk copy never arrived: flag it, let this warp's copies in
+                // flight land (bounded), and leave.
+                if (lane == 0) {
+                    atomicOr(&a.counters->timeout, 1);
+                    int s = c_slot;
+                    uint32_t ph = c_phase;
+                    for (long long q = g + (cc - c); q < p_g; ++q) {
+                        mbar_wait(&bar[s], ph);
+                        if (++s == kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+                __syncwarp();
+                return;
+            }
+            const unsigned char* stg = wring + c_slot * kWarpChunkBytes;
             uint4 v[kFastVecs];
 #pragma unroll
             for (int i = 0; i < kFastVecs; ++i) {
-                const int off = (i * kFastThreads + tid) * 16;
+                const int off = (i * 32 + lane) * 16;
                 if ((uint32_t)(off + 16) <= bytes)
-                    v[i] = ld_shared_v4(st + off);
+                    v[i] = ld_shared_v4(stg + off);
                 else
-                    v[i] = load_edge<DT>(row, c0 + (i * kFastThreads + tid) * EPV, a.vocab);
+                    v[i] = load_edge<DT>(row, c0 + (i * 32 + lane) * EPV, a.vocab);
+            }
+            __syncwarp();   // every lane holds its data: the stage can be refilled
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                produce();
             }
             if (++c_slot == kStages) {
                 c_slot = 0;
                 c_phase ^= 1u;
             }
-            // Per-vector NaN-propagating maxima, then their tree max: the same
-            // operation count as one running max, with independent chains.
-            float vmax[kFastVecs];
-            if (DT == 0) {
-                uint32_t m2[kFastVecs];
+            // Per-vector NaN-propagating maxima (kept for the push test), then
+            // the lane maximum.
+            uint32_t m2[kFastVecs];
+            float vmx[kFastVecs];
+            float tmax;
+            if constexpr (DT == 0) {
 #pragma unroll
-                for (int i = 0; i < kFastVecs; ++i) {
+                for (int i = 0; i < kFastVecs; ++i)
                     m2[i] = bmax2_nan(bmax2_nan(v[i].x, v[i].y), bmax2_nan(v[i].z, v[i].w));
-                    vmax[i] = fmax_nan(__uint_as_float(m2[i] << 16), __uint_as_float(m2[i] & 0xFFFF0000u));
-                }
+                const uint32_t mm = bmax2_nan(bmax2_nan(bmax2_nan(m2[0], m2[1]), bmax2_nan(m2[2], m2[3])),
+                                              bmax2_nan(bmax2_nan(m2[4], m2[5]), bmax2_nan(m2[6], m2[7])));
+                tmax = bf16x2_hmax(mm);
             } else {
 #pragma unroll
                 for (int i = 0; i < kFastVecs; ++i)
-                    vmax[i] = fmax_nan(fmax_nan(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
-                                       fmax_nan(__uint_as_float(v[i].z), __uint_as_float(v[i].w)));
+                    vmx[i] = fmax_nan(fmax_nan(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
+                                      fmax_nan(__uint_as_float(v[i].z), __uint_as_float(v[i].w)));
+                tmax = fmax_nan(fmax_nan(fmax_nan(vmx[0], vmx[1]), fmax_nan(vmx[2], vmx[3])),
+                                fmax_nan(fmax_nan(vmx[4], vmx[5]), fmax_nan(vmx[6], vmx[7])));
             }
-            const float tmax = fmax_nan(fmax_nan(fmax_nan(vmax[0], vmax[1]), fmax_nan(vmax[2], vmax[3])),
-                                        fmax_nan(fmax_nan(vmax[4], vmax[5]), fmax_nan(vmax[6], vmax[7])));
             bad |= (isnan(tmax) || tmax == INFINITY) ? 1 : 0;
-            // Thread 0 decides whether to compact before this chunk's pushes (a
-            // slightly stale count is fine; the flag is double-buffered so the
-            // previous chunk's readers are not overtaken).
-            if (lane == 0) s_wcnt[warp] = wcnt;
-            if (tid == 0) {
-                int tot = 0;   // possibly a little stale: the decision only needs to be shared
-                for (int w = 0; w < kFastThreads / 32; ++w) tot += s_wcnt[w];
-                s_compact[j & 1] = (j > 0 && s_strict == 0 && tot > compact_at) ? 1 : 0;
+            if (cc == c) {   // first chunk of the part: k-th largest lane maximum
+                if constexpr (DT == 0)
+                    theta = f32_of_key16(warp_kth_key<16>(key16_of_bf16(__float_as_uint(tmax) >> 16), k));
+                else
+                    theta = f32_of_key(warp_kth_key<32>(key_of_f32_bits(__float_as_uint(tmax)), k));
             }
-            // One barrier per chunk: every thread holds its data (the stage can
-            // be refilled), the compaction decision is published, and a bulk
-            // copy that never arrived stops the whole CTA.
-            if (__syncthreads_or(!arrived)) {
-                if (tid == 0) {
-                    atomicOr(&a.counters->timeout, 1);
-                    // let the copies already issued land (bounded), then leave
-                    for (int q = 0; q < kStages; ++q) mbar_wait(&full_bar[q], c_phase ^ (q < c_slot ? 1u : 0u));
-                }
-                __syncthreads();
-                return;
-            }
-            if (tid == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                produce();
-            }
-            float theta;
-            int strict;
-            if (j == 0) {   // exact k-th largest of the 256 thread maxima
-                const uint32_t key = key_of_f32_bits(__float_as_uint(tmax));
-                theta = f32_of_key(block_kth_largest(key, k, DT == 0 ? 2 : 4, s_hist, &s_digit, &s_kk));
-                strict = 0;
-                if (tid == 0) s_theta = theta;
-            } else {
-                if (s_compact[j & 1]) {
-                    compact_candidates(s_cand, s_wcnt, s_all, &s_theta, &s_strict, &s_n, k);
-                    wcnt = s_wcnt[warp];
-                }
-                theta = s_theta;
-                strict = s_strict;
-            }
-            // Warp-cooperative push: one ballot per vector slot; for each lane
-            // whose vector maximum reaches theta, the warp takes that vector
-            // (broadcast), EPV lanes test one element each, and one atomic
-            // reserves the slots.  Uniform control flow, no calls.
+            if (__ballot_sync(FULL, strict ? tmax > theta : tmax >= theta)) {
+                // Warp-cooperative push in element order: for each lane whose
+                // vector reaches theta, the warp takes that vector (broadcast),
+                // EPV lanes test one element each and write their keys.
 #pragma unroll
-            for (int i = 0; i < kFastVecs; ++i) {
-                unsigned bal = __ballot_sync(0xFFFFFFFFu, strict ? (vmax[i] > theta) : (vmax[i] >= theta));
-                while (bal) {
-                    const int src = __ffs(bal) - 1;
-                    bal &= bal - 1u;
-                    const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, v[i].x, src);
-                    const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, v[i].y, src);
-                    const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, v[i].z, src);
-                    const uint32_t w3 = __shfl_sync(0xFFFFFFFFu, v[i].w, src);
-                    const int q = DT == 0 ? (lane >> 1) : lane;
-                    const uint32_t word = q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
-                    const float val = DT == 0 ? __uint_as_float((lane & 1) ? (word & 0xFFFF0000u) : (word << 16))
-                                              : __uint_as_float(word);
-                    const int e = c0 + (i * kFastThreads + warp * 32 + src) * EPV + lane;
-                    const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
-                    const unsigned tb = __ballot_sync(0xFFFFFFFFu, take);
-                    if (take) {
-                        const int pos = wcnt + __popc(tb & ((1u << lane) - 1u));
-                        if (pos < kWarpCap)
-                            s_cand[warp * kWarpCap + pos] = ckey(val, (uint32_t)e);
-                        else
-                            s_overflow = 1;
-                    }
-                    wcnt += __popc(tb);
-                }
-            }
-        }
-        Partial* out = a.partials + u;
-        const int any_bad = __syncthreads_or(bad);
-        if (any_bad) {
-            if (tid == 0) {
-                out->status = kNonfinite;
-                out->count = 0u;
-            }
-            continue;
-        }
-        if (lane == 0) s_wcnt[warp] = wcnt;
-        if (!s_overflow) {
-            compact_candidates(s_cand, s_wcnt, s_all, &s_theta, &s_strict, &s_n, k);
-            const int m = s_n;
-            if (tid < m) out->keys[tid] = s_cand[tid];
-            if (tid == 0) {
-                out->status = 0u;
-                out->count = (uint32_t)m;
-            }
-            continue;
-        }
-        // Too many elements reached theta (heavy ties): exact k rounds of a
-        // block max over the segment, re-read from the row.
-        const int seg0 = chunk0 * CHUNK;
-        const int n_out = exact_segment_topk<DT>(row, seg0, min(a.vocab, seg0 + ns * CHUNK), k, out->keys, s_red64);
-        if (tid == 0) {
-            out->status = 0u;
-            out->count = (uint32_t)n_out;
-        }
-    }
-}
-
-constexpr int kFinalizeWarps = 8;
-constexpr int kMaxChunkSlots = 4;   // segment lists per lane in the merge: up to 128 per row
-constexpr int kStagedLists = 8;     // rows with at most this many lists merge in shared memory
-
-template <int DT>
-__global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(RowsArgs a)
-{
-    constexpr int EPV = DT == 0 ? 8 : 4;
-    constexpr int CHUNK = kFastThreads * kFastVecs * EPV;
-    __shared__ unsigned long long s_top[kFinalizeWarps][kFastK];
-    __shared__ unsigned long long s_lists[kFinalizeWarps][kStagedLists][kFastK];
-    __shared__ double s_e[kFinalizeWarps][kFastK];
-    __shared__ int s_kept[kFinalizeWarps];
-    __shared__ double s_z[kFinalizeWarps];
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n_tasks = a.counters->n_fast;
-    const int nchunks = ((a.vocab + CHUNK - 1) / CHUNK + kSegChunks - 1) / kSegChunks;   // segment lists per row
-    for (int t = blockIdx.x * kFinalizeWarps + warp; t < n_tasks; t += gridDim.x * kFinalizeWarps) {
-        const RowTask task = a.fast_tasks[t];
-        const Partial* P = a.partials + (size_t)t * nchunks;
-        RowInfo* info = a.info + task.slot;
-        uint32_t st = 0u;
-        for (int c = lane; c < nchunks; c += 32) st |= P[c].status;
-        st = __reduce_or_sync(0xFFFFFFFFu, st);
-
-        const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
-        int n_top = 0;
-        if (!(st & kNonfinite)) {
-            if (nchunks <= kStagedLists) {
-                // Stage the lists in shared memory with independent loads, then
-                // merge: lane c holds the head of list c.
-                for (int c = 0; c < nchunks; ++c) s_lists[warp][c][lane] = P[c].keys[lane];
-                const int cnt = lane < nchunks ? (int)P[lane].count : 0;
-                __syncwarp();
-                int head = 0;
-                for (int r = 0; r < k; ++r) {
-                    const unsigned long long key = head < cnt ? s_lists[warp][lane][head] : 0ull;
-                    const unsigned long long wbest = warp_max_u64(key);
-                    if (wbest == 0ull) break;
-                    if (key == wbest) ++head;
-                    if (lane == 0) s_top[warp][r] = wbest;
-                    n_top = r + 1;
-                }
-            } else {
-                int head[kMaxChunkSlots];
-#pragma unroll
-                for (int j = 0; j < kMaxChunkSlots; ++j) head[j] = 0;
-                for (int r = 0; r < k; ++r) {
-                    unsigned long long best = 0ull;
-                    int bj = -1;
-#pragma unroll
-                    for (int j = 0; j < kMaxChunkSlots; ++j) {
-                        const int c = lane + 32 * j;
-                        if (c < nchunks && head[j] < (int)P[c].count) {
-                            const unsigned long long key = P[c].keys[head[j]];
-                            if (key > best) {
-                                best = key;
-                                bj = j;
+                for (int i = 0; i < kFastVecs; ++i) {
+                    float vm;
+                    if constexpr (DT == 0)
+                        vm = bf16x2_hmax(m2[i]);
+                    else
+                        vm = vmx[i];
+                    unsigned bal = __ballot_sync(FULL, strict ? vm > theta : vm >= theta);
+                    while (bal) {
+                        if (wcnt > kWarpCap - EPV) {   // no room for a whole vector: cut to k
+                            wcnt = warp_compact(cand, wcnt, k);
+                            if (wcnt == k) {
+                                theta = ckey_value(cand[k - 1]);
+                                strict = 1;
                             }
                         }
+                        const int src = __ffs(bal) - 1;
+                        bal &= bal - 1u;
+                        const uint32_t w0 = __shfl_sync(FULL, v[i].x, src);
+                        const uint32_t w1 = __shfl_sync(FULL, v[i].y, src);
+                        const uint32_t w2 = __shfl_sync(FULL, v[i].z, src);
+                        const uint32_t w3 = __shfl_sync(FULL, v[i].w, src);
+                        const int q = DT == 0 ? (lane >> 1) : lane;
+                        const uint32_t word = q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
+                        const float val = DT == 0 ? __uint_as_float((lane & 1) ? (word & 0xFFFF0000u) : (word << 16))
+                                                  : __uint_as_float(word);
+                        const int e = c0 + (i * 32 + src) * EPV + lane;
+                        const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
+                        const unsigned tb = __ballot_sync(FULL, take);
+                        if (take) cand[wcnt + __popc(tb & ((1u << lane) - 1u))] = ckey(val, (uint32_t)e);
+                        wcnt += __popc(tb);
                     }
-                    const unsigned long long wbest = warp_max_u64(best);
-                    if (wbest == 0ull) break;
-#pragma unroll
-                    for (int j = 0; j < kMaxChunkSlots; ++j)
-                        if (best == wbest && bj == j) head[j] += 1;
-                    if (lane == 0) s_top[warp][r] = wbest;
-                    n_top = r + 1;
+                }
+            }
+            if (cc == c) {   // exact threshold after the first chunk (>= k candidates unless it is short)
+                wcnt = warp_compact(cand, wcnt, k);
+                if (wcnt == k) {
+                    theta = ckey_value(cand[k - 1]);
+                    strict = 1;
                 }
             }
         }
-        __syncwarp();
 
-        const unsigned long long ck = lane < n_top ? s_top[warp][lane] : 0ull;
-        const float lv = ckey_value(ck);
-        const int li = ckey_index(ck);
-        const float m = __shfl_sync(0xFFFFFFFFu, lv, 0);
-        const int amax = __shfl_sync(0xFFFFFFFFu, li, 0);
-        const float T = task.temp;
-        int status = (int)st & kNonfinite;
-        if (status == 0 && T > 0.0f && m == -INFINITY) status = kEmpty;
+        // The part's list, then the row's counter; the last part finalises.
+        const int m = warp_compact(cand, wcnt, k);
+        const int any_bad = __any_sync(FULL, bad);
+        Partial* P = a.partials + part_slot(sp, w, t);
+        if (!any_bad && lane < m) P->keys[lane] = cand[lane];
         if (lane == 0) {
-            info->desc.max_logit = m;
-            info->desc.argmax = amax;
-            info->desc.status = status;
-            info->desc.temperature = T;
-            info->cut_count = -1;
+            P->status = any_bad ? (uint32_t)kNonfinite : 0u;
+            P->count = any_bad ? 0u : (uint32_t)m;
         }
-        if (status != 0) {
-            if (lane == 0) {
-                info->desc.log_norm = 0.0f;
-                info->desc.cutoff_logit = m;
-                info->desc.cutoff_ties = 0;
-                info->desc.kept = 0;
-                info->p_token = nan("");
-                info->z = 0.0;
-                info->n_list = -1;
-            }
-            continue;
-        }
-        if (T == 0.0f) {
-            if (lane == 0) {
-                info->desc.log_norm = 0.0f;
-                info->desc.cutoff_logit = m;
-                info->desc.cutoff_ties = 1;
-                info->desc.kept = 1;
-                info->p_token = task.token >= 0 ? (task.token == amax ? 1.0 : 0.0) : nan("");
-                info->z = 1.0;
-                info->n_list = 1;
-                info->list_idx[0] = amax;
-                info->list_p[0] = 1.0;
-            }
-            continue;
-        }
-        // Sampling row: masses of the kept values in fp64, in sorted order.
-        const double e = lane < n_top ? exp(((double)lv - (double)m) / (double)T) : 0.0;
-        s_e[warp][lane] = e;
+        __threadfence();
         __syncwarp();
+        int last = 0;
         if (lane == 0) {
-            double z1 = 0.0;
-            for (int i = 0; i < n_top; ++i) z1 += s_e[warp][i];
-            int kept = n_top;
-            if (task.top_p < 1.0f) {
-                const double target = (double)task.top_p * z1;
-                double cum = 0.0;
-                for (int i = 0; i < n_top; ++i) {
-                    cum += s_e[warp][i];
-                    if (cum >= target) {
-                        kept = i + 1;
-                        break;
-                    }
-                }
-            }
-            double z = 0.0;
-            for (int i = 0; i < kept; ++i) z += s_e[warp][i];
-            s_kept[warp] = kept;
-            s_z[warp] = z;
+            const long long g0 = (long long)t * sp.nc;
+            const int parts = (int)(split_owner(sp, g0 + sp.nc - 1) - split_owner(sp, g0) + 1);
+            last = atomicAdd(&a.row_done[t], 1) == parts - 1;
         }
-        __syncwarp();
-        const int kept = s_kept[warp];
-        const double z = s_z[warp];
-        const bool in = lane < kept;
-        const double p = in ? e / z : 0.0;
-        const float cut = __shfl_sync(0xFFFFFFFFu, lv, kept - 1);
-        const int ties = __popc(__ballot_sync(0xFFFFFFFFu, in && lv == cut));
-        int rank = 0;
-        for (int j = 0; j < kept; ++j) rank += (__shfl_sync(0xFFFFFFFFu, li, j) < li) ? 1 : 0;
-        if (in) {
-            info->list_idx[rank] = li;
-            info->list_p[rank] = p;
+        if (__shfl_sync(FULL, last, 0)) {
+            __threadfence();
+            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, reinterpret_cast<double*>(cand));
         }
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, in && li == task.token);
-        const double ptok = hit ? __shfl_sync(0xFFFFFFFFu, p, __ffs(hit) - 1) : 0.0;
-        if (lane == 0) {
-            info->desc.log_norm = (float)log(z);
-            info->desc.cutoff_logit = cut;
-            info->desc.cutoff_ties = ties;
-            info->desc.kept = kept;
-            info->p_token = task.token >= 0 ? ptok : nan("");
-            info->z = z;
-            info->n_list = kept;
-        }
+        g += c_end - c;
+        ++t;
+        c = 0;
     }
 }
 
@@ -702,8 +564,9 @@ __global__ void __launch_bounds__(kFinalizeWarps * 32) fast_finalize_kernel(Rows
 template <int DT>
 cudaError_t launch_fast_rows_t(const RowsArgs& a, cudaStream_t s)
 {
-    // Persistent grid: exactly the CTAs that fit at once, each with its ring.
-    const size_t smem = (size_t)kStages * kChunkBytes;
+    // Persistent grid: the CTAs that fit at once (at most kMaxRowWarps warps),
+    // each warp with its own ring.
+    const size_t smem = (size_t)kCtaWarps * kStages * kWarpChunkBytes;
     static int blocks_per_sm[128] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -715,25 +578,15 @@ cudaError_t launch_fast_rows_t(const RowsArgs& a, cudaStream_t s)
         if (e != cudaSuccess) return e;
         if (nb < 1) nb = 1;
     }
-    fast_rows_kernel<DT><<<a.num_sms * nb, kFastThreads, smem, s>>>(a);
+    int grid = a.num_sms * nb;
+    if (grid > kMaxRowWarps / kCtaWarps) grid = kMaxRowWarps / kCtaWarps;
+    fast_rows_kernel<DT><<<grid, kFastThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s)
 {
     return a.dtype == 0 ? launch_fast_rows_t<0>(a, s) : launch_fast_rows_t<1>(a, s);
-}
-
-cudaError_t launch_fast_finalize(const RowsArgs& a, cudaStream_t s)
-{
-    int grid = (a.max_tasks + kFinalizeWarps - 1) / kFinalizeWarps;
-    if (grid > a.num_sms * 8) grid = a.num_sms * 8;
-    if (grid < 1) grid = 1;
-    if (a.dtype == 0)
-        fast_finalize_kernel<0><<<grid, kFinalizeWarps * 32, 0, s>>>(a);
-    else
-        fast_finalize_kernel<1><<<grid, kFinalizeWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace sv

@@ -17,9 +17,8 @@ namespace sv {
 // ----------------------------------------------------------------------------
 constexpr int kFastK = 32;          // largest top-k served by the one-pass select kernel
 constexpr int kFastThreads = 256;   // threads of the one-pass select kernel
-constexpr int kFastVecs = 8;        // 16-byte vectors per thread per chunk
-constexpr int kCandCap = 256;       // candidate buffer of one chunk
-constexpr int kMinChunk = kFastThreads * kFastVecs * 4;   // fp32 chunk (bf16 chunks are twice as long)
+constexpr int kFastVecs = 8;        // 16-byte vectors per lane per warp chunk (4 KB a warp)
+constexpr int kMaxRowWarps = 4096;  // warps of the one-pass select grid (sizes the partial lists)
 constexpr int kHistThreads = 512;   // threads of the exact-histogram kernel
 constexpr int kHistWords = 32768;   // 65536 16-bit counters, two per 32-bit word
 constexpr int kHistMaxSlice = 65535;// elements per CTA so a 16-bit counter cannot wrap
@@ -61,7 +60,7 @@ struct RowInfo {
     double list_p[kFastK];
 };
 
-// Top candidates of one chunk of one row: composite keys, descending.
+// Top candidates of one warp's part of one row: composite keys, descending.
 struct Partial {
     uint32_t status;
     uint32_t count;
@@ -98,8 +97,9 @@ struct Counters {
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, info, partials, req, jobs, total;
-    int slots, max_tasks, nchunks;
+    size_t counters, fast_tasks, slow_tasks, info, partials, row_done, req, jobs, total;
+    int slots, max_tasks;
+    size_t n_partials;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -110,13 +110,17 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     WsLayout L{};
     L.slots = n_req * (2 * k_max + 1);
     L.max_tasks = L.slots;
-    L.nchunks = vocab > 0 ? (vocab + kMinChunk - 1) / kMinChunk : 1;
+    (void)vocab;
+    // A grid of W warps splits T tasks into parts; W * (parts per warp) stays
+    // below T + 3 W (see the range arithmetic of the row kernel).
+    L.n_partials = (size_t)L.max_tasks + 3 * (size_t)kMaxRowWarps;
     size_t off = 0;
     L.counters = off;   off = align256(off + sizeof(Counters));
     L.fast_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
     L.slow_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
     L.info = off;       off = align256(off + sizeof(RowInfo) * (size_t)L.slots);
-    L.partials = off;   off = align256(off + sizeof(Partial) * (size_t)L.max_tasks * (size_t)L.nchunks);
+    L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
+    L.row_done = off;   off = align256(off + sizeof(int32_t) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
     L.total = off;
@@ -269,18 +273,17 @@ struct RowsArgs {
     int64_t stride_t, stride_d;
     int vocab;
     int dtype;
-    int nchunks;
     RowTask* fast_tasks;
     RowTask* slow_tasks;
     Counters* counters;
     RowInfo* info;
     Partial* partials;
+    int32_t* row_done;   // per fast task: parts finished (zeroed by the prep kernel)
     int max_tasks;
     int num_sms;
 };
 
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
-cudaError_t launch_fast_finalize(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
 
 struct ChainArgs {
@@ -306,6 +309,7 @@ struct ChainArgs {
     Counters* counters;
     RowTask* fast_tasks;
     RowTask* slow_tasks;
+    int32_t* row_done;
     RowInfo* info;
     ReqState* req;
     ResampleJob* jobs;
