@@ -16,12 +16,12 @@
 //  * Each lane takes a NaN-propagating packed max (max.NaN.bf16x2) of its
 //    8 x 16 B of a chunk.  In a part's first chunk theta = the k-th largest of
 //    the 32 lane maxima (bisection on the key bits with warp votes): at least
-//    k elements reach it.  Those are pushed as composite keys (logit, inverted
-//    index) into the warp's 64 shared-memory slots and cut to the exact top k;
-//    from then on theta is the k-th best so far and an element must beat it
-//    strictly (its index is higher, so a tie cannot win).  A chunk with no
-//    lane maximum above theta costs one vote; the slots are cut back to k
-//    whenever a push could overflow them.
+//    k elements reach it.  The warp keeps the part's best k composite keys
+//    (logit, inverted index) as a sorted list across its lanes; an element
+//    that reaches theta is re-read from the stage and inserted (one vote and
+//    one shift).  Once k entries exist theta is the exact k-th best so far
+//    and an element must beat it strictly (its index is higher, so a tie
+//    cannot win).  A chunk with no lane maximum above theta costs one vote.
 //  * At a part's end the warp writes its top k, ordered by (logit desc, index
 //    asc), and counts the part in the row's counter.  The warp that finishes a
 //    row's last part merges the row's lists (bitonic merges of sorted lists of
@@ -59,7 +59,6 @@ constexpr int kCtaWarps = kFastThreads / 32;
 constexpr int kStages = 3;                                  // chunks in flight per warp
 constexpr int kWarpChunkBytes = 32 * kFastVecs * 16;        // 4 KB: one warp chunk of either dtype
 constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
-constexpr int kWarpCap = 64;                                // candidate slots per warp
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -188,38 +187,6 @@ __device__ __forceinline__ uint32_t warp_kth_key(uint32_t key, int k)
     return pre;
 }
 
-// Keeps the top k (<= 32) of the n (<= kWarpCap) candidates in a warp's slots,
-// descending, in the first min(n, k) slots.  Composite keys are distinct, so a
-// candidate's rank is the number of larger ones.  Out of line: it is cold.
-__device__ __noinline__ int warp_compact(unsigned long long* cand, int n, int k)
-{
-    const int lane = threadIdx.x & 31;
-    __syncwarp();
-    const unsigned long long a0 = lane < n ? cand[lane] : 0ull;
-    const unsigned long long a1 = lane + 32 < n ? cand[lane + 32] : 0ull;
-    int r0 = 0, r1 = 0, s0 = 0, s1 = 0;
-    int j = 0;
-    for (; j + 2 <= n; j += 2) {
-        const unsigned long long x = cand[j], y = cand[j + 1];
-        r0 += x > a0 ? 1 : 0;
-        r1 += x > a1 ? 1 : 0;
-        s0 += y > a0 ? 1 : 0;
-        s1 += y > a1 ? 1 : 0;
-    }
-    if (j < n) {
-        const unsigned long long x = cand[j];
-        r0 += x > a0 ? 1 : 0;
-        r1 += x > a1 ? 1 : 0;
-    }
-    r0 += s0;
-    r1 += s1;
-    __syncwarp();
-    if (lane < n && r0 < k) cand[r0] = a0;
-    if (lane + 32 < n && r1 < k) cand[r1] = a1;
-    __syncwarp();
-    return n < k ? n : k;
-}
-
 // Top 32 of two descending lists of 32 (lane i holds element i of each), as a
 // descending list: the elementwise max against the reversed second list is
 // bitonic and holds the top 32; five compare-exchange stages sort it.
@@ -234,6 +201,18 @@ __device__ __forceinline__ unsigned long long merge_desc(unsigned long long acc,
         c = (lane & j) ? (x < c ? x : c) : (x > c ? x : c);
     }
     return c;
+}
+
+// Inserts composite key x into a warp's descending list (lane i holds entry
+// i, empty entries are 0) when it beats entry k-1; the last entry drops out.
+__device__ __forceinline__ unsigned long long list_insert(unsigned long long list, unsigned long long x, int k)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned long long kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
+    if (x <= kth) return list;
+    const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));
+    const unsigned long long up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
+    return lane < pos ? list : (lane == pos ? x : up);
 }
 
 // The distribution of fast task t from its parts' lists (one warp; s_e is 32
@@ -356,7 +335,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     constexpr unsigned FULL = 0xFFFFFFFFu;
     extern __shared__ __align__(128) unsigned char ring[];   // warps x kStages x 4 KB
     __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
-    __shared__ unsigned long long s_cand[kCtaWarps][kWarpCap];
+    __shared__ double s_fin[kCtaWarps][32];                  // finalisation scratch
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
@@ -370,7 +349,6 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     const long long lo = split_lo(sp, w), hi = split_lo(sp, w + 1);
     unsigned long long* bar = s_bar[warp];
     unsigned char* wring = ring + (size_t)warp * (kStages * kWarpChunkBytes);
-    unsigned long long* cand = s_cand[warp];
 
     // Producer (lane 0): the next unit to copy, its row and its ring stage.
     long long p_g = lo;
@@ -411,12 +389,14 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     int t = (int)(lo / sp.nc);
     int c = (int)(lo - (long long)t * sp.nc);
     while (g < hi) {
-        // One row part: chunks [c, c_end) of task t.
+        // One row part: chunks [c, c_end) of task t.  The part's top k live in
+        // `list` (lane i: i-th best composite key, 0 = empty).
         const RowTask task = a.fast_tasks[t];
         const char* row = task_row<DT>(a, task);
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
         const int c_end = (int)min((long long)sp.nc, (long long)c + (hi - g));
-        int wcnt = 0, strict = 0, bad = 0;
+        unsigned long long list = 0ull;
+        int strict = 0, bad = 0;
         float theta = -INFINITY;
         for (int cc = c; cc < c_end; ++cc) {
             const int c0 = cc * CHUNK;
@@ -449,17 +429,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                 else
                     v[i] = load_edge<DT>(row, c0 + (i * 32 + lane) * EPV, a.vocab);
             }
-            __syncwarp();   // every lane holds its data: the stage can be refilled
-            if (lane == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                produce();
-            }
-            if (++c_slot == kStages) {
-                c_slot = 0;
-                c_phase ^= 1u;
-            }
-            // Per-vector NaN-propagating maxima (kept for the push test), then
-            // the lane maximum.
+            // Per-vector NaN-propagating maxima, then the lane maximum.
             uint32_t m2[kFastVecs];
             float vmx[kFastVecs];
             float tmax;
@@ -486,9 +456,10 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                     theta = f32_of_key(warp_kth_key<32>(key_of_f32_bits(__float_as_uint(tmax)), k));
             }
             if (__ballot_sync(FULL, strict ? tmax > theta : tmax >= theta)) {
-                // Warp-cooperative push in element order: for each lane whose
-                // vector reaches theta, the warp takes that vector (broadcast),
-                // EPV lanes test one element each and write their keys.
+                // Vectors that reach theta, visited in element order (vector
+                // index i * 32 + lane); EPV lanes re-read one element each from
+                // the stage and the taken ones enter the list one by one.
+                uint32_t pend = 0u;
 #pragma unroll
                 for (int i = 0; i < kFastVecs; ++i) {
                     float vm;
@@ -496,47 +467,63 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                         vm = bf16x2_hmax(m2[i]);
                     else
                         vm = vmx[i];
-                    unsigned bal = __ballot_sync(FULL, strict ? vm > theta : vm >= theta);
+                    pend |= ((strict ? vm > theta : vm >= theta) ? 1u : 0u) << i;
+                }
+                unsigned ibits = __reduce_or_sync(FULL, pend);
+                while (ibits) {
+                    const int i = __ffs(ibits) - 1;
+                    ibits &= ibits - 1u;
+                    unsigned bal = __ballot_sync(FULL, (pend >> i) & 1u);
                     while (bal) {
-                        if (wcnt > kWarpCap - EPV) {   // no room for a whole vector: cut to k
-                            wcnt = warp_compact(cand, wcnt, k);
-                            if (wcnt == k) {
-                                theta = ckey_value(cand[k - 1]);
+                        const int src = __ffs(bal) - 1;
+                        bal &= bal - 1u;
+                        const int vi = i * 32 + src;        // vector index in the chunk
+                        const int e = c0 + vi * EPV + lane;
+                        float val = -INFINITY;
+                        if (lane < EPV) {
+                            if ((uint32_t)(vi * 16 + 16) <= bytes) {
+                                if constexpr (DT == 0)
+                                    val = __uint_as_float((uint32_t)(*(const uint16_t*)(stg + vi * 16 + lane * 2)) << 16);
+                                else
+                                    val = *(const float*)(stg + vi * 16 + lane * 4);
+                            } else if (e < a.vocab) {
+                                val = load_logit<DT>(row, e);
+                            }
+                        }
+                        const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
+                        unsigned tb = __ballot_sync(FULL, take);
+                        if (tb) {
+                            const unsigned long long mine = ckey(val, (uint32_t)e);
+                            while (tb) {
+                                const int sl = __ffs(tb) - 1;
+                                tb &= tb - 1u;
+                                list = list_insert(list, __shfl_sync(FULL, mine, sl), k);
+                            }
+                            const unsigned long long kth = __shfl_sync(FULL, list, k - 1);
+                            if (kth != 0ull) {   // k entries: theta is the exact k-th best
+                                theta = ckey_value(kth);
                                 strict = 1;
                             }
                         }
-                        const int src = __ffs(bal) - 1;
-                        bal &= bal - 1u;
-                        const uint32_t w0 = __shfl_sync(FULL, v[i].x, src);
-                        const uint32_t w1 = __shfl_sync(FULL, v[i].y, src);
-                        const uint32_t w2 = __shfl_sync(FULL, v[i].z, src);
-                        const uint32_t w3 = __shfl_sync(FULL, v[i].w, src);
-                        const int q = DT == 0 ? (lane >> 1) : lane;
-                        const uint32_t word = q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
-                        const float val = DT == 0 ? __uint_as_float((lane & 1) ? (word & 0xFFFF0000u) : (word << 16))
-                                                  : __uint_as_float(word);
-                        const int e = c0 + (i * 32 + src) * EPV + lane;
-                        const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
-                        const unsigned tb = __ballot_sync(FULL, take);
-                        if (take) cand[wcnt + __popc(tb & ((1u << lane) - 1u))] = ckey(val, (uint32_t)e);
-                        wcnt += __popc(tb);
                     }
                 }
             }
-            if (cc == c) {   // exact threshold after the first chunk (>= k candidates unless it is short)
-                wcnt = warp_compact(cand, wcnt, k);
-                if (wcnt == k) {
-                    theta = ckey_value(cand[k - 1]);
-                    strict = 1;
-                }
+            __syncwarp();   // every lane is done with the stage: refill it
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                produce();
+            }
+            if (++c_slot == kStages) {
+                c_slot = 0;
+                c_phase ^= 1u;
             }
         }
 
         // The part's list, then the row's counter; the last part finalises.
-        const int m = warp_compact(cand, wcnt, k);
+        const int m = __popc(__ballot_sync(FULL, lane < k && list != 0ull));
         const int any_bad = __any_sync(FULL, bad);
         Partial* P = a.partials + part_slot(sp, w, t);
-        if (!any_bad && lane < m) P->keys[lane] = cand[lane];
+        if (!any_bad && lane < m) P->keys[lane] = list;
         if (lane == 0) {
             P->status = any_bad ? (uint32_t)kNonfinite : 0u;
             P->count = any_bad ? 0u : (uint32_t)m;
@@ -551,7 +538,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         }
         if (__shfl_sync(FULL, last, 0)) {
             __threadfence();
-            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, reinterpret_cast<double*>(cand));
+            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, s_fin[warp]);
         }
         g += c_end - c;
         ++t;
