@@ -78,7 +78,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ra.counters = at<Counters>(ws, L.counters);
     ra.info = at<RowInfo>(ws, L.info);
     ra.partials = at<Partial>(ws, L.partials);
-    ra.row_done = at<int32_t>(ws, L.row_done);
+    ra.row_sync = at<RowSync>(ws, L.row_sync);
     ra.max_tasks = L.max_tasks;
     ra.num_sms = sm_count();
     ChainArgs& ca = c.ca;
@@ -94,7 +94,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.counters = ra.counters;
     ca.fast_tasks = ra.fast_tasks;
     ca.slow_tasks = ra.slow_tasks;
-    ca.row_done = ra.row_done;
+    ca.row_sync = ra.row_sync;
     ca.info = ra.info;
     ca.req = at<ReqState>(ws, L.req);
     ca.jobs = at<ResampleJob>(ws, L.jobs);

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                     t.token = has_tok ? a.draft_tokens[(size_t)u * K + j] : -1;
                 }
                 list[pos + i] = t;
-                if (nf) a.row_done[pos + i] = 0;
+                if (nf) a.row_sync[pos + i] = RowSync{0, 0u};
             }
             if (a.layout == 2) {
                 if (err) {

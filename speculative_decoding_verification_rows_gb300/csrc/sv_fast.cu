@@ -17,11 +17,22 @@
 //    8 x 16 B of a chunk.  In a part's first chunk theta = the k-th largest of
 //    the 32 lane maxima (bisection on the key bits with warp votes): at least
 //    k elements reach it.  The warp keeps the part's best k composite keys
-//    (logit, inverted index) as a sorted list across its lanes; an element
-//    that reaches theta is re-read from the stage and inserted (one vote and
-//    one shift).  Once k entries exist theta is the exact k-th best so far
-//    and an element must beat it strictly (its index is higher, so a tie
-//    cannot win).  A chunk with no lane maximum above theta costs one vote.
+//    (logit, inverted index) as a sorted list across its lanes.  Lanes whose
+//    vectors reach theta re-read them from the stage and append the elements
+//    that do to a 32-key buffer of the warp; a full buffer is sorted (bitonic
+//    network) and merged into the list.  theta moves only between chunks: to
+//    the exact k-th best so far after a part's first chunk and whenever a
+//    chunk ends with the buffer half full.  Once k entries exist an element
+//    must beat theta strictly (its index is higher than those of the entries,
+//    so a tie cannot win).  A chunk with no lane maximum above theta costs one
+//    vote.
+//  * The k-th entry of a full part list is a lower bound on the row's k-th
+//    largest logit.  Parts publish it (atomicMax on the row's order key) and
+//    read the others' one chunk ahead; an element below the best bound
+//    cannot be kept (one equal to it can: it may have a lower index).  The
+//    row's parts run at different times (a range starts with the tail of one
+//    row and ends with the head of the next), so a part that starts late
+//    starts with a near-final threshold.
 //  * At a part's end the warp writes its top k, ordered by (logit desc, index
 //    asc), and counts the part in the row's counter.  The warp that finishes a
 //    row's last part merges the row's lists (bitonic merges of sorted lists of
@@ -59,6 +70,8 @@ constexpr int kCtaWarps = kFastThreads / 32;
 constexpr int kStages = 3;                                  // chunks in flight per warp
 constexpr int kWarpChunkBytes = 32 * kFastVecs * 16;        // 4 KB: one warp chunk of either dtype
 constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
+constexpr int kBufCap = 32;                                 // buffered candidates per warp
+constexpr int kMergeAt = 16;                                // a chunk's end merges a buffer this full
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -139,6 +152,37 @@ __device__ __forceinline__ uint4 load_edge(const char* row, int e0, int vocab)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Vector vi (16 bytes) of a chunk whose first `bytes` bytes sit in the stage:
+// from the stage when it is all there, else from the row.
+template <int DT>
+__device__ __forceinline__ uint4 stage_or_edge(const unsigned char* stg, uint32_t bytes, const char* row, int c0, int vi,
+                                               int vocab)
+{
+    constexpr int EPV = DT == 0 ? 8 : 4;
+    if ((uint32_t)(vi * 16 + 16) <= bytes) return ld_shared_v4(stg + vi * 16);
+    return load_edge<DT>(row, c0 + vi * EPV, vocab);
+}
+// Element q (0 .. EPV-1) of a 16-byte vector as fp32, for a q known at compile time.
+template <int DT>
+__device__ __forceinline__ float vec_elem(const uint4& v, int q)
+{
+    const uint32_t w = (DT == 0 ? (q >> 1) : q) == 0 ? v.x
+                     : (DT == 0 ? (q >> 1) : q) == 1 ? v.y
+                     : (DT == 0 ? (q >> 1) : q) == 2 ? v.z : v.w;
+    if (DT == 0) return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    return __uint_as_float(w);
+}
+// The same for a run-time q, by selects rather than an indexed register array.
+template <int DT>
+__device__ __forceinline__ float vec_elem_dyn(const uint4& v, int q)
+{
+    const int j = DT == 0 ? (q >> 1) : q;
+    const uint32_t lo = (j & 1) ? v.y : v.x, hi = (j & 1) ? v.w : v.z;
+    const uint32_t w = (j & 2) ? hi : lo;
+    if (DT == 0) return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    return __uint_as_float(w);
+}
+
 // Byte offset of a row and the bulk-copied bytes of one warp chunk of it.
 template <int DT>
 __device__ __forceinline__ const char* task_row(const RowsArgs& a, const RowTask& t)
@@ -203,16 +247,31 @@ __device__ __forceinline__ unsigned long long merge_desc(unsigned long long acc,
     return c;
 }
 
-// Inserts composite key x into a warp's descending list (lane i holds entry
-// i, empty entries are 0) when it beats entry k-1; the last entry drops out.
-__device__ __forceinline__ unsigned long long list_insert(unsigned long long list, unsigned long long x, int k)
+// Descending bitonic sort of one key per lane over the first P lanes, P the
+// power of two >= n (lanes >= n hold 0 and stay below every key).
+__device__ __forceinline__ unsigned long long sort_desc(unsigned long long v, int n)
 {
     const int lane = threadIdx.x & 31;
-    const unsigned long long kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
-    if (x <= kth) return list;
-    const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));
-    const unsigned long long up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
-    return lane < pos ? list : (lane == pos ? x : up);
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride; stride >>= 1) {
+            const unsigned long long x = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+            v = keep_max ? (x > v ? x : v) : (x < v ? x : v);
+        }
+    }
+    return v;
+}
+
+// Merges the n (<= 32) buffered keys of a warp into its descending list.
+__device__ __noinline__ unsigned long long merge_buffer(unsigned long long list, const unsigned long long* buf, int n)
+{
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    const unsigned long long b = lane < n ? buf[lane] : 0ull;
+    __syncwarp();   // the buffer may be refilled after this
+    return merge_desc(list, sort_desc(b, n));
 }
 
 // The distribution of fast task t from its parts' lists (one warp; s_e is 32
@@ -228,12 +287,22 @@ __device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, 
     const long long w0 = split_owner(sp, g0), w1 = split_owner(sp, g0 + sp.nc - 1);
     unsigned long long acc = 0ull;
     uint32_t st = 0u;
-    for (long long w = w0; w <= w1; ++w) {
-        const Partial* P = parts + part_slot(sp, w, t);
-        const uint32_t cnt = __ldcg(&P->count);
-        st |= __ldcg(&P->status);
-        const unsigned long long key = lane < (int)cnt ? __ldcg(&P->keys[lane]) : 0ull;
-        acc = merge_desc(acc, key);
+    for (long long wb = w0; wb <= w1; wb += 4) {   // four parts' loads in flight at once
+        unsigned long long key[4];
+        uint32_t cnt[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            cnt[j] = 0u;
+            key[j] = 0ull;
+            if (wb + j <= w1) {
+                const Partial* P = parts + part_slot(sp, wb + j, t);
+                cnt[j] = __ldcg(&P->count);
+                st |= __ldcg(&P->status);
+                key[j] = __ldcg(&P->keys[lane]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc = merge_desc(acc, lane < (int)cnt[j] ? key[j] : 0ull);
     }
     const unsigned long long ck = lane < k ? acc : 0ull;
     const int n_top = __popc(__ballot_sync(0xFFFFFFFFu, ck != 0ull));
@@ -335,7 +404,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     constexpr unsigned FULL = 0xFFFFFFFFu;
     extern __shared__ __align__(128) unsigned char ring[];   // warps x kStages x 4 KB
     __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
-    __shared__ double s_fin[kCtaWarps][32];                  // finalisation scratch
+    __shared__ unsigned long long s_buf[kCtaWarps][kBufCap]; // candidate buffer, then finalisation
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
@@ -349,6 +418,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     const long long lo = split_lo(sp, w), hi = split_lo(sp, w + 1);
     unsigned long long* bar = s_bar[warp];
     unsigned char* wring = ring + (size_t)warp * (kStages * kWarpChunkBytes);
+    unsigned long long* buf = s_buf[warp];
 
     // Producer (lane 0): the next unit to copy, its row and its ring stage.
     long long p_g = lo;
@@ -396,8 +466,16 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
         const int c_end = (int)min((long long)sp.nc, (long long)c + (hi - g));
         unsigned long long list = 0ull;
+        int nb = 0;   // keys in the warp's buffer
         int strict = 0, bad = 0;
         float theta = -INFINITY;
+        // Lower bound on the row's k-th largest logit published by the row's
+        // other parts (the k-th entry of a full part list is one): elements
+        // below it cannot be kept, ties with it can (they may have lower
+        // indices).  Read one chunk ahead so its latency stays hidden.
+        uint32_t* bound_at = &a.row_sync[t].bound;
+        uint32_t bkey = 0u, bnext = __ldcg(bound_at);
+        float bval = -INFINITY;
         for (int cc = c; cc < c_end; ++cc) {
             const int c0 = cc * CHUNK;
             const uint32_t bytes = chunk_bytes<DT>(row, c0, a.vocab);
@@ -420,14 +498,14 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                 return;
             }
             const unsigned char* stg = wring + c_slot * kWarpChunkBytes;
+            const bool full = bytes == (uint32_t)kWarpChunkBytes;   // the chunk is all in the stage
             uint4 v[kFastVecs];
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < kFastVecs; ++i) {
-                const int off = (i * 32 + lane) * 16;
-                if ((uint32_t)(off + 16) <= bytes)
-                    v[i] = ld_shared_v4(stg + off);
-                else
-                    v[i] = load_edge<DT>(row, c0 + (i * 32 + lane) * EPV, a.vocab);
+                for (int i = 0; i < kFastVecs; ++i) v[i] = ld_shared_v4(stg + (i * 32 + lane) * 16);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kFastVecs; ++i) v[i] = stage_or_edge<DT>(stg, bytes, row, c0, i * 32 + lane, a.vocab);
             }
             // Per-vector NaN-propagating maxima, then the lane maximum.
             uint32_t m2[kFastVecs];
@@ -455,10 +533,22 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                 else
                     theta = f32_of_key(warp_kth_key<32>(key_of_f32_bits(__float_as_uint(tmax)), k));
             }
-            if (__ballot_sync(FULL, strict ? tmax > theta : tmax >= theta)) {
-                // Vectors that reach theta, visited in element order (vector
-                // index i * 32 + lane); EPV lanes re-read one element each from
-                // the stage and the taken ones enter the list one by one.
+            // The chunk's filter: the part's own threshold, or the published
+            // bound when that is higher.
+            float th = theta;
+            int sf = strict;
+            if (bval > th) {
+                th = bval;
+                sf = 0;
+            }
+            if (__ballot_sync(FULL, sf ? tmax > th : tmax >= th)) {
+                // Each lane re-reads its vectors that reach theta from the
+                // stage and marks their elements that do; the marked elements
+                // of the warp are merged into the list.  Every element of this
+                // chunk has a higher index than the entries kept from earlier
+                // chunks, so the order of the merges does not matter and, once
+                // the list was full at the chunk's start, a tie with theta
+                // cannot enter.
                 uint32_t pend = 0u;
 #pragma unroll
                 for (int i = 0; i < kFastVecs; ++i) {
@@ -467,47 +557,65 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                         vm = bf16x2_hmax(m2[i]);
                     else
                         vm = vmx[i];
-                    pend |= ((strict ? vm > theta : vm >= theta) ? 1u : 0u) << i;
+                    pend |= ((sf ? vm > th : vm >= th) ? 1u : 0u) << i;
                 }
-                unsigned ibits = __reduce_or_sync(FULL, pend);
-                while (ibits) {
-                    const int i = __ffs(ibits) - 1;
-                    ibits &= ibits - 1u;
-                    unsigned bal = __ballot_sync(FULL, (pend >> i) & 1u);
-                    while (bal) {
-                        const int src = __ffs(bal) - 1;
-                        bal &= bal - 1u;
-                        const int vi = i * 32 + src;        // vector index in the chunk
-                        const int e = c0 + vi * EPV + lane;
-                        float val = -INFINITY;
-                        if (lane < EPV) {
-                            if ((uint32_t)(vi * 16 + 16) <= bytes) {
-                                if constexpr (DT == 0)
-                                    val = __uint_as_float((uint32_t)(*(const uint16_t*)(stg + vi * 16 + lane * 2)) << 16);
-                                else
-                                    val = *(const float*)(stg + vi * 16 + lane * 4);
-                            } else if (e < a.vocab) {
-                                val = load_logit<DT>(row, e);
-                            }
+                while (__any_sync(FULL, pend != 0u)) {
+                    uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+                    int e0 = 0;
+                    uint32_t cm = 0u;   // elements of vv to insert
+                    if (pend) {
+                        const int i = __ffs(pend) - 1;
+                        pend &= pend - 1u;
+                        vv = full ? ld_shared_v4(stg + (i * 32 + lane) * 16)
+                                  : stage_or_edge<DT>(stg, bytes, row, c0, i * 32 + lane, a.vocab);
+                        e0 = c0 + (i * 32 + lane) * EPV;
+#pragma unroll
+                        for (int q = 0; q < EPV; ++q) {
+                            const float x = vec_elem<DT>(vv, q);
+                            cm |= ((sf ? x > th : x >= th) && e0 + q < a.vocab ? 1u : 0u) << q;
                         }
-                        const bool take = lane < EPV && e < a.vocab && (strict ? val > theta : val >= theta);
-                        unsigned tb = __ballot_sync(FULL, take);
-                        if (tb) {
-                            const unsigned long long mine = ckey(val, (uint32_t)e);
-                            while (tb) {
-                                const int sl = __ffs(tb) - 1;
-                                tb &= tb - 1u;
-                                list = list_insert(list, __shfl_sync(FULL, mine, sl), k);
-                            }
-                            const unsigned long long kth = __shfl_sync(FULL, list, k - 1);
-                            if (kth != 0ull) {   // k entries: theta is the exact k-th best
-                                theta = ckey_value(kth);
-                                strict = 1;
-                            }
+                    }
+                    // One marked element per lane at a time goes to the
+                    // warp's buffer (merged into the list when it is full).
+                    while (__any_sync(FULL, cm != 0u)) {
+                        unsigned long long key = 0ull;
+                        if (cm) {
+                            const int q = __ffs(cm) - 1;
+                            cm &= cm - 1u;
+                            key = ckey(vec_elem_dyn<DT>(vv, q), (uint32_t)(e0 + q));
                         }
+                        const unsigned own = __ballot_sync(FULL, key != 0ull);
+                        const int add = __popc(own);
+                        if (nb + add > kBufCap) {
+                            list = merge_buffer(list, buf, nb);
+                            nb = 0;
+                        }
+                        if (key) buf[nb + __popc(own & ((1u << lane) - 1u))] = key;
+                        nb += add;
                     }
                 }
             }
+            // theta moves only between chunks: after a part's first chunk, or
+            // when the buffer holds enough to be worth a merge.
+            if (cc == c || nb >= kMergeAt) {
+                if (nb) {
+                    list = merge_buffer(list, buf, nb);
+                    nb = 0;
+                }
+                const unsigned long long kth = __shfl_sync(FULL, list, k - 1);
+                if (kth != 0ull) {   // k entries: theta is the exact k-th best so far
+                    const float nt = ckey_value(kth);
+                    if (lane == 0 && (!strict || nt > theta) && nt > bval)
+                        atomicMax(bound_at, key_of_f32_bits(__float_as_uint(nt)));
+                    theta = nt;
+                    strict = 1;
+                }
+            }
+            if (bnext > bkey) {
+                bkey = bnext;
+                bval = f32_of_key(bkey);
+            }
+            bnext = __ldcg(bound_at);
             __syncwarp();   // every lane is done with the stage: refill it
             if (lane == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -519,7 +627,14 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             }
         }
 
-        // The part's list, then the row's counter; the last part finalises.
+        // The part's list (and its bound), then the row's counter; the last
+        // part finalises.
+        if (nb) list = merge_buffer(list, buf, nb);
+        {
+            const unsigned long long kth = __shfl_sync(FULL, list, k - 1);
+            if (lane == 0 && kth != 0ull && ckey_value(kth) > bval)
+                atomicMax(bound_at, key_of_f32_bits(__float_as_uint(ckey_value(kth))));
+        }
         const int m = __popc(__ballot_sync(FULL, lane < k && list != 0ull));
         const int any_bad = __any_sync(FULL, bad);
         Partial* P = a.partials + part_slot(sp, w, t);
@@ -534,11 +649,11 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         if (lane == 0) {
             const long long g0 = (long long)t * sp.nc;
             const int parts = (int)(split_owner(sp, g0 + sp.nc - 1) - split_owner(sp, g0) + 1);
-            last = atomicAdd(&a.row_done[t], 1) == parts - 1;
+            last = atomicAdd(&a.row_sync[t].done, 1) == parts - 1;
         }
         if (__shfl_sync(FULL, last, 0)) {
             __threadfence();
-            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, s_fin[warp]);
+            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, reinterpret_cast<double*>(buf));
         }
         g += c_end - c;
         ++t;

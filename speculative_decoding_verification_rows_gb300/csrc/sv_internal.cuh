@@ -67,6 +67,14 @@ struct Partial {
     unsigned long long keys[kFastK];
 };
 
+// Per fast task: parts of the row finished so far, and the best lower bound
+// on the row's k-th largest logit that a part has published (order key of
+// the value, 0 = none).  Zeroed by the prep kernel.
+struct RowSync {
+    int32_t done;
+    uint32_t bound;
+};
+
 // Per-request state written by the prep kernel.
 struct ReqState {
     int32_t v;        // verified drafts (window = v + 1 target rows)
@@ -97,7 +105,7 @@ struct Counters {
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, info, partials, row_done, req, jobs, total;
+    size_t counters, fast_tasks, slow_tasks, info, partials, row_sync, req, jobs, total;
     int slots, max_tasks;
     size_t n_partials;
 };
@@ -120,7 +128,7 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.slow_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
     L.info = off;       off = align256(off + sizeof(RowInfo) * (size_t)L.slots);
     L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
-    L.row_done = off;   off = align256(off + sizeof(int32_t) * (size_t)L.max_tasks);
+    L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
     L.total = off;
@@ -278,7 +286,7 @@ struct RowsArgs {
     Counters* counters;
     RowInfo* info;
     Partial* partials;
-    int32_t* row_done;   // per fast task: parts finished (zeroed by the prep kernel)
+    RowSync* row_sync;   // per fast task (zeroed by the prep kernel)
     int max_tasks;
     int num_sms;
 };
@@ -309,7 +317,7 @@ struct ChainArgs {
     Counters* counters;
     RowTask* fast_tasks;
     RowTask* slow_tasks;
-    int32_t* row_done;
+    RowSync* row_sync;
     RowInfo* info;
     ReqState* req;
     ResampleJob* jobs;
