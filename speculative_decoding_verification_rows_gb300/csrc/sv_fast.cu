@@ -274,15 +274,12 @@ __device__ __noinline__ unsigned long long merge_buffer(unsigned long long list,
     return merge_desc(list, sort_desc(b, n));
 }
 
-// The distribution of fast task t from its parts' lists (one warp; s_e is 32
-// doubles of the warp's shared memory).  Out of line: it runs once per row.
-__device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, const Partial* parts, int t,
-                                          Split sp, double* s_e)
+// The distribution of fast task t from its parts' lists (one warp).  Out of
+// line: it runs once per row.
+__device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, const Partial* parts, int t, Split sp)
 {
     const int lane = threadIdx.x & 31;
     const RowTask task = tasks[t];
-    RowInfo* info = infos + task.slot;
-    const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
     const long long g0 = (long long)t * sp.nc;
     const long long w0 = split_owner(sp, g0), w1 = split_owner(sp, g0 + sp.nc - 1);
     unsigned long long acc = 0ull;
@@ -302,8 +299,11 @@ __device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, 
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc = merge_desc(acc, lane < (int)cnt[j] ? key[j] : 0ull);
+        for (int j = 0; j < 4; ++j)
+            if (wb + j <= w1) acc = merge_desc(acc, lane < (int)cnt[j] ? key[j] : 0ull);
     }
+    RowInfo* info = infos + task.slot;
+    const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
     const unsigned long long ck = lane < k ? acc : 0ull;
     const int n_top = __popc(__ballot_sync(0xFFFFFFFFu, ck != 0ull));
     const float lv = ckey_value(ck);
@@ -346,33 +346,26 @@ __device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, 
         }
         return;
     }
-    // Sampling row: masses of the kept values in fp64, in sorted order.
-    const double e = lane < n_top ? exp(((double)lv - (double)m) / (double)T) : 0.0;
-    s_e[lane] = e;
-    __syncwarp();
-    int kept = n_top;
-    double z = 0.0;
-    if (lane == 0) {
-        double z1 = 0.0;
-        for (int i = 0; i < n_top; ++i) z1 += s_e[i];
-        if (task.top_p < 1.0f) {
-            const double target = (double)task.top_p * z1;
-            double cum = 0.0;
-            for (int i = 0; i < n_top; ++i) {
-                cum += s_e[i];
-                if (cum >= target) {
-                    kept = i + 1;
-                    break;
-                }
-            }
-        }
-        for (int i = 0; i < kept; ++i) z += s_e[i];
+    // Sampling row: masses of the kept values in fp64, in sorted order, and
+    // their running sums (a warp scan): the top-p prefix is the first one
+    // whose running sum reaches top_p times the top-k mass.
+    const double inv_t = 1.0 / (double)T;
+    const double e = lane < n_top ? exp(((double)lv - (double)m) * inv_t) : 0.0;
+    double cum = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+        if (lane >= o) cum += y;
     }
-    kept = __shfl_sync(0xFFFFFFFFu, kept, 0);
-    z = __shfl_sync(0xFFFFFFFFu, z, 0);
-    __syncwarp();   // s_e is the warp's candidate space again after this
+    int kept = n_top;
+    if (task.top_p < 1.0f) {
+        const double target = (double)task.top_p * __shfl_sync(0xFFFFFFFFu, cum, 31);
+        const unsigned reach = __ballot_sync(0xFFFFFFFFu, lane < n_top && cum >= target);
+        if (reach) kept = __ffs(reach);
+    }
+    const double z = __shfl_sync(0xFFFFFFFFu, cum, kept - 1);
     const bool in = lane < kept;
-    const double p = in ? e / z : 0.0;
+    const double p = in ? e * (1.0 / z) : 0.0;
     const float cut = __shfl_sync(0xFFFFFFFFu, lv, kept - 1);
     const int ties = __popc(__ballot_sync(0xFFFFFFFFu, in && lv == cut));
     int rank = 0;
@@ -384,7 +377,7 @@ __device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, 
     const unsigned hit = __ballot_sync(0xFFFFFFFFu, in && li == task.token);
     const double ptok = hit ? __shfl_sync(0xFFFFFFFFu, p, __ffs(hit) - 1) : 0.0;
     if (lane == 0) {
-        info->desc.log_norm = (float)log(z);
+        info->desc.log_norm = logf((float)z);   // z is in [1, 32]: fp32 is exact enough for a float output
         info->desc.cutoff_logit = cut;
         info->desc.cutoff_ties = ties;
         info->desc.kept = kept;
@@ -404,7 +397,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     constexpr unsigned FULL = 0xFFFFFFFFu;
     extern __shared__ __align__(128) unsigned char ring[];   // warps x kStages x 4 KB
     __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
-    __shared__ unsigned long long s_buf[kCtaWarps][kBufCap]; // candidate buffer, then finalisation
+    __shared__ unsigned long long s_buf[kCtaWarps][kBufCap]; // candidate buffer of each warp
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
@@ -420,14 +413,26 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     unsigned char* wring = ring + (size_t)warp * (kStages * kWarpChunkBytes);
     unsigned long long* buf = s_buf[warp];
 
-    // Producer (lane 0): the next unit to copy, its row and its ring stage.
-    long long p_g = lo;
-    int p_t = (int)(lo / sp.nc);
-    int p_c = (int)(lo - (long long)p_t * sp.nc);
-    int p_slot = 0;
+    // The range's parts: part j is row t_lo + j, chunks [part_c0(j),
+    // part_c1(j)).  Odd warps take their parts last to first (chunks still in
+    // order within a part): a row split between an even warp and the odd one
+    // after it is then the first part of both or the last part of both, so
+    // only every other split row finishes at the end of the ranges.
+    const int t_lo = (int)(lo / sp.nc);
+    const int np = (int)((hi - 1) / sp.nc) - t_lo + 1;
+    const bool rev = (w & 1) != 0;
+    auto part_c0 = [&](int j) { return (int)(max(lo, (long long)(t_lo + j) * sp.nc) - (long long)(t_lo + j) * sp.nc); };
+    auto part_c1 = [&](int j) {
+        return (int)(min(hi, (long long)(t_lo + j + 1) * sp.nc) - (long long)(t_lo + j) * sp.nc);
+    };
+
+    // Producer (lane 0): the part and chunk to copy next, the row, the stage.
+    int p_i = 0, p_j = rev ? np - 1 : 0;
+    int p_c = part_c0(p_j), p_c1 = part_c1(p_j);
+    int p_slot = 0, p_n = 0;   // p_n: copies issued
     const char* p_row = nullptr;
     auto produce = [&]() {
-        if (p_g >= hi) return;
+        if (p_i >= np) return;
         const int c0 = p_c * CHUNK;
         const uint32_t bytes = chunk_bytes<DT>(p_row, c0, a.vocab);
         unsigned long long* b = &bar[p_slot];
@@ -438,33 +443,33 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             mbar_arrive(b);
         }
         if (++p_slot == kStages) p_slot = 0;
-        ++p_g;
-        if (++p_c == sp.nc) {
-            p_c = 0;
-            ++p_t;
-            if (p_g < hi) p_row = task_row<DT>(a, a.fast_tasks[p_t]);
+        ++p_n;
+        if (++p_c == p_c1 && ++p_i < np) {
+            p_j = rev ? np - 1 - p_i : p_i;
+            p_c = part_c0(p_j);
+            p_c1 = part_c1(p_j);
+            p_row = task_row<DT>(a, a.fast_tasks[t_lo + p_j]);
         }
     };
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1u);
         mbar_fence_init();
-        p_row = task_row<DT>(a, a.fast_tasks[p_t]);
+        p_row = task_row<DT>(a, a.fast_tasks[t_lo + p_j]);
         for (int s = 0; s < kStages; ++s) produce();
     }
     __syncwarp();
 
-    int c_slot = 0;
+    int c_slot = 0, c_n = 0;   // c_n: chunks consumed
     uint32_t c_phase = 0u;
-    long long g = lo;
-    int t = (int)(lo / sp.nc);
-    int c = (int)(lo - (long long)t * sp.nc);
-    while (g < hi) {
+    for (int i = 0; i < np; ++i) {
         // One row part: chunks [c, c_end) of task t.  The part's top k live in
         // `list` (lane i: i-th best composite key, 0 = empty).
+        const int j = rev ? np - 1 - i : i;
+        const int t = t_lo + j;
+        const int c = part_c0(j), c_end = part_c1(j);
         const RowTask task = a.fast_tasks[t];
         const char* row = task_row<DT>(a, task);
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
-        const int c_end = (int)min((long long)sp.nc, (long long)c + (hi - g));
         unsigned long long list = 0ull;
         int nb = 0;   // keys in the warp's buffer
         int strict = 0, bad = 0;
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                     atomicOr(&a.counters->timeout, 1);
                     int s = c_slot;
                     uint32_t ph = c_phase;
-                    for (long long q = g + (cc - c); q < p_g; ++q) {
+                    for (int q = c_n; q < p_n; ++q) {
                         mbar_wait(&bar[s], ph);
                         if (++s == kStages) {
                             s = 0;
@@ -625,6 +630,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
                 c_slot = 0;
                 c_phase ^= 1u;
             }
+            ++c_n;
         }
 
         // The part's list (and its bound), then the row's counter; the last
@@ -653,11 +659,8 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         }
         if (__shfl_sync(FULL, last, 0)) {
             __threadfence();
-            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, reinterpret_cast<double*>(buf));
+            finalize_row(a.fast_tasks, a.info, a.partials, t, sp);
         }
-        g += c_end - c;
-        ++t;
-        c = 0;
     }
 }
 
