@@ -81,6 +81,7 @@ __device__ void block_scan2(int a, int b, int* ea, int* eb, int* ta, int* tb, in
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
 {
+    pdl_enter();
     __shared__ int s_wa[32], s_wb[32];
     __shared__ int s_tot_a, s_tot_b;
     int base_fast = 0, base_slow = 0;
@@ -230,6 +231,7 @@ constexpr int kChainWarps = 8;
 // from them in fp64, in index order.
 __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
 {
+    pdl_enter();
     __shared__ double s_w[kChainWarps][kFastK];
     __shared__ int s_i[kChainWarps][kFastK];
     __shared__ double s_qp[kChainWarps][kFastK];
@@ -422,6 +424,7 @@ __device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_ra
 
 __global__ void __launch_bounds__(kResampleThreads, 1) resample_kernel(ChainArgs a)
 {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ResampleSmem& sm = *reinterpret_cast<ResampleSmem*>(smem_raw);
     if ((int)blockIdx.x >= a.counters->n_jobs) return;
@@ -706,6 +709,7 @@ __global__ void __launch_bounds__(kResampleThreads, 1) resample_kernel(ChainArgs
 // ----------------------------------------------------------------------------
 __global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t* desc)
 {
+    pdl_enter();
     const int rows = a.n_req;
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
         const RowInfo& I = a.info[r];
@@ -722,6 +726,7 @@ __global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t
 // per row, tiles of blockDim elements in index order for the tie ranks.
 __global__ void __launch_bounds__(1024) dense_kernel(ChainArgs a, float* dense)
 {
+    pdl_enter();
     __shared__ int s_w[32];
     const int row = blockIdx.x;
     const RowInfo& I = a.info[row];
@@ -769,15 +774,13 @@ __global__ void __launch_bounds__(1024) dense_kernel(ChainArgs a, float* dense)
 
 cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s)
 {
-    prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s)
 {
     const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
-    chain_kernel<<<grid, kChainWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(chain_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
 }
 
 cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
@@ -791,8 +794,7 @@ cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < 128) attr_set[dev] = 1;
     }
-    resample_kernel<<<a.n_req, kResampleThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(resample_kernel, dim3(a.n_req), dim3(kResampleThreads), smem, s, a);
 }
 
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
@@ -800,11 +802,9 @@ cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_des
 {
     int grid = (a.n_req + 255) / 256;
     if (grid < 1) grid = 1;
-    rows_out_kernel<<<grid, 256, 0, s>>>(a, prob_of_token, desc);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(rows_out_kernel, dim3(grid), dim3(256), 0, s, a, prob_of_token, desc);
     if (err != cudaSuccess || !dense) return err;
-    dense_kernel<<<a.n_req, 1024, 0, s>>>(a, dense);
-    return cudaGetLastError();
+    return launch_pdl(dense_kernel, dim3(a.n_req), dim3(1024), 0, s, a, dense);
 }
 
 }  // namespace sv

@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
     __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
     __shared__ unsigned long long s_buf[kCtaWarps][kBufCap]; // candidate buffer of each warp
 
+    pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_tasks = a.counters->n_fast;
     Split sp;
@@ -685,8 +686,7 @@ cudaError_t launch_fast_rows_t(const RowsArgs& a, cudaStream_t s)
     }
     int grid = a.num_sms * nb;
     if (grid > kMaxRowWarps / kCtaWarps) grid = kMaxRowWarps / kCtaWarps;
-    fast_rows_kernel<DT><<<grid, kFastThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(fast_rows_kernel<DT>, dim3(grid), dim3(kFastThreads), smem, s, a);
 }
 
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s)

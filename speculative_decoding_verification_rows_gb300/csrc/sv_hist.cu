@@ -526,6 +526,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
 
 __global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(RowsArgs a, int slice)
 {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     HistSmem& sm = *reinterpret_cast<HistSmem*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
@@ -567,13 +568,14 @@ cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s)
     cfg.blockDim = dim3(kHistThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     err = cudaLaunchKernelEx(&cfg, hist_rows_kernel, a, slice);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();

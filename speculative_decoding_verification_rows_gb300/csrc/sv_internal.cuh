@@ -273,6 +273,42 @@ __device__ __forceinline__ float load_logit(const void* row, int64_t i)
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// the programmatic-serialisation attribute, so it may become resident while the
+// kernel before it on the stream drains.  It first waits for that kernel to
+// complete (its memory included), then lets its own dependent launch early.
+// Without a programmatic predecessor the wait returns at once.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline void pdl_attr(cudaLaunchAttribute& at)
+{
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+}
+
+// Launch with the attribute above (plus `extra` attributes, if any).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    pdl_attr(at[0]);
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
 // Launchers (host), one per kernel family.
 // ----------------------------------------------------------------------------
 struct RowsArgs {

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
                                                              int K, int budget, int32_t* verify_lens, int32_t* qo,
                                                              int32_t* total, int32_t* status, unsigned long long* keys)
 {
+    pdl_enter();
     __shared__ uint32_t hist[256];
     __shared__ int s_digit, s_kk, s_any_bad;
     __shared__ long long s_ncand;
@@ -170,9 +171,8 @@ cudaError_t launch_plan(const float* conf, int ld, const int32_t* draft_len, int
                         int32_t* verify_lens, int32_t* qo_indptr, int32_t* total, int32_t* status,
                         unsigned long long* keys, cudaStream_t s)
 {
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(conf, ld, draft_len, n, K, budget, verify_lens, qo_indptr, total, status,
-                                           keys);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, conf, ld, draft_len, n, K, budget, verify_lens,
+                      qo_indptr, total, status, keys);
 }
 
 }  // namespace sv
