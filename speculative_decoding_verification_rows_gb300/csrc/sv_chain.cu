@@ -79,21 +79,31 @@ __device__ void block_scan2(int a, int b, int* ea, int* eb, int* ta, int* tb, in
     __syncthreads();
 }
 
+// Per-unit results of the prep kernel's first phase, for its second.
+struct PrepUnit {
+    int req, k_eff, v, start, pos, n_rows, flags;   // flags: 1 fast, 2 greedy
+    float T, tp;
+};
+
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
 {
     pdl_enter();
     __shared__ int s_wa[32], s_wb[32];
     __shared__ int s_tot_a, s_tot_b;
+    __shared__ PrepUnit s_u[kPrepThreads];
+    __shared__ unsigned long long s_tokbad[kPrepThreads];
     int base_fast = 0, base_slow = 0;
     const int n_units = a.n_req;   // requests, or rows for the plain row layout
     const int K = a.K;
+    const int W2 = a.layout == 2 ? 1 : 2 * K + 1;   // row slots per unit
     for (int u0 = 0; u0 < n_units; u0 += kPrepThreads) {
+        // Phase 1, one thread per unit: parameters, window, row counts.
         const int u = u0 + threadIdx.x;
         const bool active = u < n_units;
         int nf = 0, ns = 0;
         int err = 0, v = 0, greedy = 0, k_eff = 1, req = u, start = 0;
-        uint64_t tok_bad = 0ull;
         float T = 0.0f, tp = 1.0f;
+        bool fast = true;
         if (active) {
             if (a.layout == 2) req = a.row_to_req ? a.row_to_req[u] : u;
             const bool req_ok = req >= 0 && req < a.n_params;
@@ -103,7 +113,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             if (!req_ok || bad_params(T, tp)) err |= kBadParam;
             greedy = T == 0.0f;
             k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
-            const bool fast = greedy || k_eff <= kFastK;
+            fast = greedy || k_eff <= kFastK;
             if (!err && !fast && a.dtype != 0) err |= kUnsupported;
             if (a.layout == 0) {
                 v = a.verify_len ? a.verify_len[u] : K;
@@ -114,22 +124,18 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 start = u * (K + 1);
             } else if (a.layout == 1) {
                 v = a.verify_len[u];
-                const long long s = a.qo_indptr[u], e = a.qo_indptr[u + 1];
-                if (v < 0 || v > K || s < 0 || e - s != (long long)v + 1 || e > (long long)a.bucket) {
+                const long long s0 = a.qo_indptr[u], e = a.qo_indptr[u + 1];
+                if (v < 0 || v > K || s0 < 0 || e - s0 != (long long)v + 1 || e > (long long)a.bucket) {
                     err |= kBadLayout;
                     v = 0;
                 }
-                start = (int)s;
+                start = (int)s0;
             }
             if (a.layout != 2 && !greedy && v > 0 && !a.drf) err |= kBadParam;   // q needs draft logits
             if (a.layout != 2) {
                 // one request-level error: a bad window first, then bad parameters
                 if (err & kBadLayout) err = kBadLayout;
                 else if (err & kBadParam) err = kBadParam;
-                for (int j = 0; j < v; ++j) {
-                    const int d = a.draft_tokens[(size_t)u * K + j];
-                    if (d < 0 || d >= a.vocab) tok_bad |= 1ull << j;
-                }
             }
             if (!err) {
                 const int n_rows = a.layout == 2 ? 1 : (v + 1) + (greedy ? 0 : v);
@@ -138,36 +144,64 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         }
         int off_f, off_s;
         block_scan2(nf, ns, &off_f, &off_s, &s_tot_a, &s_tot_b, s_wa, s_wb);
-        if (active) {
-            RowTask* list = nf ? a.fast_tasks : a.slow_tasks;
-            int pos = base_fast + off_f;
-            if (!nf) pos = base_slow + off_s;
-            const int n_rows = nf + ns;
-            for (int i = 0; i < n_rows; ++i) {
-                RowTask t;
-                t.req = req;
-                t.k_eff = k_eff;
-                t.temp = T;
-                t.top_p = tp;
-                t.pad = 0;
-                if (a.layout == 2) {
-                    t.row = u;
-                    t.slot = u;
-                    t.is_draft = 0;
-                    const int d = a.token_per_row ? a.token_per_row[u] : -1;
-                    t.token = (d >= 0 && d < a.vocab) ? d : -1;
-                } else {
-                    const bool draft_row = i > v;
-                    const int j = draft_row ? i - v - 1 : i;
-                    t.is_draft = draft_row;
-                    t.row = draft_row ? (int64_t)u * K + j : (int64_t)start + j;
-                    t.slot = draft_row ? slot_draft(u, K, j) : slot_target(u, K, j);
-                    const bool has_tok = j < v && !((tok_bad >> j) & 1);
-                    t.token = has_tok ? a.draft_tokens[(size_t)u * K + j] : -1;
+        PrepUnit pu;
+        pu.req = req;
+        pu.k_eff = k_eff;
+        pu.v = v;
+        pu.start = start;
+        pu.pos = nf ? base_fast + off_f : base_slow + off_s;
+        pu.n_rows = nf + ns;
+        pu.flags = (fast ? 1 : 0) | (greedy ? 2 : 0);
+        pu.T = T;
+        pu.tp = tp;
+        s_u[threadIdx.x] = pu;
+        s_tokbad[threadIdx.x] = 0ull;
+        __syncthreads();
+
+        // Phase 2, one thread per (unit, row slot): the row tasks, each with
+        // its own draft token (checked here; bad ones are collected per unit).
+        const int n_here = min(kPrepThreads, n_units - u0);
+        for (int idx = threadIdx.x; idx < n_here * W2; idx += kPrepThreads) {
+            const int ul = idx / W2, i = idx - ul * W2;
+            const PrepUnit q = s_u[ul];
+            if (i >= q.n_rows) continue;
+            const int uu = u0 + ul;
+            RowTask t;
+            t.req = q.req;
+            t.k_eff = q.k_eff;
+            t.temp = q.T;
+            t.top_p = q.tp;
+            t.pad = 0;
+            if (a.layout == 2) {
+                t.row = uu;
+                t.slot = uu;
+                t.is_draft = 0;
+                const int d = a.token_per_row ? a.token_per_row[uu] : -1;
+                t.token = (d >= 0 && d < a.vocab) ? d : -1;
+            } else {
+                const bool draft_row = i > q.v;
+                const int j = draft_row ? i - q.v - 1 : i;
+                t.is_draft = draft_row;
+                t.row = draft_row ? (int64_t)uu * K + j : (int64_t)q.start + j;
+                t.slot = draft_row ? slot_draft(uu, K, j) : slot_target(uu, K, j);
+                int tok = -1;
+                if (j < q.v) {
+                    const int d = a.draft_tokens[(size_t)uu * K + j];
+                    if (d >= 0 && d < a.vocab)
+                        tok = d;
+                    else if (!draft_row)
+                        atomicOr(&s_tokbad[ul], 1ull << j);
                 }
-                list[pos + i] = t;
-                if (nf) a.row_sync[pos + i] = RowSync{0, 0u};
+                t.token = tok;
             }
+            const bool is_fast = (q.flags & 1) != 0;
+            (is_fast ? a.fast_tasks : a.slow_tasks)[q.pos + i] = t;
+            if (is_fast) a.row_sync[q.pos + i] = RowSync{0, 0u};
+        }
+        __syncthreads();
+
+        // Phase 3, one thread per unit: the request state (or a row's error).
+        if (active) {
             if (a.layout == 2) {
                 if (err) {
                     RowInfo* info = a.info + u;
@@ -185,6 +219,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                     info->cut_count = 0;
                 }
             } else {
+                // bad draft tokens of a request that failed before its rows
+                // were listed are read here (its rows were not)
+                uint64_t tok_bad = s_tokbad[threadIdx.x];
+                if (err)
+                    for (int j = 0; j < v; ++j) {
+                        const int d = a.draft_tokens[(size_t)u * K + j];
+                        if (d < 0 || d >= a.vocab) tok_bad |= 1ull << j;
+                    }
                 ReqState st;
                 st.v = v;
                 st.greedy = greedy;
@@ -206,34 +248,30 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
     }
 }
 
-// Inverse CDF in index order over a listed distribution (fp64, sequential):
-// the smallest listed index whose cumulative weight exceeds u * W; if rounding
-// leaves none, the last one with positive weight.
-__device__ int invcdf_list(const int* idx, const double* w, int n, double u, double W)
-{
-    const double target = u * W;
-    double cum = 0.0;
-    int last = -1;
-    for (int i = 0; i < n; ++i) {
-        cum += w[i];
-        if (w[i] > 0.0) last = idx[i];
-        if (cum > target) return idx[i];
-    }
-    return last;
-}
-
 constexpr int kChainWarps = 8;
+
+// Inclusive warp scan (fp64) in lane order.
+__device__ __forceinline__ double warp_scan_f64(double x)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
 
 // One warp per request.  Every lane takes its own positions j (lane, lane + 32):
 // it loads the rows' results, draws u(r, j, 0) and decides acceptance; a ballot
 // gives the first rejection, which is where the sequential walk would stop.
-// The emitted token's kept lists are staged in shared memory and lane 0 draws
-// from them in fp64, in index order.
+// The emitted token is drawn from the kept lists (index order), one listed
+// token per lane: weights max(0, p_x - q_x) (q_x found by binary search in the
+// draft row's list) or p_x, a warp scan of the running sums, and the first
+// lane whose running sum exceeds u * W.
 __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
 {
     pdl_enter();
-    __shared__ double s_w[kChainWarps][kFastK];
-    __shared__ int s_i[kChainWarps][kFastK];
     __shared__ double s_qp[kChainWarps][kFastK];
     __shared__ int s_qi[kChainWarps][kFastK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -246,27 +284,36 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
     const int32_t* d = a.draft_tokens + (size_t)r * K;
 
     // position status (target row j, draft row j, token j) and, for j < v,
-    // the acceptance decision
+    // the acceptance decision; the rows' results are read before the
+    // request's state is known (every slot j <= K exists)
     const int timed_out = a.counters->timeout ? kTimeout : 0;
     int any_err = st.err | timed_out;
     unsigned long long rejects = 0ull, qzero = 0ull;
     for (int j = lane; j <= K; j += 32) {
+        const RowInfo& T = a.info[slot_target(r, K, j)];
+        const int t_status = T.desc.status, t_argmax = T.desc.argmax;
+        const double p = T.p_token;
+        int q_status = 0;
+        double q = 0.0;
+        if (j < K) {
+            const RowInfo& Q = a.info[slot_draft(r, K, j)];
+            q_status = Q.desc.status;
+            q = Q.p_token;
+        }
+        const int dj = j < K ? d[j] : -1;
         int ps = 0;
         if (!st.err && j <= v) {
-            const RowInfo& T = a.info[slot_target(r, K, j)];
-            ps |= T.desc.status;
+            ps |= t_status;
             if (j < v && ((st.tok_bad >> j) & 1)) ps |= kBadToken;
             if (j < v) {
                 bool accept;
                 if (st.greedy) {
-                    accept = d[j] == T.desc.argmax;
+                    accept = dj == t_argmax;
                 } else {
-                    const RowInfo& Q = a.info[slot_draft(r, K, j)];
-                    ps |= Q.desc.status;
-                    const double p = T.p_token, q = Q.p_token;
+                    ps |= q_status;
                     const double u = uniform_f64(a.seed, (uint32_t)r, (uint32_t)j, 0u);
                     if (q > 0.0) {
-                        accept = u < p / q;
+                        accept = u * q < p;   // u < p / q without the division
                     } else {
                         qzero |= 1ull << j;
                         accept = p > 0.0;
@@ -309,41 +356,43 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
         const RowInfo* Qp = residual ? &a.info[slot_draft(r, K, acc_len)] : nullptr;
         const int nq = residual ? Qp->n_list : 0;
         if (np >= 0 && nq >= 0) {
-            if (lane < np) {
-                s_i[warp][lane] = P.list_idx[lane];
-                s_w[warp][lane] = P.list_p[lane];
-            }
-            if (residual && lane < nq) {
-                s_qi[warp][lane] = Qp->list_idx[lane];
-                s_qp[warp][lane] = Qp->list_p[lane];
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const double u1 = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u);
-                double W = 0.0;
-                if (residual) {
-                    // w_x = max(0, p_x - q_x) over p's kept tokens (index order)
-                    double wl[kFastK];
-                    int qi = 0;
-                    for (int i = 0; i < np; ++i) {
-                        const int x = s_i[warp][i];
-                        while (qi < nq && s_qi[warp][qi] < x) ++qi;
-                        const double qx = (qi < nq && s_qi[warp][qi] == x) ? s_qp[warp][qi] : 0.0;
-                        const double w = s_w[warp][i] - qx;
-                        wl[i] = w > 0.0 ? w : 0.0;
-                        W += wl[i];
-                    }
-                    if (W > 0.0) {
-                        for (int i = 0; i < np; ++i) s_w[warp][i] = wl[i];
-                    } else {
-                        extra_bits = kResidZero;   // empty residual: draw from p itself
-                        W = 0.0;
-                        for (int i = 0; i < np; ++i) W += s_w[warp][i];
-                    }
-                } else {
-                    for (int i = 0; i < np; ++i) W += s_w[warp][i];
+            const bool in = lane < np;
+            const int x = in ? P.list_idx[lane] : 0;
+            const double px = in ? P.list_p[lane] : 0.0;
+            double w = px;
+            if (residual) {
+                if (lane < nq) {
+                    s_qi[warp][lane] = Qp->list_idx[lane];
+                    s_qp[warp][lane] = Qp->list_p[lane];
                 }
-                t = invcdf_list(s_i[warp], s_w[warp], np, u1, W);
+                __syncwarp();
+                double qx = 0.0;
+                if (in) {   // first q position with index >= x
+                    int lo = 0, hi = nq;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (s_qi[warp][mid] < x) lo = mid + 1; else hi = mid;
+                    }
+                    if (lo < nq && s_qi[warp][lo] == x) qx = s_qp[warp][lo];
+                }
+                const double rw = px - qx;
+                w = (in && rw > 0.0) ? rw : 0.0;
+            }
+            double cum = warp_scan_f64(w);
+            double W = __shfl_sync(0xFFFFFFFFu, cum, 31);
+            if (residual && !(W > 0.0)) {   // empty residual: draw from p itself
+                extra_bits = kResidZero;
+                w = px;
+                cum = warp_scan_f64(w);
+                W = __shfl_sync(0xFFFFFFFFu, cum, 31);
+            }
+            const double target = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u) * W;
+            const unsigned over = __ballot_sync(0xFFFFFFFFu, in && cum > target);
+            if (over) {
+                t = __shfl_sync(0xFFFFFFFFu, x, __ffs(over) - 1);
+            } else {   // rounding left none: the last token with positive weight
+                const unsigned pos = __ballot_sync(0xFFFFFFFFu, in && w > 0.0);
+                t = pos ? __shfl_sync(0xFFFFFFFFu, x, 31 - __clz(pos)) : -1;
             }
         } else if (lane == 0) {
             // kept set too large to list: the resample kernel draws the token
