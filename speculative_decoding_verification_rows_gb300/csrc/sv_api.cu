@@ -36,6 +36,16 @@ T* at(void* ws, size_t off)
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// The three arrays of a task list carved at `off` (each 16-byte aligned).
+TaskList task_list(void* ws, size_t off, int n)
+{
+    TaskList L;
+    L.row = at<int64_t>(ws, off);
+    L.meta = at<int4>(ws, off + sizeof(int64_t) * (size_t)n + (n & 1 ? 8 : 0));
+    L.samp = reinterpret_cast<float4*>(L.meta + n);
+    return L;
+}
+
 sv_status_t to_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;   // sv_set_timing_events
@@ -73,8 +83,8 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ra.stride_d = stride_d;
     ra.vocab = vocab;
     ra.dtype = dtype;
-    ra.fast_tasks = at<RowTask>(ws, L.fast_tasks);
-    ra.slow_tasks = at<RowTask>(ws, L.slow_tasks);
+    ra.fast_tasks = task_list(ws, L.fast_tasks, L.max_tasks);
+    ra.slow_tasks = task_list(ws, L.slow_tasks, L.max_tasks);
     ra.counters = at<Counters>(ws, L.counters);
     ra.info = at<RowInfo>(ws, L.info);
     ra.partials = at<Partial>(ws, L.partials);

@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             t.k_eff = q.k_eff;
             t.temp = q.T;
             t.top_p = q.tp;
-            t.pad = 0;
             if (a.layout == 2) {
                 t.row = uu;
                 t.slot = uu;
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 t.token = tok;
             }
             const bool is_fast = (q.flags & 1) != 0;
-            (is_fast ? a.fast_tasks : a.slow_tasks)[q.pos + i] = t;
+            (is_fast ? a.fast_tasks : a.slow_tasks).put(q.pos + i, t);
             if (is_fast) a.row_sync[q.pos + i] = RowSync{0, 0u};
         }
         __syncthreads();

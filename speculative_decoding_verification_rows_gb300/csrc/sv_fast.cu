@@ -276,10 +276,10 @@ __device__ __noinline__ unsigned long long merge_buffer(unsigned long long list,
 
 // The distribution of fast task t from its parts' lists (one warp).  Out of
 // line: it runs once per row.
-__device__ __noinline__ void finalize_row(const RowTask* tasks, RowInfo* infos, const Partial* parts, int t, Split sp)
+__device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const Partial* parts, int t, Split sp)
 {
     const int lane = threadIdx.x & 31;
-    const RowTask task = tasks[t];
+    const RowTask task = tasks.get(t);
     const long long g0 = (long long)t * sp.nc;
     const long long w0 = split_owner(sp, g0), w1 = split_owner(sp, g0 + sp.nc - 1);
     unsigned long long acc = 0ull;
@@ -449,13 +449,13 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
             p_j = rev ? np - 1 - p_i : p_i;
             p_c = part_c0(p_j);
             p_c1 = part_c1(p_j);
-            p_row = task_row<DT>(a, a.fast_tasks[t_lo + p_j]);
+            p_row = task_row<DT>(a, a.fast_tasks.get(t_lo + p_j));
         }
     };
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1u);
         mbar_fence_init();
-        p_row = task_row<DT>(a, a.fast_tasks[t_lo + p_j]);
+        p_row = task_row<DT>(a, a.fast_tasks.get(t_lo + p_j));
         for (int s = 0; s < kStages; ++s) produce();
     }
     __syncwarp();
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
         const int j = rev ? np - 1 - i : i;
         const int t = t_lo + j;
         const int c = part_c0(j), c_end = part_c1(j);
-        const RowTask task = a.fast_tasks[t];
+        const RowTask task = a.fast_tasks.get(t);
         const char* row = task_row<DT>(a, task);
         const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
         unsigned long long list = 0ull;

@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(RowsArgs a, 
     const int n_clusters = gridDim.x / C;
     const int n_tasks = a.counters->n_slow;
     for (int t = cluster_id; t < n_tasks; t += n_clusters) {
-        const RowTask task = a.slow_tasks[t];
+        const RowTask task = a.slow_tasks.get(t);
         hist_row(cluster, sm, a, task, C, rank, slice);
     }
 }

@@ -46,8 +46,39 @@ struct RowTask {
     float temp;       // 0 = greedy
     float top_p;      // >= 1 = top-p off
     int32_t is_draft; // 1: row of the draft logits
-    int32_t pad;
 };
+
+// A list of row tasks, stored as three arrays (row index; slot, request,
+// token, k; temperature, top-p, draft flag) so that the tasks of consecutive
+// threads are written with whole-sector vector stores.
+struct TaskList {
+    int64_t* row;
+    int4* meta;
+    float4* samp;
+
+    __device__ __forceinline__ RowTask get(int64_t t) const
+    {
+        RowTask r;
+        r.row = row[t];
+        const int4 m = meta[t];
+        const float4 f = samp[t];
+        r.slot = m.x;
+        r.req = m.y;
+        r.token = m.z;
+        r.k_eff = m.w;
+        r.temp = f.x;
+        r.top_p = f.y;
+        r.is_draft = __float_as_int(f.z);
+        return r;
+    }
+    __device__ __forceinline__ void put(int64_t t, const RowTask& r) const
+    {
+        row[t] = r.row;
+        meta[t] = make_int4(r.slot, r.req, r.token, r.k_eff);
+        samp[t] = make_float4(r.temp, r.top_p, __int_as_float(r.is_draft), 0.0f);
+    }
+};
+constexpr size_t kTaskBytes = sizeof(int64_t) + sizeof(int4) + sizeof(float4);
 
 // Result of one row (its distribution, enough to sample from it).
 struct RowInfo {
@@ -124,8 +155,8 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.n_partials = (size_t)L.max_tasks + 3 * (size_t)kMaxRowWarps;
     size_t off = 0;
     L.counters = off;   off = align256(off + sizeof(Counters));
-    L.fast_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
-    L.slow_tasks = off; off = align256(off + sizeof(RowTask) * (size_t)L.max_tasks);
+    L.fast_tasks = off; off = align256(off + kTaskBytes * (size_t)L.max_tasks + 16);   // + alignment of the arrays
+    L.slow_tasks = off; off = align256(off + kTaskBytes * (size_t)L.max_tasks + 16);
     L.info = off;       off = align256(off + sizeof(RowInfo) * (size_t)L.slots);
     L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
@@ -317,8 +348,8 @@ struct RowsArgs {
     int64_t stride_t, stride_d;
     int vocab;
     int dtype;
-    RowTask* fast_tasks;
-    RowTask* slow_tasks;
+    TaskList fast_tasks;
+    TaskList slow_tasks;
     Counters* counters;
     RowInfo* info;
     Partial* partials;
@@ -351,8 +382,8 @@ struct ChainArgs {
     int32_t* num_emitted;
     int32_t* row_status;
     Counters* counters;
-    RowTask* fast_tasks;
-    RowTask* slow_tasks;
+    TaskList fast_tasks;
+    TaskList slow_tasks;
     RowSync* row_sync;
     RowInfo* info;
     ReqState* req;
