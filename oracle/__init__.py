@@ -89,6 +89,10 @@ def lib():
         _lib.orc_plan_budget.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, P, P, P, P]
         _lib.orc_plan_budget.restype = ctypes.c_int
+        _lib.orc_choose_budget.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+                                           ctypes.c_float, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P]
+        _lib.orc_choose_budget.restype = ctypes.c_int
+        _lib.orc_verify_stats.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, P]
     return _lib
 
 
@@ -194,3 +198,37 @@ def plan_budget(conf, budget: int, bucket: int, draft_len=None):
     if rc != 0:
         raise ValueError("invalid planner arguments")
     return vl, qo, int(tot[0]), int(st[0])
+
+
+def choose_budget(conf, cost_tokens, cost_ms, bucket: int, fixed_overhead_ms: float = 0.0,
+                  batch_sizes=None, batch_overhead_ms=None, draft_len=None):
+    """Budget from a step-cost table: returns (budget, theta_best, margin, status)."""
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    n, K = c.shape
+    dl = None if draft_len is None else np.ascontiguousarray(draft_len, dtype=np.int32)
+    ct = np.ascontiguousarray(cost_tokens if cost_tokens is not None else [], dtype=np.int32)
+    cm = np.ascontiguousarray(cost_ms if cost_ms is not None else [], dtype=np.float32)
+    bs = np.ascontiguousarray(batch_sizes if batch_sizes is not None else [], dtype=np.int32)
+    bo = np.ascontiguousarray(batch_overhead_ms if batch_overhead_ms is not None else [], dtype=np.float32)
+    if len(ct) != len(cm) or len(bs) != len(bo):
+        raise ValueError("table arrays differ in length")
+    b = np.zeros(1, np.int32)
+    th = np.zeros(1, np.float64)
+    mg = np.zeros(1, np.float64)
+    st = np.zeros(1, np.int32)
+    rc = lib().orc_choose_budget(_ptr(c), K, _ptr(dl), n, K, _ptr(ct), _ptr(cm), len(ct), fixed_overhead_ms,
+                                 _ptr(bs), _ptr(bo), len(bs), bucket, _ptr(b), _ptr(th), _ptr(mg), _ptr(st))
+    if rc != 0:
+        raise ValueError("invalid budget arguments")
+    return int(b[0]), float(th[0]), float(mg[0]), int(st[0])
+
+
+def verify_stats(accept_len, num_emitted, verify_lens, K: int, draft_len=None):
+    """(tokens emitted, tokens submitted, requests trimmed, trimmed requests that accepted their whole window)."""
+    al = np.ascontiguousarray(accept_len, dtype=np.int32)
+    ne = np.ascontiguousarray(num_emitted, dtype=np.int32)
+    vl = None if verify_lens is None else np.ascontiguousarray(verify_lens, dtype=np.int32)
+    dl = None if draft_len is None else np.ascontiguousarray(draft_len, dtype=np.int32)
+    out = np.zeros(4, np.int64)
+    lib().orc_verify_stats(_ptr(al), _ptr(ne), _ptr(vl), _ptr(dl), len(al), K, _ptr(out))
+    return tuple(int(x) for x in out)

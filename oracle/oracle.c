@@ -45,7 +45,10 @@
  *   2 top-p keeps the prefix before the crossing token
  *   3 argmax keeps the last occurrence of the maximum
  *   4 planner tie-break by request before position
- *   5 resample reuses the acceptance draw (draw 0)                          */
+ *   5 resample reuses the acceptance draw (draw 0)
+ *   6 cost table looked up by drafted tokens only (the bonus row left out)
+ *   7 budget by first descent of tau / cost instead of the global argmax
+ *   8 trim regret counts requests that stopped inside their window         */
 #ifndef ORC_PLANT
 #define ORC_PLANT 0
 #endif
@@ -550,4 +553,148 @@ int orc_plan_budget(const float* conf, int ld, const int32_t* draft_len, int n, 
     *total = qo_indptr[n];
     free(cand);
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* NEXT-1: verify budget from a profiled step-cost table.                    */
+/* ------------------------------------------------------------------------- */
+/*
+ * NVIDIA/TensorRT-LLM PR #17056, description "What is here / Planner": the
+ * budget is the argmax of tau / cost over a profiled step-cost table, a global
+ * argmax because the cost curve is a staircase and Theta = tau / T is not
+ * unimodal on it; without a profiled table the planner does not trim.  Review
+ * commit, section "Cost model": the table is indexed by tokens submitted to the
+ * target, bs * (verify_len + 1), the bonus token included; a fixed per-step
+ * overhead and an optional batch-size staircase of overheads are added (they
+ * do not cancel in the ratio).
+ *
+ * Readings (restated in the design doc):
+ *  - tau(B) = expected tokens a step that submits B tokens emits: n (one
+ *    anchor / bonus token per request) plus the survivals s_{r,i} of the
+ *    B - n candidates the planner selects, i.e. the B - n largest survivals
+ *    (ties in s do not change the sum).  Survivals as in orc_plan_budget.
+ *  - A step submitting B tokens runs on the first shelf j with
+ *    cost_tokens[j] >= B (shelves ascending) and costs cost_ms[j]; B above the
+ *    last shelf is not available.
+ *  - The batch overhead of n requests is batch_overhead_ms of the first entry
+ *    with batch_sizes >= n, or of the last entry when n exceeds them all.
+ *  - Candidates: B = n .. B_max, B_max = n + min(sum K_r, bucket - n).
+ *    Theta(B) = tau(B) / (cost(B) + fixed_overhead_ms + batch overhead); the
+ *    largest Theta wins; among equal Theta the larger B (same throughput,
+ *    more tokens per step).
+ *  - No table, or no shelf that holds B = n: B = B_max (no trimming), status
+ *    bit 2.  Status bit 1: a draft length outside [0, K] was clamped.
+ *  - *margin = (Theta_best - Theta_second) / Theta_best over candidates with
+ *    distinct Theta (1 when there is only one): how close the choice was.
+ */
+static int cmp_desc_float(const void* a, const void* b)
+{
+    const float x = *(const float*)a, y = *(const float*)b;
+    return x > y ? -1 : (x < y ? 1 : 0);
+}
+
+int orc_choose_budget(const float* conf, int ld, const int32_t* draft_len, int n, int K,
+                      const int32_t* cost_tokens, const float* cost_ms, int n_cost, float fixed_overhead_ms,
+                      const int32_t* batch_sizes, const float* batch_overhead_ms, int n_batch, int bucket,
+                      int32_t* budget, double* theta_best, double* margin, int32_t* status)
+{
+    if (n <= 0 || K < 0 || ld < K || bucket < n || n_cost < 0 || n_batch < 0) return -1;
+    *status = 0;
+    float* sv = (float*)malloc((size_t)n * (size_t)(K > 0 ? K : 1) * sizeof(float));
+    int64_t nc = 0;
+    for (int r = 0; r < n; ++r) {
+        int kr = draft_len ? draft_len[r] : K;
+        if (kr < 0 || kr > K) {
+            *status |= 1;
+            kr = kr < 0 ? 0 : K;
+        }
+        float s = 1.0f;
+        for (int i = 0; i < kr; ++i) {
+            float c = conf[(size_t)r * (size_t)ld + (size_t)i];
+            if (isnan(c)) c = 0.0f;
+            if (c < 0.0f) c = 0.0f;
+            if (c > 1.0f) c = 1.0f;
+            volatile float prod = s * c;
+            s = prod;
+            sv[nc++] = s;
+        }
+    }
+    qsort(sv, (size_t)nc, sizeof(float), cmp_desc_float);
+    int64_t m_max = nc < (int64_t)(bucket - n) ? nc : (int64_t)(bucket - n);
+    const int64_t b_max = n + m_max;
+    /* tau for every B: prefix sums of the sorted survivals, sequential */
+    double* tau = (double*)malloc((size_t)(m_max + 1) * sizeof(double));
+    tau[0] = (double)n;
+    for (int64_t m = 1; m <= m_max; ++m) tau[m] = tau[m - 1] + (double)sv[m - 1];
+    double batch_oh = 0.0;
+    if (n_batch > 0) {
+        int j = 0;
+        while (j < n_batch - 1 && batch_sizes[j] < n) ++j;
+        batch_oh = (double)batch_overhead_ms[j];
+    }
+    double best = -1.0, second = -1.0;
+    int64_t best_b = -1;
+    int shelf = 0;
+    for (int64_t b = n; b <= b_max && n_cost > 0; ++b) {
+#if ORC_PLANT == 6
+        const int64_t looked_up = b - n;
+#else
+        const int64_t looked_up = b;
+#endif
+        while (shelf < n_cost && cost_tokens[shelf] < looked_up) ++shelf;
+        if (shelf == n_cost) break;   /* above the last shelf */
+        const double th = tau[b - n] / ((double)cost_ms[shelf] + (double)fixed_overhead_ms + batch_oh);
+#if ORC_PLANT == 7
+        if (best_b >= 0 && th < best) break;   /* first descent */
+#endif
+        if (th >= best) {
+            if (th > best) second = best;
+            best = th;
+            best_b = b;
+        } else if (th > second) {
+            second = th;
+        }
+    }
+    if (best_b < 0) {
+        *status |= 2;
+        best_b = b_max;
+        best = tau[m_max];
+        second = -1.0;
+    }
+    *budget = (int32_t)best_b;
+    *theta_best = best;
+    *margin = (second < 0.0 || best <= 0.0) ? 1.0 : (best - second) / best;
+    free(tau);
+    free(sv);
+    return 0;
+}
+
+/*
+ * Acceptance against trimming (NVIDIA/TensorRT-LLM PR #17056, the commit that
+ * adds trim_regret_rate): per step, tokens emitted sum(accept_len + 1), tokens
+ * submitted sum(v_r + 1), requests trimmed (v_r < K_r), and trimmed requests
+ * that accepted their whole window (accept_len == v_r: still alive at the
+ * cut, so the cut cost acceptance).  Requests with an error (accept_len < 0
+ * or num_emitted == 0) count in none of them.  out[4] as listed.
+ */
+void orc_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, const int32_t* verify_lens,
+                      const int32_t* draft_len, int n, int K, int64_t* out)
+{
+    out[0] = out[1] = out[2] = out[3] = 0;
+    for (int r = 0; r < n; ++r) {
+        if (num_emitted[r] == 0 || accept_len[r] < 0) continue;
+        int kr = draft_len ? draft_len[r] : K;
+        kr = kr < 0 ? 0 : (kr > K ? K : kr);
+        const int v = verify_lens ? verify_lens[r] : kr;
+        out[0] += accept_len[r] + 1;
+        out[1] += v + 1;
+        if (v < kr) {
+            out[2] += 1;
+#if ORC_PLANT == 8
+            if (accept_len[r] < v) out[3] += 1;
+#else
+            if (accept_len[r] == v) out[3] += 1;
+#endif
+        }
+    }
 }
