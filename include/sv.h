@@ -213,6 +213,65 @@ sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits
                              int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * Verify budget from a profiled step-cost table, then the plan for it
+ * ([P4] description, "What is here / Planner": the budget is the argmax of
+ * tau / cost over a profiled step-cost table, a global argmax because the cost
+ * curve is a staircase; review commit, "Cost model": the table is indexed by
+ * tokens submitted, bs * (verify_len + 1), and carries a fixed per-step
+ * overhead and an optional batch-size staircase).  Everything stays on the
+ * device: the chosen budget feeds the planner without a host readback.
+ *   conf, ld_conf, draft_len, n_req, K: as sv_plan_budget.
+ *   cost_tokens (device) int32 [n_cost], strictly ascending: shelf j holds
+ *               steps that submit up to cost_tokens[j] tokens ...
+ *   cost_ms     (device) fp32 [n_cost]: ... and such a step costs cost_ms[j].
+ *   fixed_overhead_ms: per-step cost that does not depend on the budget.
+ *   batch_sizes (device) int32 [n_batch] ascending, batch_overhead_ms (device)
+ *               fp32 [n_batch]: the overhead of a batch of n_req requests is
+ *               that of the first entry with batch_sizes >= n_req (the last
+ *               entry above them all).  n_batch may be 0 (pointers NULL).
+ *   tau(B) = n_req + the sum of the B - n_req largest survivals (the expected
+ *   tokens a step that submits B tokens emits); cost(B) = cost_ms of the first
+ *   shelf with cost_tokens >= B, plus the fixed and batch overheads.  The
+ *   budget B in [n_req, n_req + min(sum K_r, bucket_tokens - n_req)] with the
+ *   largest tau(B) / cost(B) is chosen, the larger B on ties.  n_cost == 0 or
+ *   no shelf that holds n_req tokens: no trimming (the largest B), bit 2 of
+ *   *budget_status; a table that is not strictly ascending or has a negative
+ *   or non-finite cost or overhead: no trimming, bit 4; bit 1: a draft
+ *   length was clamped.
+ *   Outputs budget_out [1] (device, the chosen budget), budget_status [1]
+ *   (device, may be NULL), and the plan for that budget exactly as
+ *   sv_plan_budget writes it.  Workspace: sv_workspace_size(n_req, K, 0).
+ *   Errors: SV_ERR_INVALID_ARG for the sv_plan_budget argument errors (with
+ *   bucket_tokens < n_req in place of the budget checks), a NULL budget_out or
+ *   a NULL table array of nonzero length; SV_ERR_UNSUPPORTED for n_req * K >
+ *   16384 candidates or more than 4096 shelves or batch entries.
+ */
+sv_status_t sv_plan_budget_cost(const float* conf, int ld_conf, const int32_t* draft_len, int n_req, int K,
+                                const int32_t* cost_tokens, const float* cost_ms, int n_cost, float fixed_overhead_ms,
+                                const int32_t* batch_sizes, const float* batch_overhead_ms, int n_batch,
+                                int bucket_tokens, int32_t* budget_out, int32_t* budget_status, int32_t* verify_lens,
+                                int32_t* qo_indptr, int32_t* total_tokens, int32_t* status, void* ws, size_t ws_bytes,
+                                sv_stream_t stream);
+
+/*
+ * Acceptance against trimming for one verify step ([P4], the commit that
+ * adds trim_regret_rate): a trimmed request (verify_lens[r] < K_r) that
+ * accepted its whole window was still alive at the cut, so the cut cost
+ * acceptance; one that stopped inside its window lost nothing.
+ *   accept_len, num_emitted (device) [n_req]: a verify call's outputs;
+ *   requests with num_emitted == 0 (errors) are not counted.
+ *   verify_lens (device) [n_req] or NULL (every window K_r: nothing trimmed).
+ *   draft_len   (device) [n_req] or NULL (= K); clamped to [0, K].
+ *   out (device) int64 [4]: tokens emitted sum(accept_len + 1), tokens
+ *   submitted sum(verify_lens + 1), requests trimmed, trimmed requests that
+ *   accepted their whole window.
+ *   Errors: SV_ERR_INVALID_ARG if n_req < 1, K < 0, or a required pointer is
+ *   NULL.
+ */
+sv_status_t sv_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, const int32_t* verify_lens,
+                            const int32_t* draft_len, int n_req, int K, int64_t* out, sv_stream_t stream);
+
+/*
  * sv_verify_chain without a workspace argument.  The pages have no
  * counterpart: this is for callers that cannot allocate device memory where
  * they verify -- code running while a CUDA graph is captured (cudaMalloc is

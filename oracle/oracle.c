@@ -583,7 +583,9 @@ int orc_plan_budget(const float* conf, int ld, const int32_t* draft_len, int n, 
  *    largest Theta wins; among equal Theta the larger B (same throughput,
  *    more tokens per step).
  *  - No table, or no shelf that holds B = n: B = B_max (no trimming), status
- *    bit 2.  Status bit 1: a draft length outside [0, K] was clamped.
+ *    bit 2.  A table whose shelves are not strictly ascending, or with a cost
+ *    or overhead that is negative or not finite: B = B_max, status bit 4.
+ *    Status bit 1: a draft length outside [0, K] was clamped.
  *  - *margin = (Theta_best - Theta_second) / Theta_best over candidates with
  *    distinct Theta (1 when there is only one): how close the choice was.
  */
@@ -632,10 +634,17 @@ int orc_choose_budget(const float* conf, int ld, const int32_t* draft_len, int n
         while (j < n_batch - 1 && batch_sizes[j] < n) ++j;
         batch_oh = (double)batch_overhead_ms[j];
     }
+    int table_ok = isfinite(fixed_overhead_ms) && fixed_overhead_ms >= 0.0f && isfinite(batch_oh) && batch_oh >= 0.0;
+    for (int j = 0; j < n_cost; ++j)
+        if (!(isfinite(cost_ms[j]) && cost_ms[j] >= 0.0f) || (j > 0 && cost_tokens[j] <= cost_tokens[j - 1]))
+            table_ok = 0;
+    for (int j = 0; j < n_batch; ++j)
+        if (!(isfinite(batch_overhead_ms[j]) && batch_overhead_ms[j] >= 0.0f)) table_ok = 0;
+    if (!table_ok) *status |= 4;
     double best = -1.0, second = -1.0;
     int64_t best_b = -1;
     int shelf = 0;
-    for (int64_t b = n; b <= b_max && n_cost > 0; ++b) {
+    for (int64_t b = n; b <= b_max && n_cost > 0 && table_ok; ++b) {
 #if ORC_PLANT == 6
         const int64_t looked_up = b - n;
 #else
@@ -656,7 +665,7 @@ int orc_choose_budget(const float* conf, int ld, const int32_t* draft_len, int n
         }
     }
     if (best_b < 0) {
-        *status |= 2;
+        if (table_ok) *status |= 2;
         best_b = b_max;
         best = tau[m_max];
         second = -1.0;

@@ -188,8 +188,41 @@ sv_status_t sv_plan_budget(const float* conf, int ld_conf, const int32_t* draft_
     const size_t need = sv_workspace_size(n_req, K, 0);
     if (need == 0) return SV_ERR_UNSUPPORTED;
     if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
-    return to_status(launch_plan(conf, ld_conf, draft_len, n_req, K, budget_tokens, verify_lens, qo_indptr,
+    return to_status(launch_plan(conf, ld_conf, draft_len, n_req, K, budget_tokens, nullptr, verify_lens, qo_indptr,
                                  total_tokens, status, static_cast<unsigned long long*>(ws), stream));
+}
+
+sv_status_t sv_plan_budget_cost(const float* conf, int ld_conf, const int32_t* draft_len, int n_req, int K,
+                                const int32_t* cost_tokens, const float* cost_ms, int n_cost, float fixed_overhead_ms,
+                                const int32_t* batch_sizes, const float* batch_overhead_ms, int n_batch,
+                                int bucket_tokens, int32_t* budget_out, int32_t* budget_status, int32_t* verify_lens,
+                                int32_t* qo_indptr, int32_t* total_tokens, int32_t* status, void* ws, size_t ws_bytes,
+                                sv_stream_t stream)
+{
+    if (n_req < 1 || K < 0 || ld_conf < K || bucket_tokens < n_req || n_cost < 0 || n_batch < 0)
+        return SV_ERR_INVALID_ARG;
+    if ((K > 0 && !conf) || !verify_lens || !qo_indptr || !total_tokens || !budget_out) return SV_ERR_INVALID_ARG;
+    if ((n_cost > 0 && (!cost_tokens || !cost_ms)) || (n_batch > 0 && (!batch_sizes || !batch_overhead_ms)))
+        return SV_ERR_INVALID_ARG;
+    if ((long long)n_req * K > kBudgetMaxCand || n_cost > kBudgetMaxShelves || n_batch > kBudgetMaxShelves)
+        return SV_ERR_UNSUPPORTED;
+    const size_t need = sv_workspace_size(n_req, K, 0);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    cudaError_t e = launch_budget(conf, ld_conf, draft_len, n_req, K, cost_tokens, cost_ms, n_cost, fixed_overhead_ms,
+                                  batch_sizes, batch_overhead_ms, n_batch, bucket_tokens, budget_out, budget_status,
+                                  stream);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    return to_status(launch_plan(conf, ld_conf, draft_len, n_req, K, 0, budget_out, verify_lens, qo_indptr,
+                                 total_tokens, status, static_cast<unsigned long long*>(ws), stream));
+}
+
+sv_status_t sv_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, const int32_t* verify_lens,
+                            const int32_t* draft_len, int n_req, int K, int64_t* out, sv_stream_t stream)
+{
+    if (n_req < 1 || K < 0 || !accept_len || !num_emitted || !out) return SV_ERR_INVALID_ARG;
+    return to_status(launch_stats(accept_len, num_emitted, verify_lens, draft_len, n_req, K,
+                                  reinterpret_cast<long long*>(out), stream));
 }
 
 sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row_stride, int rows, int vocab,

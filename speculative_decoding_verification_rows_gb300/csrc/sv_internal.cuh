@@ -398,8 +398,17 @@ cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_des
                             cudaStream_t s);
 
 cudaError_t launch_plan(const float* conf, int ld, const int32_t* draft_len, int n, int K, int budget,
-                        int32_t* verify_lens, int32_t* qo_indptr, int32_t* total, int32_t* status,
-                        unsigned long long* keys, cudaStream_t s);
+                        const int32_t* budget_dev, int32_t* verify_lens, int32_t* qo_indptr, int32_t* total,
+                        int32_t* status, unsigned long long* keys, cudaStream_t s);
+
+constexpr int kBudgetMaxCand = 16384;   // candidates (n * K) the budget choice sorts in shared memory
+constexpr int kBudgetMaxShelves = 4096; // shelves and batch-overhead entries of a cost table
+cudaError_t launch_budget(const float* conf, int ld, const int32_t* draft_len, int n, int K, const int32_t* cost_tokens,
+                          const float* cost_ms, int n_cost, float fixed_ms, const int32_t* batch_sizes,
+                          const float* batch_ms, int n_batch, int bucket, int32_t* budget_out, int32_t* budget_status,
+                          cudaStream_t s);
+cudaError_t launch_stats(const int32_t* accept_len, const int32_t* num_emitted, const int32_t* verify_lens,
+                         const int32_t* draft_len, int n, int K, long long* out, cudaStream_t s);
 
 int device_sm_count();
 

@@ -24,7 +24,8 @@ ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | RO
                   | ROW_TIMEOUT)
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
-            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc")
+            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc",
+            "sv_plan_budget_cost", "sv_verify_stats")
 
 
 class SVError(RuntimeError):
@@ -73,6 +74,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_verify_ragged.restype = I
     L.sv_verify_chain_noalloc.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P]
     L.sv_verify_chain_noalloc.restype = I
+    L.sv_plan_budget_cost.argtypes = [P, I, P, I, I, P, P, I, ctypes.c_float, P, P, I, I, P, P, P, P, P, P, P, SZ, P]
+    L.sv_plan_budget_cost.restype = I
+    L.sv_verify_stats.argtypes = [P, P, P, P, I, I, P, P]
+    L.sv_verify_stats.restype = I
     L.sv_set_timing_events.argtypes = [P, P]
     L.sv_set_timing_events.restype = I
     _lib = L
@@ -172,6 +177,52 @@ def plan_budget(conf: torch.Tensor, budget: int, bucket: int, draft_len: Optiona
     _check(load().sv_plan_budget(_ptr(conf), K, _ptr(draft_len), n, K, budget, bucket, _ptr(vl), _ptr(qo),
                                  _ptr(tot), _ptr(st), _ptr(w), w.numel(), _stream(dev)))
     return vl, qo, tot, st
+
+
+def plan_budget_cost(conf: torch.Tensor, cost_tokens: Optional[torch.Tensor], cost_ms: Optional[torch.Tensor],
+                     bucket: int, fixed_overhead_ms: float = 0.0, batch_sizes: Optional[torch.Tensor] = None,
+                     batch_overhead_ms: Optional[torch.Tensor] = None, draft_len: Optional[torch.Tensor] = None,
+                     ws: Optional[Workspace] = None):
+    """sv_plan_budget_cost: (budget [1], budget_status [1], verify_lens [n], qo_indptr [n+1], total [1],
+    status [1]) on the device; the table arrays are device tensors (int32 tokens, fp32 ms) or None."""
+    conf = _dev(conf, torch.float32)
+    n, K = conf.shape
+    dev = conf.device
+    ct = None if cost_tokens is None else _dev(cost_tokens, torch.int32)
+    cm = None if cost_ms is None else _dev(cost_ms, torch.float32)
+    bs = None if batch_sizes is None else _dev(batch_sizes, torch.int32)
+    bo = None if batch_overhead_ms is None else _dev(batch_overhead_ms, torch.float32)
+    n_cost = 0 if ct is None else ct.numel()
+    n_batch = 0 if bs is None else bs.numel()
+    if (cm is None and n_cost) or (cm is not None and cm.numel() != n_cost):
+        raise SVError("cost_tokens and cost_ms differ in length")
+    if (bo is None and n_batch) or (bo is not None and bo.numel() != n_batch):
+        raise SVError("batch_sizes and batch_overhead_ms differ in length")
+    b = torch.empty(1, dtype=torch.int32, device=dev)
+    bst = torch.empty(1, dtype=torch.int32, device=dev)
+    vl = torch.empty(n, dtype=torch.int32, device=dev)
+    qo = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    tot = torch.empty(1, dtype=torch.int32, device=dev)
+    st = torch.empty(1, dtype=torch.int32, device=dev)
+    w = _ws(ws, dev, workspace_size(n, K, 0))
+    _check(load().sv_plan_budget_cost(_ptr(conf), K, _ptr(draft_len), n, K, _ptr(ct), _ptr(cm), n_cost,
+                                      float(fixed_overhead_ms), _ptr(bs), _ptr(bo), n_batch, bucket, _ptr(b),
+                                      _ptr(bst), _ptr(vl), _ptr(qo), _ptr(tot), _ptr(st), _ptr(w), w.numel(),
+                                      _stream(dev)))
+    return b, bst, vl, qo, tot, st
+
+
+def verify_stats(accept_len: torch.Tensor, num_emitted: torch.Tensor, verify_lens: Optional[torch.Tensor], K: int,
+                 draft_len: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """sv_verify_stats: int64 [4] on the device (tokens emitted, tokens submitted, requests trimmed,
+    trimmed requests that accepted their whole window)."""
+    accept_len = _dev(accept_len, torch.int32)
+    num_emitted = _dev(num_emitted, torch.int32)
+    dev = accept_len.device
+    out = torch.empty(4, dtype=torch.int64, device=dev)
+    _check(load().sv_verify_stats(_ptr(accept_len), _ptr(num_emitted), _ptr(verify_lens), _ptr(draft_len),
+                                  accept_len.numel(), K, _ptr(out), _stream(dev)))
+    return out
 
 
 def build_target_probs(logits: torch.Tensor, temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,

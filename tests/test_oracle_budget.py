@@ -108,6 +108,17 @@ def test_no_table_or_flat_table_does_not_trim():
     assert B == 20
 
 
+def test_bad_tables_do_not_trim():
+    conf = np.full((4, 3), 0.7, np.float32)
+    full = 4 + 4 * 3
+    for toks, costs, kw in [([8, 8, 16], [1.0, 1.2, 2.0], {}), ([8, 4], [1.0, 2.0], {}),
+                            ([8, 16], [1.0, float("nan")], {}), ([8, 16], [-1.0, 2.0], {}),
+                            ([8, 16], [1.0, 2.0], {"fixed_overhead_ms": float("inf")}),
+                            ([8, 16], [1.0, 2.0], {"batch_sizes": [4], "batch_overhead_ms": [-0.5]})]:
+        B, _, _, st = oracle.choose_budget(conf, toks, costs, bucket=64, **kw)
+        assert B == full and st == 4, (toks, costs, kw)
+
+
 def test_fixed_overheads_move_the_choice_and_scaling_does_not():
     n, K, c = 8, 6, 0.8
     toks, costs = _shelves(n, K, lambda m: 1.0 + 0.5 * m)
