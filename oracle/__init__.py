@@ -83,6 +83,8 @@ def lib():
         _lib.orc_row_transform.restype = ctypes.c_int
         _lib.orc_verify_chain.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                           P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P]
+        _lib.orc_verify_block.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P]
         _lib.orc_verify_ragged.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                            ctypes.c_int64, P, P, P, P, P, P, ctypes.c_uint64, ctypes.c_int,
                                            P, P, P, P, P, P, P]
@@ -140,9 +142,11 @@ def _verify_outputs(n, width):
 
 
 def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=None, verify_len=None, seed=0,
-                 first_req=0):
+                 first_req=0, block=False):
     """Uniform layout: target [n, K+1, V], draft [n, K, V] (None if all greedy).
-    The requests are requests first_req.. of a larger batch (uniform keys)."""
+    The requests are requests first_req.. of a larger batch (uniform keys).
+    block=True runs block verification (joint block acceptance) instead of
+    the token-by-token chain."""
     target, dt = _logits(target)
     n, k1, V = target.shape
     K = k1 - 1
@@ -155,10 +159,10 @@ def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=Non
     tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
     vl = None if verify_len is None else np.ascontiguousarray(verify_len, dtype=np.int32)
     o = _verify_outputs(n, K + 1)
-    lib().orc_verify_chain(_ptr(target), _ptr(draft), dt, n, K, V, _ptr(tok), _ptr(vl), _ptr(T), _ptr(tk),
-                           _ptr(tp), seed, first_req, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
-                           _ptr(o["num_emitted"]), _ptr(o["pos_status"]), _ptr(o["flags"]),
-                           _ptr(o["p_tok"]), _ptr(o["q_tok"]))
+    fn = lib().orc_verify_block if block else lib().orc_verify_chain
+    fn(_ptr(target), _ptr(draft), dt, n, K, V, _ptr(tok), _ptr(vl), _ptr(T), _ptr(tk), _ptr(tp), seed, first_req,
+       _ptr(o["accept_len"]), _ptr(o["out_tokens"]), _ptr(o["num_emitted"]), _ptr(o["pos_status"]),
+       _ptr(o["flags"]), _ptr(o["p_tok"]), _ptr(o["q_tok"]))
     return o
 
 

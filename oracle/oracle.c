@@ -48,7 +48,8 @@
  *   5 resample reuses the acceptance draw (draw 0)
  *   6 cost table looked up by drafted tokens only (the bonus row left out)
  *   7 budget by first descent of tau / cost instead of the global argmax
- *   8 trim regret counts requests that stopped inside their window         */
+ *   8 trim regret counts requests that stopped inside their window
+ *   9 block verification: residual and stopping masses without the weight  */
 #ifndef ORC_PLANT
 #define ORC_PLANT 0
 #endif
@@ -295,13 +296,107 @@ static int64_t inv_cdf(const double* w, int64_t n, double u, double* margin)
 }
 
 /*
+ * Block verification (local-inference-lab/rtx6kpro dspark-upstream-
+ * consolidation.md: rejection_sample_method "block", joint block acceptance
+ * with residual-mass reweighting).  The pages name the method and measure
+ * it; the steps are those of the published algorithm (Sun, Mendlovic,
+ * Leviathan, Aharoni, Beirami, Ro, Suresh, "Block Verification Accelerates
+ * Speculative Decoding", 2024), in this file's notation:
+ *   w_0 = 1,  w_j = min(w_{j-1} * p_{j-1}(d_{j-1}) / q_{j-1}(d_{j-1}), 1)  (j = 1..v)
+ *   H_j = sum_x max(w_j p_j(x) - q_j(x), 0),  h_j = H_j / (H_j + 1 - w_j)  (j < v)
+ *   h_v = w_v;  accept length a = the largest j with eta_j < h_j (a >= 0)
+ *   eta_j = u(r, j - 1, 0) (the acceptance draw of draft j - 1)
+ *   next token: inverse CDF (index order, u(r, a, 1)) of max(w_a p_a - q_a, 0)
+ *   when a < v, of p_v when a = v.
+ * Readings: q(d) == 0 gives the ratio +inf when p(d) > 0 and 0 otherwise
+ * (SV_ROW_Q_ZERO), a zero weight stays zero; a zero denominator gives h = 1;
+ * eta_j < h_j is strict so that v = 1 is exactly the chain's test u < p / q;
+ * an empty residual falls back to p_a (SV_ROW_RESID_ZERO).  Flags: an
+ * |eta_j - h_j| below the ratio margin at a decided j, the residual and
+ * inverse-CDF margins as in the chain.
+ */
+static int block_accept(double* const* P, double* const* Q, const int32_t* d, int v, int64_t vocab, uint64_t seed,
+                        uint32_t req, int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok, int64_t* tok)
+{
+    double* wgt = (double*)malloc((size_t)(v + 1) * sizeof(double));
+    double* h = (double*)malloc((size_t)(v + 1) * sizeof(double));
+    wgt[0] = 1.0;
+    for (int j = 1; j <= v; ++j) {
+        const double p = P[j - 1][d[j - 1]], q = Q[j - 1][d[j - 1]];
+        p_tok[j - 1] = p;
+        q_tok[j - 1] = q;
+        double r;
+        if (q > 0.0) {
+            r = p / q;
+        } else {
+            pos_status[j - 1] |= ORC_Q_ZERO;
+            r = p > 0.0 ? INFINITY : 0.0;
+        }
+        const double x = wgt[j - 1] > 0.0 ? wgt[j - 1] * r : 0.0;
+        wgt[j] = x < 1.0 ? x : 1.0;
+    }
+    for (int j = 0; j < v; ++j) {
+#if ORC_PLANT == 9
+        const double wj = 1.0;
+#else
+        const double wj = wgt[j];
+#endif
+        double H = 0.0;
+        for (int64_t x = 0; x < vocab; ++x) {
+            const double m = wj * P[j][x] - Q[j][x];
+            H += m > 0.0 ? m : 0.0;
+        }
+        const double den = H + 1.0 - wgt[j];
+        h[j] = den > 0.0 ? H / den : 1.0;
+    }
+    h[v] = wgt[v];
+    int a = 0;
+    for (int j = v; j >= 1; --j) {
+        const double eta = orc_uniform(seed, req, (uint32_t)(j - 1), 0u);
+        if (fabs(eta - h[j]) < RATIO_MARGIN) *flags |= ORC_FLAG_RATIO;
+        if (eta < h[j]) {
+            a = j;
+            break;
+        }
+    }
+    double* w = (double*)malloc((size_t)vocab * sizeof(double));
+    if (a < v) {
+#if ORC_PLANT == 9
+        const double wa = 1.0;
+#else
+        const double wa = wgt[a];
+#endif
+        double W = 0.0;
+        for (int64_t x = 0; x < vocab; ++x) {
+            const double m = wa * P[a][x] - Q[a][x];
+            w[x] = m > 0.0 ? m : 0.0;
+            W += w[x];
+        }
+        if (W < RESID_MIN) *flags |= ORC_FLAG_RESID;
+        if (!(W > 0.0)) {
+            pos_status[a] |= ORC_RESID_ZERO;
+            for (int64_t x = 0; x < vocab; ++x) w[x] = P[a][x];
+        }
+    } else {
+        for (int64_t x = 0; x < vocab; ++x) w[x] = P[a][x];
+    }
+    double margin;
+    *tok = inv_cdf(w, vocab, orc_uniform(seed, req, (uint32_t)a, 1u), &margin);
+    if (margin < INVCDF_MARGIN) *flags |= ORC_FLAG_INVCDF;
+    free(w);
+    free(h);
+    free(wgt);
+    return a;
+}
+
+/*
  * One request's chain (C5, C6).  tgt_rows[j] (j <= v) and drf_rows[j]
  * (j < v) point at the logits rows of the window; d[j] are the drafts.
  * Outputs follow the library's layout: out_tokens has K+1 slots, -1 filled.
  */
 static void verify_request(const void* const* tgt_rows, const void* const* drf_rows, int dtype, int64_t vocab,
                            int v, int K, const int32_t* d, float T, int32_t top_k, float top_p,
-                           uint64_t seed, uint32_t req, int32_t layout_bad,
+                           uint64_t seed, uint32_t req, int32_t layout_bad, int block,
                            int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
                            int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
 {
@@ -349,6 +444,8 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
             for (int j = 0; j < v; ++j)
                 if (d[j] != tr[j].argmax) { a = j; break; }
             t = tr[a].argmax;
+        } else if (block) {
+            a = block_accept(P, Q, d, v, vocab, seed, req, pos_status, flags, p_tok, q_tok, &t);
         } else {
             for (int j = 0; j < v; ++j) {
                 double p = P[j][d[j]], q = Q[j][d[j]];
@@ -417,11 +514,11 @@ static const void* row_ptr(const void* base, int dtype, int64_t row, int64_t str
  * uniforms are keyed by that index).
  * p_tok / q_tok ([n, K+1]) receive p_j(d_j) and q_j(d_j) where tested.
  */
-void orc_verify_chain(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
-                      const int32_t* draft_tokens, const int32_t* verify_len,
-                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
-                      int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
-                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+static void verify_uniform(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
+                           const int32_t* draft_tokens, const int32_t* verify_len, const float* T,
+                           const int32_t* top_k, const float* top_p, uint64_t seed, int first_req, int block,
+                           int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted, int32_t* pos_status,
+                           int32_t* flags, double* p_tok, double* q_tok)
 {
     const void** tr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
     const void** dr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
@@ -434,13 +531,35 @@ void orc_verify_chain(const void* target, const void* draft, int dtype, int n, i
             dr[j] = (j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K + j, vocab) : NULL;
         }
         verify_request(tr, dr, dtype, vocab, v, K, draft_tokens + (size_t)r * K, T[r],
-                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad,
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad, block,
                        accept_len + r, out_tokens + (size_t)r * (K + 1), num_emitted + r,
                        pos_status + (size_t)r * (K + 1), flags + r,
                        p_tok + (size_t)r * (K + 1), q_tok + (size_t)r * (K + 1));
     }
     free(tr);
     free(dr);
+}
+
+void orc_verify_chain(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
+                      const int32_t* draft_tokens, const int32_t* verify_len,
+                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
+                      int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+{
+    verify_uniform(target, draft, dtype, n, K, vocab, draft_tokens, verify_len, T, top_k, top_p, seed, first_req, 0,
+                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok);
+}
+
+/* Block verification over the uniform layout (see block_accept); arguments
+ * and outputs as orc_verify_chain; greedy requests take the chain's rule. */
+void orc_verify_block(const void* target, const void* draft, int dtype, int n, int K, int64_t vocab,
+                      const int32_t* draft_tokens, const int32_t* verify_len,
+                      const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
+                      int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+{
+    verify_uniform(target, draft, dtype, n, K, vocab, draft_tokens, verify_len, T, top_k, top_p, seed, first_req, 1,
+                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok);
 }
 
 /*
@@ -470,7 +589,7 @@ void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, 
             dr[j] = (!bad && j < v && draft) ? row_ptr(draft, dtype, (int64_t)r * K_max + j, vocab) : NULL;
         }
         verify_request(tr, dr, dtype, vocab, v, K_max, draft_tokens + (size_t)r * K_max, T[r],
-                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad,
+                       top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad, 0,
                        accept_len + r, out_tokens + (size_t)r * (K_max + 1), num_emitted + r,
                        pos_status + (size_t)r * (K_max + 1), flags + r,
                        p_tok + (size_t)r * (K_max + 1), q_tok + (size_t)r * (K_max + 1));
