@@ -194,6 +194,33 @@ sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits,
                             int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * Block verification over the uniform layout (local-inference-lab/rtx6kpro
+ * dspark-upstream-consolidation.md: rejection_sample_method "block", joint
+ * block acceptance with residual-mass reweighting; the steps are those of
+ * Sun et al., "Block Verification Accelerates Speculative Decoding", 2024).
+ * Arguments, layouts, outputs and errors as sv_verify_chain.  Greedy
+ * requests take the chain's rule (the two agree at temperature 0).  For a
+ * sampling request with window v and drafts d_j (p_j, q_j its rows'
+ * distributions, u(r, j, k) its Philox uniforms):
+ *   w_0 = 1, w_j = min(w_{j-1} p_{j-1}(d_{j-1}) / q_{j-1}(d_{j-1}), 1);
+ *   H_j = sum_x max(w_j p_j(x) - q_j(x), 0), h_j = H_j / (H_j + 1 - w_j)
+ *   (1 when the denominator is 0) for j < v, h_v = w_v;
+ *   accept_len = the largest j in 1..v with u(r, j-1, 0) < h_j, else 0;
+ *   the emitted token after the accepted drafts is drawn by inverse CDF in
+ *   index order with u(r, accept_len, 1) from max(w_a p_a - q_a, 0) (a =
+ *   accept_len < v; an empty residual falls back to p_a with
+ *   SV_ROW_RESID_ZERO) or from p_v.  q(d) == 0 makes the ratio +inf if
+ *   p(d) > 0, else 0 (SV_ROW_Q_ZERO).  With v = 1 this is exactly
+ *   sv_verify_chain.  Needs every row of the window to have a listed kept set
+ *   (greedy or top-k <= 32); a sampling request with a larger kept set gets
+ *   SV_ROW_UNSUPPORTED and emits nothing.
+ */
+sv_status_t sv_verify_block(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                            int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                            uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                            int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
+
+/*
  * Verify in the ragged layout ([P4] "Ragged (per-request) verification",
  * `_rejection_buffers_valid`).  Request r's target rows are rows
  * qo_indptr[r] .. qo_indptr[r] + verify_lens[r] of target_logits (device,

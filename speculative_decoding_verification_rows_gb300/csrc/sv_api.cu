@@ -117,7 +117,7 @@ bool dtype_ok(sv_dtype_t dt) { return dt == SV_DTYPE_BF16 || dt == SV_DTYPE_F32;
 sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t dt, int n, int K, int V, int bucket,
                        const int32_t* qo, const int32_t* vl, const int32_t* toks, sv_sampling_t sp, uint64_t seed,
                        int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted, int32_t* row_status, void* ws,
-                       size_t ws_bytes, cudaStream_t s)
+                       size_t ws_bytes, cudaStream_t s, int block = 0)
 {
     if (!tgt || n < 1 || K < 0 || V < 1 || !sp.temperature || !accept_len || !out_tokens || !num_emitted)
         return SV_ERR_INVALID_ARG;
@@ -131,6 +131,7 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     Carved c = carve(ws, n, K, V, (int)dt, tgt, drf, V, V);
     ChainArgs& ca = c.ca;
     ca.layout = layout;
+    ca.block = block;
     ca.bucket = bucket;
     ca.qo_indptr = qo;
     ca.verify_len = vl;
@@ -258,6 +259,15 @@ sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits,
 {
     return run_verify(0, target_logits, draft_logits, dt, n_req, K, vocab, 0, nullptr, verify_len, draft_tokens, sp,
                       seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream);
+}
+
+sv_status_t sv_verify_block(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                            int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                            uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                            int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    return run_verify(0, target_logits, draft_logits, dt, n_req, K, vocab, 0, nullptr, verify_len, draft_tokens, sp,
+                      seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream, 1);
 }
 
 sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req,

@@ -419,6 +419,206 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
 }
 
 // ----------------------------------------------------------------------------
+// Block verification (local-inference-lab/rtx6kpro dspark-upstream-
+// consolidation.md, rejection_sample_method "block": joint block acceptance
+// with residual-mass reweighting; the steps of Sun et al., "Block Verification
+// Accelerates Speculative Decoding", 2024).  One warp per request, kept sets
+// listed (<= 32 tokens per row):
+//   w_0 = 1, w_j = min(w_{j-1} p_{j-1}(d_{j-1}) / q_{j-1}(d_{j-1}), 1)   (lane 0, in order)
+//   H_j = sum over p_j's kept tokens x of max(w_j p_j(x) - q_j(x), 0)   (a warp sum)
+//   h_j = H_j / (H_j + 1 - w_j) (1 if the denominator is 0), h_v = w_v
+//   accept length a = the largest j in 1..v with u(r, j-1, 0) < h_j, else 0
+//   next token: inverse CDF of max(w_a p_a - q_a, 0) (a < v) or p_v, u(r, a, 1).
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
+{
+    pdl_enter();
+    __shared__ double s_qp[kChainWarps][kFastK];
+    __shared__ int s_qi[kChainWarps][kFastK];
+    __shared__ double s_wgt[kChainWarps][kMaxK + 2];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * kChainWarps + warp;
+    if (r >= a.n_req) return;
+    const int K = a.K, width = K + 1;
+    const ReqState st = a.req[r];
+    const int v = st.v;
+    int32_t* out = a.out_tokens + (size_t)r * width;
+    const int32_t* d = a.draft_tokens + (size_t)r * K;
+    const int timed_out = a.counters->timeout ? kTimeout : 0;
+
+    // position status; every drafted position's ratio enters the weights
+    int any_err = st.err | timed_out;
+    unsigned long long qzero = 0ull, rejects = 0ull;
+    bool unlisted = false;
+    for (int j = lane; j <= K; j += 32) {
+        const RowInfo& T = a.info[slot_target(r, K, j)];
+        const int t_status = T.desc.status, t_argmax = T.desc.argmax, t_list = T.n_list;
+        const double p = T.p_token;
+        int q_status = 0, q_list = 0;
+        double q = 0.0;
+        if (j < K) {
+            const RowInfo& Q = a.info[slot_draft(r, K, j)];
+            q_status = Q.desc.status;
+            q = Q.p_token;
+            q_list = Q.n_list;
+        }
+        const int dj = j < K ? d[j] : -1;
+        int ps = 0;
+        if (!st.err && j <= v) {
+            ps |= t_status;
+            if (j < v && ((st.tok_bad >> j) & 1)) ps |= kBadToken;
+            if (st.greedy) {
+                if (j < v && dj != t_argmax) rejects |= 1ull << j;
+            } else {
+                if (t_list < 0) unlisted = true;
+                if (j < v) {
+                    ps |= q_status;
+                    if (q_list < 0) unlisted = true;
+                    if (!(q > 0.0)) qzero |= 1ull << j;
+                }
+            }
+        }
+        if (j == 0) ps |= st.err | timed_out;
+        any_err |= ps & kErrorMask;
+        if (a.row_status) a.row_status[(size_t)r * width + j] = ps;
+        out[j] = -1;
+    }
+    any_err = __reduce_or_sync(0xFFFFFFFFu, any_err);
+    unlisted = __any_sync(0xFFFFFFFFu, unlisted);
+    rejects |= ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)rejects)) |
+               ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(rejects >> 32)) << 32);
+    qzero |= ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)qzero)) |
+             ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(qzero >> 32)) << 32);
+    if (!any_err && !st.greedy && unlisted) {   // block mode needs listed kept sets
+        if (lane == 0 && a.row_status) a.row_status[(size_t)r * width] |= kUnsupported;
+        any_err = kUnsupported;
+    }
+    if (any_err) {
+        if (lane == 0) {
+            a.accept_len[r] = 0;
+            a.num_emitted[r] = 0;
+        }
+        return;
+    }
+
+    int acc_len, t = -1, extra_bits = 0;
+    if (st.greedy) {
+        acc_len = rejects ? (__ffsll((long long)rejects) - 1) : v;
+        t = a.info[slot_target(r, K, acc_len)].desc.argmax;
+    } else {
+        // weights, in order (lane 0)
+        if (lane == 0) {
+            double w = 1.0;
+            s_wgt[warp][0] = 1.0;
+            for (int j = 1; j <= v; ++j) {
+                const double p = a.info[slot_target(r, K, j - 1)].p_token;
+                const double q = a.info[slot_draft(r, K, j - 1)].p_token;
+                const double ratio = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
+                const double x = w > 0.0 ? w * ratio : 0.0;
+                w = x < 1.0 ? x : 1.0;
+                s_wgt[warp][j] = w;
+            }
+        }
+        __syncwarp();
+        // stopping probabilities for positions 1..v: one position at a time,
+        // a kept token of p_j per lane (q_j's list staged for a binary search)
+        unsigned long long stop = 0ull;
+        for (int j = 1; j <= v; ++j) {
+            const double wj = s_wgt[warp][j];
+            double h = wj;
+            if (j < v) {
+                const RowInfo& Pj = a.info[slot_target(r, K, j)];
+                const RowInfo& Qj = a.info[slot_draft(r, K, j)];
+                const int np = Pj.n_list, nq = Qj.n_list;
+                const bool in = lane < np;
+                const int x = in ? Pj.list_idx[lane] : 0;
+                const double px = in ? Pj.list_p[lane] : 0.0;
+                __syncwarp();
+                if (lane < nq) {
+                    s_qi[warp][lane] = Qj.list_idx[lane];
+                    s_qp[warp][lane] = Qj.list_p[lane];
+                }
+                __syncwarp();
+                double qx = 0.0;
+                if (in) {
+                    int lo = 0, hi = nq;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (s_qi[warp][mid] < x) lo = mid + 1; else hi = mid;
+                    }
+                    if (lo < nq && s_qi[warp][lo] == x) qx = s_qp[warp][lo];
+                }
+                const double m = in ? wj * px - qx : 0.0;
+                double H = m > 0.0 ? m : 0.0;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) H += __shfl_xor_sync(0xFFFFFFFFu, H, o);
+                const double den = H + 1.0 - wj;
+                h = den > 0.0 ? H / den : 1.0;
+            }
+            if (uniform_f64(a.seed, (uint32_t)r, (uint32_t)(j - 1), 0u) < h) stop |= 1ull << j;
+        }
+        acc_len = stop ? 63 - __clzll((long long)stop) : 0;
+        __syncwarp();
+
+        // the next token, one listed token per lane
+        const bool residual = acc_len < v;
+        const RowInfo& P = a.info[slot_target(r, K, acc_len)];
+        const int np = P.n_list;
+        const bool in = lane < np;
+        const int x = in ? P.list_idx[lane] : 0;
+        const double px = in ? P.list_p[lane] : 0.0;
+        double w = px;
+        if (residual) {
+            const RowInfo& Q = a.info[slot_draft(r, K, acc_len)];
+            const int nq = Q.n_list;
+            if (lane < nq) {
+                s_qi[warp][lane] = Q.list_idx[lane];
+                s_qp[warp][lane] = Q.list_p[lane];
+            }
+            __syncwarp();
+            double qx = 0.0;
+            if (in) {
+                int lo = 0, hi = nq;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_qi[warp][mid] < x) lo = mid + 1; else hi = mid;
+                }
+                if (lo < nq && s_qi[warp][lo] == x) qx = s_qp[warp][lo];
+            }
+            const double rw = s_wgt[warp][acc_len] * px - qx;
+            w = (in && rw > 0.0) ? rw : 0.0;
+        }
+        double cum = warp_scan_f64(w);
+        double W = __shfl_sync(0xFFFFFFFFu, cum, 31);
+        if (residual && !(W > 0.0)) {
+            extra_bits = kResidZero;
+            w = px;
+            cum = warp_scan_f64(w);
+            W = __shfl_sync(0xFFFFFFFFu, cum, 31);
+        }
+        const double target = uniform_f64(a.seed, (uint32_t)r, (uint32_t)acc_len, 1u) * W;
+        const unsigned over = __ballot_sync(0xFFFFFFFFu, in && cum > target);
+        if (over) {
+            t = __shfl_sync(0xFFFFFFFFu, x, __ffs(over) - 1);
+        } else {
+            const unsigned pos = __ballot_sync(0xFFFFFFFFu, in && w > 0.0);
+            t = pos ? __shfl_sync(0xFFFFFFFFu, x, 31 - __clz(pos)) : -1;
+        }
+    }
+    for (int j = lane; j < acc_len; j += 32) out[j] = d[j];
+    if (lane == 0) {
+        out[acc_len] = t;
+        a.accept_len[r] = acc_len;
+        a.num_emitted[r] = acc_len + 1;
+        if (a.row_status) {
+            for (int j = 0; j < v; ++j)
+                if ((qzero >> j) & 1) a.row_status[(size_t)r * width + j] |= kQZero;
+            if (extra_bits) a.row_status[(size_t)r * width + acc_len] |= extra_bits;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
 // Full-row resample with exact fixed-point weights.
 // ----------------------------------------------------------------------------
 constexpr int kTableEntries = kTableBinades * 128;
@@ -828,6 +1028,7 @@ cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s)
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s)
 {
     const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
+    if (a.block) return launch_pdl(block_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
     return launch_pdl(chain_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
 }
 

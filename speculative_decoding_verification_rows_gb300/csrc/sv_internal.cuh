@@ -366,6 +366,7 @@ struct ChainArgs {
     int n_params;          // length of the sampling-parameter arrays
     int vocab, dtype;
     int layout;            // 0 uniform, 1 ragged, 2 plain rows (build_target_probs)
+    int block;             // 1: block verification instead of the token-by-token chain
     const void* tgt;
     const void* drf;
     int64_t stride_t, stride_d;

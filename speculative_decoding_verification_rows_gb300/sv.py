@@ -25,7 +25,7 @@ ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | RO
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
             "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc",
-            "sv_plan_budget_cost", "sv_verify_stats")
+            "sv_plan_budget_cost", "sv_verify_stats", "sv_verify_block")
 
 
 class SVError(RuntimeError):
@@ -70,6 +70,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_build_target_probs.restype = I
     L.sv_verify_chain.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
     L.sv_verify_chain.restype = I
+    L.sv_verify_block.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
+    L.sv_verify_block.restype = I
     L.sv_verify_ragged.argtypes = [P, P, I, I, I, I, I, P, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
     L.sv_verify_ragged.restype = I
     L.sv_verify_chain_noalloc.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P]
@@ -266,8 +268,9 @@ def _outs(n, K, dev):
 def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
                  temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
                  top_p: Optional[torch.Tensor] = None, verify_len: Optional[torch.Tensor] = None, seed: int = 0,
-                 ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None) -> VerifyOut:
-    """sv_verify_chain: target [n, K+1, V], draft [n, K, V] (or None if all greedy)."""
+                 ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None, block: bool = False) -> VerifyOut:
+    """sv_verify_chain (or, with block=True, sv_verify_block): target [n, K+1, V], draft [n, K, V]
+    (or None if all greedy)."""
     target = _dev(target)
     n, k1, V = target.shape
     K = k1 - 1
@@ -277,10 +280,10 @@ def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_toke
         assert draft.shape == (n, K, V)
     o = out or _outs(n, K, dev)
     w = _ws(ws, dev, workspace_size(n, K, V))
-    _check(load().sv_verify_chain(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens),
-                                  _ptr(verify_len), _sampling(temperature, top_k, top_p), seed,
-                                  _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status),
-                                  _ptr(w), w.numel(), _stream(dev)))
+    fn = load().sv_verify_block if block else load().sv_verify_chain
+    _check(fn(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens), _ptr(verify_len),
+              _sampling(temperature, top_k, top_p), seed, _ptr(o.accept_len), _ptr(o.out_tokens),
+              _ptr(o.num_emitted), _ptr(o.row_status), _ptr(w), w.numel(), _stream(dev)))
     return o
 
 
