@@ -59,6 +59,10 @@ def parse():
     p.add_argument("--quick", action="store_true",
                    help="profiling runs: no settle loop, no end-to-end pass, no CPU baseline")
     p.add_argument("--requests", type=int, default=0, help="scale the batch to this many requests (profiling)")
+    p.add_argument("--method", choices=["chain", "block"], default="chain",
+                   help="token-by-token chain test, or block verification (uniform layout only)")
+    p.add_argument("--cost-table", action="store_true",
+                   help="ragged workload: choose the budget from a synthetic step-cost table on the device")
     return p.parse_args()
 
 
@@ -197,7 +201,17 @@ def algorithmic_bytes(w) -> tuple[int, int]:
     return (rows_t + rows_d) * w.V * esz, rows_t
 
 
-def make_step(w, sv, dev):
+def synthetic_cost_table(w, dev):
+    """A step-cost table shaped like profiled CUDA-graph buckets: shelves every
+    256 submitted tokens up to the bucket, cost rising with the tokens and a
+    jump at every 1024 (a larger graph), plus a fixed per-step overhead."""
+    toks = list(range(256, w.bucket + 1, 256))
+    costs = [1.0 + 0.0006 * t + 0.35 * (t // 1024) for t in toks]
+    return (torch.tensor(toks, dtype=torch.int32, device=dev), torch.tensor(costs, dtype=torch.float32, device=dev),
+            0.8)
+
+
+def make_step(w, sv, dev, method="chain", cost_table=False):
     """A closure running one verify step with preallocated outputs/workspace."""
     ws = sv.Workspace(dev)
     n, K = w.n, w.K
@@ -206,18 +220,30 @@ def make_step(w, sv, dev):
                        torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
                                                                                  device=dev))
     if w.layout == "chain":
+        block = method == "block"
+
         def step(tgt=w.target, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
-            return sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out)
+            return sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block)
         return step, out, None
+    if method != "chain":
+        raise SystemExit("block verification is built for the uniform layout only")
     # ragged: planner then verify over target rows packed by the plan
     from speculative_decoding_verification_rows_gb300 import workloads
     ws_p = sv.Workspace(dev)
-    vl, qo, tot, _ = sv.plan_budget(w.conf, w.budget, w.bucket, ws=ws_p)
+    table = synthetic_cost_table(w, dev) if cost_table else None
+
+    def plan():
+        if table is None:
+            return sv.plan_budget(w.conf, w.budget, w.bucket, ws=ws_p)
+        _, _, vl_, qo_, tot_, st_ = sv.plan_budget_cost(w.conf, table[0], table[1], w.bucket, table[2], ws=ws_p)
+        return vl_, qo_, tot_, st_
+
+    vl, qo, tot, _ = plan()
     packed = workloads.pack_rows(w.target, qo.cpu(), vl.cpu(), w.bucket)
-    extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()))
+    extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()), rows=int(tot), plan=plan, table=table)
 
     def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
-        vl_, qo_, _, _ = sv.plan_budget(w.conf, w.budget, w.bucket, ws=ws_p)
+        vl_, qo_, _, _ = plan()
         return sv.verify_ragged(tgt, drf, qo_, vl_, toks, T, tk, tp, seed=w.seed, ws=ws, out=out)
     return step, out, extra
 
@@ -230,10 +256,11 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
-    step, out, extra = make_step(w, sv, dev)
+    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table)
     alg_bytes, rows_t = algorithmic_bytes(w)
     if extra is not None:
-        alg_bytes += extra["draft_rows"] * w.V * 2
+        rows_t = extra["rows"]
+        alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2
     # prep, row select (with finalisation), cluster histogram, chain, resample
     # (+ the planner for ragged batches)
     launches_per_step = 5 + (1 if w.layout == "ragged" else 0)
@@ -283,7 +310,7 @@ def run_ours(args, rank, world, local):
     ms_worst = max_over_ranks(ms_per_step, world)
 
     # end to end through the public API: pinned host inputs in, results out, every step
-    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)))
+    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)), args.method)
     torch.cuda.synchronize()
     clk = clocks.stop()
 
@@ -297,7 +324,11 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_worst, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "impl": "ours",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "rows_per_step": rows_t,
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                   + (f" (scaled to {w.n} requests)" if args.requests else "")
+                   + (" -- block verification" if args.method == "block" else "")
+                   + (" -- budget from a synthetic step-cost table" if args.cost_table else ""),
+                   "rows_per_step": rows_t,
                    "vocab": w.V, "logits_bytes_per_step": alg_bytes,
                    "logits_gbs_step": round(logits_gbs_step, 1),
                    "logits_frac_of_8tbs_step": round(logits_gbs_step / 8000.0, 4),
@@ -319,7 +350,7 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(w, sv, dev, extra, steps):
+def run_e2e(w, sv, dev, extra, steps, method="chain"):
     """Same metric through the public API from pinned host buffers: H2D of the
     step's inputs and D2H of its results inside the timed region."""
     names = ["target", "draft", "draft_tokens", "temperature", "top_k", "top_p"]
@@ -344,10 +375,14 @@ def run_e2e(w, sv, dev, extra, steps):
                 dbuf[k].copy_(host[k], non_blocking=True)
         if extra is None:
             o = sv.verify_chain(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["temperature"],
-                                dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws)
+                                dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws, block=method == "block")
         else:
             conf_d.copy_(conf_h, non_blocking=True)
-            vl, qo, _, _ = sv.plan_budget(conf_d, w.budget, w.bucket, ws=ws_p)
+            if extra["table"] is None:
+                vl, qo, _, _ = sv.plan_budget(conf_d, w.budget, w.bucket, ws=ws_p)
+            else:
+                tb = extra["table"]
+                _, _, vl, qo, _, _ = sv.plan_budget_cost(conf_d, tb[0], tb[1], w.bucket, tb[2], ws=ws_p)
             o = sv.verify_ragged(dbuf["target"], dbuf["draft"], qo, vl, dbuf["draft_tokens"], dbuf["temperature"],
                                  dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws)
         res_host[0].copy_(o.accept_len, non_blocking=True)
@@ -365,7 +400,7 @@ def run_e2e(w, sv, dev, extra, steps):
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    rows = w.budget if extra is not None else w.n * (w.K + 1)
+    rows = extra["rows"] if extra is not None else w.n * (w.K + 1)
     return {"value": rows / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "inputs copied from pinned host memory and results read back inside the timed region"}
