@@ -48,9 +48,9 @@ struct RowPlan {               // decided by CTA 0, read by the others
 };
 
 struct WalkState {             // CTA 0's walk, phase to phase
-    double z_all, z1, mk_bin, mass_above_bk, mass_above_bp;
-    uint32_t cnt_above_bk, k_key, k_ties;
-    int bk, bp, bmin, found;
+    double z_all, z1, mk_bin, mass_above_bk, mass_above_bp, z;
+    uint32_t cnt_above_bk, k_key, k_ties, cut_key, cut_ties, kept;
+    int bk, bp, bmin, found, done, slot;
 };
 
 struct HistSmem {
@@ -65,6 +65,7 @@ struct HistSmem {
     unsigned long long red64[kHistThreads / 32];
     int redi[kHistThreads / 32];
     uint32_t kc[2][128];       // per-key counts of up to two binades (walk)
+    uint32_t csc[kHistThreads][33];   // per-thread key counts of one binade quarter
     double ke[2][128];         // per-key masses exp((v - m) / T)
     WalkState walk;
 };
@@ -76,29 +77,73 @@ __device__ __forceinline__ uint32_t hist_count(const uint32_t* h, uint32_t k)
     return (k & 1u) ? (w >> 16) : (w & 0xFFFFu);
 }
 
-// Per-key counts (summed over the cluster) and masses of binade b into
-// slot s of the walk scratch.  Run by threads 0..15 of CTA 0.
+// Counts of the 32 keys b*128 + 32 q .. + 31, summed over the cluster's
+// histograms: 16 words (two counters each) read as four 16-byte vectors per
+// rank.
+__device__ __forceinline__ void cluster_counts32(cg::cluster_group& cluster, HistSmem& sm, int C, int b, int q,
+                                                 uint32_t c[32])
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c[j] = 0u;
+    for (int r = 0; r < C; ++r) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(cluster.map_shared_rank(sm.hist, r)) + (b * 64 + q * 16) / 4;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 x = h4[v];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                c[8 * v + 2 * i] += w[i] & 0xFFFFu;
+                c[8 * v + 2 * i + 1] += w[i] >> 16;
+            }
+        }
+    }
+}
+
+// exp((v - m) / T) of the 32 keys b*128 + 32 q + j in fp64, handed to f(j, e)
+// in key order: along a binade the mantissa step is constant, so while the
+// step is small against T the masses follow a geometric recurrence from two
+// exps; otherwise one exp per key.  Binade 0 holds -inf (mass 0).
+template <typename F>
+__device__ __forceinline__ void for_binade_masses32(int b, int q, double m, double T, F f)
+{
+    if (b == 0) {
+        for (int j = 0; j < 32; ++j) f(j, 0.0);
+        return;
+    }
+    const uint32_t kb = (uint32_t)b * 128u + 32u * (uint32_t)q;
+    const double v_first = key_value(kb);
+    const double step = key_value(kb + 1u) - v_first;
+    if (step / T <= 1.0) {
+        const double R = exp(step / T);
+        double cur = exp((v_first - m) / T);
+        for (int j = 0; j < 32; ++j) {
+            f(j, cur);
+            cur *= R;
+        }
+    } else {
+        for (int j = 0; j < 32; ++j) f(j, exp((key_value(kb + j) - m) / T));
+    }
+}
+
+// Per-key counts (summed over the cluster) and masses of binade b into slot s
+// of the walk scratch.  Run by threads 0..3 of CTA 0 (32 keys each).
 __device__ void load_binade_keys(cg::cluster_group& cluster, HistSmem& sm, int C, int b, int s, double m, double T)
 {
-    const int g = threadIdx.x;
-    if (g >= 16) return;
+    const int q = threadIdx.x;
+    if (q >= 4) return;
     if (b < 0 || b > 511) {
-        for (int j = 0; j < 8; ++j) {
-            sm.kc[s][8 * g + j] = 0u;
-            sm.ke[s][8 * g + j] = 0.0;
+        for (int j = 0; j < 32; ++j) {
+            sm.kc[s][32 * q + j] = 0u;
+            sm.ke[s][32 * q + j] = 0.0;
         }
         return;
     }
-    double e[8];
-    binade_masses(b, g, m, T, e);
+    uint32_t c[32];
+    cluster_counts32(cluster, sm, C, b, q, c);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t k = (uint32_t)b * 128u + 8u * g + j;
-        uint32_t c = 0;
-        for (int r = 0; r < C; ++r) c += hist_count(cluster.map_shared_rank(sm.hist, r), k);
-        sm.kc[s][8 * g + j] = c;
-        sm.ke[s][8 * g + j] = e[j];
-    }
+    for (int j = 0; j < 32; ++j) sm.kc[s][32 * q + j] = c[j];
+    for_binade_masses32(b, q, m, T, [&](int j, double e) { sm.ke[s][32 * q + j] = e; });
 }
 
 // Process one row with the whole cluster; CTA 0 writes the RowInfo.
@@ -138,7 +183,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
             best_idx = idx;
         }
     };
-    constexpr int kUnroll = 4;
+    constexpr int kUnroll = 8;   // 8 x 16 B per thread in flight
     for (int base = s0 + tid * 8; base < s1; base += kHistThreads * 8 * kUnroll) {
         uint4 v[kUnroll];
         bool full[kUnroll];
@@ -236,38 +281,40 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
             if (lane == 31) sm.n_occ = incl;
         }
         __syncthreads();
-        // 5. binade sums: this CTA owns occupied binades j = rank, rank + C, ...
+        // 5. binade sums: this CTA owns occupied binades j = rank, rank + C,
+        //    ...; four threads per binade, 32 keys each.  Every thread of a
+        //    warp runs the same number of rounds (the loop bound is uniform
+        //    per warp), so the 4-lane reductions below see all their lanes.
         const int n_occ = sm.n_occ;
         BinSum* sums0 = cluster.map_shared_rank(sm.sums, 0);
-        const int g = tid & 15;
-        for (int q = tid >> 4; rank + C * q < n_occ; q += kHistThreads / 16) {
-            const int b = sm.occ_list[rank + C * q];
-            uint32_t c[8];
+        const int q4 = tid & 3;
+        const int n_mine = n_occ > rank ? (n_occ - rank + C - 1) / C : 0;
+        for (int i0 = (tid >> 2) - (lane >> 2); i0 < n_mine; i0 += kHistThreads / 4) {
+            const int i = i0 + (lane >> 2);
+            const bool act = i < n_mine;
+            const int b = act ? sm.occ_list[rank + C * i] : 0;
             uint32_t csum = 0u;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t k = (uint32_t)b * 128u + 8u * g + j;
-                uint32_t cc = 0u;
-                for (int r = 0; r < C; ++r) cc += hist_count(cluster.map_shared_rank(sm.hist, r), k);
-                c[j] = cc;
-                csum += cc;
-            }
             double mass = 0.0;
-            if (csum) {
-                double e[8];
-                binade_masses(b, g, m, T, e);
+            if (act) {
+                uint32_t c[32];
+                cluster_counts32(cluster, sm, C, b, q4, c);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) mass += (double)c[j] * e[j];
-            }
-            // fixed-order reduction over the 16 threads of this binade: the two
-            // half-warps walk different binade lists, so each names only itself
-            const unsigned half = (lane < 16) ? 0x0000FFFFu : 0xFFFF0000u;
+                for (int j = 0; j < 32; ++j) csum += c[j];
+                if (csum) {
+                    // counts go to shared scratch so the mass loop indexes them freely
+                    uint32_t* cs = sm.csc[tid];
 #pragma unroll
-            for (int o = 8; o; o >>= 1) {
-                mass += __shfl_xor_sync(half, mass, o, 16);
-                csum += __shfl_xor_sync(half, csum, o, 16);
+                    for (int j = 0; j < 32; ++j) cs[j] = c[j];
+                    for_binade_masses32(b, q4, m, T, [&](int j, double e) { mass += (double)cs[j] * e; });
+                }
             }
-            if (g == 0) {
+            // fixed-order reduction over the 4 threads of each binade
+#pragma unroll
+            for (int o = 2; o; o >>= 1) {
+                mass += __shfl_xor_sync(0xFFFFFFFFu, mass, o, 4);
+                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
+            }
+            if (act && q4 == 0) {
                 sums0[b].mass = mass;
                 sums0[b].count = csum;
             }
@@ -336,28 +383,53 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
         // Phase B: keys of the top-k boundary binade.
         if (status == 0 && topk_on) load_binade_keys(cluster, sm, C, W.bk, 0, m, T);
         __syncthreads();
-        // Phase C (thread 0): top-k cutoff key, kept ties, Z1.
-        if (status == 0 && tid == 0) {
+        // Phase C (warp 0): top-k cutoff key, kept ties, Z1.  Lane l holds
+        // keys 127 - 4l .. 124 - 4l (descending); warp scans give the counts
+        // and masses above each lane's keys.
+        if (status == 0 && warp == 0) {
             if (topk_on) {
-                uint32_t cum = W.cnt_above_bk;
-                double mass = W.mass_above_bk;
-                for (int f = 127; f >= 0; --f) {
-                    const uint32_t c = sm.kc[0][f];
-                    if (c == 0u) continue;
-                    if (cum + c >= (uint32_t)kk) {
-                        W.k_key = (uint32_t)W.bk * 128u + f;
-                        W.k_ties = (uint32_t)kk - cum;
-                        W.mk_bin = mass - W.mass_above_bk + (double)W.k_ties * sm.ke[0][f];
-                        W.z1 = mass + (double)W.k_ties * sm.ke[0][f];
-                        break;
-                    }
-                    cum += c;
-                    mass += (double)c * sm.ke[0][f];
+                uint32_t c4 = 0u;
+                double m4 = 0.0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int f = 127 - 4 * lane - i;
+                    c4 += sm.kc[0][f];
+                    m4 += (double)sm.kc[0][f] * sm.ke[0][f];
                 }
-            } else {
+                uint32_t ci = c4;
+                double mi = m4;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+                    const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+                    if (lane >= o) {
+                        ci += y;
+                        mi += z;
+                    }
+                }
+                uint32_t cum = W.cnt_above_bk + (ci - c4);
+                double mass = W.mass_above_bk + (mi - m4);
+                const bool mine = cum < (uint32_t)kk && (uint32_t)kk <= cum + c4;
+                if (mine) {
+                    for (int i = 0; i < 4; ++i) {
+                        const int f = 127 - 4 * lane - i;
+                        const uint32_t c = sm.kc[0][f];
+                        if (c == 0u) continue;
+                        if (cum + c >= (uint32_t)kk) {
+                            W.k_key = (uint32_t)W.bk * 128u + f;
+                            W.k_ties = (uint32_t)kk - cum;
+                            W.mk_bin = mass - W.mass_above_bk + (double)W.k_ties * sm.ke[0][f];
+                            W.z1 = mass + (double)W.k_ties * sm.ke[0][f];
+                            break;
+                        }
+                        cum += c;
+                        mass += (double)c * sm.ke[0][f];
+                    }
+                }
+            } else if (lane == 0) {
                 W.z1 = W.z_all;
             }
-            W.found = 0;
+            if (lane == 0) W.found = 0;
         }
         __syncthreads();
         // Phase D (warp 0): top-p binade on masses capped at the top-k cutoff.
@@ -402,42 +474,85 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
         }
         if (load_b >= 0) load_binade_keys(cluster, sm, C, load_b, 1, m, T);
         __syncthreads();
-        // Phase F (thread 0): the final cutoff and the row's record.
-        if (status == 0 && tid == 0) {
-            uint32_t cut_key = 0u, cut_ties = 0u, kept = 0u;
-            double z = 0.0;
-            int slot = 0;
-            bool done = false;
+        // Phase F (warp 0): the final cutoff, by a warp walk over the keys of
+        // binade bp (lane l: keys 127 - 4l .. 124 - 4l), then thread 0
+        // writes the row's record.
+        if (status == 0 && warp == 0) {
             if (W.found) {
                 const int bp = W.bp;
-                slot = (topk_on && bp == W.bk) ? 0 : 1;
+                const int slot = (topk_on && bp == W.bk) ? 0 : 1;
                 const double target = (double)task.top_p * W.z1;
-                uint32_t cnt_above = 0u;
-                for (int b = 511; b > bp; --b) cnt_above += sm.sums[b].count;
-                double cum = W.mass_above_bp;
-                for (int f = 127; f >= 0; --f) {
+                uint32_t above = 0u;   // elements in binades above bp
+                for (int b = 511 - lane; b > bp; b -= 32) above += sm.sums[b].count;
+                above = __reduce_add_sync(0xFFFFFFFFu, above);
+                uint32_t ce4[4];
+                double e4[4];
+                uint32_t c4 = 0u;
+                double m4 = 0.0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int f = 127 - 4 * lane - i;
                     const uint32_t key = (uint32_t)bp * 128u + f;
                     uint32_t ce = sm.kc[slot][f];
                     if (topk_on && bp == W.bk) ce = key > W.k_key ? ce : (key == W.k_key ? W.k_ties : 0u);
+                    ce4[i] = ce;
+                    e4[i] = sm.ke[slot][f];
+                    c4 += ce;
+                    m4 += (double)ce * e4[i];
+                }
+                uint32_t ci = c4;
+                double mi = m4;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+                    const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+                    if (lane >= o) {
+                        ci += y;
+                        mi += z;
+                    }
+                }
+                uint32_t cnt_above = above + (ci - c4);
+                double cum = W.mass_above_bp + (mi - m4);
+                int hit_f = -1;
+                uint32_t hit_j = 0u, hit_kept = 0u;
+                double hit_z = 0.0;
+                for (int i = 0; i < 4 && hit_f < 0; ++i) {
+                    const uint32_t ce = ce4[i];
                     if (ce == 0u) continue;
-                    const double e = sm.ke[slot][f];
+                    const double e = e4[i];
                     if (cum + (double)ce * e >= target) {
                         const double jd = ceil((target - cum) / e);
                         uint32_t j = jd < 1.0 ? 1u : (jd > (double)ce ? ce : (uint32_t)jd);
                         while (j > 1u && cum + (double)(j - 1u) * e >= target) --j;
                         while (j < ce && cum + (double)j * e < target) ++j;
-                        cut_key = key;
-                        cut_ties = j;
-                        kept = cnt_above + j;
-                        z = cum + (double)j * e;
-                        done = true;
+                        hit_f = 127 - 4 * lane - i;
+                        hit_j = j;
+                        hit_kept = cnt_above + j;
+                        hit_z = cum + (double)j * e;
                         break;
                     }
                     cum += (double)ce * e;
                     cnt_above += ce;
                 }
+                const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit_f >= 0);
+                if (hits && lane == __ffs(hits) - 1) {
+                    W.cut_key = (uint32_t)bp * 128u + hit_f;
+                    W.cut_ties = hit_j;
+                    W.kept = hit_kept;
+                    W.z = hit_z;
+                    W.slot = slot;
+                }
+                if (lane == 0) W.done = hits != 0u;
+            } else if (lane == 0) {
+                W.done = 0;
             }
-            if (!done) {
+        }
+        __syncthreads();
+        if (status == 0 && tid == 0) {
+            uint32_t cut_key = W.cut_key, cut_ties = W.cut_ties, kept = W.kept;
+            double z = W.z;
+            int slot = W.slot;
+            if (!W.done) {
                 if (topk_on) {
                     cut_key = W.k_key;
                     cut_ties = W.k_ties;
@@ -456,7 +571,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
             }
             const uint32_t cut_count = sm.kc[slot][cut_key & 127u];
             info->desc.max_logit = (float)m;
-            info->desc.log_norm = (float)log(z);
+            info->desc.log_norm = logf((float)z);
             info->desc.cutoff_logit = f32_of_key16(cut_key);
             info->desc.cutoff_ties = (int)cut_ties;
             info->desc.kept = (int)kept;
