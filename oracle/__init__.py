@@ -95,6 +95,10 @@ def lib():
                                            ctypes.c_float, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P]
         _lib.orc_choose_budget.restype = ctypes.c_int
         _lib.orc_verify_stats.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, P]
+        _lib.orc_est_init.argtypes = [P, ctypes.c_int]
+        _lib.orc_est_features.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, P, P, P, P]
+        _lib.orc_est_predict.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P]
+        _lib.orc_est_observe.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     return _lib
 
 
@@ -236,3 +240,46 @@ def verify_stats(accept_len, num_emitted, verify_lens, K: int, draft_len=None):
     out = np.zeros(4, np.int64)
     lib().orc_verify_stats(_ptr(al), _ptr(ne), _ptr(vl), _ptr(dl), len(al), K, _ptr(out))
     return tuple(int(x) for x in out)
+
+
+class Estimator:
+    """The oracle's online acceptance estimator (state as the C side lays it out)."""
+
+    def __init__(self, K: int):
+        self.K = K
+        self.state = np.zeros(4 * K + 5, np.float64)
+        lib().orc_est_init(_ptr(self.state), K)
+
+    @property
+    def slope(self) -> float:
+        return float(self.state[0])
+
+    @property
+    def bias(self) -> np.ndarray:
+        return self.state[1:1 + self.K].copy()
+
+    def predict(self, x) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        n = x.shape[0]
+        p = np.zeros((n, self.K), np.float64)
+        lib().orc_est_predict(_ptr(self.state), _ptr(x), n, self.K, _ptr(p))
+        return p
+
+    def observe(self, x, accept_len, num_emitted, verify_lens=None, refit_every: int = 100):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        al = np.ascontiguousarray(accept_len, dtype=np.int32)
+        ne = np.ascontiguousarray(num_emitted, dtype=np.int32)
+        vl = None if verify_lens is None else np.ascontiguousarray(verify_lens, dtype=np.int32)
+        lib().orc_est_observe(_ptr(self.state), _ptr(x), _ptr(al), _ptr(ne), _ptr(vl), len(al), self.K, refit_every)
+
+
+def est_features(draft, temperature, top_k=None, top_p=None) -> np.ndarray:
+    """x [n, K] = clamp(logit(q_max), +-40) of every draft row (T = 1 for greedy requests)."""
+    draft, dt = _logits(draft)
+    n, K, V = draft.shape
+    T = np.ascontiguousarray(temperature, dtype=np.float32)
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
+    tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
+    x = np.zeros((n, K), np.float64)
+    lib().orc_est_features(_ptr(draft), dt, n, K, V, _ptr(T), _ptr(tk), _ptr(tp), _ptr(x))
+    return x

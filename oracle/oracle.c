@@ -49,7 +49,10 @@
  *   6 cost table looked up by drafted tokens only (the bonus row left out)
  *   7 budget by first descent of tau / cost instead of the global argmax
  *   8 trim regret counts requests that stopped inside their window
- *   9 block verification: residual and stopping masses without the weight  */
+ *   9 block verification: residual and stopping masses without the weight
+ *  10 estimator: every position of the window observed, not only up to the
+ *     first rejection
+ *  11 estimator: a slope step that crosses zero is dropped, not halved     */
 #ifndef ORC_PLANT
 #define ORC_PLANT 0
 #endif
@@ -158,6 +161,8 @@ typedef struct {
     int32_t argmax;      /* smallest index holding m                         */
     int32_t status;      /* ORC_* bits                                       */
     double cut_margin;   /* top-p decision margin / Z1 (inf when top-p off)  */
+    double z_rest;       /* kept mass after the first kept token, sum of     */
+                         /* exp((l - m) / T) over kept tokens 2..kept        */
 } orc_row_t;
 
 static int bad_params(float T, float top_p)
@@ -253,6 +258,7 @@ int orc_row_transform(const void* row, int dtype, int64_t vocab, float T, int32_
     double z = 0.0;
     for (int64_t i = 0; i < kept; ++i) z += e[i];
     out->log_norm = log(z);
+    for (int64_t i = 1; i < kept; ++i) out->z_rest += e[i];
     out->kept = (int32_t)kept;
     out->cutoff_logit = ord[kept - 1].value;
     int32_t ties = 0;
@@ -825,4 +831,144 @@ void orc_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, con
 #endif
         }
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* NEXT-3: online acceptance estimator.                                      */
+/* ------------------------------------------------------------------------- */
+/*
+ * jianc99/sglang PR #8, the DFLASH adaptive-verification commits: a logistic
+ * model calibrated while serving, p_k = sigmoid(slope * x_k + bias_k), x_k =
+ * logit(q_max) of the temperature-scaled draft distribution at position k
+ * (greedy rows at T = 1), clamped to +-40; one slope shared by all positions,
+ * one intercept per position, starting from 0.5 and -0.2; observe() labels the
+ * accepted drafts and the first rejected one and adds them to the Newton
+ * (IRLS) statistics; every 100 calls the arrowhead system is solved with ridge
+ * 1e-3, each update is damped by n / (n + 50), non-finite steps are dropped,
+ * and a slope step that would make the slope negative is halved up to 8 times
+ * and dropped only if it still crosses zero; the intercepts take their Newton
+ * step given the slope step actually taken; the statistics are then cleared.
+ *
+ * Readings (restated in the design doc):
+ *  - q is the distribution the draft token is drawn from, the request's
+ *    transform (temperature, top-k, top-p) of the draft row -- the same q the
+ *    verification uses -- at T = 1 for greedy requests.  q_max = 1 / z (the
+ *    top token has mass exp(0)), so x = logit(q_max) = -ln(z - 1); z - 1 is the
+ *    kept mass after the first kept token (no cancellation).  A row with an
+ *    error gives x = NaN; a single kept token gives +40.
+ *  - Observed positions of request r: k = 0 .. min(accept_len, v_r - 1); label
+ *    1 for k < accept_len, 0 for the first rejected one.  Requests that
+ *    emitted nothing (errors) and non-finite features are skipped.
+ *  - Newton statistics at the current coefficients: g_a = sum (y - p) x,
+ *    g_k = sum_k (y - p), H_aa = sum w x^2, H_ak = sum_k w x, H_kk = sum_k w,
+ *    w = p (1 - p), n = observation count.  Refit: with lambda = 1e-3 on the
+ *    diagonal, t = (g_a - sum_k H_ak g_k / (H_kk + l)) / (H_aa + l - sum_k
+ *    H_ak^2 / (H_kk + l)); d = n / (n + 50); while slope + d t < 0 (at most 8
+ *    times) t /= 2; if it is still negative t = 0; intercept steps u_k =
+ *    (g_k - H_ak t) / (H_kk + l); if t and every u_k are finite, slope += d t
+ *    and bias_k += d u_k.  The statistics are cleared either way.  A refit
+ *    with no observations changes nothing.
+ *
+ * State (doubles): [0] slope, [1..K] bias, [K+1] g_a, [K+2] H_aa,
+ * [K+3 ..] g_k (K), H_ak (K), H_kk (K), [4K+3] n, [4K+4] calls.
+ */
+void orc_est_init(double* state, int K)
+{
+    for (int i = 0; i < 4 * K + 5; ++i) state[i] = 0.0;
+    state[0] = 0.5;
+    for (int k = 0; k < K; ++k) state[1 + k] = -0.2;
+}
+
+void orc_est_features(const void* draft, int dtype, int n, int K, int64_t vocab, const float* T,
+                      const int32_t* top_k, const float* top_p, double* x)
+{
+    for (int r = 0; r < n; ++r) {
+        const float t = T[r] > 0.0f ? T[r] : 1.0f;
+        for (int k = 0; k < K; ++k) {
+            orc_row_t tr;
+            const int st = orc_row_transform(row_ptr(draft, dtype, (int64_t)r * K + k, vocab), dtype, vocab, t,
+                                             top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, &tr, NULL);
+            double xv;
+            if (st & ORC_ERROR_MASK) {
+                xv = NAN;
+            } else {
+                xv = tr.z_rest > 0.0 ? -log(tr.z_rest) : INFINITY;
+                xv = xv > 40.0 ? 40.0 : (xv < -40.0 ? -40.0 : xv);
+            }
+            x[(size_t)r * K + k] = xv;
+        }
+    }
+}
+
+void orc_est_predict(const double* state, const double* x, int n, int K, double* p)
+{
+    for (int r = 0; r < n; ++r)
+        for (int k = 0; k < K; ++k) {
+            const double s = state[0] * x[(size_t)r * K + k] + state[1 + k];
+            p[(size_t)r * K + k] = 1.0 / (1.0 + exp(-s));
+        }
+}
+
+static void est_refit(double* st, int K)
+{
+    double* g_b = st + K + 3;
+    double* h_ab = g_b + K;
+    double* h_bb = h_ab + K;
+    const double lam = 1e-3, n = st[4 * K + 3];
+    if (n > 0.0) {
+        double num = st[K + 1], den = st[K + 2] + lam;
+        for (int k = 0; k < K; ++k) {
+            num -= h_ab[k] * g_b[k] / (h_bb[k] + lam);
+            den -= h_ab[k] * h_ab[k] / (h_bb[k] + lam);
+        }
+        double t = num / den;
+        const double d = n / (n + 50.0);
+#if ORC_PLANT == 11
+        if (st[0] + d * t < 0.0) t = 0.0;
+#else
+        for (int i = 0; i < 8 && st[0] + d * t < 0.0; ++i) t *= 0.5;
+        if (st[0] + d * t < 0.0) t = 0.0;
+#endif
+        int ok = isfinite(t);
+        for (int k = 0; k < K; ++k) ok = ok && isfinite((g_b[k] - h_ab[k] * t) / (h_bb[k] + lam));
+        if (ok) {
+            for (int k = 0; k < K; ++k) st[1 + k] += d * (g_b[k] - h_ab[k] * t) / (h_bb[k] + lam);
+            st[0] += d * t;
+        }
+    }
+    for (int i = K + 1; i < 4 * K + 4; ++i) st[i] = 0.0;
+}
+
+void orc_est_observe(double* state, const double* x, const int32_t* accept_len, const int32_t* num_emitted,
+                     const int32_t* verify_lens, int n, int K, int refit_every)
+{
+    double* g_b = state + K + 3;
+    double* h_ab = g_b + K;
+    double* h_bb = h_ab + K;
+    for (int r = 0; r < n; ++r) {
+        if (num_emitted[r] == 0 || accept_len[r] < 0) continue;
+        int v = verify_lens ? verify_lens[r] : K;
+        v = v < 0 ? 0 : (v > K ? K : v);
+        const int a = accept_len[r];
+#if ORC_PLANT == 10
+        const int last = v - 1;
+#else
+        const int last = a < v - 1 ? a : v - 1;
+#endif
+        for (int k = 0; k <= last; ++k) {
+            const double xv = x[(size_t)r * K + k];
+            if (!isfinite(xv)) continue;
+            const double y = k < a ? 1.0 : 0.0;
+            const double p = 1.0 / (1.0 + exp(-(state[0] * xv + state[1 + k])));
+            const double w = p * (1.0 - p);
+            state[K + 1] += (y - p) * xv;
+            state[K + 2] += w * xv * xv;
+            g_b[k] += y - p;
+            h_ab[k] += w * xv;
+            h_bb[k] += w;
+            state[4 * K + 3] += 1.0;
+        }
+    }
+    state[4 * K + 4] += 1.0;
+    if (refit_every > 0 && fmod(state[4 * K + 4], (double)refit_every) == 0.0) est_refit(state, K);
 }
