@@ -67,7 +67,7 @@ class RowOut(ctypes.Structure):
     _fields_ = [("max_logit", ctypes.c_double), ("log_norm", ctypes.c_double),
                 ("cutoff_logit", ctypes.c_double), ("cutoff_ties", ctypes.c_int32),
                 ("kept", ctypes.c_int32), ("argmax", ctypes.c_int32), ("status", ctypes.c_int32),
-                ("cut_margin", ctypes.c_double)]
+                ("cut_margin", ctypes.c_double), ("z_rest", ctypes.c_double)]
 
 
 def lib():
