@@ -299,6 +299,51 @@ sv_status_t sv_verify_stats(const int32_t* accept_len, const int32_t* num_emitte
                             const int32_t* draft_len, int n_req, int K, int64_t* out, sv_stream_t stream);
 
 /*
+ * Online acceptance estimator (jianc99/sglang PR #8, DFLASH adaptive-
+ * verification commits): the confidence source of the planner for drafts
+ * without a confidence head.  p_k = sigmoid(slope * x_k + bias_k), x_k =
+ * logit(q_max) of the draft distribution at position k, clamped to +-40.
+ * q is the request's transform (temperature, top-k, top-p) of draft row k --
+ * the q verification uses -- at temperature 1 for greedy requests; q_max = 1/z
+ * (z the kept mass relative to the top token), so x = -ln(z - 1).
+ * The state is caller-owned device memory of sv_estimator_state_bytes(K)
+ * bytes, doubles laid out as [0] slope, [1..K] bias, then the Newton
+ * statistics (g_a, H_aa, g_k x K, H_ak x K, H_kk x K, observations, calls).
+ * Everything runs on the stream without host synchronisation.
+ */
+size_t sv_estimator_state_bytes(int K);                          /* 0 unless 1 <= K <= 63 */
+
+/* slope 0.5, every bias -0.2, statistics cleared. */
+sv_status_t sv_estimator_init(double* state, int K, sv_stream_t stream);
+
+/*
+ * Features and predictions for draft logits (device, [n_req, K, vocab], bf16
+ * or fp32; fp32 needs top-k <= 32): x_out, p_out (device) fp32 [n_req, K].
+ * p_out is the planner's conf input (sv_plan_budget / sv_plan_budget_cost).
+ * A row with an error gives x = p = NaN (the planner reads NaN as 0).
+ * Workspace: sv_workspace_size(n_req * K, 0, vocab).
+ */
+sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_req, int K, int vocab,
+                                 sv_sampling_t sp, const double* state, float* x_out, float* p_out, void* ws,
+                                 size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * After a verify call: request r's positions 0 .. min(accept_len[r],
+ * v_r - 1) are observed (label 1 below accept_len, 0 for the first rejected
+ * one; v_r = verify_lens[r], or K when NULL); requests with num_emitted == 0
+ * and non-finite features are skipped.  The Newton statistics at the current
+ * coefficients accumulate in the state; every refit_every calls (0: never)
+ * one ridge (1e-3) Newton step on the arrowhead system, damped by n / (n + 50)
+ * for n observations, updates the coefficients: a slope step that would make
+ * the slope negative is halved up to 8 times and dropped if it still does;
+ * the intercepts step given the slope step taken; non-finite steps are
+ * dropped; the statistics are then cleared.  One CTA reduces in a fixed
+ * order, so identical inputs give identical coefficients.
+ */
+sv_status_t sv_estimator_observe(double* state, const float* x, const int32_t* accept_len, const int32_t* num_emitted,
+                                 const int32_t* verify_lens, int n_req, int K, int refit_every, sv_stream_t stream);
+
+/*
  * sv_verify_chain without a workspace argument.  The pages have no
  * counterpart: this is for callers that cannot allocate device memory where
  * they verify -- code running while a CUDA graph is captured (cudaMalloc is

@@ -94,6 +94,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ChainArgs& ca = c.ca;
     ca.n_req = n_req;
     ca.n_params = n_req;
+    ca.rows_per_req = 1;
     ca.K = k_max;
     ca.vocab = vocab;
     ca.dtype = dtype;
@@ -216,6 +217,51 @@ sv_status_t sv_plan_budget_cost(const float* conf, int ld_conf, const int32_t* d
     if (e != cudaSuccess) return SV_ERR_CUDA;
     return to_status(launch_plan(conf, ld_conf, draft_len, n_req, K, 0, budget_out, verify_lens, qo_indptr,
                                  total_tokens, status, static_cast<unsigned long long*>(ws), stream));
+}
+
+size_t sv_estimator_state_bytes(int K)
+{
+    if (K < 1 || K > kMaxK) return 0;
+    return sizeof(double) * (size_t)(4 * K + 5);
+}
+
+sv_status_t sv_estimator_init(double* state, int K, sv_stream_t stream)
+{
+    if (!state || K < 1 || K > kMaxK) return SV_ERR_INVALID_ARG;
+    return to_status(launch_est_init(state, K, stream));
+}
+
+sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_req, int K, int vocab,
+                                 sv_sampling_t sp, const double* state, float* x_out, float* p_out, void* ws,
+                                 size_t ws_bytes, sv_stream_t stream)
+{
+    if (!draft_logits || n_req < 1 || K < 1 || K > kMaxK || vocab < 1 || !sp.temperature || !state || !x_out ||
+        !p_out)
+        return SV_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
+    if (vocab > kMaxVocab || (long long)n_req * K > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const int rows = n_req * K;
+    const size_t need = sv_workspace_size(rows, 0, vocab);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, rows, 0, vocab, (int)dt, draft_logits, nullptr, vocab, vocab);
+    ChainArgs& ca = c.ca;
+    ca.layout = 2;
+    ca.est = 1;
+    ca.rows_per_req = K;
+    ca.n_params = n_req;
+    ca.sp = sp;
+    if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
+    sv_status_t st = run_rows(c.ra, stream);
+    if (st != SV_OK) return st;
+    return to_status(launch_est_predict(c.ra.info, state, n_req, K, x_out, p_out, c.ra.counters, stream));
+}
+
+sv_status_t sv_estimator_observe(double* state, const float* x, const int32_t* accept_len, const int32_t* num_emitted,
+                                 const int32_t* verify_lens, int n_req, int K, int refit_every, sv_stream_t stream)
+{
+    if (!state || !x || !accept_len || !num_emitted || n_req < 1 || K < 1 || K > kMaxK) return SV_ERR_INVALID_ARG;
+    return to_status(launch_est_observe(state, x, accept_len, num_emitted, verify_lens, n_req, K, refit_every, stream));
 }
 
 sv_status_t sv_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, const int32_t* verify_lens,

@@ -105,9 +105,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         float T = 0.0f, tp = 1.0f;
         bool fast = true;
         if (active) {
-            if (a.layout == 2) req = a.row_to_req ? a.row_to_req[u] : u;
+            if (a.layout == 2) req = a.row_to_req ? a.row_to_req[u] : u / a.rows_per_req;
             const bool req_ok = req >= 0 && req < a.n_params;
             T = req_ok ? a.sp.temperature[req] : 0.0f;
+            if (a.est && T == 0.0f) T = 1.0f;   // estimator features: greedy requests at T = 1
             const int tk = (req_ok && a.sp.top_k) ? a.sp.top_k[req] : 0;
             tp = (req_ok && a.sp.top_p) ? a.sp.top_p[req] : 1.0f;
             if (!req_ok || bad_params(T, tp)) err |= kBadParam;

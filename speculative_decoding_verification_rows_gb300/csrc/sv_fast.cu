@@ -340,6 +340,7 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
             info->desc.kept = 1;
             info->p_token = task.token >= 0 ? (task.token == amax ? 1.0 : 0.0) : nan("");
             info->z = 1.0;
+            info->z_rest = 0.0;
             info->n_list = 1;
             info->list_idx[0] = amax;
             info->list_p[0] = 1.0;
@@ -365,6 +366,9 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
     }
     const double z = __shfl_sync(0xFFFFFFFFu, cum, kept - 1);
     const bool in = lane < kept;
+    double z_rest = (in && lane > 0) ? e : 0.0;   // kept mass after the top token
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z_rest += __shfl_xor_sync(0xFFFFFFFFu, z_rest, o);
     const double p = in ? e * (1.0 / z) : 0.0;
     const float cut = __shfl_sync(0xFFFFFFFFu, lv, kept - 1);
     const int ties = __popc(__ballot_sync(0xFFFFFFFFu, in && lv == cut));
@@ -383,6 +387,7 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
         info->desc.kept = kept;
         info->p_token = task.token >= 0 ? ptok : nan("");
         info->z = z;
+        info->z_rest = z_rest;
         info->n_list = kept;
     }
 }

@@ -579,6 +579,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
             info->desc.status = 0;
             info->desc.temperature = task.temp;
             info->z = z;
+            info->z_rest = z - 1.0;   // the top token's mass is exp(0)
             info->n_list = -1;
             info->cut_count = (int)cut_count;
             sm.plan.cut_key = cut_key;

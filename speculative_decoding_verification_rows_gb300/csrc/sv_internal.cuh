@@ -85,6 +85,7 @@ struct RowInfo {
     sv_row_desc_t desc;         // 32 B, the public descriptor
     double p_token;             // probability of the task's token (NaN if none)
     double z;                   // normaliser: sum over kept of exp((l - m) / T)
+    double z_rest;              // kept mass after the top token (z - 1, summed without cancellation)
     int32_t n_list;             // kept tokens listed below (ascending index), -1 if not listed
     int32_t cut_count;          // tokens whose logit equals the cutoff (all of them, kept or not)
     int32_t list_idx[kFastK];
@@ -367,6 +368,8 @@ struct ChainArgs {
     int vocab, dtype;
     int layout;            // 0 uniform, 1 ragged, 2 plain rows (build_target_probs)
     int block;             // 1: block verification instead of the token-by-token chain
+    int est;               // 1: estimator features (layout 2, greedy requests at T = 1)
+    int rows_per_req;      // layout 2 without row_to_req: request = row / rows_per_req
     const void* tgt;
     const void* drf;
     int64_t stride_t, stride_d;
@@ -397,6 +400,12 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
                             cudaStream_t s);
+
+cudaError_t launch_est_init(double* state, int K, cudaStream_t s);
+cudaError_t launch_est_predict(const RowInfo* info, const double* state, int n, int K, float* x, float* p,
+                               const Counters* counters, cudaStream_t s);
+cudaError_t launch_est_observe(double* state, const float* x, const int32_t* accept_len, const int32_t* num_emitted,
+                               const int32_t* verify_lens, int n, int K, int refit_every, cudaStream_t s);
 
 cudaError_t launch_plan(const float* conf, int ld, const int32_t* draft_len, int n, int K, int budget,
                         const int32_t* budget_dev, int32_t* verify_lens, int32_t* qo_indptr, int32_t* total,

@@ -25,7 +25,8 @@ ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | RO
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
             "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc",
-            "sv_plan_budget_cost", "sv_verify_stats", "sv_verify_block")
+            "sv_plan_budget_cost", "sv_verify_stats", "sv_verify_block", "sv_estimator_state_bytes",
+            "sv_estimator_init", "sv_estimator_predict", "sv_estimator_observe")
 
 
 class SVError(RuntimeError):
@@ -80,6 +81,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_plan_budget_cost.restype = I
     L.sv_verify_stats.argtypes = [P, P, P, P, I, I, P, P]
     L.sv_verify_stats.restype = I
+    L.sv_estimator_state_bytes.argtypes = [I]
+    L.sv_estimator_state_bytes.restype = SZ
+    L.sv_estimator_init.argtypes = [P, I, P]
+    L.sv_estimator_init.restype = I
+    L.sv_estimator_predict.argtypes = [P, I, I, I, I, Sampling, P, P, P, P, SZ, P]
+    L.sv_estimator_predict.restype = I
+    L.sv_estimator_observe.argtypes = [P, P, P, P, P, I, I, I, P]
+    L.sv_estimator_observe.restype = I
     L.sv_set_timing_events.argtypes = [P, P]
     L.sv_set_timing_events.restype = I
     _lib = L
@@ -225,6 +234,47 @@ def verify_stats(accept_len: torch.Tensor, num_emitted: torch.Tensor, verify_len
     _check(load().sv_verify_stats(_ptr(accept_len), _ptr(num_emitted), _ptr(verify_lens), _ptr(draft_len),
                                   accept_len.numel(), K, _ptr(out), _stream(dev)))
     return out
+
+
+class Estimator:
+    """The online acceptance estimator: a device state and its three calls."""
+
+    def __init__(self, K: int, device="cuda"):
+        self.K = K
+        self.state = torch.empty(4 * K + 5, dtype=torch.float64, device=device)
+        _check(load().sv_estimator_init(_ptr(self.state), K, _stream(self.state.device)))
+        self.ws = Workspace(self.state.device)
+
+    @property
+    def slope(self) -> torch.Tensor:
+        return self.state[0]
+
+    @property
+    def bias(self) -> torch.Tensor:
+        return self.state[1:1 + self.K]
+
+    def predict(self, draft: torch.Tensor, temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
+                top_p: Optional[torch.Tensor] = None):
+        """(x [n, K], p [n, K]) fp32 on the device for draft logits [n, K, V]."""
+        draft = _dev(draft)
+        n, K, V = draft.shape
+        assert K == self.K
+        dev = draft.device
+        x = torch.empty((n, K), dtype=torch.float32, device=dev)
+        p = torch.empty((n, K), dtype=torch.float32, device=dev)
+        w = _ws(self.ws, dev, workspace_size(n * K, 0, V))
+        _check(load().sv_estimator_predict(_ptr(draft), _dtype_code(draft), n, K, V,
+                                           _sampling(temperature, top_k, top_p), _ptr(self.state), _ptr(x), _ptr(p),
+                                           _ptr(w), w.numel(), _stream(dev)))
+        return x, p
+
+    def observe(self, x: torch.Tensor, accept_len: torch.Tensor, num_emitted: torch.Tensor,
+                verify_lens: Optional[torch.Tensor] = None, refit_every: int = 100):
+        x = _dev(x, torch.float32)
+        n = x.shape[0]
+        _check(load().sv_estimator_observe(_ptr(self.state), _ptr(x), _ptr(_dev(accept_len, torch.int32)),
+                                           _ptr(_dev(num_emitted, torch.int32)), _ptr(verify_lens), n, self.K,
+                                           refit_every, _stream(x.device)))
 
 
 def build_target_probs(logits: torch.Tensor, temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
