@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--requests", type=int, default=0, help="scale the batch to this many requests (profiling)")
     p.add_argument("--method", choices=["chain", "block"], default="chain",
                    help="token-by-token chain test, or block verification (uniform layout only)")
+    p.add_argument("--estimator", action="store_true",
+                   help="uniform layout: each step also predicts acceptance from the draft rows and observes the result")
     p.add_argument("--cost-table", action="store_true",
                    help="ragged workload: choose the budget from a synthetic step-cost table on the device")
     return p.parse_args()
@@ -211,7 +213,7 @@ def synthetic_cost_table(w, dev):
             0.8)
 
 
-def make_step(w, sv, dev, method="chain", cost_table=False):
+def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
     """A closure running one verify step with preallocated outputs/workspace."""
     ws = sv.Workspace(dev)
     n, K = w.n, w.K
@@ -221,9 +223,15 @@ def make_step(w, sv, dev, method="chain", cost_table=False):
                                                                                  device=dev))
     if w.layout == "chain":
         block = method == "block"
+        est = sv.Estimator(w.K, dev) if estimator else None
 
         def step(tgt=w.target, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
-            return sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block)
+            if est is not None:
+                x, _ = est.predict(drf, T, tk, tp)
+            o = sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block)
+            if est is not None:
+                est.observe(x, o.accept_len, o.num_emitted)
+            return o
         return step, out, None
     if method != "chain":
         raise SystemExit("block verification is built for the uniform layout only")
@@ -256,14 +264,16 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
-    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table)
+    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator)
     alg_bytes, rows_t = algorithmic_bytes(w)
     if extra is not None:
         rows_t = extra["rows"]
         alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2
     # prep, row select (with finalisation), cluster histogram, chain, resample
-    # (+ the planner for ragged batches)
-    launches_per_step = 5 + (1 if w.layout == "ragged" else 0)
+    # (+ the planner for ragged batches, + the budget choice with a cost table)
+    launches_per_step = 5 + (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
+    if args.estimator:   # prep, row select, cluster histogram, features for the draft rows; observe
+        launches_per_step += 5
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     if not args.quick:
@@ -327,6 +337,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
                    + (f" (scaled to {w.n} requests)" if args.requests else "")
                    + (" -- block verification" if args.method == "block" else "")
+                   + (" -- with the online acceptance estimator (predict + observe)" if args.estimator else "")
                    + (" -- budget from a synthetic step-cost table" if args.cost_table else ""),
                    "rows_per_step": rows_t,
                    "vocab": w.V, "logits_bytes_per_step": alg_bytes,
