@@ -89,6 +89,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ra.info = at<RowInfo>(ws, L.info);
     ra.partials = at<Partial>(ws, L.partials);
     ra.row_sync = at<RowSync>(ws, L.row_sync);
+    ra.ovf_idx = at<int32_t>(ws, L.ovf);
     ra.max_tasks = L.max_tasks;
     ra.num_sms = sm_count();
     ChainArgs& ca = c.ca;

@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         a.counters->n_slow = base_slow;
         a.counters->n_jobs = 0;
         a.counters->timeout = 0;
+        a.counters->n_ovf = 0;
     }
 }
 

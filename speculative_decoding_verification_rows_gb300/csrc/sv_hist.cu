@@ -1,5 +1,5 @@
-// sv_hist.cu -- exact per-value histogram kernel for sampling rows whose kept
-// set can be large (top-k off or above 32, with or without top-p).
+// sv_hist.cu -- exact per-value histogram kernels for sampling rows whose
+// kept set can be large (top-k off or above 32, with or without top-p).
 //
 // The target distribution of jianc99/sglang PR #8 ("build_speculative_verify_
 // target_probs") needs, for top-p, the mass-ordered cutoff over the whole
@@ -8,16 +8,25 @@
 // the transform follows from it exactly: the mass of a value is its count
 // times exp((v - m) / T), computed once per distinct value in fp64.
 //
-// One thread-block cluster handles one row at a time.  Each CTA streams its
-// slice (<= 65,535 elements, so a 16-bit counter cannot wrap) from HBM once
-// and counts keys in a 128 KB shared-memory histogram (two 16-bit counters
-// per word).  The cluster then works only on occupied binades (the 128 keys
-// of one sign+exponent): the CTAs sum their counters through distributed
-// shared memory, turn counts into fp64 masses (one exp per binade and a
-// geometric recurrence along the mantissa), and the first CTA walks binades
-// and then keys from the top to the top-k and top-p cutoffs.  Only the
+// Two kernels share the cutoff walk:
+//
+// * wide_rows_kernel (every row first): one CTA per row, several rows in
+//   flight per SM.  The row is streamed once with 16-byte loads; each key is
+//   counted in a 32-bit shared-memory counter of its binade (the 128 keys of
+//   one sign + exponent), and a binade gets its 128 counters the first time
+//   one of its keys is seen.  Rows of ordinary logits occupy a few dozen
+//   binades; a row that needs more than kWideSlots of them is handed on.
+// * hist_rows_kernel (rows handed on): one thread-block cluster per row, each
+//   CTA counting a slice of <= 65,535 elements in a full 65,536-key 16-bit
+//   histogram (so a counter cannot wrap), summed through distributed shared
+//   memory.
+//
+// Either way the occupied binades' counts become fp64 masses (one exp per
+// binade and a geometric recurrence along the mantissa), and one CTA walks
+// binades and then keys from the top to the top-k and top-p cutoffs.  Only the
 // probability of the row's own token may need one more look at the row (the
 // rank of a tied token at the cutoff).
+#include <climits>
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -40,42 +49,41 @@ struct CtaRes {
     int tie_count;             // tie-rank pass: ties below the token in this slice
 };
 
-struct RowPlan {               // decided by CTA 0, read by the others
+struct RowPlan {               // decided by the walking CTA, read by the others
     int skip;                  // 1: row is an error or done
     int need_tie;              // 1: run the tie-rank pass
     uint32_t cut_key;
     int token;
 };
 
-struct WalkState {             // CTA 0's walk, phase to phase
+struct WalkState {             // the walk, phase to phase
     double z_all, z1, mk_bin, mass_above_bk, mass_above_bp, z;
     uint32_t cnt_above_bk, k_key, k_ties, cut_key, cut_ties, kept;
     int bk, bp, bmin, found, done, slot;
 };
 
+// Shared memory of the cutoff walk: per-binade count and mass (zero where a
+// binade is empty), per-key counts and masses of up to two binades.
+struct WalkSmem {
+    BinSum sums[512];
+    uint32_t kc[2][128];
+    double ke[2][128];
+    WalkState walk;
+    RowPlan plan;
+};
+
 struct HistSmem {
     uint32_t hist[kHistWords];
-    BinSum sums[512];
     uint32_t occ[16];
     uint32_t occ_all[16];
     int occ_list[512];
     int n_occ;
     CtaRes res;
-    RowPlan plan;
     unsigned long long red64[kHistThreads / 32];
     int redi[kHistThreads / 32];
-    uint32_t kc[2][128];       // per-key counts of up to two binades (walk)
     uint32_t csc[kHistThreads][33];   // per-thread key counts of one binade quarter
-    double ke[2][128];         // per-key masses exp((v - m) / T)
-    WalkState walk;
+    WalkSmem w;
 };
-
-// 16-bit counter of key k in a histogram.
-__device__ __forceinline__ uint32_t hist_count(const uint32_t* h, uint32_t k)
-{
-    const uint32_t w = h[k >> 1];
-    return (k & 1u) ? (w >> 16) : (w & 0xFFFFu);
-}
 
 // Counts of the 32 keys b*128 + 32 q .. + 31, summed over the cluster's
 // histograms: 16 words (two counters each) read as four 16-byte vectors per
@@ -134,16 +142,328 @@ __device__ void load_binade_keys(cg::cluster_group& cluster, HistSmem& sm, int C
     if (q >= 4) return;
     if (b < 0 || b > 511) {
         for (int j = 0; j < 32; ++j) {
-            sm.kc[s][32 * q + j] = 0u;
-            sm.ke[s][32 * q + j] = 0.0;
+            sm.w.kc[s][32 * q + j] = 0u;
+            sm.w.ke[s][32 * q + j] = 0.0;
         }
         return;
     }
     uint32_t c[32];
     cluster_counts32(cluster, sm, C, b, q, c);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sm.kc[s][32 * q + j] = c[j];
-    for_binade_masses32(b, q, m, T, [&](int j, double e) { sm.ke[s][32 * q + j] = e; });
+    for (int j = 0; j < 32; ++j) sm.w.kc[s][32 * q + j] = c[j];
+    for_binade_masses32(b, q, m, T, [&](int j, double e) { sm.w.ke[s][32 * q + j] = e; });
+}
+
+// The cutoff walk of one row on one CTA, from the per-binade sums in sm.sums
+// (filled for every occupied binade, zero elsewhere): binade scans run on
+// warp 0, key walks on warp 0 and thread 0 (fp64 is scarce), and the
+// decisions travel through shared memory between phases.  load_keys(b, s)
+// fills sm.kc[s] / sm.ke[s] with the per-key counts and masses of binade b
+// (every thread calls it; it may use threads 0..3).  Writes the row's record
+// unless status != 0, and leaves in sm.plan whether the token's tie rank is
+// needed.  Every thread of the CTA must call it.
+template <typename LoadKeys>
+__device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const RowTask& task, const uint16_t* row, RowInfo* info,
+                         double m, int argmax, int status, LoadKeys load_keys)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const double T = (double)task.temp;
+    WalkState& W = sm.walk;
+    const int kk = task.k_eff;
+    const bool topk_on = kk < a.vocab;
+    if (tid == 0) {
+        sm.plan.skip = status != 0;
+        sm.plan.need_tie = 0;
+        sm.plan.token = task.token;
+    }
+    // Phase A (warp 0): binade scan on counts and masses, descending.
+    if (status == 0 && warp == 0) {
+        uint32_t cs = 0u;
+        double ms = 0.0;
+        int lowest = 1 << 30;
+        for (int i = 0; i < 16; ++i) {
+            const int b = 511 - 16 * lane - i;
+            cs += sm.sums[b].count;
+            ms += sm.sums[b].mass;
+            if (sm.sums[b].count) lowest = b;
+        }
+        uint32_t cin = cs;
+        double min_ = ms;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, cin, o);
+            const double z = __shfl_up_sync(0xFFFFFFFFu, min_, o);
+            if (lane >= o) {
+                cin += y;
+                min_ += z;
+            }
+        }
+        lowest = __reduce_min_sync(0xFFFFFFFFu, lowest);
+        if (lane == 31) W.z_all = min_;
+        if (lane == 0) {
+            W.bmin = lowest;
+            W.bk = -1;
+        }
+        __syncwarp();
+        uint32_t cex = cin - cs;
+        double mex = min_ - ms;
+        if (topk_on && cex < (uint32_t)kk && (uint32_t)kk <= cin) {
+            for (int i = 0; i < 16; ++i) {
+                const int b = 511 - 16 * lane - i;
+                if (cex + sm.sums[b].count >= (uint32_t)kk) {
+                    W.bk = b;
+                    W.cnt_above_bk = cex;
+                    W.mass_above_bk = mex;
+                    break;
+                }
+                cex += sm.sums[b].count;
+                mex += sm.sums[b].mass;
+            }
+        }
+    }
+    __syncthreads();
+    // Phase B: keys of the top-k boundary binade.
+    if (status == 0 && topk_on) load_keys(W.bk, 0);
+    __syncthreads();
+    // Phase C (warp 0): top-k cutoff key, kept ties, Z1.  Lane l holds
+    // keys 127 - 4l .. 124 - 4l (descending); warp scans give the counts
+    // and masses above each lane's keys.
+    if (status == 0 && warp == 0) {
+        if (topk_on) {
+            uint32_t c4 = 0u;
+            double m4 = 0.0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = 127 - 4 * lane - i;
+                c4 += sm.kc[0][f];
+                m4 += (double)sm.kc[0][f] * sm.ke[0][f];
+            }
+            uint32_t ci = c4;
+            double mi = m4;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+                const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+                if (lane >= o) {
+                    ci += y;
+                    mi += z;
+                }
+            }
+            uint32_t cum = W.cnt_above_bk + (ci - c4);
+            double mass = W.mass_above_bk + (mi - m4);
+            const bool mine = cum < (uint32_t)kk && (uint32_t)kk <= cum + c4;
+            if (mine) {
+                for (int i = 0; i < 4; ++i) {
+                    const int f = 127 - 4 * lane - i;
+                    const uint32_t c = sm.kc[0][f];
+                    if (c == 0u) continue;
+                    if (cum + c >= (uint32_t)kk) {
+                        W.k_key = (uint32_t)W.bk * 128u + f;
+                        W.k_ties = (uint32_t)kk - cum;
+                        W.mk_bin = mass - W.mass_above_bk + (double)W.k_ties * sm.ke[0][f];
+                        W.z1 = mass + (double)W.k_ties * sm.ke[0][f];
+                        break;
+                    }
+                    cum += c;
+                    mass += (double)c * sm.ke[0][f];
+                }
+            }
+        } else if (lane == 0) {
+            W.z1 = W.z_all;
+        }
+        if (lane == 0) W.found = 0;
+    }
+    __syncthreads();
+    // Phase D (warp 0): top-p binade on masses capped at the top-k cutoff.
+    const bool topp_on = task.top_p < 1.0f;
+    if (status == 0 && topp_on && warp == 0) {
+        const double target = (double)task.top_p * W.z1;
+        const int bk = W.bk;
+        double ms = 0.0;
+        for (int i = 0; i < 16; ++i) {
+            const int b = 511 - 16 * lane - i;
+            ms += (!topk_on || b > bk) ? sm.sums[b].mass : (b == bk ? W.mk_bin : 0.0);
+        }
+        double min_ = ms;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, min_, o);
+            if (lane >= o) min_ += y;
+        }
+        double mex = min_ - ms;
+        if (mex < target && target <= min_) {
+            for (int i = 0; i < 16; ++i) {
+                const int b = 511 - 16 * lane - i;
+                const double mb = (!topk_on || b > bk) ? sm.sums[b].mass : (b == bk ? W.mk_bin : 0.0);
+                if (mb > 0.0 && mex + mb >= target) {
+                    W.bp = b;
+                    W.mass_above_bp = mex;
+                    W.found = 1;
+                    break;
+                }
+                mex += mb;
+            }
+        }
+    }
+    __syncthreads();
+    // Phase E: keys of the binade that holds the final cutoff (slot 1).
+    int load_b = -1;
+    if (status == 0) {
+        if (W.found)
+            load_b = (topk_on && W.bp == W.bk) ? -1 : W.bp;
+        else if (!topk_on)
+            load_b = W.bmin;
+    }
+    if (load_b >= 0) load_keys(load_b, 1);
+    __syncthreads();
+    // Phase F (warp 0): the final cutoff, by a warp walk over the keys of
+    // binade bp (lane l: keys 127 - 4l .. 124 - 4l), then thread 0
+    // writes the row's record.
+    if (status == 0 && warp == 0) {
+        if (W.found) {
+            const int bp = W.bp;
+            const int slot = (topk_on && bp == W.bk) ? 0 : 1;
+            const double target = (double)task.top_p * W.z1;
+            uint32_t above = 0u;   // elements in binades above bp
+            for (int b = 511 - lane; b > bp; b -= 32) above += sm.sums[b].count;
+            above = __reduce_add_sync(0xFFFFFFFFu, above);
+            uint32_t ce4[4];
+            double e4[4];
+            uint32_t c4 = 0u;
+            double m4 = 0.0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int f = 127 - 4 * lane - i;
+                const uint32_t key = (uint32_t)bp * 128u + f;
+                uint32_t ce = sm.kc[slot][f];
+                if (topk_on && bp == W.bk) ce = key > W.k_key ? ce : (key == W.k_key ? W.k_ties : 0u);
+                ce4[i] = ce;
+                e4[i] = sm.ke[slot][f];
+                c4 += ce;
+                m4 += (double)ce * e4[i];
+            }
+            uint32_t ci = c4;
+            double mi = m4;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+                const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+                if (lane >= o) {
+                    ci += y;
+                    mi += z;
+                }
+            }
+            uint32_t cnt_above = above + (ci - c4);
+            double cum = W.mass_above_bp + (mi - m4);
+            int hit_f = -1;
+            uint32_t hit_j = 0u, hit_kept = 0u;
+            double hit_z = 0.0;
+            for (int i = 0; i < 4 && hit_f < 0; ++i) {
+                const uint32_t ce = ce4[i];
+                if (ce == 0u) continue;
+                const double e = e4[i];
+                if (cum + (double)ce * e >= target) {
+                    const double jd = ceil((target - cum) / e);
+                    uint32_t j = jd < 1.0 ? 1u : (jd > (double)ce ? ce : (uint32_t)jd);
+                    while (j > 1u && cum + (double)(j - 1u) * e >= target) --j;
+                    while (j < ce && cum + (double)j * e < target) ++j;
+                    hit_f = 127 - 4 * lane - i;
+                    hit_j = j;
+                    hit_kept = cnt_above + j;
+                    hit_z = cum + (double)j * e;
+                    break;
+                }
+                cum += (double)ce * e;
+                cnt_above += ce;
+            }
+            const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit_f >= 0);
+            if (hits && lane == __ffs(hits) - 1) {
+                W.cut_key = (uint32_t)bp * 128u + hit_f;
+                W.cut_ties = hit_j;
+                W.kept = hit_kept;
+                W.z = hit_z;
+                W.slot = slot;
+            }
+            if (lane == 0) W.done = hits != 0u;
+        } else if (lane == 0) {
+            W.done = 0;
+        }
+    }
+    __syncthreads();
+    if (status == 0 && tid == 0) {
+        uint32_t cut_key = W.cut_key, cut_ties = W.cut_ties, kept = W.kept;
+        double z = W.z;
+        int slot = W.slot;
+        if (!W.done) {
+            if (topk_on) {
+                cut_key = W.k_key;
+                cut_ties = W.k_ties;
+                kept = (uint32_t)kk;
+                z = W.z1;
+                slot = 0;
+            } else {
+                int f = 0;
+                while (f < 127 && sm.kc[1][f] == 0u) ++f;
+                cut_key = (uint32_t)W.bmin * 128u + f;
+                cut_ties = sm.kc[1][f];
+                kept = (uint32_t)a.vocab;
+                z = W.z1;
+                slot = 1;
+            }
+        }
+        const uint32_t cut_count = sm.kc[slot][cut_key & 127u];
+        info->desc.max_logit = (float)m;
+        info->desc.log_norm = logf((float)z);
+        info->desc.cutoff_logit = f32_of_key16(cut_key);
+        info->desc.cutoff_ties = (int)cut_ties;
+        info->desc.kept = (int)kept;
+        info->desc.argmax = argmax;
+        info->desc.status = 0;
+        info->desc.temperature = task.temp;
+        info->z = z;
+        info->z_rest = z - 1.0;   // the top token's mass is exp(0)
+        info->n_list = -1;
+        info->cut_count = (int)cut_count;
+        sm.plan.cut_key = cut_key;
+        // the row's token: kept unless it sits in a partial tie group
+        const int d = task.token;
+        if (d >= 0 && d < a.vocab) {
+            const uint32_t kd = key16_of_bf16(row[d]);
+            if (kd == cut_key && cut_ties < cut_count) {
+                sm.plan.need_tie = 1;
+            } else {
+                info->p_token = kd >= cut_key ? exp((key_value(kd) - m) / T) / z : 0.0;
+            }
+        } else {
+            info->p_token = nan("");
+        }
+    }
+}
+
+// Record of a row that failed (non-finite logits, or nothing but -inf).
+__device__ void write_error_row(RowInfo* info, double m, int argmax, int status, float temp)
+{
+    info->desc.max_logit = (float)m;
+    info->desc.log_norm = 0.0f;
+    info->desc.cutoff_logit = (float)m;
+    info->desc.cutoff_ties = 0;
+    info->desc.kept = 0;
+    info->desc.argmax = argmax;
+    info->desc.status = status;
+    info->desc.temperature = temp;
+    info->p_token = nan("");
+    info->z = 0.0;
+    info->z_rest = 0.0;
+    info->n_list = -1;
+    info->cut_count = 0;
+}
+
+// p of a token tied with the cutoff: kept when fewer than cutoff_ties of its
+// ties come before it.
+__device__ void finish_tied_token(RowInfo* info, uint32_t cut_key, int rank_d, double m, double T)
+{
+    const bool keep = rank_d < info->desc.cutoff_ties;
+    info->p_token = keep ? exp((key_value(cut_key) - m) / T) / info->z : 0.0;
 }
 
 // Process one row with the whole cluster; CTA 0 writes the RowInfo.
@@ -161,8 +481,8 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
         uint4* h4 = reinterpret_cast<uint4*>(sm.hist);
         for (int i = tid; i < kHistWords / 4; i += kHistThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
         for (int i = tid; i < 512; i += kHistThreads) {
-            sm.sums[i].mass = 0.0;
-            sm.sums[i].count = 0u;
+            sm.w.sums[i].mass = 0.0;
+            sm.w.sums[i].count = 0u;
         }
     }
     cluster.sync();
@@ -286,7 +606,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
         //    warp runs the same number of rounds (the loop bound is uniform
         //    per warp), so the 4-lane reductions below see all their lanes.
         const int n_occ = sm.n_occ;
-        BinSum* sums0 = cluster.map_shared_rank(sm.sums, 0);
+        BinSum* sums0 = cluster.map_shared_rank(sm.w.sums, 0);
         const int q4 = tid & 3;
         const int n_mine = n_occ > rank ? (n_occ - rank + C - 1) / C : 0;
         for (int i0 = (tid >> 2) - (lane >> 2); i0 < n_mine; i0 += kHistThreads / 4) {
@@ -322,285 +642,14 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
     }
     cluster.sync();
 
-    // 6. CTA 0: walk binades and keys from the top to the cutoffs.  Binade
-    //    scans run on warp 0, key walks on thread 0 (fp64 is scarce), and the
-    //    decisions travel through shared memory between phases.
-    if (rank == 0) {
-        WalkState& W = sm.walk;
-        const int kk = task.k_eff;
-        const bool topk_on = kk < a.vocab;
-        if (tid == 0) {
-            sm.plan.skip = status != 0;
-            sm.plan.need_tie = 0;
-            sm.plan.token = task.token;
-        }
-        // Phase A (warp 0): binade scan on counts and masses, descending.
-        if (status == 0 && warp == 0) {
-            uint32_t cs = 0u;
-            double ms = 0.0;
-            int lowest = 1 << 30;
-            for (int i = 0; i < 16; ++i) {
-                const int b = 511 - 16 * lane - i;
-                cs += sm.sums[b].count;
-                ms += sm.sums[b].mass;
-                if (sm.sums[b].count) lowest = b;
-            }
-            uint32_t cin = cs;
-            double min_ = ms;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, cin, o);
-                const double z = __shfl_up_sync(0xFFFFFFFFu, min_, o);
-                if (lane >= o) {
-                    cin += y;
-                    min_ += z;
-                }
-            }
-            lowest = __reduce_min_sync(0xFFFFFFFFu, lowest);
-            if (lane == 31) W.z_all = min_;
-            if (lane == 0) {
-                W.bmin = lowest;
-                W.bk = -1;
-            }
-            __syncwarp();
-            uint32_t cex = cin - cs;
-            double mex = min_ - ms;
-            if (topk_on && cex < (uint32_t)kk && (uint32_t)kk <= cin) {
-                for (int i = 0; i < 16; ++i) {
-                    const int b = 511 - 16 * lane - i;
-                    if (cex + sm.sums[b].count >= (uint32_t)kk) {
-                        W.bk = b;
-                        W.cnt_above_bk = cex;
-                        W.mass_above_bk = mex;
-                        break;
-                    }
-                    cex += sm.sums[b].count;
-                    mex += sm.sums[b].mass;
-                }
-            }
-        }
-        __syncthreads();
-        // Phase B: keys of the top-k boundary binade.
-        if (status == 0 && topk_on) load_binade_keys(cluster, sm, C, W.bk, 0, m, T);
-        __syncthreads();
-        // Phase C (warp 0): top-k cutoff key, kept ties, Z1.  Lane l holds
-        // keys 127 - 4l .. 124 - 4l (descending); warp scans give the counts
-        // and masses above each lane's keys.
-        if (status == 0 && warp == 0) {
-            if (topk_on) {
-                uint32_t c4 = 0u;
-                double m4 = 0.0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int f = 127 - 4 * lane - i;
-                    c4 += sm.kc[0][f];
-                    m4 += (double)sm.kc[0][f] * sm.ke[0][f];
-                }
-                uint32_t ci = c4;
-                double mi = m4;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
-                    const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
-                    if (lane >= o) {
-                        ci += y;
-                        mi += z;
-                    }
-                }
-                uint32_t cum = W.cnt_above_bk + (ci - c4);
-                double mass = W.mass_above_bk + (mi - m4);
-                const bool mine = cum < (uint32_t)kk && (uint32_t)kk <= cum + c4;
-                if (mine) {
-                    for (int i = 0; i < 4; ++i) {
-                        const int f = 127 - 4 * lane - i;
-                        const uint32_t c = sm.kc[0][f];
-                        if (c == 0u) continue;
-                        if (cum + c >= (uint32_t)kk) {
-                            W.k_key = (uint32_t)W.bk * 128u + f;
-                            W.k_ties = (uint32_t)kk - cum;
-                            W.mk_bin = mass - W.mass_above_bk + (double)W.k_ties * sm.ke[0][f];
-                            W.z1 = mass + (double)W.k_ties * sm.ke[0][f];
-                            break;
-                        }
-                        cum += c;
-                        mass += (double)c * sm.ke[0][f];
-                    }
-                }
-            } else if (lane == 0) {
-                W.z1 = W.z_all;
-            }
-            if (lane == 0) W.found = 0;
-        }
-        __syncthreads();
-        // Phase D (warp 0): top-p binade on masses capped at the top-k cutoff.
-        const bool topp_on = task.top_p < 1.0f;
-        if (status == 0 && topp_on && warp == 0) {
-            const double target = (double)task.top_p * W.z1;
-            const int bk = W.bk;
-            double ms = 0.0;
-            for (int i = 0; i < 16; ++i) {
-                const int b = 511 - 16 * lane - i;
-                ms += (!topk_on || b > bk) ? sm.sums[b].mass : (b == bk ? W.mk_bin : 0.0);
-            }
-            double min_ = ms;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xFFFFFFFFu, min_, o);
-                if (lane >= o) min_ += y;
-            }
-            double mex = min_ - ms;
-            if (mex < target && target <= min_) {
-                for (int i = 0; i < 16; ++i) {
-                    const int b = 511 - 16 * lane - i;
-                    const double mb = (!topk_on || b > bk) ? sm.sums[b].mass : (b == bk ? W.mk_bin : 0.0);
-                    if (mb > 0.0 && mex + mb >= target) {
-                        W.bp = b;
-                        W.mass_above_bp = mex;
-                        W.found = 1;
-                        break;
-                    }
-                    mex += mb;
-                }
-            }
-        }
-        __syncthreads();
-        // Phase E: keys of the binade that holds the final cutoff (slot 1).
-        int load_b = -1;
-        if (status == 0) {
-            if (W.found)
-                load_b = (topk_on && W.bp == W.bk) ? -1 : W.bp;
-            else if (!topk_on)
-                load_b = W.bmin;
-        }
-        if (load_b >= 0) load_binade_keys(cluster, sm, C, load_b, 1, m, T);
-        __syncthreads();
-        // Phase F (warp 0): the final cutoff, by a warp walk over the keys of
-        // binade bp (lane l: keys 127 - 4l .. 124 - 4l), then thread 0
-        // writes the row's record.
-        if (status == 0 && warp == 0) {
-            if (W.found) {
-                const int bp = W.bp;
-                const int slot = (topk_on && bp == W.bk) ? 0 : 1;
-                const double target = (double)task.top_p * W.z1;
-                uint32_t above = 0u;   // elements in binades above bp
-                for (int b = 511 - lane; b > bp; b -= 32) above += sm.sums[b].count;
-                above = __reduce_add_sync(0xFFFFFFFFu, above);
-                uint32_t ce4[4];
-                double e4[4];
-                uint32_t c4 = 0u;
-                double m4 = 0.0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int f = 127 - 4 * lane - i;
-                    const uint32_t key = (uint32_t)bp * 128u + f;
-                    uint32_t ce = sm.kc[slot][f];
-                    if (topk_on && bp == W.bk) ce = key > W.k_key ? ce : (key == W.k_key ? W.k_ties : 0u);
-                    ce4[i] = ce;
-                    e4[i] = sm.ke[slot][f];
-                    c4 += ce;
-                    m4 += (double)ce * e4[i];
-                }
-                uint32_t ci = c4;
-                double mi = m4;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
-                    const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
-                    if (lane >= o) {
-                        ci += y;
-                        mi += z;
-                    }
-                }
-                uint32_t cnt_above = above + (ci - c4);
-                double cum = W.mass_above_bp + (mi - m4);
-                int hit_f = -1;
-                uint32_t hit_j = 0u, hit_kept = 0u;
-                double hit_z = 0.0;
-                for (int i = 0; i < 4 && hit_f < 0; ++i) {
-                    const uint32_t ce = ce4[i];
-                    if (ce == 0u) continue;
-                    const double e = e4[i];
-                    if (cum + (double)ce * e >= target) {
-                        const double jd = ceil((target - cum) / e);
-                        uint32_t j = jd < 1.0 ? 1u : (jd > (double)ce ? ce : (uint32_t)jd);
-                        while (j > 1u && cum + (double)(j - 1u) * e >= target) --j;
-                        while (j < ce && cum + (double)j * e < target) ++j;
-                        hit_f = 127 - 4 * lane - i;
-                        hit_j = j;
-                        hit_kept = cnt_above + j;
-                        hit_z = cum + (double)j * e;
-                        break;
-                    }
-                    cum += (double)ce * e;
-                    cnt_above += ce;
-                }
-                const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit_f >= 0);
-                if (hits && lane == __ffs(hits) - 1) {
-                    W.cut_key = (uint32_t)bp * 128u + hit_f;
-                    W.cut_ties = hit_j;
-                    W.kept = hit_kept;
-                    W.z = hit_z;
-                    W.slot = slot;
-                }
-                if (lane == 0) W.done = hits != 0u;
-            } else if (lane == 0) {
-                W.done = 0;
-            }
-        }
-        __syncthreads();
-        if (status == 0 && tid == 0) {
-            uint32_t cut_key = W.cut_key, cut_ties = W.cut_ties, kept = W.kept;
-            double z = W.z;
-            int slot = W.slot;
-            if (!W.done) {
-                if (topk_on) {
-                    cut_key = W.k_key;
-                    cut_ties = W.k_ties;
-                    kept = (uint32_t)kk;
-                    z = W.z1;
-                    slot = 0;
-                } else {
-                    int f = 0;
-                    while (f < 127 && sm.kc[1][f] == 0u) ++f;
-                    cut_key = (uint32_t)W.bmin * 128u + f;
-                    cut_ties = sm.kc[1][f];
-                    kept = (uint32_t)a.vocab;
-                    z = W.z1;
-                    slot = 1;
-                }
-            }
-            const uint32_t cut_count = sm.kc[slot][cut_key & 127u];
-            info->desc.max_logit = (float)m;
-            info->desc.log_norm = logf((float)z);
-            info->desc.cutoff_logit = f32_of_key16(cut_key);
-            info->desc.cutoff_ties = (int)cut_ties;
-            info->desc.kept = (int)kept;
-            info->desc.argmax = argmax;
-            info->desc.status = 0;
-            info->desc.temperature = task.temp;
-            info->z = z;
-            info->z_rest = z - 1.0;   // the top token's mass is exp(0)
-            info->n_list = -1;
-            info->cut_count = (int)cut_count;
-            sm.plan.cut_key = cut_key;
-            // the row's token: kept unless it sits in a partial tie group
-            const int d = task.token;
-            if (d >= 0 && d < a.vocab) {
-                const uint32_t kd = key16_of_bf16(row[d]);
-                if (kd == cut_key && cut_ties < cut_count) {
-                    sm.plan.need_tie = 1;
-                } else {
-                    info->p_token = kd >= cut_key ? exp((key_value(kd) - m) / T) / z : 0.0;
-                }
-            } else {
-                info->p_token = nan("");
-            }
-        }
-    }
+    // 6. CTA 0: the cutoff walk on the cluster's sums.
+    if (rank == 0)
+        walk_row(sm.w, a, task, row, info, m, argmax, status,
+                 [&](int b, int s) { load_binade_keys(cluster, sm, C, b, s, m, T); });
     cluster.sync();
 
     // 7. tie rank of the row's token inside a partial tie group
-    const RowPlan plan = *cluster.map_shared_rank(&sm.plan, 0);
+    const RowPlan plan = *cluster.map_shared_rank(&sm.w.plan, 0);
     if (!plan.skip && plan.need_tie) {
         const int d = plan.token;
         const int e1 = min(s1, d);
@@ -618,23 +667,11 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
     cluster.sync();
     if (rank == 0 && tid == 0) {
         if (status != 0) {
-            info->desc.max_logit = (float)m;
-            info->desc.log_norm = 0.0f;
-            info->desc.cutoff_logit = (float)m;
-            info->desc.cutoff_ties = 0;
-            info->desc.kept = 0;
-            info->desc.argmax = argmax;
-            info->desc.status = status;
-            info->desc.temperature = task.temp;
-            info->p_token = nan("");
-            info->z = 0.0;
-            info->n_list = -1;
-            info->cut_count = 0;
+            write_error_row(info, m, argmax, status, task.temp);
         } else if (plan.need_tie) {
             int rank_d = 0;
             for (int r = 0; r < C; ++r) rank_d += cluster.map_shared_rank(&sm.res, r)->tie_count;
-            const bool keep = rank_d < info->desc.cutoff_ties;
-            info->p_token = keep ? exp((key_value(plan.cut_key) - m) / T) / info->z : 0.0;
+            finish_tied_token(info, plan.cut_key, rank_d, m, T);
         }
     }
     cluster.sync();   // the histograms may be cleared for the next row
@@ -650,17 +687,353 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(RowsArgs a, 
     const int rank = (int)cluster.block_rank();
     const int cluster_id = blockIdx.x / C;
     const int n_clusters = gridDim.x / C;
-    const int n_tasks = a.counters->n_slow;
+    const int n_tasks = a.counters->n_ovf;   // rows the one-CTA kernel handed on
     for (int t = cluster_id; t < n_tasks; t += n_clusters) {
-        const RowTask task = a.slow_tasks.get(t);
+        const RowTask task = a.slow_tasks.get(a.ovf_idx[t]);
         hist_row(cluster, sm, a, task, C, rank, slice);
     }
 }
 
+// ----------------------------------------------------------------------------
+// One CTA per row, counters for the binades the row occupies
+// ----------------------------------------------------------------------------
+constexpr int kWideThreads = 256;
+constexpr int kWideSlots = 64;           // binades with counters per row (4 threads per slot in the mass pass)
+constexpr int kWideUnroll = 8;           // 16-byte vectors per thread in flight
+constexpr int kUnclaimed = INT_MIN;      // base[] of a binade not seen yet in this row
+constexpr int kClaiming = INT_MIN + 1;   // base[] while a thread assigns the binade its counters
+constexpr int kBaseMin = -65536;         // a claimed base is 128 * (slot - b) >= -65,408
+constexpr int kClaimSpins = 1 << 14;     // polls before a thread stops waiting for a claim
+static_assert(kWideThreads == 4 * kWideSlots, "the mass pass takes four threads per slot");
+
+struct WideSmem {
+    uint32_t cnt[(kWideSlots + 1) * 128];   // per-key counters of the claimed binades, then 128 catch-alls
+    int32_t base[512];                      // binade b: 128 * (slot - b), so base + key indexes cnt
+    int32_t bin_of[kWideSlots];             // binade of each slot
+    int32_t n_slots;                        // slots handed out (beyond kWideSlots: overflow)
+    int32_t ovf;                            // 1: a key found no counter; the cluster kernel redoes the row
+    int32_t zero_mix;                       // 1: the row holds both -0 and +0
+    int32_t neg_nan;                        // 1: a key below that of -inf (a NaN with the sign bit set)
+    unsigned long long red64[kWideThreads / 32];
+    int32_t redi[kWideThreads / 32];
+    WalkSmem w;
+};
+
+// Counter base of binade b, giving it the next slot if it has none.  The
+// first thread to see b takes a slot and publishes the base; a thread that
+// sees b meanwhile polls (a bounded number of times) until it is published.
+// Out of slots, or out of patience, the keys go to the catch-all counters and
+// the row is marked for the cluster kernel.
+__device__ __noinline__ int claim_binade(WideSmem& sm, int b)
+{
+    int v = atomicCAS(&sm.base[b], kUnclaimed, kClaiming);
+    if (v == kUnclaimed) {
+        const int n = atomicAdd(&sm.n_slots, 1);
+        int nb;
+        if (n < kWideSlots) {
+            sm.bin_of[n] = b;
+            nb = 128 * (n - b);
+        } else {
+            sm.ovf = 1;
+            nb = 128 * (kWideSlots - b);
+        }
+        atomicExch(&sm.base[b], nb);
+        return nb;
+    }
+    volatile int* vb = &sm.base[b];
+    for (int i = 0; v == kClaiming && i < kClaimSpins; ++i) v = *vb;
+    if (v == kClaiming) {
+        sm.ovf = 1;
+        return 128 * (kWideSlots - b);
+    }
+    return v;
+}
+
+__device__ __forceinline__ void count_key(WideSmem& sm, uint32_t key)
+{
+    const int b = (int)(key >> 7);
+    int bs = sm.base[b];
+    if (bs < kBaseMin) bs = claim_binade(sm, b);
+    atomicAdd(&sm.cnt[bs + (int)key], 1u);
+}
+
+// Order key of a bf16 pattern without folding -0 into +0 (-0 gets the key
+// just below that of +0; the two counters are merged after the row).
+__device__ __forceinline__ uint32_t key_raw16(uint32_t h)
+{
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+// The same for both halves of a word: a byte permute replicates each half's
+// sign bit over the half, which selects the flip mask.
+__device__ __forceinline__ uint32_t keys2_raw(uint32_t w)
+{
+    uint32_t sgn;
+    asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(sgn) : "r"(w), "r"(0u));
+    return w ^ (sgn | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t x, uint32_t y)
+{
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+
+__device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, int t)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
+    const uint16_t* row = (const uint16_t*)(task.is_draft ? a.drf : a.tgt) + (size_t)task.row * (size_t)stride;
+    RowInfo* info = a.info + task.slot;
+    const double T = (double)task.temp;
+    const int V = a.vocab;
+
+    // 1. stream the row once: per-key counts and the first maximum.  The
+    //    elements before the first 16-byte boundary and after the last whole
+    //    vector are taken one by one.
+    uint32_t best_key = 0u;
+    int best_idx = INT_MAX;
+    auto note = [&](uint32_t key, int idx) {
+        if (key > best_key || (key == best_key && idx < best_idx)) {
+            best_key = key;
+            best_idx = idx;
+        }
+    };
+    const int head = min(V, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 1));
+    const int nvec = (V - head) >> 3;
+    const int tail0 = head + 8 * nvec;
+    if (tid < head) {
+        const uint32_t k = key_raw16(row[tid]);
+        count_key(sm, k);
+        note(k, tid);
+    }
+    if (tail0 + tid < V) {
+        const uint32_t k = key_raw16(row[tail0 + tid]);
+        count_key(sm, k);
+        note(k, tail0 + tid);
+    }
+    const uint4* vp = reinterpret_cast<const uint4*>(row + head);
+    for (int v0 = tid; v0 < nvec; v0 += kWideThreads * kWideUnroll) {
+        uint4 x[kWideUnroll];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            const int vi = v0 + u * kWideThreads;
+            x[u] = vi < nvec ? __ldg(vp + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            const int vi = v0 + u * kWideThreads;
+            if (vi < nvec) {
+                const uint32_t k0 = keys2_raw(x[u].x), k1 = keys2_raw(x[u].y), k2 = keys2_raw(x[u].z),
+                               k3 = keys2_raw(x[u].w);
+                count_key(sm, k0 & 0xFFFFu);
+                count_key(sm, k0 >> 16);
+                count_key(sm, k1 & 0xFFFFu);
+                count_key(sm, k1 >> 16);
+                count_key(sm, k2 & 0xFFFFu);
+                count_key(sm, k2 >> 16);
+                count_key(sm, k3 & 0xFFFFu);
+                count_key(sm, k3 >> 16);
+                const uint32_t mx = max_u16x2(max_u16x2(k0, k1), max_u16x2(k2, k3));
+                const uint32_t vmax = max(mx & 0xFFFFu, mx >> 16);
+                if (vmax >= best_key) {   // first element of the vector holding its maximum
+                    const int j = (k0 & 0xFFFFu) == vmax ? 0
+                                  : (k0 >> 16) == vmax   ? 1
+                                  : (k1 & 0xFFFFu) == vmax ? 2
+                                  : (k1 >> 16) == vmax   ? 3
+                                  : (k2 & 0xFFFFu) == vmax ? 4
+                                  : (k2 >> 16) == vmax   ? 5
+                                  : (k3 & 0xFFFFu) == vmax ? 6
+                                                           : 7;
+                    note(vmax, head + 8 * vi + j);
+                }
+            }
+        }
+    }
+    {
+        unsigned long long c = best_idx == INT_MAX ? 0ull
+                                                   : (((unsigned long long)best_key << 32) |
+                                                      (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_idx));
+        c = warp_max_u64(c);
+        if (lane == 0) sm.red64[warp] = c;
+    }
+    __syncthreads();   // every count is in
+
+    // 2. thread 0: fold -0 into +0, look for negative NaNs
+    if (tid == 0) {
+        int mix = 0;
+        const int bn = sm.base[255];   // binade of -0 (key 0x7FFF)
+        if (bn >= kBaseMin && sm.cnt[bn + 0x7FFF] != 0u) {
+            int bp = sm.base[256];     // binade of +0 (key 0x8000)
+            mix = bp >= kBaseMin && sm.cnt[bp + 0x8000] != 0u;
+            if (bp < kBaseMin) bp = claim_binade(sm, 256);
+            sm.cnt[bp + 0x8000] += sm.cnt[bn + 0x7FFF];
+            sm.cnt[bn + 0x7FFF] = 0u;
+        }
+        sm.zero_mix = mix;
+        int nn = 0;
+        const int b0 = sm.base[0];
+        if (b0 >= kBaseMin)
+            for (int k = 0; k < 0x7F; ++k) nn |= sm.cnt[b0 + k] != 0u ? 1 : 0;
+        sm.neg_nan = nn;
+    }
+    __syncthreads();
+    unsigned long long maxc = 0ull;
+#pragma unroll
+    for (int w = 0; w < kWideThreads / 32; ++w) maxc = sm.red64[w] > maxc ? sm.red64[w] : maxc;
+    const uint32_t raw_key = (uint32_t)(maxc >> 32);
+    const uint32_t m_key = raw_key == 0x7FFFu ? 0x8000u : raw_key;
+    int argmax = (int)(0xFFFFFFFFu - (uint32_t)maxc);
+    const double m = key_value(m_key);
+    const int status = (m_key >= 0xFF80u || sm.neg_nan) ? kNonfinite : (m_key == 0x007Fu ? kEmpty : 0);
+    const bool ovf = sm.ovf != 0;
+    const int used = ovf ? kWideSlots + 1 : sm.n_slots;
+
+    if (ovf) {
+        if (tid == 0) a.ovf_idx[atomicAdd(&a.counters->n_ovf, 1)] = t;
+    } else {
+        // the maximum is a zero and both signs occur: the first zero of either sign
+        if (sm.zero_mix && m_key == 0x8000u) {
+            int first = INT_MAX;
+            for (int i = tid; i < V; i += kWideThreads)
+                if ((row[i] & 0x7FFFu) == 0u) {
+                    first = i;
+                    break;
+                }
+            first = __reduce_min_sync(0xFFFFFFFFu, first);
+            if (lane == 0) sm.redi[warp] = first;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < kWideThreads / 32; ++w) first = min(first, sm.redi[w]);
+            argmax = first;
+            __syncthreads();
+        }
+
+        // 3. per-binade count and mass: four threads per slot, 32 keys each
+        {
+            const int s = tid >> 2, q = tid & 3;
+            const bool act = status == 0 && s < used;
+            const int b = act ? sm.bin_of[s] : 0;
+            double mass = 0.0;
+            uint32_t csum = 0u;
+            if (act) {
+                const uint32_t* c = sm.cnt + s * 128 + 32 * q;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) csum += c[j];
+                if (csum) for_binade_masses32(b, q, m, T, [&](int j, double e) { mass += (double)c[j] * e; });
+            }
+#pragma unroll
+            for (int o = 2; o; o >>= 1) {
+                mass += __shfl_xor_sync(0xFFFFFFFFu, mass, o, 4);
+                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
+            }
+            if (act && q == 0) {
+                sm.w.sums[b].mass = mass;
+                sm.w.sums[b].count = csum;
+            }
+        }
+        __syncthreads();
+
+        // 4. the cutoff walk, with per-key counts straight from the slots
+        walk_row(sm.w, a, task, row, info, m, argmax, status, [&](int b, int s) {
+            const int q = threadIdx.x;
+            if (q >= 4) return;
+            const int bs = (b >= 0 && b < 512) ? sm.base[b] : kUnclaimed;
+            if (bs < kBaseMin) {
+                for (int j = 0; j < 32; ++j) {
+                    sm.w.kc[s][32 * q + j] = 0u;
+                    sm.w.ke[s][32 * q + j] = 0.0;
+                }
+                return;
+            }
+            const uint32_t* c = sm.cnt + bs + 128 * b + 32 * q;
+            for (int j = 0; j < 32; ++j) sm.w.kc[s][32 * q + j] = c[j];
+            for_binade_masses32(b, q, m, T, [&](int j, double e) { sm.w.ke[s][32 * q + j] = e; });
+        });
+        __syncthreads();
+
+        // 5. tie rank of the row's token inside a partial tie group, or the
+        //    record of a failed row
+        const RowPlan plan = sm.w.plan;
+        if (status == 0 && plan.need_tie) {
+            int cnt = 0;
+            for (int i = tid; i < plan.token; i += kWideThreads) cnt += key16_of_bf16(row[i]) == plan.cut_key ? 1 : 0;
+            cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+            if (lane == 0) sm.redi[warp] = cnt;
+            __syncthreads();
+            if (tid == 0) {
+                int tot = 0;
+#pragma unroll
+                for (int w = 0; w < kWideThreads / 32; ++w) tot += sm.redi[w];
+                finish_tied_token(info, plan.cut_key, tot, m, T);
+            }
+        }
+        if (status != 0 && tid == 0) write_error_row(info, m, argmax, status, task.temp);
+    }
+
+    // 6. clear what the row used
+    __syncthreads();
+    {
+        uint4* c4 = reinterpret_cast<uint4*>(sm.cnt);
+        for (int i = tid; i < used * 32; i += kWideThreads) c4[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < 512; i += kWideThreads) {
+            sm.base[i] = kUnclaimed;
+            sm.w.sums[i].mass = 0.0;
+            sm.w.sums[i].count = 0u;
+        }
+        if (tid == 0) {
+            sm.n_slots = 0;
+            sm.ovf = 0;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kWideThreads, 4) wide_rows_kernel(RowsArgs a)
+{
+    pdl_enter();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw);
+    const int tid = threadIdx.x;
+    for (int i = tid; i < (kWideSlots + 1) * 128; i += kWideThreads) sm.cnt[i] = 0u;
+    for (int i = tid; i < 512; i += kWideThreads) {
+        sm.base[i] = kUnclaimed;
+        sm.w.sums[i].mass = 0.0;
+        sm.w.sums[i].count = 0u;
+    }
+    if (tid == 0) {
+        sm.n_slots = 0;
+        sm.ovf = 0;
+    }
+    __syncthreads();
+    const int n_tasks = a.counters->n_slow;
+    for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) wide_row(sm, a, a.slow_tasks.get(t), t);
+}
+
 }  // namespace
 
+// Every histogram row goes to the one-CTA kernel; the rows it hands on (more
+// occupied binades than it has counters for) go to the cluster kernel, which
+// finds their number on the device.
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s)
 {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int di = (dev >= 0 && dev < 128) ? dev : 0;
+    cudaError_t err = cudaSuccess;
+    {
+        static int wide_blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
+        const size_t smem = sizeof(WideSmem);
+        int& nb = wide_blocks[di];
+        if (nb == 0) {
+            err = cudaFuncSetAttribute(wide_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err != cudaSuccess) return err;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, wide_rows_kernel, kWideThreads, smem);
+            if (err != cudaSuccess) return err;
+            if (nb < 1) nb = 1;
+        }
+        err = launch_pdl(wide_rows_kernel, dim3(a.num_sms * nb), dim3(kWideThreads), smem, s, a);
+        if (err != cudaSuccess) return err;
+    }
     int C = (a.vocab + kHistMaxSlice - 1) / kHistMaxSlice;
     if (C < 1) C = 1;
     if (C > kMaxCluster) return cudaErrorInvalidValue;
@@ -669,13 +1042,10 @@ cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s)
     if (slice > kHistMaxSlice) slice = kHistMaxSlice & ~7;
     const size_t smem = sizeof(HistSmem);
     static int attr_set[128] = {0};   // once per device, before any graph capture
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t err = cudaSuccess;
-    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+    if (!attr_set[di]) {
         err = cudaFuncSetAttribute(hist_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        if (dev >= 0 && dev < 128) attr_set[dev] = 1;
+        attr_set[di] = 1;
     }
     int n_clusters = a.num_sms / C;
     if (n_clusters < 1) n_clusters = 1;

@@ -132,12 +132,13 @@ struct Counters {
     int32_t n_slow;
     int32_t n_jobs;
     int32_t timeout;   // set by a row kernel whose bounded wait gave up
-    int32_t pad[12];
+    int32_t n_ovf;     // histogram rows handed from the one-CTA kernel to the cluster kernel
+    int32_t pad[11];
 };
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, info, partials, row_sync, req, jobs, total;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, total;
     int slots, max_tasks;
     size_t n_partials;
 };
@@ -158,6 +159,7 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.counters = off;   off = align256(off + sizeof(Counters));
     L.fast_tasks = off; off = align256(off + kTaskBytes * (size_t)L.max_tasks + 16);   // + alignment of the arrays
     L.slow_tasks = off; off = align256(off + kTaskBytes * (size_t)L.max_tasks + 16);
+    L.ovf = off;        off = align256(off + sizeof(int32_t) * (size_t)L.max_tasks);
     L.info = off;       off = align256(off + sizeof(RowInfo) * (size_t)L.slots);
     L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
@@ -355,6 +357,7 @@ struct RowsArgs {
     RowInfo* info;
     Partial* partials;
     RowSync* row_sync;   // per fast task (zeroed by the prep kernel)
+    int32_t* ovf_idx;    // slow tasks the one-CTA histogram kernel could not hold (counted in n_ovf)
     int max_tasks;
     int num_sms;
 };
