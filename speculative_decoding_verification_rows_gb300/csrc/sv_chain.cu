@@ -26,8 +26,6 @@ namespace {
 
 constexpr int kPrepThreads = 1024;
 
-__device__ __forceinline__ int slot_target(int r, int K, int j) { return r * (2 * K + 1) + j; }
-__device__ __forceinline__ int slot_draft(int r, int K, int j) { return r * (2 * K + 1) + K + 1 + j; }
 
 __device__ __forceinline__ int bad_params(float T, float top_p)
 {
@@ -402,7 +400,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
             job.req = r;
             job.a = acc_len;
             job.residual = residual ? 1 : 0;
-            job.pad = 0;
+            job.done = 0;
             a.jobs[slot] = job;
             t = -2;
         }
@@ -621,340 +619,6 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
 }
 
 // ----------------------------------------------------------------------------
-// Full-row resample with exact fixed-point weights.
-// ----------------------------------------------------------------------------
-constexpr int kTableEntries = kTableBinades * 128;
-constexpr double kFix = 4611686018427387904.0;   // 2^62
-
-struct Dist {                 // one row's distribution, as the weight pass needs it
-    const uint16_t* row;
-    double m, T, z;
-    uint32_t cut_key;
-    int ties;                 // kept ties at the cutoff
-    int partial;              // ties < tokens at the cutoff: ranks are needed
-    int16_t* map;             // binade -> table slot, -1 = none
-    unsigned long long* tab;
-};
-
-struct ResampleSmem {
-    unsigned long long tab[kTableEntries];
-    int16_t map[2][512];
-    unsigned long long wsum_res[32], wsum_p[32];
-    int last_res[32], last_p[32];
-    int tie_p[32], tie_q[32];
-    int n_slots;
-    int fail;
-};
-
-// A binade is "tiny" when its values are below 2^-40 in magnitude: their
-// masses differ from exp(-m / T) by less than one part in 2^40 / T and are
-// computed per element instead of tabulated.
-__device__ __forceinline__ bool tiny_binade(int b) { return (b >= 256 && b < 256 + 87) || (b >= 169 && b <= 255); }
-
-__device__ __forceinline__ unsigned long long fix_of(double p)
-{
-    const double x = floor(p * kFix);
-    return x <= 0.0 ? 0ull : (x >= kFix ? (unsigned long long)kFix : (unsigned long long)x);
-}
-
-// 62-bit fixed-point probability of a key under a distribution (kept test
-// done by the caller).
-__device__ __forceinline__ unsigned long long fixp(const Dist& D, uint32_t key)
-{
-    const int b = (int)(key >> 7);
-    const int s = D.map[b];
-    if (s >= 0) return D.tab[s * 128 + (key & 127u)];
-    return fix_of(exp((key_value(key) - D.m) / D.T) / D.z);
-}
-
-__device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_rank)
-{
-    return key > D.cut_key || (key == D.cut_key && tie_rank < D.ties);
-}
-
-__global__ void __launch_bounds__(kResampleThreads, 1) resample_kernel(ChainArgs a)
-{
-    pdl_enter();
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ResampleSmem& sm = *reinterpret_cast<ResampleSmem*>(smem_raw);
-    if ((int)blockIdx.x >= a.counters->n_jobs) return;
-    const ResampleJob job = a.jobs[blockIdx.x];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r = job.req, pa = job.a, K = a.K, V = a.vocab;
-    const RowInfo& IP = a.info[slot_target(r, K, pa)];
-    const RowInfo& IQ = a.info[slot_draft(r, K, pa)];
-    const bool residual = job.residual != 0;
-    const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (K + 1) + pa;
-    Dist P, Q;
-    P.row = (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
-    P.m = IP.desc.max_logit;
-    P.T = IP.desc.temperature;
-    P.z = IP.z;
-    P.cut_key = key16_of_bf16(__float_as_uint(IP.desc.cutoff_logit) >> 16);
-    P.ties = IP.desc.cutoff_ties;
-    P.partial = IP.desc.cutoff_ties < IP.cut_count;
-    P.map = sm.map[0];
-    P.tab = sm.tab;
-    Q = P;
-    if (residual) {
-        Q.row = (const uint16_t*)a.drf + ((size_t)r * K + pa) * (size_t)a.stride_d;
-        Q.m = IQ.desc.max_logit;
-        Q.T = IQ.desc.temperature;
-        Q.z = IQ.z;
-        Q.cut_key = key16_of_bf16(__float_as_uint(IQ.desc.cutoff_logit) >> 16);
-        Q.ties = IQ.desc.cutoff_ties;
-        Q.partial = IQ.desc.cutoff_ties < IQ.cut_count;
-        Q.map = sm.map[1];
-    }
-
-    // 1. binade -> slot maps over each kept key range [cutoff, max]
-    if (tid == 0) {
-        int n = 0;
-        sm.fail = 0;
-        for (int dd = 0; dd < 2; ++dd) {
-            const Dist& D = dd == 0 ? P : Q;
-            int16_t* map = sm.map[dd];
-            for (int b = 0; b < 512; ++b) map[b] = -1;
-            if (dd == 1 && !residual) continue;
-            const int lo = (int)(D.cut_key >> 7);
-            const int hi = (int)(key16_of_bf16(__float_as_uint((float)D.m) >> 16) >> 7);
-            for (int b = lo; b <= hi; ++b) {
-                if (b == 0 || tiny_binade(b)) continue;
-                if (n < kTableBinades) map[b] = (int16_t)n;
-                ++n;
-            }
-        }
-        if (n > kTableBinades) sm.fail = 1;
-        sm.n_slots = n < kTableBinades ? n : kTableBinades;
-    }
-    __syncthreads();
-    if (sm.fail) {
-        if (tid == 0) {
-            int32_t* out = a.out_tokens + (size_t)r * (K + 1);
-            for (int j = 0; j <= K; ++j) out[j] = -1;
-            a.accept_len[r] = 0;
-            a.num_emitted[r] = 0;
-            if (a.row_status) a.row_status[(size_t)r * (K + 1) + pa] |= kUnsupported;
-        }
-        return;
-    }
-    // 2. fill the tables: thread -> (slot, 8 keys)
-    for (int dd = 0; dd < (residual ? 2 : 1); ++dd) {
-        const Dist& D = dd == 0 ? P : Q;
-        const int16_t* map = sm.map[dd];
-        for (int item = tid; item < 512 * 16; item += kResampleThreads) {
-            const int b = item >> 4, g = item & 15;
-            const int s = map[b];
-            if (s < 0) continue;
-            double e[8];
-            binade_masses(b, g, D.m, D.T, e);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sm.tab[s * 128 + 8 * g + j] = fix_of(e[j] / D.z);
-        }
-    }
-    __syncthreads();
-
-    // Contiguous range of each warp, in 256-element tiles (32 lanes x 8).
-    const int tiles = (V + 255) / 256;
-    const int tiles_per_warp = (tiles + 31) / 32;
-    const int w_begin = warp * tiles_per_warp * 256;
-    const int w_end = min(V, w_begin + tiles_per_warp * 256);
-    const bool need_ranks = P.partial || (residual && Q.partial);
-
-    // Weights of one lane's 8 elements starting at e0 (tie ranks advanced in order).
-    auto lane_weights = [&](int e0, int& rank_p, int& rank_q, unsigned long long wr[8], unsigned long long wp[8]) {
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            wr[s] = 0ull;
-            wp[s] = 0ull;
-            const int x = e0 + s;
-            if (x >= w_end) continue;
-            const uint32_t kp = key16_of_bf16(P.row[x]);
-            const bool inp = kept_key(P, kp, rank_p);
-            if (kp == P.cut_key) ++rank_p;
-            const unsigned long long fp_ = inp ? fixp(P, kp) : 0ull;
-            wp[s] = fp_;
-            if (residual) {
-                const uint32_t kq = key16_of_bf16(Q.row[x]);
-                const bool inq = kept_key(Q, kq, rank_q);
-                if (kq == Q.cut_key) ++rank_q;
-                const unsigned long long fq = inq ? fixp(Q, kq) : 0ull;
-                wr[s] = fp_ > fq ? fp_ - fq : 0ull;
-            } else {
-                wr[s] = fp_;
-            }
-        }
-    };
-    // Tie counts of one lane's 8 elements.
-    auto lane_ties = [&](int e0, int& tp_, int& tq_) {
-        tp_ = 0;
-        tq_ = 0;
-        if (!need_ranks) return;
-        for (int s = 0; s < 8; ++s) {
-            const int x = e0 + s;
-            if (x >= w_end) break;
-            tp_ += key16_of_bf16(P.row[x]) == P.cut_key;
-            if (residual) tq_ += key16_of_bf16(Q.row[x]) == Q.cut_key;
-        }
-    };
-    auto warp_excl_scan = [&](int v_) {
-        int incl = v_;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        return incl - v_;
-    };
-
-    // 3. tie bases of each warp range (only with partial tie groups)
-    {
-        int tp_tot = 0, tq_tot = 0;
-        if (need_ranks) {
-            for (int e = w_begin + lane * 8; e < w_end; e += 256) {
-                int tp_, tq_;
-                lane_ties(e, tp_, tq_);
-                tp_tot += tp_;
-                tq_tot += tq_;
-            }
-            tp_tot = __reduce_add_sync(0xFFFFFFFFu, tp_tot);
-            tq_tot = __reduce_add_sync(0xFFFFFFFFu, tq_tot);
-        }
-        if (lane == 0) {
-            sm.tie_p[warp] = tp_tot;
-            sm.tie_q[warp] = tq_tot;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int cp = 0, cq = 0;
-            for (int w = 0; w < 32; ++w) {
-                const int xp = sm.tie_p[w], xq = sm.tie_q[w];
-                sm.tie_p[w] = cp;
-                sm.tie_q[w] = cq;
-                cp += xp;
-                cq += xq;
-            }
-        }
-        __syncthreads();
-    }
-
-    // 4. pass A: exact weight sums per warp range (residual and p alone)
-    {
-        unsigned long long sr = 0ull, sp_ = 0ull;
-        int last_r = -1, last_p = -1;
-        int run_p = sm.tie_p[warp], run_q = sm.tie_q[warp];
-        for (int e = w_begin; e < w_end; e += 256) {
-            const int e0 = e + lane * 8;
-            int tp_, tq_;
-            lane_ties(e0, tp_, tq_);
-            int rp = run_p + warp_excl_scan(tp_), rq = run_q + warp_excl_scan(tq_);
-            run_p += __reduce_add_sync(0xFFFFFFFFu, tp_);
-            run_q += __reduce_add_sync(0xFFFFFFFFu, tq_);
-            unsigned long long wr[8], wp[8];
-            lane_weights(e0, rp, rq, wr, wp);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                sr += wr[s];
-                sp_ += wp[s];
-                if (wr[s]) last_r = e0 + s;
-                if (wp[s]) last_p = e0 + s;
-            }
-        }
-        sr = warp_sum_u64(sr);
-        sp_ = warp_sum_u64(sp_);
-        last_r = __reduce_max_sync(0xFFFFFFFFu, last_r);
-        last_p = __reduce_max_sync(0xFFFFFFFFu, last_p);
-        if (lane == 0) {
-            sm.wsum_res[warp] = sr;
-            sm.wsum_p[warp] = sp_;
-            sm.last_res[warp] = last_r;
-            sm.last_p[warp] = last_p;
-        }
-    }
-    __syncthreads();
-
-    // 5. the target, the warp range that holds it, and pass B inside it
-    unsigned long long W = 0ull, Wp = 0ull;
-    int last_r = -1, last_p = -1;
-    for (int w = 0; w < 32; ++w) {
-        W += sm.wsum_res[w];
-        Wp += sm.wsum_p[w];
-        last_r = max(last_r, sm.last_res[w]);
-        last_p = max(last_p, sm.last_p[w]);
-    }
-    bool use_p = !residual;
-    int resid_zero = 0;
-    if (residual && W == 0ull) {
-        use_p = true;
-        resid_zero = 1;
-    }
-    const unsigned long long Wuse = use_p ? Wp : W;
-    const unsigned long long* wsum = use_p ? sm.wsum_p : sm.wsum_res;
-    const unsigned long long u24 = uniform24(a.seed, (uint32_t)r, (uint32_t)pa, 1u);
-    const unsigned long long hi = __umul64hi(Wuse, u24), lo = Wuse * u24;
-    const unsigned long long target = (hi << 40) | (lo >> 24);   // floor(W * u)
-    int wstar = -1;
-    unsigned long long before = 0ull;
-    for (int w = 0; w < 32; ++w) {
-        if (before + wsum[w] > target) {
-            wstar = w;
-            break;
-        }
-        before += wsum[w];
-    }
-    __shared__ int s_x;
-    if (tid == 0) s_x = -1;
-    __syncthreads();
-    if (warp == wstar) {
-        unsigned long long cum = before;
-        int run_p = sm.tie_p[warp], run_q = sm.tie_q[warp];
-        for (int e = w_begin; e < w_end; e += 256) {
-            const int e0 = e + lane * 8;
-            int tp_, tq_;
-            lane_ties(e0, tp_, tq_);
-            int rp = run_p + warp_excl_scan(tp_), rq = run_q + warp_excl_scan(tq_);
-            run_p += __reduce_add_sync(0xFFFFFFFFu, tp_);
-            run_q += __reduce_add_sync(0xFFFFFFFFu, tq_);
-            unsigned long long wr[8], wp[8];
-            lane_weights(e0, rp, rq, wr, wp);
-            unsigned long long ls = 0ull;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) ls += use_p ? wp[s] : wr[s];
-            unsigned long long incl = ls;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned long long tile = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            if (cum + tile > target) {
-                const unsigned hitmask = __ballot_sync(0xFFFFFFFFu, cum + incl > target);
-                const int L = __ffs(hitmask) - 1;
-                if (lane == L) {
-                    unsigned long long c = cum + incl - ls;
-                    for (int s = 0; s < 8; ++s) {
-                        c += use_p ? wp[s] : wr[s];
-                        if (c > target) {
-                            s_x = e0 + s;
-                            break;
-                        }
-                    }
-                }
-                break;
-            }
-            cum += tile;
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int x = s_x;
-        if (x < 0) x = use_p ? last_p : last_r;
-        a.out_tokens[(size_t)r * (K + 1) + pa] = x;
-        if (resid_zero && a.row_status) a.row_status[(size_t)r * (K + 1) + pa] |= kResidZero;
-    }
-}
-
-// ----------------------------------------------------------------------------
 // sv_build_target_probs outputs
 // ----------------------------------------------------------------------------
 __global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t* desc)
@@ -1032,20 +696,6 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s)
     const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
     if (a.block) return launch_pdl(block_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
     return launch_pdl(chain_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
-}
-
-cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
-{
-    const size_t smem = sizeof(ResampleSmem);
-    static int attr_set[128] = {0};   // once per device, before any graph capture
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(resample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        if (dev >= 0 && dev < 128) attr_set[dev] = 1;
-    }
-    return launch_pdl(resample_kernel, dim3(a.n_req), dim3(kResampleThreads), smem, s, a);
 }
 
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,

@@ -69,66 +69,8 @@ __device__ __forceinline__ float bf16x2_hmax(uint32_t w)
 constexpr int kCtaWarps = kFastThreads / 32;
 constexpr int kStages = 3;                                  // chunks in flight per warp
 constexpr int kWarpChunkBytes = 32 * kFastVecs * 16;        // 4 KB: one warp chunk of either dtype
-constexpr long long kWaitPolls = 1ll << 20;                 // try_wait polls before a wait gives up
 constexpr int kBufCap = 32;                                 // buffered candidates per warp
 constexpr int kMergeAt = 16;                                // a chunk's end merges a buffer this full
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0u;
-}
-// Bounded wait: false when the phase did not complete within kWaitPolls polls.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
-{
-    for (long long i = 0; i < kWaitPolls; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-// Global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
-// aligned) completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(const void* p)
-{
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(smem_u32(p)));
-    return r;
-}
 
 // Ragged edge of a row (or a misaligned row): element loads, -inf past the end.
 template <int DT>

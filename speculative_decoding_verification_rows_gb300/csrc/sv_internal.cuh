@@ -23,8 +23,6 @@ constexpr int kHistThreads = 512;   // threads of the exact-histogram kernel
 constexpr int kHistWords = 32768;   // 65536 16-bit counters, two per 32-bit word
 constexpr int kHistMaxSlice = 65535;// elements per CTA so a 16-bit counter cannot wrap
 constexpr int kMaxCluster = 8;      // portable cluster size limit
-constexpr int kResampleThreads = 1024;
-constexpr int kTableBinades = 96;   // binades of fixed-point p / q a resample table holds
 
 // Row / position status bits (the public SV_ROW_* values).
 constexpr int kNonfinite = SV_ROW_NONFINITE, kEmpty = SV_ROW_EMPTY, kBadToken = SV_ROW_BAD_TOKEN,
@@ -123,8 +121,26 @@ struct ResampleJob {
     int32_t req;
     int32_t a;        // position of the emitted token
     int32_t residual; // 1: max(0, p_a - q_a); 0: p_a (bonus)
-    int32_t pad;
+    int32_t done;     // row chunks of the job the resample has finished (0 when listed)
 };
+
+// Row chunks of the full-row resample, and what each one leaves for the job's
+// last chunk: exact fixed-point sums of the residual and of p over the chunk,
+// with the elements tied at a partially kept cutoff summed apart in both of
+// their possible states (kept or not, for p and for q), and the tie counts.
+constexpr int kResampleUnit = 8192;
+constexpr int kMaxResampleUnits = (kMaxCluster * kHistMaxSlice + kResampleUnit - 1) / kResampleUnit;
+struct UnitSums {
+    unsigned long long base_res, base_p;   // elements not tied at a partial cutoff
+    unsigned long long tie_res[4];         // tied elements, [p ties kept * 2 + q ties kept]
+    unsigned long long tie_p[2];           // tied elements, [p ties kept]
+    int32_t tp, tq;                        // elements at p's / q's cutoff (partial groups only)
+};
+
+// Request slots of the RowInfo array: target positions 0..K, then draft
+// positions 0..K-1.
+__host__ __device__ __forceinline__ int slot_target(int r, int K, int j) { return r * (2 * K + 1) + j; }
+__host__ __device__ __forceinline__ int slot_draft(int r, int K, int j) { return r * (2 * K + 1) + K + 1 + j; }
 
 // Counters at the head of the workspace.
 struct Counters {
@@ -138,7 +154,7 @@ struct Counters {
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, total;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, units, total;
     int slots, max_tasks;
     size_t n_partials;
 };
@@ -165,6 +181,7 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
+    L.units = off;      off = align256(off + sizeof(UnitSums) * (size_t)n_req * (size_t)kMaxResampleUnits);
     L.total = off;
     return L;
 }
@@ -307,6 +324,69 @@ __device__ __forceinline__ float load_logit(const void* row, int64_t i)
 }
 
 // ----------------------------------------------------------------------------
+// mbarriers and bulk asynchronous copies (cp.async.bulk) into shared memory.
+// Every wait is bounded: it gives up after kWaitPolls polls.
+// ----------------------------------------------------------------------------
+constexpr long long kWaitPolls = 1ll << 20;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+// false when the phase did not complete within kWaitPolls polls
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
+{
+    for (long long i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// Global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
+// aligned) completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
+
+// ----------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // the programmatic-serialisation attribute, so it may become resident while the
 // kernel before it on the stream drains.  It first waits for that kernel to
@@ -395,6 +475,7 @@ struct ChainArgs {
     RowInfo* info;
     ReqState* req;
     ResampleJob* jobs;
+    UnitSums* units;   // [n_req][kMaxResampleUnits]
     int num_sms;
 };
 

@@ -1,0 +1,583 @@
+// sv_resample.cu -- full-row resample of the emitted token when the kept set
+// is not listed (more than 32 tokens): the residual max(0, p_a - q_a) at the
+// first rejection, or p at the bonus position (the "Identical rejection
+// scheme" of local-inference-lab/rtx6kpro dspark-upstream-consolidation.md).
+//
+// Weights are exact fixed-point numbers, p and q times 2^62, floored, so
+// sums of them do not depend on the order of summation.  The token is the
+// first index, in index order, where the running sum passes floor(W * u) for
+// the job's uniform u(r, a, 1).  Elements tied at a partially kept cutoff are
+// kept in index order up to the row's cutoff_ties.
+//
+// The weight of a key comes from a per-binade table in shared memory (fp64
+// exp((v - m) / T) / Z along the binade's mantissa, then floored), built for
+// the kept binades of magnitude 2^-6 and up, where ordinary logits sit; keys
+// below the one whose weight floors to 0 weigh 0; any other kept key (small
+// magnitudes, or binades beyond the table) gets its own fp64 exp.
+//
+// Every row is cut into chunks of kResampleUnit elements spread over a
+// persistent grid.  A chunk's CTA bulk-copies the chunk of p's and q's rows
+// into shared memory, streams it once and leaves the chunk's sums, with the
+// tied elements summed in each of their possible states.  The CTA that
+// finishes a job's last chunk combines the sums, rescans in index order the
+// (at most two) chunks where a tie group's kept part ends, and then the one
+// chunk that holds the target, to find the token.
+#include <math.h>
+
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace {
+
+constexpr double kFix = 4611686018427387904.0;   // 2^62
+constexpr int kSmallLo = 135, kSmallHi = 377;      // binades of |v| < 2^-6 (both signs, and the zeros)
+
+struct Dist {                 // one row's distribution, as the weight passes need it
+    const uint16_t* row;
+    double m, T, z;
+    uint32_t cut_key;         // smallest kept key
+    uint32_t zero_key;        // keys below it weigh 0 (p < 2^-62)
+    int ties;                 // kept ties at the cutoff
+    int partial;              // ties < tokens at the cutoff: ranks are needed
+    int16_t* map;             // binade -> table slot, -1: weight computed per key
+    unsigned long long* tab;
+};
+
+__device__ __forceinline__ unsigned long long fix_of(double p)
+{
+    const double x = floor(p * kFix);
+    return x <= 0.0 ? 0ull : (x >= kFix ? (unsigned long long)kFix : (unsigned long long)x);
+}
+
+// 62-bit fixed-point probability of a key under a distribution (kept test
+// done by the caller).
+__device__ __forceinline__ unsigned long long fixp(const Dist& D, uint32_t key)
+{
+    if (key < D.zero_key) return 0ull;
+    const int s = D.map[key >> 7];
+    if (s >= 0) return D.tab[s * 128 + (key & 127u)];
+    return fix_of(exp((key_value(key) - D.m) / D.T) / D.z);
+}
+
+__device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_rank)
+{
+    return key > D.cut_key || (key == D.cut_key && tie_rank < D.ties);
+}
+
+// Key below which every weight floors to 0: values under m + T (ln Z - 62 ln 2),
+// less two keys for the roundings of the bound (0 when the bound is too close
+// to zero for that margin to mean anything).
+__device__ __forceinline__ uint32_t zero_key_of(double m, double T, double z)
+{
+    const double v0 = m + T * (log(z) - 62.0 * 0.69314718055994530942);
+    if (!(fabs(v0) > 1e-3 * T) || !(v0 > -3.0e38)) return 0u;
+    const uint32_t k = key16_of_bf16(__float_as_uint((float)v0) >> 16);
+    return k >= 2u ? k - 2u : 0u;
+}
+
+constexpr int kResThreads = 256;
+constexpr int kResBinades = 48;    // table slots, p's and q's binades together
+constexpr int kResTile = kResThreads * 8;
+
+struct ResSmem {
+    alignas(16) uint16_t stage[2][kResampleUnit];   // the chunk of p's row and of q's row
+    unsigned long long bar;                         // completion of the chunk's bulk copies
+    int stage_ok;                                   // 0 after a copy did not arrive in time: plain loads from then on
+    unsigned long long tab[kResBinades * 128];
+    int16_t map[2][512];
+    int slot_bin[kResBinades];
+    int slot_dist[kResBinades];
+    int cur_job;      // job whose tables are loaded (-1: none)
+    int last;         // this CTA finished the job's last chunk
+    int found;        // token found by the target search (-1: not yet)
+    int halt;         // the target search is over
+    unsigned long long red[kResThreads / 32][10];
+    unsigned long long scan[kResThreads / 32];
+    // the combine
+    int state_p[kMaxResampleUnits], state_q[kMaxResampleUnits];   // 0 none kept, 1 all kept, 2 split
+    int off_p[kMaxResampleUnits], off_q[kMaxResampleUnits];       // ties before the chunk
+    unsigned long long ex_res[2], ex_p[2];                        // exact sums of the split chunks
+    int ex_unit[2];
+    int n_ex;
+};
+
+// Binades of a range that may hold a table: not binade 0 (-inf and negative
+// NaN) and not of small magnitude.  Count of them in [x, y).
+__device__ __forceinline__ int tabled_in(int x, int y)
+{
+    if (y <= x) return 0;
+    int n = y - x;
+    const int t0 = max(x, kSmallLo), t1 = min(y, kSmallHi);
+    if (t1 > t0) n -= t1 - t0;
+    if (x == 0) n -= 1;
+    return n;
+}
+
+// The job's p and q as the weight passes need them (tables in shared memory).
+__device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob& job, ResSmem& sm, Dist& P, Dist& Q)
+{
+    const int r = job.req, pa = job.a, K = a.K;
+    const RowInfo& IP = a.info[slot_target(r, K, pa)];
+    const RowInfo& IQ = a.info[slot_draft(r, K, pa)];
+    const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (K + 1) + pa;
+    P.row = (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
+    P.m = IP.desc.max_logit;
+    P.T = IP.desc.temperature;
+    P.z = IP.z;
+    P.cut_key = key16_of_bf16(__float_as_uint(IP.desc.cutoff_logit) >> 16);
+    P.zero_key = zero_key_of(P.m, P.T, P.z);
+    P.ties = IP.desc.cutoff_ties;
+    P.partial = IP.desc.cutoff_ties < IP.cut_count;
+    P.map = sm.map[0];
+    P.tab = sm.tab;
+    Q = P;
+    if (job.residual) {
+        Q.row = (const uint16_t*)a.drf + ((size_t)r * K + pa) * (size_t)a.stride_d;
+        Q.m = IQ.desc.max_logit;
+        Q.T = IQ.desc.temperature;
+        Q.z = IQ.z;
+        Q.cut_key = key16_of_bf16(__float_as_uint(IQ.desc.cutoff_logit) >> 16);
+        Q.zero_key = zero_key_of(Q.m, Q.T, Q.z);
+        Q.ties = IQ.desc.cutoff_ties;
+        Q.partial = IQ.desc.cutoff_ties < IQ.cut_count;
+        Q.map = sm.map[1];
+    }
+}
+
+// Tables of the job's kept binades that may hold one, from the top binade of
+// each distribution down, p's first; q keeps at least half of the slots when
+// it needs them.  Every thread calls it.
+__device__ void load_tables(ResSmem& sm, const Dist& P, const Dist& Q, bool residual)
+{
+    const int tid = threadIdx.x;
+    const int hiP = (int)(key16_of_bf16(__float_as_uint((float)P.m) >> 16) >> 7);
+    const int loP = (int)(max(P.cut_key, P.zero_key) >> 7);
+    const int hiQ = (int)(key16_of_bf16(__float_as_uint((float)Q.m) >> 16) >> 7);
+    const int loQ = (int)(max(Q.cut_key, Q.zero_key) >> 7);
+    const int nP = tabled_in(loP, hiP + 1);
+    const int nQ = residual ? tabled_in(loQ, hiQ + 1) : 0;
+    const int capP = min(nP, kResBinades - min(nQ, kResBinades / 2));
+    const int capQ = min(nQ, kResBinades - capP);
+    for (int b = tid; b < 512; b += kResThreads) {
+        const bool tb = b != 0 && (b < kSmallLo || b >= kSmallHi);
+        int sP = -1, sQ = -1;
+        if (tb && b >= loP && b <= hiP) {
+            const int above = tabled_in(b + 1, hiP + 1);
+            if (above < capP) sP = above;
+        }
+        if (residual && tb && b >= loQ && b <= hiQ) {
+            const int above = tabled_in(b + 1, hiQ + 1);
+            if (above < capQ) sQ = capP + above;
+        }
+        sm.map[0][b] = (int16_t)sP;
+        sm.map[1][b] = (int16_t)sQ;
+        if (sP >= 0) {
+            sm.slot_bin[sP] = b;
+            sm.slot_dist[sP] = 0;
+        }
+        if (sQ >= 0) {
+            sm.slot_bin[sQ] = b;
+            sm.slot_dist[sQ] = 1;
+        }
+    }
+    __syncthreads();
+    for (int item = tid; item < (capP + capQ) * 16; item += kResThreads) {
+        const int s = item >> 4, g = item & 15;
+        const Dist& D = sm.slot_dist[s] ? Q : P;
+        double e[8];
+        binade_masses(sm.slot_bin[s], g, D.m, D.T, e);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sm.tab[s * 128 + 8 * g + j] = fix_of(e[j] / D.z);
+    }
+    __syncthreads();
+}
+
+// Canonical keys of eight consecutive elements of a row (x0 .. x0 + 7, those
+// at or past x_end read as -inf, which no kept set holds).
+__device__ __forceinline__ void load_keys8(const uint16_t* row, int x0, int x_end, bool vec_ok, uint32_t k[8])
+{
+    if (vec_ok && x0 + 8 <= x_end) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + x0));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            k[2 * i] = key16_of_bf16(w[i] & 0xFFFFu);
+            k[2 * i + 1] = key16_of_bf16(w[i] >> 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) k[i] = x0 + i < x_end ? key16_of_bf16(row[x0 + i]) : 0x007Fu;
+    }
+}
+
+// Canonical keys of eight consecutive staged elements.
+__device__ __forceinline__ void stage_keys8(const uint16_t* st, uint32_t k[8])
+{
+    const uint4 v = ld_shared_v4(st);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        k[2 * i] = key16_of_bf16(w[i] & 0xFFFFu);
+        k[2 * i + 1] = key16_of_bf16(w[i] >> 16);
+    }
+}
+
+// Bulk-copies elements [x_begin, x_end) of p's row (and q's) into the stage,
+// when the rows allow it (16-byte aligned, a whole number of 8-element
+// vectors).  Returns whether the chunk is staged.  Every thread calls it;
+// `phase` is the barrier's parity, tracked alike by every thread.
+__device__ bool stage_unit(ResSmem& sm, const Dist& P, const Dist& Q, bool residual, int x_begin, int x_end,
+                           bool vec_ok, uint32_t& phase)
+{
+    const int n = x_end - x_begin;
+    if (!sm.stage_ok || !vec_ok || (n & 7)) return false;
+    const uint32_t bytes = (uint32_t)n * 2u;
+    __syncthreads();   // nobody reads the previous chunk any more
+    if (threadIdx.x == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(&sm.bar, residual ? 2u * bytes : bytes);
+        bulk_g2s(sm.stage[0], P.row + x_begin, bytes, &sm.bar);
+        if (residual) bulk_g2s(sm.stage[1], Q.row + x_begin, bytes, &sm.bar);
+    }
+    const bool ok = __syncthreads_and(mbar_wait(&sm.bar, phase)) != 0;
+    if (!ok) {   // stop staging; the copies in flight are waited for before the CTA leaves
+        __syncthreads();
+        if (threadIdx.x == 0) sm.stage_ok = 0;
+        __syncthreads();
+        return false;
+    }
+    phase ^= 1u;
+    return true;
+}
+
+__device__ __forceinline__ unsigned long long sat_sub(unsigned long long x, unsigned long long y)
+{
+    return x > y ? x - y : 0ull;
+}
+
+// Sum of x over the CTA (every thread gets it).
+__device__ __forceinline__ unsigned long long block_sum_u64(ResSmem& sm, unsigned long long x)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    x = warp_sum_u64(x);
+    __syncthreads();
+    if (lane == 0) sm.scan[warp] = x;
+    __syncthreads();
+    unsigned long long t = 0ull;
+#pragma unroll
+    for (int w = 0; w < kResThreads / 32; ++w) t += sm.scan[w];
+    return t;
+}
+
+// Exclusive prefix of x over the CTA in thread order, and the total.
+__device__ __forceinline__ unsigned long long block_excl_u64(ResSmem& sm, unsigned long long x,
+                                                             unsigned long long& total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    __syncthreads();
+    if (lane == 31) sm.scan[warp] = incl;
+    __syncthreads();
+    unsigned long long before = 0ull;
+    total = 0ull;
+#pragma unroll
+    for (int w = 0; w < kResThreads / 32; ++w) {
+        const unsigned long long t = sm.scan[w];
+        before += w < warp ? t : 0ull;
+        total += t;
+    }
+    return before + incl - x;
+}
+
+// One chunk in index order with the exact tie ranks: the residual and p sums
+// (mode 0), or the index where the running sum of the chosen weights passes
+// `target` (mode 1; -1 if it does not within the chunk).  Every thread calls it.
+__device__ int rescan_unit(ResSmem& sm, const Dist& P, const Dist& Q, bool residual, int x_begin, int x_end,
+                           int run_p, int run_q, bool vec_ok, int mode, bool use_p, unsigned long long target,
+                           unsigned long long& sum_res, unsigned long long& sum_p, uint32_t& phase)
+{
+    const int tid = threadIdx.x;
+    unsigned long long acc_r = 0ull, acc_p = 0ull, cum = 0ull;
+    const bool staged = stage_unit(sm, P, Q, residual, x_begin, x_end, vec_ok, phase);
+    if (tid == 0) {
+        sm.found = -1;
+        sm.halt = 0;
+    }
+    __syncthreads();
+    for (int t0 = x_begin; t0 < x_end; t0 += kResTile) {
+        const int x0 = t0 + 8 * tid;
+        uint32_t kp[8], kq[8];
+        if (staged && x0 < x_end) {
+            stage_keys8(sm.stage[0] + (x0 - x_begin), kp);
+            if (residual) stage_keys8(sm.stage[1] + (x0 - x_begin), kq);
+        } else {
+            load_keys8(P.row, x0, x_end, vec_ok, kp);
+            if (residual) load_keys8(Q.row, x0, x_end, vec_ok, kq);
+        }
+        uint32_t cp = 0u, cq = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            cp += (P.partial && kp[i] == P.cut_key) ? 1u : 0u;
+            cq += (residual && Q.partial && kq[i] == Q.cut_key) ? 1u : 0u;
+        }
+        unsigned long long tot;
+        const unsigned long long ex = block_excl_u64(sm, ((unsigned long long)cp << 32) | cq, tot);
+        int rp = run_p + (int)(ex >> 32), rq = run_q + (int)(ex & 0xFFFFFFFFu);
+        run_p += (int)(tot >> 32);
+        run_q += (int)(tot & 0xFFFFFFFFu);
+        unsigned long long w8[8];
+        unsigned long long tr = 0ull, tpp = 0ull;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool inp = kept_key(P, kp[i], rp);
+            if (P.partial && kp[i] == P.cut_key) ++rp;
+            const unsigned long long wp = inp ? fixp(P, kp[i]) : 0ull;
+            unsigned long long wr = wp;
+            if (residual) {
+                const bool inq = kept_key(Q, kq[i], rq);
+                if (Q.partial && kq[i] == Q.cut_key) ++rq;
+                wr = sat_sub(wp, inq && wp ? fixp(Q, kq[i]) : 0ull);
+            }
+            tr += wr;
+            tpp += wp;
+            w8[i] = use_p ? wp : wr;
+        }
+        acc_r += tr;
+        acc_p += tpp;
+        if (mode == 1) {
+            const unsigned long long mine = use_p ? tpp : tr;
+            unsigned long long tile;
+            const unsigned long long before = cum + block_excl_u64(sm, mine, tile);
+            if (before <= target && target < before + mine) {   // this thread holds the crossing
+                unsigned long long c = before;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c += w8[i];
+                    if (c > target) {
+                        sm.found = x0 + i;
+                        break;
+                    }
+                }
+                sm.halt = 1;
+            }
+            cum += tile;
+            __syncthreads();
+            if (sm.halt) break;
+        }
+    }
+    if (mode == 0) {
+        sum_res = block_sum_u64(sm, acc_r);
+        sum_p = block_sum_u64(sm, acc_p);
+    }
+    __syncthreads();
+    return sm.found;
+}
+
+__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units)
+{
+    pdl_enter();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ResSmem& sm = *reinterpret_cast<ResSmem*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int V = a.vocab, K = a.K;
+    const long long total = (long long)a.counters->n_jobs * n_units;
+    const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) {
+        sm.cur_job = -1;
+        sm.stage_ok = 1;
+        mbar_init(&sm.bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0u;
+    for (long long u = u_lo; u < u_hi; ++u) {
+        const int j = (int)(u / n_units), c = (int)(u % n_units);
+        const ResampleJob job = a.jobs[j];
+        const bool residual = job.residual != 0;
+        Dist P, Q;
+        job_dists(a, job, sm, P, Q);
+        if (sm.cur_job != j) {
+            load_tables(sm, P, Q, residual);
+            if (tid == 0) sm.cur_job = j;
+        }
+        const bool vec_ok = ((uintptr_t)P.row & 15u) == 0u && (!residual || ((uintptr_t)Q.row & 15u) == 0u);
+        const int x_begin = c * kResampleUnit, x_end = min(V, x_begin + kResampleUnit);
+
+        // 1. the chunk's sums in one pass
+        unsigned long long base_r = 0ull, base_p = 0ull, tie_r[4] = {0ull, 0ull, 0ull, 0ull}, tie_p[2] = {0ull, 0ull};
+        uint32_t tp = 0u, tq = 0u;
+        const bool staged = stage_unit(sm, P, Q, residual, x_begin, x_end, vec_ok, phase);
+        for (int x0 = x_begin + 8 * tid; x0 < x_end; x0 += kResTile) {
+            uint32_t kp[8], kq[8];
+            if (staged) {
+                stage_keys8(sm.stage[0] + (x0 - x_begin), kp);
+                if (residual) stage_keys8(sm.stage[1] + (x0 - x_begin), kq);
+            } else {
+                load_keys8(P.row, x0, x_end, vec_ok, kp);
+                if (residual) load_keys8(Q.row, x0, x_end, vec_ok, kq);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const bool tP = P.partial && kp[i] == P.cut_key;
+                const bool tQ = residual && Q.partial && kq[i] == Q.cut_key;
+                tp += tP ? 1u : 0u;
+                tq += tQ ? 1u : 0u;
+                if (kp[i] < P.cut_key) continue;   // outside p's kept set in every state
+                const unsigned long long wp = fixp(P, kp[i]);
+                const bool qk = residual && (kq[i] > Q.cut_key || (kq[i] == Q.cut_key && !Q.partial));
+                const unsigned long long wq = qk ? fixp(Q, kq[i]) : 0ull;
+                if (!tP && !tQ) {
+                    base_p += wp;
+                    base_r += residual ? sat_sub(wp, wq) : wp;
+                } else {
+                    const unsigned long long wqt = tQ ? fixp(Q, kq[i]) : wq;
+#pragma unroll
+                    for (int sp_ = 0; sp_ < 2; ++sp_) {
+                        const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
+                        tie_p[sp_] += p_;
+#pragma unroll
+                        for (int sq = 0; sq < 2; ++sq) {
+                            const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
+                            tie_r[2 * sp_ + sq] += residual ? sat_sub(p_, q_) : p_;
+                        }
+                    }
+                }
+            }
+        }
+        {
+            unsigned long long v[10] = {base_r, base_p, tie_r[0], tie_r[1], tie_r[2], tie_r[3], tie_p[0], tie_p[1],
+                                        (unsigned long long)tp, (unsigned long long)tq};
+#pragma unroll
+            for (int i = 0; i < 10; ++i) v[i] = warp_sum_u64(v[i]);
+            if (lane == 0)
+#pragma unroll
+                for (int i = 0; i < 10; ++i) sm.red[warp][i] = v[i];
+            __syncthreads();
+            if (tid == 0) {
+                unsigned long long s[10] = {};
+                for (int w = 0; w < kResThreads / 32; ++w)
+                    for (int i = 0; i < 10; ++i) s[i] += sm.red[w][i];
+                UnitSums& U = a.units[(size_t)j * kMaxResampleUnits + c];
+                U.base_res = s[0];
+                U.base_p = s[1];
+                for (int i = 0; i < 4; ++i) U.tie_res[i] = s[2 + i];
+                U.tie_p[0] = s[6];
+                U.tie_p[1] = s[7];
+                U.tp = (int32_t)s[8];
+                U.tq = (int32_t)s[9];
+                __threadfence();
+                sm.last = atomicAdd(&a.jobs[j].done, 1) == n_units - 1;
+            }
+            __syncthreads();
+        }
+        if (!sm.last) continue;
+        __threadfence();
+
+        // 2. the job's last chunk: states of the tie groups per chunk
+        const UnitSums* U = a.units + (size_t)j * kMaxResampleUnits;
+        if (tid == 0) {
+            int op = 0, oq = 0;
+            sm.n_ex = 0;
+            for (int cc = 0; cc < n_units; ++cc) {
+                const int tpc = U[cc].tp, tqc = U[cc].tq;
+                sm.off_p[cc] = op;
+                sm.off_q[cc] = oq;
+                sm.state_p[cc] = op + tpc <= P.ties ? 1 : (op >= P.ties ? 0 : 2);
+                sm.state_q[cc] = oq + tqc <= Q.ties ? 1 : (oq >= Q.ties ? 0 : 2);
+                if ((sm.state_p[cc] == 2 || sm.state_q[cc] == 2) && sm.n_ex < 2) sm.ex_unit[sm.n_ex++] = cc;
+                op += tpc;
+                oq += tqc;
+            }
+        }
+        __syncthreads();
+        const int n_ex = sm.n_ex;
+        for (int e = 0; e < n_ex; ++e) {
+            const int cc = sm.ex_unit[e];
+            unsigned long long sr, sp_;
+            rescan_unit(sm, P, Q, residual, cc * kResampleUnit, min(V, (cc + 1) * kResampleUnit), sm.off_p[cc],
+                        sm.off_q[cc], vec_ok, 0, false, 0ull, sr, sp_, phase);
+            if (tid == 0) {
+                sm.ex_res[e] = sr;
+                sm.ex_p[e] = sp_;
+            }
+        }
+        __syncthreads();
+        // 3. totals, the target and its chunk (thread 0), then the token
+        __shared__ unsigned long long s_target;
+        __shared__ int s_unit, s_use_p, s_zero;
+        if (tid == 0) {
+            auto unit_sum = [&](int cc, bool want_p) {
+                for (int e = 0; e < n_ex; ++e)
+                    if (sm.ex_unit[e] == cc) return want_p ? sm.ex_p[e] : sm.ex_res[e];
+                const int sp_ = sm.state_p[cc], sq = sm.state_q[cc];
+                return want_p ? U[cc].base_p + U[cc].tie_p[sp_] : U[cc].base_res + U[cc].tie_res[2 * sp_ + sq];
+            };
+            unsigned long long W = 0ull, Wp = 0ull;
+            for (int cc = 0; cc < n_units; ++cc) {
+                W += unit_sum(cc, false);
+                Wp += unit_sum(cc, true);
+            }
+            const bool zero = residual && W == 0ull;
+            const bool use_p = !residual || zero;
+            const unsigned long long Wu = use_p ? Wp : W;
+            const unsigned long long u24 = uniform24(a.seed, (uint32_t)job.req, (uint32_t)job.a, 1u);
+            const unsigned long long hi = __umul64hi(Wu, u24), lo = Wu * u24;
+            unsigned long long target = (hi << 40) | (lo >> 24);   // floor(W * u)
+            int unit = -1;
+            for (int cc = 0; cc < n_units; ++cc) {
+                const unsigned long long s = unit_sum(cc, use_p);
+                if (target < s) {
+                    unit = cc;
+                    break;
+                }
+                target -= s;
+            }
+            s_target = target;
+            s_unit = unit;
+            s_use_p = use_p ? 1 : 0;
+            s_zero = zero ? 1 : 0;
+        }
+        __syncthreads();
+        const int unit = s_unit;
+        int x = -1;
+        if (unit >= 0) {
+            unsigned long long d0, d1;
+            x = rescan_unit(sm, P, Q, residual, unit * kResampleUnit, min(V, (unit + 1) * kResampleUnit),
+                            sm.off_p[unit], sm.off_q[unit], vec_ok, 1, s_use_p != 0, s_target, d0, d1, phase);
+        }
+        if (tid == 0) {
+            if (x < 0) x = a.info[slot_target(job.req, K, job.a)].desc.argmax;   // not reached: sums are exact
+            a.out_tokens[(size_t)job.req * (K + 1) + job.a] = x;
+            if (s_zero && a.row_status) a.row_status[(size_t)job.req * (K + 1) + job.a] |= kResidZero;
+        }
+        __syncthreads();
+    }
+    if (!sm.stage_ok && tid == 0) mbar_wait(&sm.bar, phase);   // let a late copy land before the CTA leaves
+}
+
+}  // namespace
+
+cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
+{
+    static int blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = sizeof(ResSmem);
+    int& nb = blocks[(dev >= 0 && dev < 128) ? dev : 0];
+    if (nb == 0) {
+        cudaError_t err = cudaFuncSetAttribute(resample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, resample_kernel, kResThreads, smem);
+        if (err != cudaSuccess) return err;
+        if (nb < 1) nb = 1;
+    }
+    const int n_units = (a.vocab + kResampleUnit - 1) / kResampleUnit;
+    return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units);
+}
+
+}  // namespace sv
