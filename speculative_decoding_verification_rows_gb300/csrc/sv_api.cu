@@ -110,7 +110,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.info = ra.info;
     ca.req = at<ReqState>(ws, L.req);
     ca.jobs = at<ResampleJob>(ws, L.jobs);
-    ca.units = at<UnitSums>(ws, L.units);
+    ca.tiles = at<TileSums>(ws, L.tiles);
     ca.num_sms = ra.num_sms;
     return c;
 }

@@ -124,18 +124,28 @@ struct ResampleJob {
     int32_t done;     // row chunks of the job the resample has finished (0 when listed)
 };
 
-// Row chunks of the full-row resample, and what each one leaves for the job's
-// last chunk: exact fixed-point sums of the residual and of p over the chunk,
-// with the elements tied at a partially kept cutoff summed apart in both of
-// their possible states (kept or not, for p and for q), and the tie counts.
+// Chunks and tiles of the full-row resample.  A chunk (kResampleUnit
+// elements) is what one CTA of the resample kernel streams at a time; each
+// tile of it (kResampleTile elements, eight per thread) leaves a record for
+// the job's last chunk: exact fixed-point sums of the residual and of p over
+// the tile, with the elements tied at a partially kept cutoff summed apart in
+// both of their possible states (kept or not, for p and for q), and the tie
+// counts.
 constexpr int kResampleUnit = 8192;
-constexpr int kMaxResampleUnits = (kMaxCluster * kHistMaxSlice + kResampleUnit - 1) / kResampleUnit;
-struct UnitSums {
-    unsigned long long base_res, base_p;   // elements not tied at a partial cutoff
-    unsigned long long tie_res[4];         // tied elements, [p ties kept * 2 + q ties kept]
-    unsigned long long tie_p[2];           // tied elements, [p ties kept]
-    int32_t tp, tq;                        // elements at p's / q's cutoff (partial groups only)
+constexpr int kResampleTile = 2048;
+enum TileField {
+    kTsBaseRes = 0,   // residual over elements not tied at a partial cutoff
+    kTsBaseP = 1,     // p over the same
+    kTsTieRes = 2,    // 2..5: tied elements' residual, [p ties kept * 2 + q ties kept]
+    kTsTieP = 6,      // 6..7: tied elements' p, [p ties kept]
+    kTsTiesP = 8,     // elements at p's cutoff (partial groups only)
+    kTsTiesQ = 9,     // elements at q's cutoff (partial groups only)
+    kTsFields = 10
 };
+struct TileSums {
+    unsigned long long v[kTsFields];
+};
+__host__ __device__ __forceinline__ int resample_tiles(int vocab) { return (vocab + kResampleTile - 1) / kResampleTile; }
 
 // Request slots of the RowInfo array: target positions 0..K, then draft
 // positions 0..K-1.
@@ -154,7 +164,7 @@ struct Counters {
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, units, total;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, tiles, total;
     int slots, max_tasks;
     size_t n_partials;
 };
@@ -167,7 +177,6 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     WsLayout L{};
     L.slots = n_req * (2 * k_max + 1);
     L.max_tasks = L.slots;
-    (void)vocab;
     // A grid of W warps splits T tasks into parts; W * (parts per warp) stays
     // below T + 3 W (see the range arithmetic of the row kernel).
     L.n_partials = (size_t)L.max_tasks + 3 * (size_t)kMaxRowWarps;
@@ -181,7 +190,7 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
-    L.units = off;      off = align256(off + sizeof(UnitSums) * (size_t)n_req * (size_t)kMaxResampleUnits);
+    L.tiles = off;      off = align256(off + sizeof(TileSums) * (size_t)n_req * (size_t)resample_tiles(vocab));
     L.total = off;
     return L;
 }
@@ -475,7 +484,7 @@ struct ChainArgs {
     RowInfo* info;
     ReqState* req;
     ResampleJob* jobs;
-    UnitSums* units;   // [n_req][kMaxResampleUnits]
+    TileSums* tiles;   // [n_req][resample_tiles(vocab)]
     int num_sms;
 };
 

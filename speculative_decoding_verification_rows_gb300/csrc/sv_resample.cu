@@ -77,13 +77,18 @@ __device__ __forceinline__ uint32_t zero_key_of(double m, double T, double z)
 
 constexpr int kResThreads = 256;
 constexpr int kResBinades = 48;    // table slots, p's and q's binades together
-constexpr int kResTile = kResThreads * 8;
+constexpr int kResTile = kResampleTile;
+static_assert(kResampleTile == kResThreads * 8, "a tile is eight elements per thread");
+static_assert(kResampleUnit % kResampleTile == 0, "a chunk is whole tiles");
 
 struct ResSmem {
     alignas(16) uint16_t stage[2][kResampleUnit];   // the chunk of p's row and of q's row
     unsigned long long bar;                         // completion of the chunk's bulk copies
     int stage_ok;                                   // 0 after a copy did not arrive in time: plain loads from then on
+    unsigned long long buf[kResThreads * 8];        // per warp: its tile's candidates, then (rescan) their weights
     unsigned long long tab[kResBinades * 128];
+    double ratio[kResBinades];                      // per slot: exp(step / T) along the binade (0: one exp per key)
+    uint32_t zkey[2];                               // the loaded job's zero keys of p and q
     int16_t map[2][512];
     int slot_bin[kResBinades];
     int slot_dist[kResBinades];
@@ -91,14 +96,14 @@ struct ResSmem {
     int last;         // this CTA finished the job's last chunk
     int found;        // token found by the target search (-1: not yet)
     int halt;         // the target search is over
-    unsigned long long red[kResThreads / 32][10];
+    unsigned long long red[2][kResThreads / 32][kTsFields];   // per-warp tile sums (two tiles in flight)
     unsigned long long scan[kResThreads / 32];
     // the combine
-    int state_p[kMaxResampleUnits], state_q[kMaxResampleUnits];   // 0 none kept, 1 all kept, 2 split
-    int off_p[kMaxResampleUnits], off_q[kMaxResampleUnits];       // ties before the chunk
-    unsigned long long ex_res[2], ex_p[2];                        // exact sums of the split chunks
-    int ex_unit[2];
+    unsigned long long ex_res[2], ex_p[2];   // exact sums of the tiles where a tie group's kept part ends
+    int ex_tile[2], ex_off_p[2], ex_off_q[2];
     int n_ex;
+    int found_tile, tile_off_p, tile_off_q;  // the tile that holds the target
+    unsigned long long tile_target;
 };
 
 // Binades of a range that may hold a table: not binade 0 (-inf and negative
@@ -113,7 +118,8 @@ __device__ __forceinline__ int tabled_in(int x, int y)
     return n;
 }
 
-// The job's p and q as the weight passes need them (tables in shared memory).
+// The job's p and q as the weight passes need them (tables in shared memory;
+// the zero keys are those load_tables found for the loaded job).
 __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob& job, ResSmem& sm, Dist& P, Dist& Q)
 {
     const int r = job.req, pa = job.a, K = a.K;
@@ -125,7 +131,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
     P.T = IP.desc.temperature;
     P.z = IP.z;
     P.cut_key = key16_of_bf16(__float_as_uint(IP.desc.cutoff_logit) >> 16);
-    P.zero_key = zero_key_of(P.m, P.T, P.z);
+    P.zero_key = sm.zkey[0];
     P.ties = IP.desc.cutoff_ties;
     P.partial = IP.desc.cutoff_ties < IP.cut_count;
     P.map = sm.map[0];
@@ -137,7 +143,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
         Q.T = IQ.desc.temperature;
         Q.z = IQ.z;
         Q.cut_key = key16_of_bf16(__float_as_uint(IQ.desc.cutoff_logit) >> 16);
-        Q.zero_key = zero_key_of(Q.m, Q.T, Q.z);
+        Q.zero_key = sm.zkey[1];
         Q.ties = IQ.desc.cutoff_ties;
         Q.partial = IQ.desc.cutoff_ties < IQ.cut_count;
         Q.map = sm.map[1];
@@ -147,9 +153,16 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
 // Tables of the job's kept binades that may hold one, from the top binade of
 // each distribution down, p's first; q keeps at least half of the slots when
 // it needs them.  Every thread calls it.
-__device__ void load_tables(ResSmem& sm, const Dist& P, const Dist& Q, bool residual)
+__device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
 {
     const int tid = threadIdx.x;
+    if (tid == 0) {   // one fp64 log per distribution for the whole CTA
+        sm.zkey[0] = zero_key_of(P.m, P.T, P.z);
+        sm.zkey[1] = residual ? zero_key_of(Q.m, Q.T, Q.z) : sm.zkey[0];
+    }
+    __syncthreads();
+    P.zero_key = sm.zkey[0];
+    Q.zero_key = sm.zkey[1];
     const int hiP = (int)(key16_of_bf16(__float_as_uint((float)P.m) >> 16) >> 7);
     const int loP = (int)(max(P.cut_key, P.zero_key) >> 7);
     const int hiQ = (int)(key16_of_bf16(__float_as_uint((float)Q.m) >> 16) >> 7);
@@ -181,13 +194,32 @@ __device__ void load_tables(ResSmem& sm, const Dist& P, const Dist& Q, bool resi
         }
     }
     __syncthreads();
+    // the step ratio of each slot's binade, then 8 keys per thread: one exp,
+    // a geometric recurrence along the mantissa, a product with 1 / Z
+    for (int sl = tid; sl < capP + capQ; sl += kResThreads) {
+        const Dist& D = sm.slot_dist[sl] ? Q : P;
+        const uint32_t kb = (uint32_t)sm.slot_bin[sl] * 128u;
+        const double x = (key_value(kb + 1u) - key_value(kb)) / D.T;
+        sm.ratio[sl] = x <= 1.0 ? exp(x) : 0.0;
+    }
+    __syncthreads();
     for (int item = tid; item < (capP + capQ) * 16; item += kResThreads) {
-        const int s = item >> 4, g = item & 15;
-        const Dist& D = sm.slot_dist[s] ? Q : P;
-        double e[8];
-        binade_masses(sm.slot_bin[s], g, D.m, D.T, e);
+        const int sl = item >> 4, g = item & 15;
+        const Dist& D = sm.slot_dist[sl] ? Q : P;
+        const uint32_t k0 = (uint32_t)sm.slot_bin[sl] * 128u + 8u * (uint32_t)g;
+        const double R = sm.ratio[sl], inv_z = 1.0 / D.z;
+        unsigned long long* out = sm.tab + sl * 128 + 8 * g;
+        if (R > 0.0) {
+            double cur = exp((key_value(k0) - D.m) / D.T);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sm.tab[s * 128 + 8 * g + j] = fix_of(e[j] / D.z);
+            for (int j = 0; j < 8; ++j) {
+                out[j] = fix_of(cur * inv_z);
+                cur *= R;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) out[j] = fix_of(exp((key_value(k0 + j) - D.m) / D.T) * inv_z);
+        }
     }
     __syncthreads();
 }
@@ -294,88 +326,132 @@ __device__ __forceinline__ unsigned long long block_excl_u64(ResSmem& sm, unsign
     return before + incl - x;
 }
 
-// One chunk in index order with the exact tie ranks: the residual and p sums
-// (mode 0), or the index where the running sum of the chosen weights passes
-// `target` (mode 1; -1 if it does not within the chunk).  Every thread calls it.
-__device__ int rescan_unit(ResSmem& sm, const Dist& P, const Dist& Q, bool residual, int x_begin, int x_end,
-                           int run_p, int run_q, bool vec_ok, int mode, bool use_p, unsigned long long target,
-                           unsigned long long& sum_res, unsigned long long& sum_p, uint32_t& phase)
+// A warp's candidates of one tile, packed into its part of sm.buf in lane
+// order: the elements of mask `cm` (bit i: element i of the lane's eight),
+// each as pack(i).  Returns the warp's count.
+template <typename Pack>
+__device__ __forceinline__ int compact8(unsigned long long* wb, uint32_t cm, Pack pack)
 {
-    const int tid = threadIdx.x;
-    unsigned long long acc_r = 0ull, acc_p = 0ull, cum = 0ull;
-    const bool staged = stage_unit(sm, P, Q, residual, x_begin, x_end, vec_ok, phase);
-    if (tid == 0) {
-        sm.found = -1;
-        sm.halt = 0;
+    const int lane = threadIdx.x & 31;
+    const int nm = __popc(cm);
+    int incl = nm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
     }
-    __syncthreads();
-    for (int t0 = x_begin; t0 < x_end; t0 += kResTile) {
-        const int x0 = t0 + 8 * tid;
-        uint32_t kp[8], kq[8];
-        if (staged && x0 < x_end) {
-            stage_keys8(sm.stage[0] + (x0 - x_begin), kp);
-            if (residual) stage_keys8(sm.stage[1] + (x0 - x_begin), kq);
-        } else {
-            load_keys8(P.row, x0, x_end, vec_ok, kp);
-            if (residual) load_keys8(Q.row, x0, x_end, vec_ok, kq);
-        }
-        uint32_t cp = 0u, cq = 0u;
+    const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    int pos = incl - nm;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cp += (P.partial && kp[i] == P.cut_key) ? 1u : 0u;
-            cq += (residual && Q.partial && kq[i] == Q.cut_key) ? 1u : 0u;
-        }
-        unsigned long long tot;
-        const unsigned long long ex = block_excl_u64(sm, ((unsigned long long)cp << 32) | cq, tot);
-        int rp = run_p + (int)(ex >> 32), rq = run_q + (int)(ex & 0xFFFFFFFFu);
-        run_p += (int)(tot >> 32);
-        run_q += (int)(tot & 0xFFFFFFFFu);
-        unsigned long long w8[8];
-        unsigned long long tr = 0ull, tpp = 0ull;
+    for (int i = 0; i < 8; ++i)
+        if ((cm >> i) & 1u) wb[pos++] = pack(i);
+    __syncwarp();
+    return total;
+}
+
+// One tile in index order with the exact tie ranks (thread i: elements
+// t0 + 8 i .. + 7; run_p / run_q ties before the tile): the residual and p
+// sums (mode 0), or the index where the running sum of the chosen weights
+// passes `target` (mode 1; -1 if it does not within the tile).  Each thread
+// decides its elements' kept states from their ranks; each warp then computes
+// the weights of its elements kept in p, packed densely.  Every thread calls
+// it.
+__device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool residual, int t0, int x_end, int run_p,
+                           int run_q, bool vec_ok, int mode, bool use_p, unsigned long long target,
+                           unsigned long long& sum_res, unsigned long long& sum_p)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long* wb = sm.buf + warp * 256;
+    const int x0 = t0 + 8 * tid;
+    uint32_t kp[8], kq[8];
+    load_keys8(P.row, x0, x_end, vec_ok, kp);
+    if (residual)
+        load_keys8(Q.row, x0, x_end, vec_ok, kq);
+    else
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const bool inp = kept_key(P, kp[i], rp);
-            if (P.partial && kp[i] == P.cut_key) ++rp;
-            const unsigned long long wp = inp ? fixp(P, kp[i]) : 0ull;
-            unsigned long long wr = wp;
-            if (residual) {
-                const bool inq = kept_key(Q, kq[i], rq);
-                if (Q.partial && kq[i] == Q.cut_key) ++rq;
-                wr = sat_sub(wp, inq && wp ? fixp(Q, kq[i]) : 0ull);
-            }
+        for (int i = 0; i < 8; ++i) kq[i] = 0u;
+    if (tid == 0) sm.found = -1;
+    uint32_t cp = 0u, cq = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        cp += (P.partial && kp[i] == P.cut_key) ? 1u : 0u;
+        cq += (residual && Q.partial && kq[i] == Q.cut_key) ? 1u : 0u;
+    }
+    unsigned long long tot;
+    const unsigned long long ex = block_excl_u64(sm, ((unsigned long long)cp << 32) | cq, tot);
+    int rp = run_p + (int)(ex >> 32), rq = run_q + (int)(ex & 0xFFFFFFFFu);
+    uint32_t inp = 0u, inq = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (kept_key(P, kp[i], rp)) inp |= 1u << i;
+        if (P.partial && kp[i] == P.cut_key) ++rp;
+        if (residual) {
+            if (kept_key(Q, kq[i], rq)) inq |= 1u << i;
+            if (Q.partial && kq[i] == Q.cut_key) ++rq;
+        }
+    }
+    const int total = compact8(wb, inp, [&](int i) {
+        return (unsigned long long)kp[i] | ((unsigned long long)kq[i] << 16) |
+               ((unsigned long long)((inq >> i) & 1u) << 32) | ((unsigned long long)(lane * 8 + i) << 33);
+    });
+    unsigned long long wv[8];   // this lane's entries lane, lane + 32, ... (at most 8)
+    int ws[8];
+    unsigned long long tr = 0ull, tpp = 0ull;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = lane + 32 * q;
+        wv[q] = 0ull;
+        ws[q] = -1;
+        if (e < total) {
+            const unsigned long long en = wb[e];
+            const uint32_t ekp = (uint32_t)(en & 0xFFFFu), ekq = (uint32_t)((en >> 16) & 0xFFFFu);
+            const unsigned long long wp = fixp(P, ekp);
+            const unsigned long long wr = residual ? sat_sub(wp, ((en >> 32) & 1ull) ? fixp(Q, ekq) : 0ull) : wp;
             tr += wr;
             tpp += wp;
-            w8[i] = use_p ? wp : wr;
-        }
-        acc_r += tr;
-        acc_p += tpp;
-        if (mode == 1) {
-            const unsigned long long mine = use_p ? tpp : tr;
-            unsigned long long tile;
-            const unsigned long long before = cum + block_excl_u64(sm, mine, tile);
-            if (before <= target && target < before + mine) {   // this thread holds the crossing
-                unsigned long long c = before;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    c += w8[i];
-                    if (c > target) {
-                        sm.found = x0 + i;
-                        break;
-                    }
-                }
-                sm.halt = 1;
-            }
-            cum += tile;
-            __syncthreads();
-            if (sm.halt) break;
+            wv[q] = use_p ? wp : wr;
+            ws[q] = (int)(en >> 33);
         }
     }
     if (mode == 0) {
-        sum_res = block_sum_u64(sm, acc_r);
-        sum_p = block_sum_u64(sm, acc_p);
+        sum_res = block_sum_u64(sm, tr);
+        sum_p = block_sum_u64(sm, tpp);
+        __syncthreads();
+        return -1;
+    }
+    // back to index order: each weight in its element's slot, per-thread
+    // sums, the CTA's prefix, and the walk of the thread holding the crossing
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wb[lane * 8 + i] = 0ull;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (ws[q] >= 0) wb[ws[q]] = wv[q];
+    __syncwarp();
+    unsigned long long w8[8], mine = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w8[i] = wb[lane * 8 + i];
+        mine += w8[i];
+    }
+    unsigned long long tile;
+    const unsigned long long before = block_excl_u64(sm, mine, tile);
+    if (before <= target && target < before + mine) {
+        unsigned long long c = before;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c += w8[i];
+            if (c > target) {
+                sm.found = x0 + i;
+                break;
+            }
+        }
     }
     __syncthreads();
-    return sm.found;
+    const int found = sm.found;
+    __syncthreads();
+    return found;
 }
 
 __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units)
@@ -385,6 +461,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     ResSmem& sm = *reinterpret_cast<ResSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int V = a.vocab, K = a.K;
+    const int n_tiles = resample_tiles(V);
     const long long total = (long long)a.counters->n_jobs * n_units;
     const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
     if (tid == 0) {
@@ -407,153 +484,163 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
         }
         const bool vec_ok = ((uintptr_t)P.row & 15u) == 0u && (!residual || ((uintptr_t)Q.row & 15u) == 0u);
         const int x_begin = c * kResampleUnit, x_end = min(V, x_begin + kResampleUnit);
+        TileSums* recs = a.tiles + (size_t)j * n_tiles;
 
-        // 1. the chunk's sums in one pass
-        unsigned long long base_r = 0ull, base_p = 0ull, tie_r[4] = {0ull, 0ull, 0ull, 0ull}, tie_p[2] = {0ull, 0ull};
-        uint32_t tp = 0u, tq = 0u;
+        // 1. per tile of the chunk: tie counts over every element, weights
+        //    over the elements at or above p's cutoff (the others have p = 0
+        //    in every state), packed densely per warp; then the tile's record
         const bool staged = stage_unit(sm, P, Q, residual, x_begin, x_end, vec_ok, phase);
-        for (int x0 = x_begin + 8 * tid; x0 < x_end; x0 += kResTile) {
+        unsigned long long* wb = sm.buf + warp * 256;
+        for (int t0 = x_begin; t0 < x_end; t0 += kResTile) {
+            const int x0 = t0 + 8 * tid;
+            unsigned long long acc[kTsFields] = {};
             uint32_t kp[8], kq[8];
-            if (staged) {
+            if (staged && x0 < x_end) {
                 stage_keys8(sm.stage[0] + (x0 - x_begin), kp);
                 if (residual) stage_keys8(sm.stage[1] + (x0 - x_begin), kq);
             } else {
                 load_keys8(P.row, x0, x_end, vec_ok, kp);
                 if (residual) load_keys8(Q.row, x0, x_end, vec_ok, kq);
             }
+            if (!residual)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) kq[i] = 0u;
+            uint32_t cm = 0u;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const bool tP = P.partial && kp[i] == P.cut_key;
-                const bool tQ = residual && Q.partial && kq[i] == Q.cut_key;
-                tp += tP ? 1u : 0u;
-                tq += tQ ? 1u : 0u;
-                if (kp[i] < P.cut_key) continue;   // outside p's kept set in every state
-                const unsigned long long wp = fixp(P, kp[i]);
-                const bool qk = residual && (kq[i] > Q.cut_key || (kq[i] == Q.cut_key && !Q.partial));
-                const unsigned long long wq = qk ? fixp(Q, kq[i]) : 0ull;
+                acc[kTsTiesP] += (P.partial && kp[i] == P.cut_key) ? 1u : 0u;
+                acc[kTsTiesQ] += (residual && Q.partial && kq[i] == Q.cut_key) ? 1u : 0u;
+                if (kp[i] >= P.cut_key) cm |= 1u << i;
+            }
+            const int cnt =
+                compact8(wb, cm, [&](int i) { return (unsigned long long)kp[i] | ((unsigned long long)kq[i] << 16); });
+            for (int e = lane; e < cnt; e += 32) {
+                const uint32_t en = (uint32_t)wb[e];
+                const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
+                const bool tP = P.partial && ekp == P.cut_key;
+                const bool tQ = residual && Q.partial && ekq == Q.cut_key;
+                const unsigned long long wp = fixp(P, ekp);
+                const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
+                const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
                 if (!tP && !tQ) {
-                    base_p += wp;
-                    base_r += residual ? sat_sub(wp, wq) : wp;
+                    acc[kTsBaseP] += wp;
+                    acc[kTsBaseRes] += residual ? sat_sub(wp, wq) : wp;
                 } else {
-                    const unsigned long long wqt = tQ ? fixp(Q, kq[i]) : wq;
+                    const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
 #pragma unroll
                     for (int sp_ = 0; sp_ < 2; ++sp_) {
                         const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
-                        tie_p[sp_] += p_;
+                        acc[kTsTieP + sp_] += p_;
 #pragma unroll
                         for (int sq = 0; sq < 2; ++sq) {
                             const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
-                            tie_r[2 * sp_ + sq] += residual ? sat_sub(p_, q_) : p_;
+                            acc[kTsTieRes + 2 * sp_ + sq] += residual ? sat_sub(p_, q_) : p_;
                         }
                     }
                 }
             }
-        }
-        {
-            unsigned long long v[10] = {base_r, base_p, tie_r[0], tie_r[1], tie_r[2], tie_r[3], tie_p[0], tie_p[1],
-                                        (unsigned long long)tp, (unsigned long long)tq};
+            __syncwarp();
+            const int buf = (t0 / kResTile) & 1;
 #pragma unroll
-            for (int i = 0; i < 10; ++i) v[i] = warp_sum_u64(v[i]);
-            if (lane == 0)
-#pragma unroll
-                for (int i = 0; i < 10; ++i) sm.red[warp][i] = v[i];
-            __syncthreads();
-            if (tid == 0) {
-                unsigned long long s[10] = {};
-                for (int w = 0; w < kResThreads / 32; ++w)
-                    for (int i = 0; i < 10; ++i) s[i] += sm.red[w][i];
-                UnitSums& U = a.units[(size_t)j * kMaxResampleUnits + c];
-                U.base_res = s[0];
-                U.base_p = s[1];
-                for (int i = 0; i < 4; ++i) U.tie_res[i] = s[2 + i];
-                U.tie_p[0] = s[6];
-                U.tie_p[1] = s[7];
-                U.tp = (int32_t)s[8];
-                U.tq = (int32_t)s[9];
-                __threadfence();
-                sm.last = atomicAdd(&a.jobs[j].done, 1) == n_units - 1;
+            for (int f = 0; f < kTsFields; ++f) {
+                const unsigned long long v = warp_sum_u64(acc[f]);
+                if (lane == 0) sm.red[buf][warp][f] = v;
             }
             __syncthreads();
-        }
-        if (!sm.last) continue;
-        __threadfence();
-
-        // 2. the job's last chunk: states of the tie groups per chunk
-        const UnitSums* U = a.units + (size_t)j * kMaxResampleUnits;
-        if (tid == 0) {
-            int op = 0, oq = 0;
-            sm.n_ex = 0;
-            for (int cc = 0; cc < n_units; ++cc) {
-                const int tpc = U[cc].tp, tqc = U[cc].tq;
-                sm.off_p[cc] = op;
-                sm.off_q[cc] = oq;
-                sm.state_p[cc] = op + tpc <= P.ties ? 1 : (op >= P.ties ? 0 : 2);
-                sm.state_q[cc] = oq + tqc <= Q.ties ? 1 : (oq >= Q.ties ? 0 : 2);
-                if ((sm.state_p[cc] == 2 || sm.state_q[cc] == 2) && sm.n_ex < 2) sm.ex_unit[sm.n_ex++] = cc;
-                op += tpc;
-                oq += tqc;
+            if (tid < kTsFields) {
+                unsigned long long v = 0ull;
+#pragma unroll
+                for (int w = 0; w < kResThreads / 32; ++w) v += sm.red[buf][w][tid];
+                recs[t0 / kResTile].v[tid] = v;
+                __threadfence();
             }
         }
         __syncthreads();
-        const int n_ex = sm.n_ex;
+        if (tid == 0) sm.last = atomicAdd(&a.jobs[j].done, 1) == n_units - 1;
+        __syncthreads();
+        if (!sm.last) continue;
+        __threadfence();
+
+        // 2. the job's last chunk: one thread per tile record (read through
+        //    L2: they come from other SMs); tie offsets and states by a scan
+        const int t = tid;
+        unsigned long long R[kTsFields] = {};
+        if (t < n_tiles)
+#pragma unroll
+            for (int f = 0; f < kTsFields; ++f) R[f] = __ldcg(&recs[t].v[f]);
+        if (tid == 0) {
+            sm.n_ex = 0;
+            sm.found_tile = -1;
+        }
+        unsigned long long tot;
+        const unsigned long long ex = block_excl_u64(sm, (R[kTsTiesP] << 32) | R[kTsTiesQ], tot);
+        const int op = (int)(ex >> 32), oq = (int)(ex & 0xFFFFFFFFu);
+        const int stp = op + (int)R[kTsTiesP] <= P.ties ? 1 : (op >= P.ties ? 0 : 2);
+        const int stq = oq + (int)R[kTsTiesQ] <= Q.ties ? 1 : (oq >= Q.ties ? 0 : 2);
+        const bool split = t < n_tiles && (stp == 2 || stq == 2);
+        if (split) {   // at most one tile for p and one for q
+            const int k = atomicAdd(&sm.n_ex, 1);
+            if (k < 2) {
+                sm.ex_tile[k] = t;
+                sm.ex_off_p[k] = op;
+                sm.ex_off_q[k] = oq;
+            }
+        }
+        __syncthreads();
+        const int n_ex = min(sm.n_ex, 2);
         for (int e = 0; e < n_ex; ++e) {
-            const int cc = sm.ex_unit[e];
             unsigned long long sr, sp_;
-            rescan_unit(sm, P, Q, residual, cc * kResampleUnit, min(V, (cc + 1) * kResampleUnit), sm.off_p[cc],
-                        sm.off_q[cc], vec_ok, 0, false, 0ull, sr, sp_, phase);
+            rescan_tile(sm, P, Q, residual, sm.ex_tile[e] * kResTile, V, sm.ex_off_p[e], sm.ex_off_q[e], vec_ok, 0,
+                        false, 0ull, sr, sp_);
             if (tid == 0) {
                 sm.ex_res[e] = sr;
                 sm.ex_p[e] = sp_;
             }
         }
         __syncthreads();
-        // 3. totals, the target and its chunk (thread 0), then the token
-        __shared__ unsigned long long s_target;
-        __shared__ int s_unit, s_use_p, s_zero;
-        if (tid == 0) {
-            auto unit_sum = [&](int cc, bool want_p) {
+        // 3. tile sums, totals, the target and the tile that holds it
+        unsigned long long s_res = 0ull, s_p = 0ull;
+        if (t < n_tiles) {
+            if (split) {
                 for (int e = 0; e < n_ex; ++e)
-                    if (sm.ex_unit[e] == cc) return want_p ? sm.ex_p[e] : sm.ex_res[e];
-                const int sp_ = sm.state_p[cc], sq = sm.state_q[cc];
-                return want_p ? U[cc].base_p + U[cc].tie_p[sp_] : U[cc].base_res + U[cc].tie_res[2 * sp_ + sq];
-            };
-            unsigned long long W = 0ull, Wp = 0ull;
-            for (int cc = 0; cc < n_units; ++cc) {
-                W += unit_sum(cc, false);
-                Wp += unit_sum(cc, true);
+                    if (sm.ex_tile[e] == t) {
+                        s_res = sm.ex_res[e];
+                        s_p = sm.ex_p[e];
+                    }
+            } else {
+                const unsigned long long tr0 = stq ? R[kTsTieRes + 1] : R[kTsTieRes];
+                const unsigned long long tr1 = stq ? R[kTsTieRes + 3] : R[kTsTieRes + 2];
+                s_res = R[kTsBaseRes] + (stp ? tr1 : tr0);
+                s_p = R[kTsBaseP] + (stp ? R[kTsTieP + 1] : R[kTsTieP]);
             }
-            const bool zero = residual && W == 0ull;
-            const bool use_p = !residual || zero;
-            const unsigned long long Wu = use_p ? Wp : W;
-            const unsigned long long u24 = uniform24(a.seed, (uint32_t)job.req, (uint32_t)job.a, 1u);
-            const unsigned long long hi = __umul64hi(Wu, u24), lo = Wu * u24;
-            unsigned long long target = (hi << 40) | (lo >> 24);   // floor(W * u)
-            int unit = -1;
-            for (int cc = 0; cc < n_units; ++cc) {
-                const unsigned long long s = unit_sum(cc, use_p);
-                if (target < s) {
-                    unit = cc;
-                    break;
-                }
-                target -= s;
-            }
-            s_target = target;
-            s_unit = unit;
-            s_use_p = use_p ? 1 : 0;
-            s_zero = zero ? 1 : 0;
+        }
+        const unsigned long long W = block_sum_u64(sm, s_res), Wp = block_sum_u64(sm, s_p);
+        const bool zero = residual && W == 0ull;
+        const bool use_p = !residual || zero;
+        const unsigned long long Wu = use_p ? Wp : W;
+        const unsigned long long u24 = uniform24(a.seed, (uint32_t)job.req, (uint32_t)job.a, 1u);
+        const unsigned long long hi = __umul64hi(Wu, u24), lo = Wu * u24;
+        const unsigned long long target = (hi << 40) | (lo >> 24);   // floor(W * u)
+        const unsigned long long mine = use_p ? s_p : s_res;
+        unsigned long long all;
+        const unsigned long long pre = block_excl_u64(sm, mine, all);
+        if (t < n_tiles && pre <= target && target < pre + mine) {
+            sm.found_tile = t;
+            sm.tile_target = target - pre;
+            sm.tile_off_p = op;
+            sm.tile_off_q = oq;
         }
         __syncthreads();
-        const int unit = s_unit;
         int x = -1;
-        if (unit >= 0) {
+        if (sm.found_tile >= 0) {
             unsigned long long d0, d1;
-            x = rescan_unit(sm, P, Q, residual, unit * kResampleUnit, min(V, (unit + 1) * kResampleUnit),
-                            sm.off_p[unit], sm.off_q[unit], vec_ok, 1, s_use_p != 0, s_target, d0, d1, phase);
+            x = rescan_tile(sm, P, Q, residual, sm.found_tile * kResTile, V, sm.tile_off_p, sm.tile_off_q, vec_ok, 1,
+                            use_p, sm.tile_target, d0, d1);
         }
         if (tid == 0) {
             if (x < 0) x = a.info[slot_target(job.req, K, job.a)].desc.argmax;   // not reached: sums are exact
             a.out_tokens[(size_t)job.req * (K + 1) + job.a] = x;
-            if (s_zero && a.row_status) a.row_status[(size_t)job.req * (K + 1) + job.a] |= kResidZero;
+            if (zero && a.row_status) a.row_status[(size_t)job.req * (K + 1) + job.a] |= kResidZero;
         }
         __syncthreads();
     }
