@@ -21,8 +21,9 @@
 //   histogram (so a counter cannot wrap), summed through distributed shared
 //   memory.
 //
-// Either way the occupied binades' counts become fp64 masses (one exp per
-// binade and a geometric recurrence along the mantissa), and one CTA walks
+// Either way the occupied binades' counts become fp64 masses (two exps per
+// binade and a geometric polynomial along the mantissa evaluated in
+// double-float arithmetic), and one CTA walks
 // binades and then keys from the top to the top-k and top-p cutoffs.  Only the
 // probability of the row's own token may need one more look at the row (the
 // rank of a tied token at the cutoff).
@@ -132,6 +133,57 @@ __device__ __forceinline__ void for_binade_masses32(int b, int q, double m, doub
     } else {
         for (int j = 0; j < 32; ++j) f(j, exp((key_value(kb + j) - m) / T));
     }
+}
+
+// Mass of one binade, the sum over its 128 keys of c_k exp((v_k - m) / T),
+// by its four quarter threads (adjacent lanes q = 0..3; c[j] is the count of
+// key 128 b + 32 q + j).  Every lane of the warp calls it; a lane group with
+// act false gets 0.  Along a binade the value step s is constant, so with
+// r = exp(-s / T) a quarter's sum is exp((v_top - m) / T) r^(96 - 32 q) times
+// the polynomial sum_j c_j r^(31 - j), evaluated by Horner's rule in
+// double-float arithmetic; fp64 is left for the first lane's two exps and
+// the products that join the quarters (a fixed-order 4-lane sum).  A step
+// above T (keys far apart against T) takes one exp per key instead.
+__device__ double binade_mass4(int b, int q, double m, double T, bool act, const uint32_t* c)
+{
+    const int lead = (threadIdx.x & 31) & ~3;
+    const bool on = act && b > 0;
+    const uint32_t kb = (uint32_t)b * 128u;
+    double r64 = 0.0, etop = 0.0, r32 = 0.0;
+    int geo = 0;   // the step is at most T: geometric masses
+    if (on && q == 0) {
+        const double x = (key_value(kb + 1u) - key_value(kb)) / T;
+        geo = x <= 1.0;
+        if (geo) {
+            r64 = exp(-x);
+            etop = exp((key_value(kb + 127u) - m) / T);
+            r32 = r64;
+#pragma unroll
+            for (int i = 0; i < 5; ++i) r32 *= r32;
+        }
+    }
+    geo = __shfl_sync(0xFFFFFFFFu, geo, lead);
+    r64 = __shfl_sync(0xFFFFFFFFu, r64, lead);
+    etop = __shfl_sync(0xFFFFFFFFu, etop, lead);
+    r32 = __shfl_sync(0xFFFFFFFFu, r32, lead);
+    double part = 0.0;
+    if (on) {
+        if (geo) {
+            const dfloat r = df_of(r64);
+            dfloat acc = {0.0f, 0.0f};
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) acc = df_add_f(df_mul(acc, r), (float)c[j]);
+            double w = etop;
+            for (int i = q; i < 3; ++i) w *= r32;
+            part = w * df_val(acc);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (c[j]) part += (double)c[j] * exp((key_value(kb + 32u * (uint32_t)q + (uint32_t)j) - m) / T);
+        }
+    }
+#pragma unroll
+    for (int o = 2; o; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o, 4);
+    return part;
 }
 
 // Per-key counts (summed over the cluster) and masses of binade b into slot s
@@ -614,26 +666,19 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
             const bool act = i < n_mine;
             const int b = act ? sm.occ_list[rank + C * i] : 0;
             uint32_t csum = 0u;
-            double mass = 0.0;
+            uint32_t* cs = sm.csc[tid];   // counts in shared scratch, indexed freely by the mass loop
             if (act) {
                 uint32_t c[32];
                 cluster_counts32(cluster, sm, C, b, q4, c);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) csum += c[j];
-                if (csum) {
-                    // counts go to shared scratch so the mass loop indexes them freely
-                    uint32_t* cs = sm.csc[tid];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) cs[j] = c[j];
-                    for_binade_masses32(b, q4, m, T, [&](int j, double e) { mass += (double)cs[j] * e; });
+                for (int j = 0; j < 32; ++j) {
+                    csum += c[j];
+                    cs[j] = c[j];
                 }
             }
-            // fixed-order reduction over the 4 threads of each binade
+            const double mass = binade_mass4(b, q4, m, T, act, cs);
 #pragma unroll
-            for (int o = 2; o; o >>= 1) {
-                mass += __shfl_xor_sync(0xFFFFFFFFu, mass, o, 4);
-                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
-            }
+            for (int o = 2; o; o >>= 1) csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
             if (act && q4 == 0) {
                 sums0[b].mass = mass;
                 sums0[b].count = csum;
@@ -913,19 +958,14 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
             const int s = tid >> 2, q = tid & 3;
             const bool act = status == 0 && s < used;
             const int b = act ? sm.bin_of[s] : 0;
-            double mass = 0.0;
+            const uint32_t* c = sm.cnt + (act ? s : 0) * 128 + 32 * q;
             uint32_t csum = 0u;
-            if (act) {
-                const uint32_t* c = sm.cnt + s * 128 + 32 * q;
+            if (act)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) csum += c[j];
-                if (csum) for_binade_masses32(b, q, m, T, [&](int j, double e) { mass += (double)c[j] * e; });
-            }
+            const double mass = binade_mass4(b, q, m, T, act, c);
 #pragma unroll
-            for (int o = 2; o; o >>= 1) {
-                mass += __shfl_xor_sync(0xFFFFFFFFu, mass, o, 4);
-                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
-            }
+            for (int o = 2; o; o >>= 1) csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
             if (act && q == 0) {
                 sm.w.sums[b].mass = mass;
                 sm.w.sums[b].count = csum;

@@ -276,6 +276,41 @@ __device__ __forceinline__ void binade_masses(int b, int g, double m, double T, 
 }
 
 // ----------------------------------------------------------------------------
+// Double-float arithmetic (Dekker, "A floating-point technique for extending
+// the available precision", 1971; the error-free sum is Knuth's two-sum): a
+// value held as the unevaluated sum hi + lo of two floats, about 48
+// significant bits, so that sums which must agree with fp64 far below 1e-9
+// run on the fp32 pipes instead of the narrow fp64 one.
+// ----------------------------------------------------------------------------
+struct dfloat {
+    float hi, lo;
+};
+__device__ __forceinline__ dfloat df_of(double x)
+{
+    const float h = (float)x;
+    return dfloat{h, (float)(x - (double)h)};
+}
+__device__ __forceinline__ double df_val(dfloat a) { return (double)a.hi + (double)a.lo; }
+// a + f for a float f, renormalised.
+__device__ __forceinline__ dfloat df_add_f(dfloat a, float f)
+{
+    const float s = a.hi + f;
+    const float bb = s - a.hi;
+    const float e = (a.hi - (s - bb)) + (f - bb) + a.lo;
+    const float hi = s + e;
+    return dfloat{hi, e - (hi - s)};
+}
+// a * b, renormalised (the product's rounding error recovered by an FMA).
+__device__ __forceinline__ dfloat df_mul(dfloat a, dfloat b)
+{
+    const float p = a.hi * b.hi;
+    float e = fmaf(a.hi, b.hi, -p);
+    e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
+    const float hi = p + e;
+    return dfloat{hi, e - (hi - p)};
+}
+
+// ----------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): counter (req, pos, draw, 0),
 // key (seed low, seed high); u = (word0 >> 8) * 2^-24.
 // ----------------------------------------------------------------------------
