@@ -211,7 +211,7 @@ __device__ void load_binade_keys(cg::cluster_group& cluster, HistSmem& sm, int C
 // warp 0, key walks on warp 0 and thread 0 (fp64 is scarce), and the
 // decisions travel through shared memory between phases.  load_keys(b, s)
 // fills sm.kc[s] / sm.ke[s] with the per-key counts and masses of binade b
-// (every thread calls it; it may use threads 0..3).  Writes the row's record
+// (every thread calls it; it may use threads 0..127).  Writes the row's record
 // unless status != 0, and leaves in sm.plan whether the token's tie rank is
 // needed.  Every thread of the CTA must call it.
 template <typename LoadKeys>
@@ -761,6 +761,10 @@ struct WideSmem {
     int32_t neg_nan;                        // 1: a key below that of -inf (a NaN with the sign bit set)
     unsigned long long red64[kWideThreads / 32];
     int32_t redi[kWideThreads / 32];
+    double inv_t;                           // 1 / T of the row
+    double g_r[kWideSlots];                 // per slot: r = exp(-step / T) along its binade (0: one exp per key)
+    double g_r32[kWideSlots];               // r^32
+    double g_etop[kWideSlots];              // exp((v - m) / T) of the binade's top key
     WalkSmem w;
 };
 
@@ -953,41 +957,105 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
             __syncthreads();
         }
 
-        // 3. per-binade count and mass: four threads per slot, 32 keys each
+        // 3. per-binade count and mass.  Each fp64 warp instruction holds the
+        //    narrow fp64 pipe for the whole warp, so the two exps of each
+        //    occupied binade go one per lane (r = exp(-step / T) and the top
+        //    key's exp((v - m) / T)), and the mantissa polynomials run in
+        //    double-float arithmetic on four threads per slot (32 keys each).
+        if (status == 0) {
+            if (tid == 0) sm.inv_t = 1.0 / T;
+            __syncthreads();
+            const double inv_t = sm.inv_t;
+            for (int i = tid; i < 2 * used; i += kWideThreads) {
+                const int sl = i < used ? i : i - used;
+                const int b = sm.bin_of[sl];
+                const uint32_t kb = (uint32_t)b * 128u;
+                if (i < used) {
+                    const double x = (key_value(kb + 1u) - key_value(kb)) * inv_t;
+                    double r = 0.0, r32 = 0.0;
+                    if (b > 0 && x <= 1.0) {
+                        r = exp(-x);
+                        r32 = r;
+#pragma unroll
+                        for (int k = 0; k < 5; ++k) r32 *= r32;
+                    }
+                    sm.g_r[sl] = r;
+                    sm.g_r32[sl] = r32;
+                } else {
+                    sm.g_etop[sl] = b > 0 ? exp((key_value(kb + 127u) - m) * inv_t) : 0.0;
+                }
+            }
+            __syncthreads();
+        }
         {
-            const int s = tid >> 2, q = tid & 3;
-            const bool act = status == 0 && s < used;
-            const int b = act ? sm.bin_of[s] : 0;
-            const uint32_t* c = sm.cnt + (act ? s : 0) * 128 + 32 * q;
+            const int sl = tid >> 2, q = tid & 3;
+            const bool act = status == 0 && sl < used;
+            const int b = act ? sm.bin_of[sl] : 0;
+            const uint32_t* c = sm.cnt + (act ? sl : 0) * 128 + 32 * q;
             uint32_t csum = 0u;
-            if (act)
+            double part = 0.0;
+            if (act) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) csum += c[j];
-            const double mass = binade_mass4(b, q, m, T, act, c);
+                if (b > 0 && csum) {
+                    const double r64 = sm.g_r[sl];
+                    if (r64 > 0.0) {   // sum_j c_j r^(31 - j), relative to the quarter's top key
+                        const dfloat r = df_of(r64);
+                        dfloat acc = {0.0f, 0.0f};
+#pragma unroll 8
+                        for (int j = 0; j < 32; ++j) acc = df_add_f(df_mul(acc, r), (float)c[j]);
+                        double w = sm.g_etop[sl];
+                        for (int i = q; i < 3; ++i) w *= sm.g_r32[sl];
+                        part = w * df_val(acc);
+                    } else {   // keys far apart against T: one exp per key
+                        for (int j = 0; j < 32; ++j)
+                            if (c[j])
+                                part += (double)c[j] *
+                                        exp((key_value((uint32_t)b * 128u + 32u * (uint32_t)q + (uint32_t)j) - m) * sm.inv_t);
+                    }
+                }
+            }
 #pragma unroll
-            for (int o = 2; o; o >>= 1) csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
+            for (int o = 2; o; o >>= 1) {   // fixed-order sum over the four threads of a slot
+                part += __shfl_xor_sync(0xFFFFFFFFu, part, o, 4);
+                csum += __shfl_xor_sync(0xFFFFFFFFu, csum, o, 4);
+            }
             if (act && q == 0) {
-                sm.w.sums[b].mass = mass;
+                sm.w.sums[b].mass = part;
                 sm.w.sums[b].count = csum;
             }
         }
         __syncthreads();
 
-        // 4. the cutoff walk, with per-key counts straight from the slots
+        // 4. the cutoff walk, with per-key counts straight from the slots and
+        //    per-key masses e_top r^(127 - k) (double-float powers), one key
+        //    per thread
         walk_row(sm.w, a, task, row, info, m, argmax, status, [&](int b, int s) {
-            const int q = threadIdx.x;
-            if (q >= 4) return;
+            const int k = threadIdx.x;
+            if (k >= 128) return;
             const int bs = (b >= 0 && b < 512) ? sm.base[b] : kUnclaimed;
             if (bs < kBaseMin) {
-                for (int j = 0; j < 32; ++j) {
-                    sm.w.kc[s][32 * q + j] = 0u;
-                    sm.w.ke[s][32 * q + j] = 0.0;
-                }
+                sm.w.kc[s][k] = 0u;
+                sm.w.ke[s][k] = 0.0;
                 return;
             }
-            const uint32_t* c = sm.cnt + bs + 128 * b + 32 * q;
-            for (int j = 0; j < 32; ++j) sm.w.kc[s][32 * q + j] = c[j];
-            for_binade_masses32(b, q, m, T, [&](int j, double e) { sm.w.ke[s][32 * q + j] = e; });
+            const int sl = (bs >> 7) + b;   // bs = 128 (slot - b)
+            sm.w.kc[s][k] = sm.cnt[sl * 128 + k];
+            double e = 0.0;
+            if (b > 0) {
+                const double r64 = sm.g_r[sl];
+                if (r64 > 0.0) {
+                    dfloat p = {1.0f, 0.0f}, base = df_of(r64);
+                    for (int n = 127 - k; n; n >>= 1) {
+                        if (n & 1) p = df_mul(p, base);
+                        base = df_mul(base, base);
+                    }
+                    e = sm.g_etop[sl] * df_val(p);
+                } else {
+                    e = exp((key_value((uint32_t)b * 128u + (uint32_t)k) - m) * sm.inv_t);
+                }
+            }
+            sm.w.ke[s][k] = e;
         });
         __syncthreads();
 
