@@ -164,24 +164,33 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# The two row-transform paths: their kernels, the sources that define them,
+# and the timing hook of each.
+ROW_PATHS = {
+    "fast": dict(kernel="fast_rows_kernel (one-pass top-k / argmax row select)", sources=("sv_fast.cu",)),
+    "hist": dict(kernel="wide_rows_kernel + hist_rows_kernel (exact per-value histogram, top-p over the vocabulary)",
+                 sources=("sv_hist.cu",)),
+}
+
+
+def kernel_source_hash(path_name: str = "fast"):
     h = hashlib.sha256()
-    for name in ("sv_fast.cu", "sv_internal.cuh"):
+    for name in ROW_PATHS[path_name]["sources"] + ("sv_internal.cuh",):
         with open(os.path.join(ROOT, "speculative_decoding_verification_rows_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the row kernel from a committed ncu summary,
-    if it was taken on the current kernel source."""
+def recorded_traffic(workload: str, path_name: str = "fast"):
+    """DRAM bytes per launch of the workload's dominant row kernel from a
+    committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_source") != kernel_source_hash():
+    if not rec or rec.get("path", "fast") != path_name or rec.get("kernel_source") != kernel_source_hash(path_name):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -201,6 +210,21 @@ def algorithmic_bytes(w) -> tuple[int, int]:
     rows_t = w.n * (w.K + 1)
     rows_d = sampling * w.K
     return (rows_t + rows_d) * w.V * esz, rows_t
+
+
+def path_bytes(w, verify_len=None) -> tuple[int, int]:
+    """Bytes of the rows read by the one-pass kernel (greedy, top-k <= 32) and
+    by the histogram kernels (the other sampling rows) in one step: a request
+    with window v reads v + 1 target rows, and v draft rows if it samples."""
+    esz = 2 if w.dtype == torch.bfloat16 else 4
+    T = w.temperature.detach().cpu()
+    tk = w.top_k.detach().cpu() if w.top_k is not None else torch.zeros_like(T, dtype=torch.int32)
+    greedy = T == 0
+    k_eff = torch.where(greedy, torch.ones_like(tk), torch.where((tk > 0) & (tk < w.V), tk, torch.full_like(tk, w.V)))
+    fast = greedy | (k_eff <= 32)
+    v = torch.full_like(tk, w.K) if verify_len is None else verify_len.detach().cpu().to(tk.dtype)
+    rows = (v + 1) + torch.where(greedy, torch.zeros_like(v), v)
+    return int(rows[fast].sum()) * w.V * esz, int(rows[~fast].sum()) * w.V * esz
 
 
 def synthetic_cost_table(w, dev):
@@ -248,7 +272,8 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
 
     vl, qo, tot, _ = plan()
     packed = workloads.pack_rows(w.target, qo.cpu(), vl.cpu(), w.bucket)
-    extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()), rows=int(tot), plan=plan, table=table)
+    extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()), rows=int(tot), plan=plan, table=table,
+                 path_bytes=path_bytes(w, vl))
 
     def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
         vl_, qo_, _, _ = plan()
@@ -266,14 +291,20 @@ def run_ours(args, rank, world, local):
     w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
     step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator)
     alg_bytes, rows_t = algorithmic_bytes(w)
+    fast_bytes, hist_bytes = path_bytes(w)
     if extra is not None:
         rows_t = extra["rows"]
         alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2
-    # prep, row select (with finalisation), cluster histogram, chain, resample
-    # (+ the planner for ragged batches, + the budget choice with a cost table)
-    launches_per_step = 5 + (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
-    if args.estimator:   # prep, row select, cluster histogram, features for the draft rows; observe
-        launches_per_step += 5
+        fast_bytes, hist_bytes = extra["path_bytes"]
+    # the roofline is taken on the path that reads more of the logits
+    roof_path = "hist" if hist_bytes > fast_bytes else "fast"
+    roof_bytes = hist_bytes if roof_path == "hist" else fast_bytes
+    # prep, row select (with finalisation), one-CTA histogram, cluster
+    # histogram (rows handed on), chain, resample (+ the planner for ragged
+    # batches, + the budget choice with a cost table)
+    launches_per_step = 6 + (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
+    if args.estimator:   # prep, row select, two histogram kernels, features for the draft rows; observe
+        launches_per_step += 6
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     if not args.quick:
@@ -301,19 +332,20 @@ def run_ours(args, rank, world, local):
     barrier(world)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    # The row kernel alone, for the roofline: events recorded by the library
-    # on its stream right around that launch (a separate pass, because events
-    # between kernels stop the launches from overlapping).
+    # The dominant row kernel(s) alone, for the roofline: events recorded by
+    # the library on its stream right around those launches (a separate pass,
+    # because events between kernels stop the launches from overlapping).
     n_k = max(3, min(args.steps, 20))
     k0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
     k1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
     for ev in k0 + k1:      # torch creates the CUDA event on its first record
         ev.record(stream)
     torch.cuda.synchronize()
+    set_events = sv.set_hist_timing_events if roof_path == "hist" else sv.set_timing_events
     for i in range(n_k):
-        sv.set_timing_events(k0[i], k1[i])
+        set_events(k0[i], k1[i])
         step()
-    sv.set_timing_events(None, None)
+    set_events(None, None)
     torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
     ms_per_step = sum(step_ms) / len(step_ms)
@@ -327,7 +359,7 @@ def run_ours(args, rank, world, local):
     value = world * rows_t / (ms_worst / 1e3)
     kern_avg_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
-    achieved = alg_bytes / kern_avg_s / 1e9
+    achieved = roof_bytes / kern_avg_s / 1e9
     logits_gbs_step = alg_bytes / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -346,11 +378,12 @@ def run_ours(args, rank, world, local):
                    "l2": f"no flush: inputs of {alg_bytes / 1e6:.1f} MB per step exceed the 129 MB L2",
                    "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms)},
-        "roofline": {"bound": "hbm", "kernel": "fast_rows_kernel (one-pass top-k / argmax row select)",
+        "roofline": {"bound": "hbm", "kernel": ROW_PATHS[roof_path]["kernel"],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
-                     "traffic": recorded_traffic(args.workload), "kernel_ms_mean": statistics.mean(kern_ms),
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     "traffic": recorded_traffic(args.workload, roof_path), "kernel_ms_mean": statistics.mean(kern_ms),
+                     "algorithmic_bytes_per_launch": roof_bytes,
+                     "other_path_bytes_per_step": fast_bytes if roof_path == "hist" else hist_bytes},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -376,6 +376,16 @@ sv_status_t sv_verify_chain_noalloc(const void* target_logits, const void* draft
  */
 sv_status_t sv_set_timing_events(void* start_event, void* stop_event);
 
+/*
+ * Measurement aid (not part of the method), as sv_set_timing_events but
+ * around the exact-histogram row kernels (rows whose kept set can exceed 32
+ * tokens: the one-CTA-per-row kernel and the cluster kernel that takes the
+ * rows it hands on), recorded on bf16 calls.  Pass NULLs to stop.
+ * Process-wide; not for calls issued concurrently from several host
+ * threads.  Always returns SV_OK.
+ */
+sv_status_t sv_set_hist_timing_events(void* start_event, void* stop_event);
+
 #ifdef __cplusplus
 }
 #endif

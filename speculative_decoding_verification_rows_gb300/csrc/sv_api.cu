@@ -49,6 +49,7 @@ TaskList task_list(void* ws, size_t off, int n)
 sv_status_t to_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;   // sv_set_timing_events
+cudaEvent_t g_hv_start = nullptr, g_hv_stop = nullptr;   // sv_set_hist_timing_events
 
 // Row kernels for whatever tasks the prep kernel listed (the one-pass kernel
 // also finalises its rows).
@@ -60,8 +61,11 @@ sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s)
     if (e != cudaSuccess) return SV_ERR_CUDA;
     if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SV_ERR_CUDA;
     if (ra.dtype == 0) {   // fp32 rows never take the histogram path (refused in prep)
+        const cudaEvent_t hv0 = g_hv_start, hv1 = g_hv_stop;
+        if (hv0 && hv1 && cudaEventRecord(hv0, s) != cudaSuccess) return SV_ERR_CUDA;
         e = launch_hist_rows(ra, s);
         if (e != cudaSuccess) return SV_ERR_CUDA;
+        if (hv0 && hv1 && cudaEventRecord(hv1, s) != cudaSuccess) return SV_ERR_CUDA;
     }
     return SV_OK;
 }
@@ -332,6 +336,13 @@ sv_status_t sv_set_timing_events(void* start_event, void* stop_event)
 {
     g_ev_start = static_cast<cudaEvent_t>(start_event);
     g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+    return SV_OK;
+}
+
+sv_status_t sv_set_hist_timing_events(void* start_event, void* stop_event)
+{
+    g_hv_start = static_cast<cudaEvent_t>(start_event);
+    g_hv_stop = static_cast<cudaEvent_t>(stop_event);
     return SV_OK;
 }
 

@@ -24,7 +24,8 @@ ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | RO
                   | ROW_TIMEOUT)
 
 EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
-            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_verify_chain_noalloc",
+            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_set_hist_timing_events",
+            "sv_verify_chain_noalloc",
             "sv_plan_budget_cost", "sv_verify_stats", "sv_verify_block", "sv_estimator_state_bytes",
             "sv_estimator_init", "sv_estimator_predict", "sv_estimator_observe")
 
@@ -91,6 +92,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_estimator_observe.restype = I
     L.sv_set_timing_events.argtypes = [P, P]
     L.sv_set_timing_events.restype = I
+    L.sv_set_hist_timing_events.argtypes = [P, P]
+    L.sv_set_hist_timing_events.restype = I
     _lib = L
     return L
 
@@ -137,6 +140,14 @@ def set_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["torch
         load().sv_set_timing_events(None, None)
     else:
         load().sv_set_timing_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
+
+
+def set_hist_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["torch.cuda.Event"]):
+    """Have later bf16 calls record these events around the exact-histogram row kernels."""
+    if start is None or stop is None:
+        load().sv_set_hist_timing_events(None, None)
+    else:
+        load().sv_set_hist_timing_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
 
 
 def workspace_size(n_req: int, k_max: int, vocab: int) -> int:
