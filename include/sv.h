@@ -354,7 +354,7 @@ sv_status_t sv_estimator_observe(double* state, const float* x, const int32_t* a
  * device array in the library, resident on each GPU that loads it until the
  * process exits.  Sizes whose sv_workspace_size(n_req, K, vocab) exceeds
  * 32 MiB return SV_ERR_UNSUPPORTED before any launch (the benchmark's
- * 128 x 8 x 248,320 batch needs about 5 MiB).  The first call on a device
+ * 128 x 8 x 248,320 batch needs about 6 MiB).  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  All calls share
  * the array: calls that overlap on the GPU race, so serialise them.  Nothing
