@@ -742,14 +742,15 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(RowsArgs a, 
 // ----------------------------------------------------------------------------
 // One CTA per row, counters for the binades the row occupies
 // ----------------------------------------------------------------------------
-constexpr int kWideThreads = 256;
+constexpr int kWideThreads = 512;
+constexpr int kWideBlocks = 3;          // CTAs per SM the launch bounds aim at (registers: 65,536 / 1,536)
 constexpr int kWideSlots = 64;           // binades with counters per row (4 threads per slot in the mass pass)
-constexpr int kWideUnroll = 8;           // 16-byte vectors per thread in flight
+constexpr int kWideUnroll = 4;           // 16-byte vectors per thread in flight
 constexpr int kUnclaimed = INT_MIN;      // base[] of a binade not seen yet in this row
 constexpr int kClaiming = INT_MIN + 1;   // base[] while a thread assigns the binade its counters
 constexpr int kBaseMin = -65536;         // a claimed base is 128 * (slot - b) >= -65,408
 constexpr int kClaimSpins = 1 << 14;     // polls before a thread stops waiting for a claim
-static_assert(kWideThreads == 4 * kWideSlots, "the mass pass takes four threads per slot");
+static_assert(kWideThreads >= 4 * kWideSlots, "the mass pass takes four threads per slot");
 
 struct WideSmem {
     uint32_t cnt[(kWideSlots + 1) * 128];   // per-key counters of the claimed binades, then 128 catch-alls
@@ -1096,7 +1097,7 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kWideThreads, 4) wide_rows_kernel(RowsArgs a)
+__global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(RowsArgs a)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
