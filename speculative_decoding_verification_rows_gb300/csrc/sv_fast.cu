@@ -335,7 +335,7 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFastThreads, 2) fast_rows_kernel(RowsArgs a)
+__global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
 {
     constexpr int EPV = DT == 0 ? 8 : 4;
     constexpr int ESZ = DT == 0 ? 2 : 4;

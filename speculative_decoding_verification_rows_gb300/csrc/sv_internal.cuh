@@ -16,7 +16,7 @@ namespace sv {
 // Sizes
 // ----------------------------------------------------------------------------
 constexpr int kFastK = 32;          // largest top-k served by the one-pass select kernel
-constexpr int kFastThreads = 256;   // threads of the one-pass select kernel
+constexpr int kFastThreads = 512;   // threads of the one-pass select kernel
 constexpr int kFastVecs = 8;        // 16-byte vectors per lane per warp chunk (4 KB a warp)
 constexpr int kMaxRowWarps = 4096;  // warps of the one-pass select grid (sizes the partial lists)
 constexpr int kHistThreads = 512;   // threads of the exact-histogram kernel
