@@ -71,7 +71,12 @@ struct WalkSmem {
     double ke[2][128];
     WalkState walk;
     RowPlan plan;
+    double wmass[16];      // block scan: per-warp mass totals, then their exclusive prefixes
+    uint32_t wcount[16];   // the same for counts
+    int wlow[16];          // per-warp lowest occupied binade
+    double e_tok;          // exp((v - m) / T) of the row's token (computed beside the scans)
 };
+constexpr int kWalkThreads = 512;   // walk_row runs on CTAs of this size: one binade per thread
 
 struct HistSmem {
     uint32_t hist[kHistWords];
@@ -211,12 +216,13 @@ __device__ void load_binade_keys(cg::cluster_group& cluster, HistSmem& sm, int C
 // warp 0, key walks on warp 0 and thread 0 (fp64 is scarce), and the
 // decisions travel through shared memory between phases.  load_keys(b, s)
 // fills sm.kc[s] / sm.ke[s] with the per-key counts and masses of binade b
-// (every thread calls it; it may use threads 0..127).  Writes the row's record
-// unless status != 0, and leaves in sm.plan whether the token's tie rank is
-// needed.  Every thread of the CTA must call it.
+// (every thread calls it; it may use threads 0..127).  sm.e_tok, the token's
+// exp((v - m) / T), is computed here unless the caller set it (tok_ready).
+// Writes the row's record unless status != 0, and leaves in sm.plan whether
+// the token's tie rank is needed.  Every thread of the CTA must call it.
 template <typename LoadKeys>
 __device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const RowTask& task, const uint16_t* row, RowInfo* info,
-                         double m, int argmax, int status, LoadKeys load_keys)
+                         double m, int argmax, int status, bool tok_ready, LoadKeys load_keys)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const double T = (double)task.temp;
@@ -228,6 +234,79 @@ __device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const Row
         sm.plan.need_tie = 0;
         sm.plan.token = task.token;
     }
+    const bool topp_on = task.top_p < 1.0f;
+    const int d_tok = task.token;
+    // the token's mass, on warp 1 while the scans below run on the others
+    if (!tok_ready && status == 0 && tid == 32 && d_tok >= 0 && d_tok < a.vocab)
+        sm.e_tok = exp((key_value(key16_of_bf16(row[d_tok])) - m) / T);
+    if (!topk_on) {
+        // Without top-k the top-p cut runs on the binade masses themselves:
+        // one block-wide scan, binade 511 - tid on thread tid (descending),
+        // gives Z1, the lowest occupied binade and the binade holding the
+        // top-p crossing (its mass above and count above).
+        const int b = 511 - tid;
+        const uint32_t cnt = status == 0 ? sm.sums[b].count : 0u;
+        const double ms = status == 0 ? sm.sums[b].mass : 0.0;
+        uint32_t ci = cnt;
+        double mi = ms;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+            const double z = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+            if (lane >= o) {
+                ci += y;
+                mi += z;
+            }
+        }
+        const int low = __reduce_max_sync(0xFFFFFFFFu, cnt ? tid : -1);   // lowest binade = highest thread
+        if (lane == 31) {
+            sm.wmass[warp] = mi;
+            sm.wcount[warp] = ci;
+            sm.wlow[warp] = low;
+        }
+        __syncthreads();
+        if (warp == 0) {   // exclusive prefixes of the 16 warp totals
+            const double wm = lane < 16 ? sm.wmass[lane] : 0.0;
+            const uint32_t wc = lane < 16 ? sm.wcount[lane] : 0u;
+            double pm = wm;
+            uint32_t pc = wc;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                const double z = __shfl_up_sync(0xFFFFFFFFu, pm, o);
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, pc, o);
+                if (lane >= o) {
+                    pm += z;
+                    pc += y;
+                }
+            }
+            const int lw = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? sm.wlow[lane] : -1);
+            __syncwarp();
+            if (lane < 16) {
+                sm.wmass[lane] = pm - wm;
+                sm.wcount[lane] = pc - wc;
+            }
+            if (lane == 15) {
+                W.z_all = pm;
+                W.z1 = pm;
+            }
+            if (lane == 0) {
+                W.bmin = lw >= 0 ? 511 - lw : (1 << 30);
+                W.bk = -1;
+                W.found = 0;
+            }
+        }
+        __syncthreads();
+        if (status == 0 && topp_on) {
+            const double target = (double)task.top_p * W.z1;
+            const double mex = sm.wmass[warp] + (mi - ms);
+            if (ms > 0.0 && mex < target && target <= mex + ms) {
+                W.bp = b;
+                W.mass_above_bp = mex;
+                W.found = 1;
+            }
+        }
+        __syncthreads();
+    } else {
     // Phase A (warp 0): binade scan on counts and masses, descending.
     if (status == 0 && warp == 0) {
         uint32_t cs = 0u;
@@ -327,7 +406,6 @@ __device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const Row
     }
     __syncthreads();
     // Phase D (warp 0): top-p binade on masses capped at the top-k cutoff.
-    const bool topp_on = task.top_p < 1.0f;
     if (status == 0 && topp_on && warp == 0) {
         const double target = (double)task.top_p * W.z1;
         const int bk = W.bk;
@@ -358,6 +436,7 @@ __device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const Row
         }
     }
     __syncthreads();
+    }
     // Phase E: keys of the binade that holds the final cutoff (slot 1).
     int load_b = -1;
     if (status == 0) {
@@ -484,7 +563,7 @@ __device__ __noinline__ void walk_row(WalkSmem& sm, const RowsArgs& a, const Row
             if (kd == cut_key && cut_ties < cut_count) {
                 sm.plan.need_tie = 1;
             } else {
-                info->p_token = kd >= cut_key ? exp((key_value(kd) - m) / T) / z : 0.0;
+                info->p_token = kd >= cut_key ? sm.e_tok / z : 0.0;
             }
         } else {
             info->p_token = nan("");
@@ -689,7 +768,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
 
     // 6. CTA 0: the cutoff walk on the cluster's sums.
     if (rank == 0)
-        walk_row(sm.w, a, task, row, info, m, argmax, status,
+        walk_row(sm.w, a, task, row, info, m, argmax, status, false,
                  [&](int b, int s) { load_binade_keys(cluster, sm, C, b, s, m, T); });
     cluster.sync();
 
@@ -751,6 +830,8 @@ constexpr int kClaiming = INT_MIN + 1;   // base[] while a thread assigns the bi
 constexpr int kBaseMin = -65536;         // a claimed base is 128 * (slot - b) >= -65,408
 constexpr int kClaimSpins = 1 << 14;     // polls before a thread stops waiting for a claim
 static_assert(kWideThreads >= 4 * kWideSlots, "the mass pass takes four threads per slot");
+static_assert(kWideThreads == kWalkThreads && kHistThreads == kWalkThreads, "walk_row takes one binade per thread");
+static_assert(2 * kWideSlots < kWideThreads, "the last thread is idle in the exps of the mass pass");
 
 struct WideSmem {
     uint32_t cnt[(kWideSlots + 1) * 128];   // per-key counters of the claimed binades, then 128 catch-alls
@@ -836,6 +917,10 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
     RowInfo* info = a.info + task.slot;
     const double T = (double)task.temp;
     const int V = a.vocab;
+
+    // the token's key, loaded now so that its latency hides behind the row
+    const int d_tok = task.token;
+    const uint32_t tok_key = (tid == kWideThreads - 1 && d_tok >= 0 && d_tok < V) ? key16_of_bf16(row[d_tok]) : 0u;
 
     // 1. stream the row once: per-key counts and the first maximum.  The
     //    elements before the first 16-byte boundary and after the last whole
@@ -967,6 +1052,8 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
             if (tid == 0) sm.inv_t = 1.0 / T;
             __syncthreads();
             const double inv_t = sm.inv_t;
+            if (tid == kWideThreads - 1)   // an idle thread here: the token's mass for the walk's record
+                sm.w.e_tok = tok_key ? exp((key_value(tok_key) - m) * inv_t) : 0.0;
             for (int i = tid; i < 2 * used; i += kWideThreads) {
                 const int sl = i < used ? i : i - used;
                 const int b = sm.bin_of[sl];
@@ -1031,7 +1118,7 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
         // 4. the cutoff walk, with per-key counts straight from the slots and
         //    per-key masses e_top r^(127 - k) (double-float powers), one key
         //    per thread
-        walk_row(sm.w, a, task, row, info, m, argmax, status, [&](int b, int s) {
+        walk_row(sm.w, a, task, row, info, m, argmax, status, true, [&](int b, int s) {
             const int k = threadIdx.x;
             if (k >= 128) return;
             const int bs = (b >= 0 && b < 512) ? sm.base[b] : kUnclaimed;
