@@ -124,6 +124,11 @@ typedef struct {
  * (rows, 0, vocab); for sv_plan_budget pass (n_req, K, 0).  0 on overflow. */
 size_t sv_workspace_size(int n_req, int k_max, int vocab);
 
+/* Workspace bytes for sv_verify_block (it keeps up to k_max + 1 full-row jobs
+ * per request and each request's weights and residual sums); 0 for sizes
+ * this build does not handle. */
+size_t sv_workspace_size_block(int n_req, int k_max, int vocab);
+
 /* Human-readable name of a status code (static string). */
 const char* sv_status_string(sv_status_t status);
 
@@ -211,9 +216,11 @@ sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits,
  *   accept_len < v; an empty residual falls back to p_a with
  *   SV_ROW_RESID_ZERO) or from p_v.  q(d) == 0 makes the ratio +inf if
  *   p(d) > 0, else 0 (SV_ROW_Q_ZERO).  With v = 1 this is exactly
- *   sv_verify_chain.  Needs every row of the window to have a listed kept set
- *   (greedy or top-k <= 32); a sampling request with a larger kept set gets
- *   SV_ROW_UNSUPPORTED and emits nothing.
+ *   sv_verify_chain.  Kept sets of any size: for sampling requests whose kept
+ *   sets are not listed (more than 32 tokens) the sums H_j and the draw run
+ *   over whole rows in exact 62-bit fixed point, with w p floored as a 64-bit
+ *   fraction.  The workspace must hold sv_workspace_size_block(n_req, K,
+ *   vocab) bytes.  fp32 logits: as sv_verify_chain.
  */
 sv_status_t sv_verify_block(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
                             int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,

@@ -76,9 +76,9 @@ struct Carved {
 };
 
 Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* tgt, const void* drf,
-             int64_t stride_t, int64_t stride_d)
+             int64_t stride_t, int64_t stride_d, int block = 0)
 {
-    const WsLayout L = ws_layout(n_req, k_max, vocab);
+    const WsLayout L = ws_layout(n_req, k_max, vocab, block);
     Carved c{};
     RowsArgs& ra = c.ra;
     ra.tgt = tgt;
@@ -115,6 +115,8 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.req = at<ReqState>(ws, L.req);
     ca.jobs = at<ResampleJob>(ws, L.jobs);
     ca.tiles = at<TileSums>(ws, L.tiles);
+    ca.blk_w = block ? at<double>(ws, L.blk) : nullptr;
+    ca.blk_h = block ? at<unsigned long long>(ws, L.blk + sizeof(double) * (size_t)n_req * (size_t)(k_max + 1)) : nullptr;
     ca.num_sms = ra.num_sms;
     return c;
 }
@@ -132,10 +134,10 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
     if (layout == 1 && (!qo || !vl || bucket < 1)) return SV_ERR_INVALID_ARG;
     if (K > kMaxK || V > kMaxVocab || n > (1 << 22)) return SV_ERR_UNSUPPORTED;
-    const size_t need = sv_workspace_size(n, K, V);
+    const size_t need = block ? sv_workspace_size_block(n, K, V) : sv_workspace_size(n, K, V);
     if (need == 0) return SV_ERR_UNSUPPORTED;
     if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
-    Carved c = carve(ws, n, K, V, (int)dt, tgt, drf, V, V);
+    Carved c = carve(ws, n, K, V, (int)dt, tgt, drf, V, V, block);
     ChainArgs& ca = c.ca;
     ca.layout = layout;
     ca.block = block;
@@ -153,13 +155,24 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     sv_status_t st = run_rows(c.ra, s);
     if (st != SV_OK) return st;
     if (launch_chain(ca, s) != cudaSuccess) return SV_ERR_CUDA;
-    if (dt == SV_DTYPE_BF16 && launch_resample(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (dt == SV_DTYPE_BF16 && launch_resample(ca, 0, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (block && dt == SV_DTYPE_BF16) {   // requests with unlisted kept sets: decide, then draw
+        if (launch_block_finish(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (launch_resample(ca, 1, s) != cudaSuccess) return SV_ERR_CUDA;
+    }
     return SV_OK;
 }
 
 }  // namespace
 
 extern "C" {
+
+size_t sv_workspace_size_block(int n_req, int k_max, int vocab)
+{
+    if (n_req < 1 || k_max < 0 || vocab < 1 || n_req > (1 << 22) || k_max > kMaxK || vocab > kMaxVocab) return 0;
+    if ((long long)n_req * (2LL * k_max + 1) > (1LL << 30)) return 0;
+    return ws_layout(n_req, k_max, vocab, 1).total;
+}
 
 size_t sv_workspace_size(int n_req, int k_max, int vocab)
 {

@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         a.counters->n_jobs = 0;
         a.counters->timeout = 0;
         a.counters->n_ovf = 0;
+        a.counters->n_jobs2 = 0;
     }
 }
 
@@ -401,6 +402,9 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(ChainArgs a)
             job.a = acc_len;
             job.residual = residual ? 1 : 0;
             job.done = 0;
+            job.kind = kJobDraw;
+            job.pad = 0;
+            job.wfix = 0ull;
             a.jobs[slot] = job;
             t = -2;
         }
@@ -489,9 +493,58 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
                ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(rejects >> 32)) << 32);
     qzero |= ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)qzero)) |
              ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(qzero >> 32)) << 32);
-    if (!any_err && !st.greedy && unlisted) {   // block mode needs listed kept sets
-        if (lane == 0 && a.row_status) a.row_status[(size_t)r * width] |= kUnsupported;
-        any_err = kUnsupported;
+    if (a.blk_h && lane == 0) a.blk_h[(size_t)r * width] = 0ull;   // not waiting for full-row sums
+    if (!any_err && !st.greedy && unlisted) {
+        // Kept sets too large to list: the weights here, the residual masses
+        // H_j (positions 1 .. v-1) as full-row sum jobs of the resample
+        // kernel, the decision in block_finish_kernel.  With v <= 1 no H_j is
+        // needed: decide now and list the draw.
+        if (lane == 0) {
+            double w = 1.0;
+            a.blk_w[(size_t)r * width] = 1.0;
+            for (int j = 1; j <= v; ++j) {
+                const double p = a.info[slot_target(r, K, j - 1)].p_token;
+                const double q = a.info[slot_draft(r, K, j - 1)].p_token;
+                const double ratio = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
+                const double x = w > 0.0 ? w * ratio : 0.0;
+                w = x < 1.0 ? x : 1.0;
+                a.blk_w[(size_t)r * width + j] = w;
+            }
+            if (a.row_status)
+                for (int j = 0; j < v; ++j)
+                    if ((qzero >> j) & 1) a.row_status[(size_t)r * width + j] |= kQZero;
+        }
+        __syncwarp();
+        if (v >= 2) {
+            for (int j = 1 + lane; j < v; j += 32) {
+                ResampleJob job;
+                job.req = r;
+                job.a = j;
+                job.residual = 1;
+                job.done = 0;
+                job.kind = kJobSum;
+                job.pad = 0;
+                job.wfix = weight_fix(a.blk_w[(size_t)r * width + j]);
+                a.jobs[atomicAdd(&a.counters->n_jobs, 1)] = job;
+            }
+            if (lane == 0) a.blk_h[(size_t)r * width] = 1ull;   // decided by block_finish_kernel
+        } else if (lane == 0) {
+            const double wv = a.blk_w[(size_t)r * width + v];
+            const int acc = (v == 1 && uniform_f64(a.seed, (uint32_t)r, 0u, 0u) < wv) ? 1 : 0;
+            if (acc) out[0] = d[0];
+            a.accept_len[r] = acc;
+            a.num_emitted[r] = acc + 1;
+            ResampleJob job;
+            job.req = r;
+            job.a = acc;
+            job.residual = acc < v ? 1 : 0;
+            job.done = 0;
+            job.kind = kJobDraw;
+            job.pad = 0;
+            job.wfix = acc < v ? weight_fix(a.blk_w[(size_t)r * width + acc]) : 0ull;
+            a.jobs[atomicAdd(&a.counters->n_jobs, 1)] = job;
+        }
+        return;
     }
     if (any_err) {
         if (lane == 0) {
@@ -619,6 +672,54 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
 }
 
 // ----------------------------------------------------------------------------
+// Block verification of requests whose kept sets are not listed: with the
+// residual sums H_j of positions 1 .. v-1 in hand (the resample kernel's sum
+// jobs), the stopping probabilities, the accepted length, and the job that
+// draws the emitted token (max(w_a p_a - q_a, 0), or p_v after full
+// acceptance).  One warp per request.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kChainWarps * 32) block_finish_kernel(ChainArgs a)
+{
+    pdl_enter();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * kChainWarps + warp;
+    if (r >= a.n_req) return;
+    const int K = a.K, width = K + 1;
+    if (a.blk_h[(size_t)r * width] == 0ull) return;   // decided in block_kernel
+    const int v = a.req[r].v;
+    int32_t* out = a.out_tokens + (size_t)r * width;
+    const int32_t* d = a.draft_tokens + (size_t)r * K;
+    unsigned long long stop = 0ull;
+    for (int j = 1 + lane; j <= v; j += 32) {
+        const double wj = a.blk_w[(size_t)r * width + j];
+        double h = wj;
+        if (j < v) {
+            const double H = (double)a.blk_h[(size_t)r * width + j] * 0x1p-62;
+            const double den = H + 1.0 - wj;
+            h = den > 0.0 ? H / den : 1.0;
+        }
+        if (uniform_f64(a.seed, (uint32_t)r, (uint32_t)(j - 1), 0u) < h) stop |= 1ull << j;
+    }
+    stop = ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)stop)) |
+           ((unsigned long long)__reduce_or_sync(0xFFFFFFFFu, (unsigned)(stop >> 32)) << 32);
+    const int acc = stop ? 63 - __clzll((long long)stop) : 0;
+    for (int j = lane; j < acc; j += 32) out[j] = d[j];
+    if (lane == 0) {
+        a.accept_len[r] = acc;
+        a.num_emitted[r] = acc + 1;
+        ResampleJob job;
+        job.req = r;
+        job.a = acc;
+        job.residual = acc < v ? 1 : 0;
+        job.done = 0;
+        job.kind = kJobDraw;
+        job.pad = 0;
+        job.wfix = acc < v ? weight_fix(a.blk_w[(size_t)r * width + acc]) : 0ull;
+        a.jobs[a.counters->n_jobs + atomicAdd(&a.counters->n_jobs2, 1)] = job;
+    }
+}
+
+// ----------------------------------------------------------------------------
 // sv_build_target_probs outputs
 // ----------------------------------------------------------------------------
 __global__ void rows_out_kernel(ChainArgs a, float* prob_of_token, sv_row_desc_t* desc)
@@ -696,6 +797,12 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s)
     const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
     if (a.block) return launch_pdl(block_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
     return launch_pdl(chain_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
+}
+
+cudaError_t launch_block_finish(const ChainArgs& a, cudaStream_t s)
+{
+    const int grid = (a.n_req + kChainWarps - 1) / kChainWarps;
+    return launch_pdl(block_finish_kernel, dim3(grid), dim3(kChainWarps * 32), 0, s, a);
 }
 
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,

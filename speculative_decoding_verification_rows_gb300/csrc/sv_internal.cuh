@@ -116,13 +116,28 @@ struct ReqState {
 
 constexpr int kMaxK = 63;           // drafted positions per request (bit masks above)
 
-// A request whose emitted token needs a full-row resample.
+// A full-row job of the resample kernel: draw the emitted token of a request
+// whose kept set is not listed, or (block verification) sum a residual mass.
 struct ResampleJob {
     int32_t req;
-    int32_t a;        // position of the emitted token
-    int32_t residual; // 1: max(0, p_a - q_a); 0: p_a (bonus)
+    int32_t a;        // position of the rows (the emitted token's, or the summed one's)
+    int32_t residual; // 1: max(0, w p_a - q_a); 0: p_a (bonus)
     int32_t done;     // row chunks of the job the resample has finished (0 when listed)
+    int32_t kind;     // kJobDraw or kJobSum
+    int32_t pad;
+    unsigned long long wfix;   // w as a 64-bit fraction (floor(w 2^64)); 0 means w = 1
 };
+constexpr int kJobDraw = 0;   // draw the emitted token by inverse CDF
+constexpr int kJobSum = 1;    // only the exact residual total (block verification's H_j)
+
+// A weight w in [0, 1] as a 64-bit fraction floor(w 2^64); w >= 1 as 0, the
+// code for "no weight".
+__device__ __forceinline__ unsigned long long weight_fix(double w)
+{
+    if (!(w < 1.0)) return 0ull;
+    if (!(w > 0.0)) return 1ull;   // w = 0: the smallest weight, p w floors to 0
+    return __double2ull_rz(w * 0x1p64);
+}
 
 // Chunks and tiles of the full-row resample.  A chunk (kResampleUnit
 // elements) is what one CTA of the resample kernel streams at a time; each
@@ -159,20 +174,23 @@ struct Counters {
     int32_t n_jobs;
     int32_t timeout;   // set by a row kernel whose bounded wait gave up
     int32_t n_ovf;     // histogram rows handed from the one-CTA kernel to the cluster kernel
-    int32_t pad[11];
+    int32_t n_jobs2;   // block verification: jobs listed after the residual sums (from index n_jobs)
+    int32_t pad[10];
 };
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, tiles, total;
-    int slots, max_tasks;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, tiles, blk, total;
+    int slots, max_tasks, max_jobs;
     size_t n_partials;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // slots: target positions 0..K and draft positions 0..K-1 of every request.
-inline WsLayout ws_layout(int n_req, int k_max, int vocab)
+// Block verification (block = 1) lists up to K + 1 full-row jobs per request
+// and keeps each request's weights w_j and residual sums H_j.
+inline WsLayout ws_layout(int n_req, int k_max, int vocab, int block = 0)
 {
     WsLayout L{};
     L.slots = n_req * (2 * k_max + 1);
@@ -189,8 +207,10 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab)
     L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
-    L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)n_req);
-    L.tiles = off;      off = align256(off + sizeof(TileSums) * (size_t)n_req * (size_t)resample_tiles(vocab));
+    L.max_jobs = block ? n_req * (k_max + 1) : n_req;
+    L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)L.max_jobs);
+    L.tiles = off;      off = align256(off + sizeof(TileSums) * (size_t)L.max_jobs * (size_t)resample_tiles(vocab));
+    L.blk = off;        off = block ? align256(off + 2 * sizeof(double) * (size_t)n_req * (size_t)(k_max + 1)) : off;
     L.total = off;
     return L;
 }
@@ -519,13 +539,16 @@ struct ChainArgs {
     RowInfo* info;
     ReqState* req;
     ResampleJob* jobs;
-    TileSums* tiles;   // [n_req][resample_tiles(vocab)]
+    TileSums* tiles;   // [max_jobs][resample_tiles(vocab)]
+    double* blk_w;     // block verification: [n_req][K + 1] weights w_j
+    unsigned long long* blk_h;   // block verification: [n_req][K + 1] residual sums H_j (2^-62 units)
     int num_sms;
 };
 
 cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
-cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_resample(const ChainArgs& a, int round, cudaStream_t s);
+cudaError_t launch_block_finish(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
                             cudaStream_t s);
 

@@ -41,7 +41,14 @@ struct Dist {                 // one row's distribution, as the weight passes ne
     int partial;              // ties < tokens at the cutoff: ranks are needed
     int16_t* map;             // binade -> table slot, -1: weight computed per key
     unsigned long long* tab;
+    unsigned long long wfix;  // p's weight in the residual (64-bit fraction; 0: none)
 };
+
+// p's weight applied to a fixed-point probability: floor(wp w).
+__device__ __forceinline__ unsigned long long pweight(const Dist& P, unsigned long long wp)
+{
+    return P.wfix ? __umul64hi(wp, P.wfix) : wp;
+}
 
 __device__ __forceinline__ unsigned long long fix_of(double p)
 {
@@ -136,6 +143,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
     P.partial = IP.desc.cutoff_ties < IP.cut_count;
     P.map = sm.map[0];
     P.tab = sm.tab;
+    P.wfix = job.wfix;
     Q = P;
     if (job.residual) {
         Q.row = (const uint16_t*)a.drf + ((size_t)r * K + pa) * (size_t)a.stride_d;
@@ -406,7 +414,8 @@ __device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool resid
             const unsigned long long en = wb[e];
             const uint32_t ekp = (uint32_t)(en & 0xFFFFu), ekq = (uint32_t)((en >> 16) & 0xFFFFu);
             const unsigned long long wp = fixp(P, ekp);
-            const unsigned long long wr = residual ? sat_sub(wp, ((en >> 32) & 1ull) ? fixp(Q, ekq) : 0ull) : wp;
+            const unsigned long long wr =
+                residual ? sat_sub(pweight(P, wp), ((en >> 32) & 1ull) ? fixp(Q, ekq) : 0ull) : wp;
             tr += wr;
             tpp += wp;
             wv[q] = use_p ? wp : wr;
@@ -454,7 +463,7 @@ __device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool resid
     return found;
 }
 
-__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units)
+__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units, int round)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -462,7 +471,10 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int V = a.vocab, K = a.K;
     const int n_tiles = resample_tiles(V);
-    const long long total = (long long)a.counters->n_jobs * n_units;
+    // round 0: the jobs the chain or block kernel listed; round 1: those the
+    // block finish kernel listed after them
+    const int j0 = round ? a.counters->n_jobs : 0;
+    const long long total = (long long)(round ? a.counters->n_jobs2 : a.counters->n_jobs) * n_units;
     const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
     if (tid == 0) {
         sm.cur_job = -1;
@@ -473,7 +485,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     __syncthreads();
     uint32_t phase = 0u;
     for (long long u = u_lo; u < u_hi; ++u) {
-        const int j = (int)(u / n_units), c = (int)(u % n_units);
+        const int j = j0 + (int)(u / n_units), c = (int)(u % n_units);
         const ResampleJob job = a.jobs[j];
         const bool residual = job.residual != 0;
         Dist P, Q;
@@ -522,19 +534,21 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
                 const unsigned long long wp = fixp(P, ekp);
                 const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
                 const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
+                const unsigned long long wpw = pweight(P, wp);   // p's weighted value in the residual
                 if (!tP && !tQ) {
                     acc[kTsBaseP] += wp;
-                    acc[kTsBaseRes] += residual ? sat_sub(wp, wq) : wp;
+                    acc[kTsBaseRes] += residual ? sat_sub(wpw, wq) : wp;
                 } else {
                     const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
 #pragma unroll
                     for (int sp_ = 0; sp_ < 2; ++sp_) {
                         const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
+                        const unsigned long long pw_ = (tP && !sp_) ? 0ull : wpw;
                         acc[kTsTieP + sp_] += p_;
 #pragma unroll
                         for (int sq = 0; sq < 2; ++sq) {
                             const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
-                            acc[kTsTieRes + 2 * sp_ + sq] += residual ? sat_sub(p_, q_) : p_;
+                            acc[kTsTieRes + 2 * sp_ + sq] += residual ? sat_sub(pw_, q_) : p_;
                         }
                     }
                 }
@@ -615,6 +629,11 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
             }
         }
         const unsigned long long W = block_sum_u64(sm, s_res), Wp = block_sum_u64(sm, s_p);
+        if (job.kind == kJobSum) {   // block verification's H_j: the exact total is all it needs
+            if (tid == 0) a.blk_h[(size_t)job.req * (K + 1) + job.a] = W;
+            __syncthreads();
+            continue;
+        }
         const bool zero = residual && W == 0ull;
         const bool use_p = !residual || zero;
         const unsigned long long Wu = use_p ? Wp : W;
@@ -649,7 +668,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
 
 }  // namespace
 
-cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
+cudaError_t launch_resample(const ChainArgs& a, int round, cudaStream_t s)
 {
     static int blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
     int dev = 0;
@@ -664,7 +683,7 @@ cudaError_t launch_resample(const ChainArgs& a, cudaStream_t s)
         if (nb < 1) nb = 1;
     }
     const int n_units = (a.vocab + kResampleUnit - 1) / kResampleUnit;
-    return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units);
+    return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units, round);
 }
 
 }  // namespace sv

@@ -23,11 +23,11 @@ ROW_Q_ZERO, ROW_RESID_ZERO, ROW_UNSUPPORTED, ROW_TIMEOUT = 32, 64, 128, 256
 ROW_ERROR_MASK = (ROW_NONFINITE | ROW_EMPTY | ROW_BAD_TOKEN | ROW_BAD_PARAM | ROW_BAD_LAYOUT | ROW_UNSUPPORTED
                   | ROW_TIMEOUT)
 
-EXPORTED = ("sv_workspace_size", "sv_status_string", "sv_plan_budget", "sv_build_target_probs",
-            "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events", "sv_set_hist_timing_events",
-            "sv_verify_chain_noalloc",
-            "sv_plan_budget_cost", "sv_verify_stats", "sv_verify_block", "sv_estimator_state_bytes",
-            "sv_estimator_init", "sv_estimator_predict", "sv_estimator_observe")
+EXPORTED = ("sv_workspace_size", "sv_workspace_size_block", "sv_status_string", "sv_plan_budget",
+            "sv_build_target_probs", "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events",
+            "sv_set_hist_timing_events", "sv_verify_chain_noalloc", "sv_plan_budget_cost", "sv_verify_stats",
+            "sv_verify_block", "sv_estimator_state_bytes", "sv_estimator_init", "sv_estimator_predict",
+            "sv_estimator_observe")
 
 
 class SVError(RuntimeError):
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     P, I, I64, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
     L.sv_workspace_size.argtypes = [I, I, I]
     L.sv_workspace_size.restype = SZ
+    L.sv_workspace_size_block.argtypes = [I, I, I]
+    L.sv_workspace_size_block.restype = SZ
     L.sv_status_string.argtypes = [I]
     L.sv_status_string.restype = ctypes.c_char_p
     L.sv_plan_budget.argtypes = [P, I, P, I, I, I, I, P, P, P, P, P, SZ, P]
@@ -152,6 +154,13 @@ def set_hist_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["
 
 def workspace_size(n_req: int, k_max: int, vocab: int) -> int:
     size = load().sv_workspace_size(n_req, k_max, vocab)
+    if size == 0:
+        raise SVError("sizes beyond what this build supports")
+    return size
+
+
+def workspace_size_block(n_req: int, k_max: int, vocab: int) -> int:
+    size = load().sv_workspace_size_block(n_req, k_max, vocab)
     if size == 0:
         raise SVError("sizes beyond what this build supports")
     return size
@@ -340,7 +349,7 @@ def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_toke
         _dev(draft, target.dtype)
         assert draft.shape == (n, K, V)
     o = out or _outs(n, K, dev)
-    w = _ws(ws, dev, workspace_size(n, K, V))
+    w = _ws(ws, dev, workspace_size_block(n, K, V) if block else workspace_size(n, K, V))
     fn = load().sv_verify_block if block else load().sv_verify_chain
     _check(fn(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens), _ptr(verify_len),
               _sampling(temperature, top_k, top_p), seed, _ptr(o.accept_len), _ptr(o.out_tokens),
