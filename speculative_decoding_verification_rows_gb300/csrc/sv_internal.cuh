@@ -547,7 +547,7 @@ struct ChainArgs {
 
 cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
-cudaError_t launch_resample(const ChainArgs& a, int round, cudaStream_t s);
+cudaError_t launch_resample(const ChainArgs& a, int wave, cudaStream_t s);
 cudaError_t launch_block_finish(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
                             cudaStream_t s);

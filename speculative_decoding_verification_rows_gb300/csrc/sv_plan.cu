@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
     if (nsel > 0) {
         unsigned long long prefix = 0ull, mask = 0ull;
         int kk = (int)nsel;
-        for (int round = 0; round < 8; ++round) {
-            const int shift = 56 - 8 * round;
+        for (int digit = 0; digit < 8; ++digit) {   // 8-bit digits, most significant first
+            const int shift = 56 - 8 * digit;
             for (int b = tid; b < 256; b += kPlanThreads) hist[b] = 0u;
             __syncthreads();
             for (long long c = tid; c < (long long)n * K; c += kPlanThreads) {

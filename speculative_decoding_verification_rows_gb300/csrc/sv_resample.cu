@@ -463,7 +463,7 @@ __device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool resid
     return found;
 }
 
-__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units, int round)
+__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units, int wave)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -471,10 +471,10 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int V = a.vocab, K = a.K;
     const int n_tiles = resample_tiles(V);
-    // round 0: the jobs the chain or block kernel listed; round 1: those the
+    // wave 0: the jobs the chain or block kernel listed; wave 1: those the
     // block finish kernel listed after them
-    const int j0 = round ? a.counters->n_jobs : 0;
-    const long long total = (long long)(round ? a.counters->n_jobs2 : a.counters->n_jobs) * n_units;
+    const int j0 = wave ? a.counters->n_jobs : 0;
+    const long long total = (long long)(wave ? a.counters->n_jobs2 : a.counters->n_jobs) * n_units;
     const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
     if (tid == 0) {
         sm.cur_job = -1;
@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
 
 }  // namespace
 
-cudaError_t launch_resample(const ChainArgs& a, int round, cudaStream_t s)
+cudaError_t launch_resample(const ChainArgs& a, int wave, cudaStream_t s)
 {
     static int blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
     int dev = 0;
@@ -683,7 +683,7 @@ cudaError_t launch_resample(const ChainArgs& a, int round, cudaStream_t s)
         if (nb < 1) nb = 1;
     }
     const int n_units = (a.vocab + kResampleUnit - 1) / kResampleUnit;
-    return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units, round);
+    return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units, wave);
 }
 
 }  // namespace sv
