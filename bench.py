@@ -395,12 +395,17 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(w, sv, dev, extra, steps, method="chain"):
-    """Same metric through the public API from pinned host buffers: H2D of the
-    step's inputs and D2H of its results inside the timed region."""
+    """Same metric through the public API from pinned host buffers: H2D of every
+    step's inputs and D2H of its results inside the timed region.  Two device
+    input buffers and a copy stream let step i+1's inputs cross the host link
+    while step i verifies (each buffer is refilled only after the step that
+    read it)."""
     names = ["target", "draft", "draft_tokens", "temperature", "top_k", "top_p"]
     dev_t = {k: (extra["packed"] if (k == "target" and extra) else getattr(w, k)) for k in names}
+    if extra is not None:
+        dev_t["conf"] = w.conf
     host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in dev_t.items()}
-    dbuf = {k: (torch.empty_like(v) if v is not None else None) for k, v in dev_t.items()}
+    dbufs = [{k: (torch.empty_like(v) if v is not None else None) for k, v in dev_t.items()} for _ in range(2)]
     res_host = [torch.empty(w.n, dtype=torch.int32).pin_memory(),
                 torch.empty((w.n, w.K + 1), dtype=torch.int32).pin_memory(),
                 torch.empty(w.n, dtype=torch.int32).pin_memory()]
@@ -408,46 +413,62 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
     ws_p = sv.Workspace(dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in res_host)
-    if extra is not None:
-        h2d += w.conf.numel() * 4
-        conf_h = w.conf.cpu().pin_memory()
-        conf_d = torch.empty_like(w.conf)
+    comp = torch.cuda.current_stream(dev)
+    copy_s = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    freed = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def one():
-        for k in names:
-            if host[k] is not None:
-                dbuf[k].copy_(host[k], non_blocking=True)
+    def load(i):
+        b = i % 2
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(freed[b])     # the step that read this buffer is done
+            for k, v in host.items():
+                if v is not None:
+                    dbufs[b][k].copy_(v, non_blocking=True)
+            copied[b].record(copy_s)
+
+    def verify(i):
+        b = i % 2
+        d = dbufs[b]
+        comp.wait_event(copied[b])
         if extra is None:
-            o = sv.verify_chain(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["temperature"],
-                                dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws, block=method == "block")
+            o = sv.verify_chain(d["target"], d["draft"], d["draft_tokens"], d["temperature"], d["top_k"], d["top_p"],
+                                seed=w.seed, ws=ws, block=method == "block")
         else:
-            conf_d.copy_(conf_h, non_blocking=True)
             if extra["table"] is None:
-                vl, qo, _, _ = sv.plan_budget(conf_d, w.budget, w.bucket, ws=ws_p)
+                vl, qo, _, _ = sv.plan_budget(d["conf"], w.budget, w.bucket, ws=ws_p)
             else:
                 tb = extra["table"]
-                _, _, vl, qo, _, _ = sv.plan_budget_cost(conf_d, tb[0], tb[1], w.bucket, tb[2], ws=ws_p)
-            o = sv.verify_ragged(dbuf["target"], dbuf["draft"], qo, vl, dbuf["draft_tokens"], dbuf["temperature"],
-                                 dbuf["top_k"], dbuf["top_p"], seed=w.seed, ws=ws)
+                _, _, vl, qo, _, _ = sv.plan_budget_cost(d["conf"], tb[0], tb[1], w.bucket, tb[2], ws=ws_p)
+            o = sv.verify_ragged(d["target"], d["draft"], qo, vl, d["draft_tokens"], d["temperature"], d["top_k"],
+                                 d["top_p"], seed=w.seed, ws=ws)
+        freed[b].record(comp)
         res_host[0].copy_(o.accept_len, non_blocking=True)
         res_host[1].copy_(o.out_tokens, non_blocking=True)
         res_host[2].copy_(o.num_emitted, non_blocking=True)
 
-    for _ in range(2):
-        one()
+    def run(n):
+        load(0)
+        for i in range(n):
+            if i + 1 < n:
+                load(i + 1)
+            verify(i)
+
+    run(2)
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        one()
-    e.record()
+    s.record(copy_s)
+    comp.wait_stream(copy_s)
+    run(steps)
+    e.record(comp)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     rows = extra["rows"] if extra is not None else w.n * (w.K + 1)
     return {"value": rows / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
-            "note": "inputs copied from pinned host memory and results read back inside the timed region"}
+            "note": "every step's inputs copied from pinned host memory and its results read back inside the "
+                    "timed region; the next step's copy overlaps this step's verify (two input buffers)"}
 
 
 # ----------------------------------------------------------------------------
