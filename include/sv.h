@@ -76,7 +76,7 @@ typedef enum {
     SV_ERR_INVALID_ARG = 1, /* null pointer, negative/zero size, inconsistent sizes */
     SV_ERR_WORKSPACE = 2,   /* ws NULL, misaligned or smaller than sv_workspace_size */
     SV_ERR_CUDA = 3,        /* a kernel launch failed                                */
-    SV_ERR_UNSUPPORTED = 4  /* a size or layout this build does not handle           */
+    SV_ERR_UNSUPPORTED = 4  /* a size or layout the library does not handle         */
 } sv_status_t;
 
 typedef enum { SV_DTYPE_BF16 = 0, SV_DTYPE_F32 = 1 } sv_dtype_t;
@@ -90,7 +90,7 @@ enum {
     SV_ROW_BAD_LAYOUT = 16,  /* ragged window does not match qo_indptr / bucket    */
     SV_ROW_Q_ZERO = 32,      /* informational: q(d) == 0 at a tested position      */
     SV_ROW_RESID_ZERO = 64,  /* informational: empty residual, sampled from p      */
-    SV_ROW_UNSUPPORTED = 128, /* combination this build refuses (see sv_verify_*)  */
+    SV_ROW_UNSUPPORTED = 128, /* combination the library refuses (sv_verify_*)  */
     SV_ROW_TIMEOUT = 256      /* a bounded wait on a bulk copy gave up: rows of the
                                  call were not processed (never seen in practice) */
 };
@@ -126,7 +126,7 @@ size_t sv_workspace_size(int n_req, int k_max, int vocab);
 
 /* Workspace bytes for sv_verify_block (it keeps up to k_max + 1 full-row jobs
  * per request and each request's weights and residual sums); 0 for sizes
- * this build does not handle. */
+ * the library does not handle. */
 size_t sv_workspace_size_block(int n_req, int k_max, int vocab);
 
 /* Human-readable name of a status code (static string). */

@@ -32,8 +32,8 @@
  *  - Uniforms: Philox4x32-10, Salmon, Moraes, Dror, Shaw, "Parallel random
  *    numbers: as easy as 1, 2, 3", SC'11.
  *
- * Readings where the pages are silent are listed in the design doc; each is
- * restated at the function that takes it.
+ * Where the pages are silent, the reading taken is stated at the function
+ * that takes it.
  */
 #include <math.h>
 #include <stdint.h>
@@ -693,7 +693,7 @@ int orc_plan_budget(const float* conf, int ld, const int32_t* draft_len, int n, 
  * overhead and an optional batch-size staircase of overheads are added (they
  * do not cancel in the ratio).
  *
- * Readings (restated in the design doc):
+ * Readings:
  *  - tau(B) = expected tokens a step that submits B tokens emits: n (one
  *    anchor / bonus token per request) plus the survivals s_{r,i} of the
  *    B - n candidates the planner selects, i.e. the B - n largest survivals
@@ -849,7 +849,7 @@ void orc_verify_stats(const int32_t* accept_len, const int32_t* num_emitted, con
  * and dropped only if it still crosses zero; the intercepts take their Newton
  * step given the slope step actually taken; the statistics are then cleared.
  *
- * Readings (restated in the design doc):
+ * Readings:
  *  - q is the distribution the draft token is drawn from, the request's
  *    transform (temperature, top-k, top-p) of the draft row -- the same q the
  *    verification uses -- at T = 1 for greedy requests.  q_max = 1 / z (the

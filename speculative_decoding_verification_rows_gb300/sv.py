@@ -155,14 +155,14 @@ def set_hist_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["
 def workspace_size(n_req: int, k_max: int, vocab: int) -> int:
     size = load().sv_workspace_size(n_req, k_max, vocab)
     if size == 0:
-        raise SVError("sizes beyond what this build supports")
+        raise SVError("sizes beyond what the library supports")
     return size
 
 
 def workspace_size_block(n_req: int, k_max: int, vocab: int) -> int:
     size = load().sv_workspace_size_block(n_req, k_max, vocab)
     if size == 0:
-        raise SVError("sizes beyond what this build supports")
+        raise SVError("sizes beyond what the library supports")
     return size
 
 
