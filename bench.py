@@ -227,6 +227,16 @@ def path_bytes(w, verify_len=None) -> tuple[int, int]:
     return int(rows[fast].sum()) * w.V * esz, int(rows[~fast].sum()) * w.V * esz
 
 
+def small_topk(w) -> bool:
+    """Whether every request is greedy or keeps at most 32 tokens by top-k: the
+    host-side promise (SAMPLING_SMALL_TOPK) a serving engine can give from the
+    batch's sampling settings, which it holds on the host.  Taken once, before
+    any timing."""
+    T = w.temperature.detach().cpu()
+    tk = w.top_k.detach().cpu() if w.top_k is not None else torch.zeros_like(T, dtype=torch.int32)
+    return bool(((T == 0) | ((tk >= 1) & (tk <= 32))).all())
+
+
 def synthetic_cost_table(w, dev):
     """A step-cost table shaped like profiled CUDA-graph buckets: shelves every
     256 submitted tokens up to the bucket, cost rising with the tokens and a
@@ -245,6 +255,7 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
                                                                                  device=dev),
                        torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
                                                                                  device=dev))
+    small = small_topk(w)
     if w.layout == "chain":
         block = method == "block"
         est = sv.Estimator(w.K, dev) if estimator else None
@@ -252,7 +263,8 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
         def step(tgt=w.target, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
             if est is not None:
                 x, _ = est.predict(drf, T, tk, tp)
-            o = sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block)
+            o = sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block,
+                                small_topk=small)
             if est is not None:
                 est.observe(x, o.accept_len, o.num_emitted)
             return o
@@ -277,7 +289,8 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
 
     def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
         vl_, qo_, _, _ = plan()
-        return sv.verify_ragged(tgt, drf, qo_, vl_, toks, T, tk, tp, seed=w.seed, ws=ws, out=out)
+        return sv.verify_ragged(tgt, drf, qo_, vl_, toks, T, tk, tp, seed=w.seed, ws=ws, out=out,
+                                small_topk=small)
     return step, out, extra
 
 
@@ -300,9 +313,18 @@ def run_ours(args, rank, world, local):
     roof_path = "hist" if hist_bytes > fast_bytes else "fast"
     roof_bytes = hist_bytes if roof_path == "hist" else fast_bytes
     # prep, row select (with finalisation), one-CTA histogram, cluster
-    # histogram (rows handed on), chain, resample (+ the planner for ragged
-    # batches, + the budget choice with a cost table)
-    launches_per_step = 6 + (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
+    # histogram (rows handed on), chain, resample (+ block decision and draw
+    # for block verification; + the planner for ragged batches, + the budget
+    # choice with a cost table).  Under the small-top-k promise: prep, row
+    # select, chain.
+    small = small_topk(w)
+    if small:
+        launches_per_step = 3
+    elif w.dtype != torch.bfloat16:
+        launches_per_step = 3
+    else:
+        launches_per_step = 6 + (2 if args.method == "block" else 0)
+    launches_per_step += (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
     if args.estimator:   # prep, row select, two histogram kernels, features for the draft rows; observe
         launches_per_step += 6
 
@@ -372,6 +394,8 @@ def run_ours(args, rank, world, local):
                    + (" -- with the online acceptance estimator (predict + observe)" if args.estimator else "")
                    + (" -- budget from a synthetic step-cost table" if args.cost_table else ""),
                    "rows_per_step": rows_t,
+                   "sampling_promise": "small_topk (every request greedy or top-k <= 32: the full-vocabulary "
+                                       "kernels are not launched)" if small else None,
                    "vocab": w.V, "logits_bytes_per_step": alg_bytes,
                    "logits_gbs_step": round(logits_gbs_step, 1),
                    "logits_frac_of_8tbs_step": round(logits_gbs_step / 8000.0, 4),
@@ -413,6 +437,7 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
     ws_p = sv.Workspace(dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in res_host)
+    small = small_topk(w)
     comp = torch.cuda.current_stream(dev)
     copy_s = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
@@ -433,7 +458,7 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
         comp.wait_event(copied[b])
         if extra is None:
             o = sv.verify_chain(d["target"], d["draft"], d["draft_tokens"], d["temperature"], d["top_k"], d["top_p"],
-                                seed=w.seed, ws=ws, block=method == "block")
+                                seed=w.seed, ws=ws, block=method == "block", small_topk=small)
         else:
             if extra["table"] is None:
                 vl, qo, _, _ = sv.plan_budget(d["conf"], w.budget, w.bucket, ws=ws_p)
@@ -441,7 +466,7 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
                 tb = extra["table"]
                 _, _, vl, qo, _, _ = sv.plan_budget_cost(d["conf"], tb[0], tb[1], w.bucket, tb[2], ws=ws_p)
             o = sv.verify_ragged(d["target"], d["draft"], qo, vl, d["draft_tokens"], d["temperature"], d["top_k"],
-                                 d["top_p"], seed=w.seed, ws=ws)
+                                 d["top_p"], seed=w.seed, ws=ws, small_topk=small)
         freed[b].record(comp)
         res_host[0].copy_(o.accept_len, non_blocking=True)
         res_host[1].copy_(o.out_tokens, non_blocking=True)

@@ -97,10 +97,25 @@ enum {
 #define SV_ROW_ERROR_MASK (SV_ROW_NONFINITE | SV_ROW_EMPTY | SV_ROW_BAD_TOKEN | SV_ROW_BAD_PARAM | \
                            SV_ROW_BAD_LAYOUT | SV_ROW_UNSUPPORTED | SV_ROW_TIMEOUT)
 
+/* Host-side promises about a batch's sampling parameters (sv_sampling_t.flags).
+ *   SV_SAMPLING_SMALL_TOPK  every request is greedy (T == 0) or keeps at most
+ *       32 tokens by top-k (1 <= top_k <= 32).  The verify and row calls then
+ *       launch only their prep, the one-pass row kernel and the chain (or row
+ *       output) kernels: the full-vocabulary histogram kernels and the
+ *       full-row resample, which such a batch never needs, are not launched.
+ *       A request that breaks the promise is refused like an fp32 request
+ *       with a full-vocabulary kept set: SV_ROW_UNSUPPORTED (at position 0 of
+ *       a verify request, accept_len = num_emitted = 0; in the row's
+ *       descriptor for sv_build_target_probs); the other requests are not
+ *       affected.  sv_estimator_predict ignores the flag (its features take
+ *       greedy requests at T = 1 over the whole row). */
+enum { SV_SAMPLING_SMALL_TOPK = 1 };
+
 typedef struct {
     const float* temperature; /* (device) [n_req]; required                       */
     const int32_t* top_k;     /* (device) [n_req] or NULL                         */
     const float* top_p;       /* (device) [n_req] or NULL                         */
+    int32_t flags;            /* (host) SV_SAMPLING_* promises, 0 for none        */
 } sv_sampling_t;
 
 /* Descriptor of one row's distribution (32 bytes).  With T = temperature,

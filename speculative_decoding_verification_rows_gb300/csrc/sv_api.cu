@@ -52,15 +52,16 @@ cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;   // sv_set_timing_events
 cudaEvent_t g_hv_start = nullptr, g_hv_stop = nullptr;   // sv_set_hist_timing_events
 
 // Row kernels for whatever tasks the prep kernel listed (the one-pass kernel
-// also finalises its rows).
-sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s)
+// also finalises its rows).  `small_topk`: the caller promised that no row
+// needs the histogram path (prep refuses any that would).
+sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s, bool small_topk)
 {
     const cudaEvent_t ev0 = g_ev_start, ev1 = g_ev_stop;
     if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return SV_ERR_CUDA;
     cudaError_t e = launch_fast_rows(ra, s);
     if (e != cudaSuccess) return SV_ERR_CUDA;
     if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SV_ERR_CUDA;
-    if (ra.dtype == 0) {   // fp32 rows never take the histogram path (refused in prep)
+    if (ra.dtype == 0 && !small_topk) {   // fp32 rows never take the histogram path (refused in prep)
         const cudaEvent_t hv0 = g_hv_start, hv1 = g_hv_stop;
         if (hv0 && hv1 && cudaEventRecord(hv0, s) != cudaSuccess) return SV_ERR_CUDA;
         e = launch_hist_rows(ra, s);
@@ -151,10 +152,14 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     ca.out_tokens = out_tokens;
     ca.num_emitted = num_emitted;
     ca.row_status = row_status;
+    // Under the small-top-k promise every kept set is listed (at most 32
+    // tokens), so no request leaves work for the full-row resample.
+    const bool small_topk = (sp.flags & SV_SAMPLING_SMALL_TOPK) != 0;
     if (launch_prep(ca, s) != cudaSuccess) return SV_ERR_CUDA;
-    sv_status_t st = run_rows(c.ra, s);
+    sv_status_t st = run_rows(c.ra, s, small_topk);
     if (st != SV_OK) return st;
     if (launch_chain(ca, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (small_topk) return SV_OK;
     if (dt == SV_DTYPE_BF16 && launch_resample(ca, 0, s) != cudaSuccess) return SV_ERR_CUDA;
     if (block && dt == SV_DTYPE_BF16) {   // requests with unlisted kept sets: decide, then draw
         if (launch_block_finish(ca, s) != cudaSuccess) return SV_ERR_CUDA;
@@ -270,8 +275,9 @@ sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_
     ca.rows_per_req = K;
     ca.n_params = n_req;
     ca.sp = sp;
+    ca.sp.flags = 0;   // greedy requests' features are taken at T = 1 over the whole row
     if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
-    sv_status_t st = run_rows(c.ra, stream);
+    sv_status_t st = run_rows(c.ra, stream, false);
     if (st != SV_OK) return st;
     return to_status(launch_est_predict(c.ra.info, state, n_req, K, x_out, p_out, c.ra.counters, stream));
 }
@@ -312,7 +318,7 @@ sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row
     ca.token_per_row = token_per_row;
     ca.sp = sp;
     if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
-    sv_status_t st = run_rows(c.ra, stream);
+    sv_status_t st = run_rows(c.ra, stream, (sp.flags & SV_SAMPLING_SMALL_TOPK) != 0);
     if (st != SV_OK) return st;
     return to_status(launch_rows_out(ca, prob_of_token, desc, dense_probs, stream));
 }

@@ -35,7 +35,14 @@ class SVError(RuntimeError):
 
 
 class Sampling(ctypes.Structure):
-    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p)]
+    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p),
+                ("flags", ctypes.c_int32)]
+
+
+# sv_sampling_t.flags: every request is greedy or keeps at most 32 tokens by
+# top-k, so the full-vocabulary kernels are not launched (a request that
+# breaks the promise is refused with ROW_UNSUPPORTED)
+SAMPLING_SMALL_TOPK = 1
 
 
 class RowDesc(ctypes.Structure):
@@ -131,9 +138,9 @@ def _dev(t: torch.Tensor, dtype=None) -> torch.Tensor:
     return t
 
 
-def _sampling(temperature, top_k, top_p) -> Sampling:
+def _sampling(temperature, top_k, top_p, small_topk: bool = False) -> Sampling:
     return Sampling(temperature.data_ptr(), None if top_k is None else top_k.data_ptr(),
-                    None if top_p is None else top_p.data_ptr())
+                    None if top_p is None else top_p.data_ptr(), SAMPLING_SMALL_TOPK if small_topk else 0)
 
 
 def set_timing_events(start: Optional["torch.cuda.Event"], stop: Optional["torch.cuda.Event"]):
@@ -300,8 +307,9 @@ class Estimator:
 def build_target_probs(logits: torch.Tensor, temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
                        top_p: Optional[torch.Tensor] = None, row_to_req: Optional[torch.Tensor] = None,
                        tokens: Optional[torch.Tensor] = None, dense: bool = False,
-                       ws: Optional[Workspace] = None):
-    """sv_build_target_probs over [rows, vocab] logits.
+                       ws: Optional[Workspace] = None, small_topk: bool = False):
+    """sv_build_target_probs over [rows, vocab] logits (small_topk: the
+    SAMPLING_SMALL_TOPK promise).
 
     Returns (desc [rows, 8] int32 view of sv_row_desc_t, prob_of_token [rows]
     or None, dense [rows, vocab] or None)."""
@@ -314,7 +322,7 @@ def build_target_probs(logits: torch.Tensor, temperature: torch.Tensor, top_k: O
     dn = torch.empty((rows, V), dtype=torch.float32, device=dev) if dense else None
     w = _ws(ws, dev, workspace_size(rows, 0, V))
     _check(load().sv_build_target_probs(_ptr(logits), _dtype_code(logits), V, rows, V, _ptr(row_to_req), n_req,
-                                        _sampling(temperature, top_k, top_p), _ptr(tokens), _ptr(ptok),
+                                        _sampling(temperature, top_k, top_p, small_topk), _ptr(tokens), _ptr(ptok),
                                         _ptr(desc), _ptr(dn), _ptr(w), w.numel(), _stream(dev)))
     return desc, ptok, dn
 
@@ -338,9 +346,10 @@ def _outs(n, K, dev):
 def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
                  temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
                  top_p: Optional[torch.Tensor] = None, verify_len: Optional[torch.Tensor] = None, seed: int = 0,
-                 ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None, block: bool = False) -> VerifyOut:
+                 ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None, block: bool = False,
+                 small_topk: bool = False) -> VerifyOut:
     """sv_verify_chain (or, with block=True, sv_verify_block): target [n, K+1, V], draft [n, K, V]
-    (or None if all greedy)."""
+    (or None if all greedy); small_topk: the SAMPLING_SMALL_TOPK promise."""
     target = _dev(target)
     n, k1, V = target.shape
     K = k1 - 1
@@ -352,7 +361,7 @@ def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_toke
     w = _ws(ws, dev, workspace_size_block(n, K, V) if block else workspace_size(n, K, V))
     fn = load().sv_verify_block if block else load().sv_verify_chain
     _check(fn(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens), _ptr(verify_len),
-              _sampling(temperature, top_k, top_p), seed, _ptr(o.accept_len), _ptr(o.out_tokens),
+              _sampling(temperature, top_k, top_p, small_topk), seed, _ptr(o.accept_len), _ptr(o.out_tokens),
               _ptr(o.num_emitted), _ptr(o.row_status), _ptr(w), w.numel(), _stream(dev)))
     return o
 
@@ -360,7 +369,7 @@ def verify_chain(target: torch.Tensor, draft: Optional[torch.Tensor], draft_toke
 def verify_chain_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
                          temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
                          top_p: Optional[torch.Tensor] = None, verify_len: Optional[torch.Tensor] = None,
-                         seed: int = 0, out: Optional[VerifyOut] = None) -> VerifyOut:
+                         seed: int = 0, out: Optional[VerifyOut] = None, small_topk: bool = False) -> VerifyOut:
     """sv_verify_chain_noalloc: sv_verify_chain with the library's static scratch
     (no workspace).  The outputs are allocated here unless `out` is given."""
     target = _dev(target)
@@ -372,7 +381,8 @@ def verify_chain_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], dr
         assert draft.shape == (n, K, V)
     o = out or _outs(n, K, dev)
     _check(load().sv_verify_chain_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V,
-                                          _ptr(draft_tokens), _ptr(verify_len), _sampling(temperature, top_k, top_p),
+                                          _ptr(draft_tokens), _ptr(verify_len),
+                                          _sampling(temperature, top_k, top_p, small_topk),
                                           seed, _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted),
                                           _ptr(o.row_status), _stream(dev)))
     return o
@@ -381,8 +391,10 @@ def verify_chain_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], dr
 def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], qo_indptr: torch.Tensor,
                   verify_lens: torch.Tensor, draft_tokens: torch.Tensor, temperature: torch.Tensor,
                   top_k: Optional[torch.Tensor] = None, top_p: Optional[torch.Tensor] = None, seed: int = 0,
-                  ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None) -> VerifyOut:
-    """sv_verify_ragged: packed target [bucket, V], draft [n, K_max, V] block layout."""
+                  ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None,
+                  small_topk: bool = False) -> VerifyOut:
+    """sv_verify_ragged: packed target [bucket, V], draft [n, K_max, V] block layout; small_topk: the
+    SAMPLING_SMALL_TOPK promise."""
     target = _dev(target)
     bucket, V = target.shape
     n, K = draft_tokens.shape
@@ -394,7 +406,7 @@ def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], qo_indptr
     w = _ws(ws, dev, workspace_size(n, K, V))
     _check(load().sv_verify_ragged(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, bucket,
                                    _ptr(qo_indptr), _ptr(verify_lens), _ptr(draft_tokens),
-                                   _sampling(temperature, top_k, top_p), seed, _ptr(o.accept_len),
+                                   _sampling(temperature, top_k, top_p, small_topk), seed, _ptr(o.accept_len),
                                    _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status), _ptr(w),
                                    w.numel(), _stream(dev)))
     return o

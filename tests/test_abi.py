@@ -96,3 +96,22 @@ def test_product_path_has_no_cpu_fallback():
         sv.verify_chain(torch.zeros((1, 2, 8)), None, torch.zeros((1, 1), dtype=torch.int32), torch.zeros(1))
     src = open(os.path.join(ROOT, "speculative_decoding_verification_rows_gb300", "sv.py")).read()
     assert "oracle" not in src.replace("no CPU fallback", "")
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    # the binding's ctypes structs against the C compiler's view of sv.h
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "sv.h"\n'
+                   "int main(void) {\n"
+                   '  printf("%zu %zu %zu\\n", sizeof(sv_sampling_t), offsetof(sv_sampling_t, top_p),\n'
+                   "         offsetof(sv_sampling_t, flags));\n"
+                   '  printf("%zu %zu\\n", sizeof(sv_row_desc_t), offsetof(sv_row_desc_t, temperature));\n'
+                   '  printf("%d\\n", (int)SV_SAMPLING_SMALL_TOPK);\n'
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert [int(x) for x in lines[0].split()] == [ctypes.sizeof(sv.Sampling), sv.Sampling.top_p.offset,
+                                                  sv.Sampling.flags.offset]
+    assert [int(x) for x in lines[1].split()] == [ctypes.sizeof(sv.RowDesc), sv.RowDesc.temperature.offset]
+    assert int(lines[2]) == sv.SAMPLING_SMALL_TOPK
