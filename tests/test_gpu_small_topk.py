@@ -117,3 +117,38 @@ def test_build_target_probs_with_promise():
     good = torch.from_numpy(np.nonzero(ok)[0]).to(DEV)
     assert torch.equal(da[good], db[good])
     assert torch.equal(pa[good], pb[good])
+
+
+class _Rows:
+    def __init__(self, o, a, b):
+        self.accept_len, self.out_tokens = o.accept_len[a:b], o.out_tokens[a:b]
+        self.num_emitted, self.row_status = o.num_emitted[a:b], o.row_status[a:b]
+
+
+@pytest.mark.parametrize("name,slices", [("large", [(0, 3), (61, 63), (125, 128)]),
+                                         ("greedy_wide", [(0, 8), (250, 258), (504, 512)])])
+def test_benchmark_step_at_full_size(name, slices):
+    # the step exactly as the benchmark times it: its own closure (with the
+    # promise), captured once as a CUDA graph and replayed
+    import bench
+    w = workloads.make(name, device=DEV)
+    step, out, extra = bench.make_step(w, sv, torch.device(DEV, torch.cuda.current_device()))
+    assert extra is None and bench.small_topk(w)
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for f in FIELDS:
+        getattr(out, f).fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    plain = sv.verify_chain(w.target, w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p, seed=w.seed)
+    torch.cuda.synchronize()
+    for f in FIELDS:
+        assert torch.equal(getattr(out, f), getattr(plain, f)), f
+    for a, b in slices:
+        o = oracle.verify_chain(np_logits(w.target[a:b]), None if w.draft is None else np_logits(w.draft[a:b]),
+                                w.draft_tokens[a:b].cpu().numpy(), w.temperature[a:b].cpu().numpy(),
+                                w.top_k[a:b].cpu().numpy(), w.top_p[a:b].cpu().numpy(), seed=w.seed, first_req=a)
+        compare_verify(o, _Rows(out, a, b), w.draft_tokens[a:b].cpu().numpy(), np.full(b - a, w.K), w.V)
