@@ -206,7 +206,9 @@ sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row
  *   [n_req, K + 1] or NULL: OR of the position's target row, draft row and
  *   token bits.
  *   fp32 logits support greedy requests and top-k <= 32; other fp32 requests
- *   get SV_ROW_UNSUPPORTED.
+ *   get SV_ROW_UNSUPPORTED.  sp.flags = SV_SAMPLING_SMALL_TOPK skips the
+ *   full-vocabulary kernels (see sv_sampling_t); sv_verify_ragged and
+ *   sv_verify_block take it the same way.
  */
 sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
                             int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
