@@ -42,7 +42,9 @@ def build(force: bool = False, plant: int = 0, out_dir: str | None = None) -> st
 
 
 _lib = None
-_lib_path = None
+# ORACLE_LIB: load another build of oracle.c (for instance one compiled with
+# -fsanitize=address or -fsanitize=undefined) instead of liboracle.so.
+_lib_path = os.environ.get("ORACLE_LIB") or None
 
 
 class planted:
