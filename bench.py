@@ -257,7 +257,7 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
                                                                                  device=dev),
                        torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
                                                                                  device=dev))
-    small = small_topk(w)
+    small = small_topk(w) and method == "chain"
     if w.layout == "chain":
         block = method == "block"
         est = sv.Estimator(w.K, dev) if estimator else None
@@ -319,7 +319,7 @@ def run_ours(args, rank, world, local):
     # for block verification; + the planner for ragged batches, + the budget
     # choice with a cost table).  Under the small-top-k promise: prep, row
     # select, chain.
-    small = small_topk(w)
+    small = small_topk(w) and args.method == "chain"
     if small:
         launches_per_step = 3
     elif w.dtype != torch.bfloat16:
@@ -458,7 +458,7 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
     ws_p = sv.Workspace(dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in res_host)
-    small = small_topk(w)
+    small = small_topk(w) and method == "chain"
     comp = torch.cuda.current_stream(dev)
     copy_s = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]

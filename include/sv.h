@@ -108,7 +108,8 @@ enum {
  *       a verify request, accept_len = num_emitted = 0; in the row's
  *       descriptor for sv_build_target_probs); the other requests are not
  *       affected.  sv_estimator_predict ignores the flag (its features take
- *       greedy requests at T = 1 over the whole row). */
+ *       greedy requests at T = 1 over the whole row), and so does
+ *       sv_verify_block (it keeps its full launch sequence). */
 enum { SV_SAMPLING_SMALL_TOPK = 1 };
 
 typedef struct {
@@ -207,8 +208,8 @@ sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row
  *   token bits.
  *   fp32 logits support greedy requests and top-k <= 32; other fp32 requests
  *   get SV_ROW_UNSUPPORTED.  sp.flags = SV_SAMPLING_SMALL_TOPK skips the
- *   full-vocabulary kernels (see sv_sampling_t); sv_verify_ragged and
- *   sv_verify_block take it the same way.
+ *   full-vocabulary kernels (see sv_sampling_t); sv_verify_ragged takes it
+ *   the same way, sv_verify_block ignores it.
  */
 sv_status_t sv_verify_chain(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
                             int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,

@@ -337,6 +337,7 @@ sv_status_t sv_verify_block(const void* target_logits, const void* draft_logits,
                             uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
                             int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream)
 {
+    sp.flags = 0;   // block verification keeps its full launch sequence
     return run_verify(0, target_logits, draft_logits, dt, n_req, K, vocab, 0, nullptr, verify_len, draft_tokens, sp,
                       seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream, 1);
 }
