@@ -25,6 +25,8 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 NONFINITE, EMPTY, BAD_TOKEN, BAD_PARAM, BAD_LAYOUT, Q_ZERO, RESID_ZERO = 1, 2, 4, 8, 16, 32, 64
 ERROR_MASK = NONFINITE | EMPTY | BAD_TOKEN | BAD_PARAM | BAD_LAYOUT
 FLAG_RATIO, FLAG_CUTOFF, FLAG_INVCDF, FLAG_RESID = 1, 2, 4, 8
+# Per-position bits of the alternative outcomes (ORC_ALT_* in oracle.c).
+ALT_ACCEPT, ALT_AMBIG, ALT_DRAW_NEAR, ALT_DRAW_ROW = 1, 2, 4, 8
 
 
 def build(force: bool = False, plant: int = 0, out_dir: str | None = None) -> str:
@@ -69,7 +71,12 @@ class RowOut(ctypes.Structure):
     _fields_ = [("max_logit", ctypes.c_double), ("log_norm", ctypes.c_double),
                 ("cutoff_logit", ctypes.c_double), ("cutoff_ties", ctypes.c_int32),
                 ("kept", ctypes.c_int32), ("argmax", ctypes.c_int32), ("status", ctypes.c_int32),
-                ("cut_margin", ctypes.c_double), ("z_rest", ctypes.c_double)]
+                ("cut_margin", ctypes.c_double), ("z_rest", ctypes.c_double), ("next_index", ctypes.c_int64)]
+
+
+class AltOut(ctypes.Structure):
+    _fields_ = [("dec", ctypes.c_void_p), ("draw", ctypes.c_void_p), ("draw_alt", ctypes.c_void_p),
+                ("n_flag", ctypes.c_void_p), ("n_dec", ctypes.c_void_p)]
 
 
 def lib():
@@ -83,13 +90,14 @@ def lib():
         _lib.orc_row_transform.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_int32,
                                            ctypes.c_float, ctypes.POINTER(RowOut), P]
         _lib.orc_row_transform.restype = ctypes.c_int
+        A = ctypes.POINTER(AltOut)
         _lib.orc_verify_chain.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P]
+                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P, A]
         _lib.orc_verify_block.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P]
+                                          P, P, P, P, P, ctypes.c_uint64, ctypes.c_int, P, P, P, P, P, P, P, A]
         _lib.orc_verify_ragged.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                            ctypes.c_int64, P, P, P, P, P, P, ctypes.c_uint64, ctypes.c_int,
-                                           P, P, P, P, P, P, P]
+                                           P, P, P, P, P, P, P, A]
         _lib.orc_plan_budget.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, P, P, P, P]
         _lib.orc_plan_budget.restype = ctypes.c_int
@@ -144,7 +152,32 @@ def _verify_outputs(n, width):
     return dict(accept_len=np.zeros(n, np.int32), out_tokens=np.zeros((n, width), np.int32),
                 num_emitted=np.zeros(n, np.int32), pos_status=np.zeros((n, width), np.int32),
                 flags=np.zeros(n, np.int32), p_tok=np.zeros((n, width), np.float64),
-                q_tok=np.zeros((n, width), np.float64))
+                q_tok=np.zeros((n, width), np.float64),
+                alt_dec=np.zeros((n, width), np.int32), alt_draw=np.zeros((n, width), np.int32),
+                alt_tokens=np.zeros((n, width, 2), np.int32), n_flag=np.zeros(n, np.int32),
+                n_dec=np.zeros(n, np.int32))
+
+
+def _alt(o):
+    """Pointers of the alternative-outcome arrays of an output dict (kept
+    alive by the dict itself)."""
+    return ctypes.byref(AltOut(_ptr(o["alt_dec"]), _ptr(o["alt_draw"]), _ptr(o["alt_tokens"]), _ptr(o["n_flag"]),
+                               _ptr(o["n_dec"])))
+
+
+def _support_fn(row_of, T, tk, tp):
+    """support(r, j): tokens a draw at position j of request r may emit when
+    the distribution it draws from is uncertain (a near top-p cut or a
+    near-empty residual): the support of the target row's p plus the token
+    its cut leaves out next.  row_of(r, j) gives the row's logits."""
+    def support(r, j):
+        d, probs = row_transform(row_of(r, j), float(T[r]), 0 if tk is None else int(tk[r]),
+                                 1.0 if tp is None else float(tp[r]))
+        mask = probs > 0.0
+        if d["next_index"] >= 0:
+            mask[d["next_index"]] = True
+        return mask
+    return support
 
 
 def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=None, verify_len=None, seed=0,
@@ -168,7 +201,9 @@ def verify_chain(target, draft, draft_tokens, temperature, top_k=None, top_p=Non
     fn = lib().orc_verify_block if block else lib().orc_verify_chain
     fn(_ptr(target), _ptr(draft), dt, n, K, V, _ptr(tok), _ptr(vl), _ptr(T), _ptr(tk), _ptr(tp), seed, first_req,
        _ptr(o["accept_len"]), _ptr(o["out_tokens"]), _ptr(o["num_emitted"]), _ptr(o["pos_status"]),
-       _ptr(o["flags"]), _ptr(o["p_tok"]), _ptr(o["q_tok"]))
+       _ptr(o["flags"]), _ptr(o["p_tok"]), _ptr(o["q_tok"]), _alt(o))
+    o["block"] = bool(block)
+    o["support"] = _support_fn(lambda r, j: target[r, j], T, tk, tp)
     return o
 
 
@@ -191,7 +226,9 @@ def verify_ragged(target, draft, qo_indptr, verify_lens, draft_tokens, temperatu
     lib().orc_verify_ragged(_ptr(target), _ptr(draft), dt, n, K, V, bucket, _ptr(qo), _ptr(vl), _ptr(tok),
                             _ptr(T), _ptr(tk), _ptr(tp), seed, first_req, _ptr(o["accept_len"]), _ptr(o["out_tokens"]),
                             _ptr(o["num_emitted"]), _ptr(o["pos_status"]), _ptr(o["flags"]),
-                            _ptr(o["p_tok"]), _ptr(o["q_tok"]))
+                            _ptr(o["p_tok"]), _ptr(o["q_tok"]), _alt(o))
+    o["block"] = False
+    o["support"] = _support_fn(lambda r, j: target[int(qo[r]) + j], T, tk, tp)
     return o
 
 

@@ -163,6 +163,8 @@ typedef struct {
     double cut_margin;   /* top-p decision margin / Z1 (inf when top-p off)  */
     double z_rest;       /* kept mass after the first kept token, sum of     */
                          /* exp((l - m) / T) over kept tokens 2..kept        */
+    int64_t next_index;  /* first token the final cut leaves out, in sorted  */
+                         /* order, among the top-k kept ones (-1: none)     */
 } orc_row_t;
 
 static int bad_params(float T, float top_p)
@@ -189,6 +191,7 @@ int orc_row_transform(const void* row, int dtype, int64_t vocab, float T, int32_
 {
     memset(out, 0, sizeof(*out));
     out->cut_margin = INFINITY;
+    out->next_index = -1;
     if (probs)
         for (int64_t i = 0; i < vocab; ++i) probs[i] = 0.0;
     if (bad_params(T, top_p)) {
@@ -265,6 +268,7 @@ int orc_row_transform(const void* row, int dtype, int64_t vocab, float T, int32_
     for (int64_t i = 0; i < kept; ++i)
         if (ord[i].value == out->cutoff_logit) ++ties;
     out->cutoff_ties = ties;
+    out->next_index = kept < kk ? ord[kept].index : -1;
     if (probs)
         for (int64_t i = 0; i < kept; ++i) probs[ord[i].index] = e[i] / z;
     free(ord);
@@ -396,6 +400,187 @@ static int block_accept(double* const* P, double* const* Q, const int32_t* d, in
 }
 
 /*
+ * Alternative outcomes of near-tie decisions (a test aid, computed beside the
+ * outputs above and never feeding them).  A decision inside its margin may
+ * go either way on another machine's rounding: the ratio test (|u - p/q| <
+ * 1e-6, the bound the task states; block verification: |eta_j - h_j|), a
+ * top-p cut (its prefix mass within 1e-9 of top_p * Z1, so the kept set may
+ * hold one token more or less, which renormalises every probability of the
+ * row), an inverse-CDF draw (u * W within 1e-9 * W of a cumulative
+ * boundary), an empty-looking residual (W below 1e-9).  For every position
+ * j of a request the oracle states the decision there and whether it is
+ * ambiguous, and the token the request would emit if its chain stopped at j,
+ * with the neighbours a near boundary admits.  A verify result is then valid
+ * iff it is one of the outcomes these decisions allow.
+ */
+#define ORC_ALT_ACCEPT    1  /* chain: the test at j accepts (j < v);          */
+                             /* block: eta_j < h_j (1 <= j <= v)               */
+#define ORC_ALT_AMBIG     2  /* that decision lies inside its margin          */
+#define ORC_ALT_DRAW_NEAR 4  /* the draw at j sits near a boundary: the       */
+                             /* tokens in draw_alt are valid too              */
+#define ORC_ALT_DRAW_ROW  8  /* the distribution drawn from at j is itself    */
+                             /* uncertain (a near top-p cut of a row it uses, */
+                             /* or a residual below 1e-9): any token of p_j's */
+                             /* support, or the token its cut leaves out next */
+
+typedef struct {
+    int32_t* dec;       /* [n, K+1] ORC_ALT_* bits per position               */
+    int32_t* draw;      /* [n, K+1] token emitted if the chain stops at j     */
+    int32_t* draw_alt;  /* [n, K+1, 2] tokens across a near boundary, or -1   */
+    int32_t* n_flag;    /* [n] decisions of the oracle's own path that are    */
+                        /* inside their margins                               */
+    int32_t* n_dec;     /* [n] decisions of the oracle's own path             */
+} orc_alt_t;
+
+/* inv_cdf (C7) with the tokens across a boundary that u * W lies within
+ * INVCDF_MARGIN * W of: alt[0] below (the last positive weight before the
+ * token), alt[1] above (the first positive weight after it); -1 where the
+ * boundary is not near or no such token exists.  Returns 1 if either is near. */
+static int inv_cdf_near(const double* w, int64_t n, double u, int64_t* tok, int32_t alt[2])
+{
+    double margin;
+    *tok = inv_cdf(w, n, u, &margin);
+    alt[0] = alt[1] = -1;
+    if (!(margin < INVCDF_MARGIN)) return 0;
+    double W = 0.0;
+    for (int64_t x = 0; x < n; ++x) W += w[x];
+    const double target = u * W;
+    double before = 0.0;
+    for (int64_t x = 0; x < *tok; ++x) before += w[x];
+    const double cum = before + (*tok >= 0 ? w[*tok] : 0.0);
+    if (*tok < 0 || target - before < INVCDF_MARGIN * W)
+        for (int64_t y = (*tok < 0 ? n : *tok) - 1; y >= 0; --y)
+            if (w[y] > 0.0) { alt[0] = (int32_t)y; break; }
+    if (*tok >= 0 && cum - target < INVCDF_MARGIN * W)
+        for (int64_t y = *tok + 1; y < n; ++y)
+            if (w[y] > 0.0) { alt[1] = (int32_t)y; break; }
+    return 1;
+}
+
+/* The alternatives of one request whose rows are all valid (see above).
+ * P, Q: dense rows; tr: target row records; qcm: the draft rows' cut
+ * margins; a_orc: the oracle's accepted length.  Writes dec, draw, draw_alt
+ * ([K+1] slots of this request) and the request's decision counts. */
+static void alternatives(double* const* P, double* const* Q, const orc_row_t* tr, const double* qcm, const int32_t* d,
+                         int v, int64_t vocab, int greedy, int block, int topp_on, uint64_t seed, uint32_t req,
+                         int a_orc, int32_t* dec, int32_t* draw, int32_t* draw_alt, int32_t* n_flag, int32_t* n_dec)
+{
+    int nf = 0, nd = 0;
+    /* near top-p cuts: per position, of the target row and of the draft row */
+    int* cut_t = (int*)calloc((size_t)(v + 1), sizeof(int));
+    int* cut_q = (int*)calloc((size_t)(v + 1), sizeof(int));
+    for (int j = 0; j <= v && !greedy; ++j) {
+        cut_t[j] = tr[j].cut_margin < CUTOFF_MARGIN;
+        cut_q[j] = j < v && qcm[j] < CUTOFF_MARGIN;
+        if (topp_on) nd += 1 + (j < v);
+        nf += cut_t[j] + cut_q[j];
+    }
+    double* wgt = (double*)malloc((size_t)(v + 1) * sizeof(double));
+    wgt[0] = 1.0;
+    if (greedy) {
+        /* greedy requests keep the chain's rule in both modes; in block mode
+         * the bits say it as stop tests: j passes iff drafts 0..j-1 all match */
+        int match = 1;
+        for (int j = 0; j < v; ++j) {
+            const int ok = d[j] == tr[j].argmax;
+            if (block) {
+                match = match && ok;
+                dec[j + 1] = match ? ORC_ALT_ACCEPT : 0;
+            } else {
+                dec[j] = ok ? ORC_ALT_ACCEPT : 0;
+            }
+        }
+        nd += a_orc < v ? a_orc + 1 : v;
+    } else if (!block) {
+        for (int j = 0; j < v; ++j) {
+            const double p = P[j][d[j]], q = Q[j][d[j]];
+            const double u = orc_uniform(seed, req, (uint32_t)j, 0u);
+            int acc, amb = cut_t[j] || cut_q[j];
+            if (q > 0.0) {
+                acc = u < p / q;
+                if (fabs(u - p / q) < RATIO_MARGIN) {
+                    amb = 1;
+                    if (j <= a_orc) ++nf;
+                }
+            } else {
+                acc = p > 0.0;
+            }
+            dec[j] = (acc ? ORC_ALT_ACCEPT : 0) | (amb ? ORC_ALT_AMBIG : 0);
+        }
+        nd += a_orc < v ? a_orc + 1 : v;
+    } else {
+        /* block verification: the weights, then stop decisions at 1..v; a
+         * near cut of any row up to j moves w_j or H_j */
+        int cut_upto = 0;
+        for (int j = 1; j <= v; ++j) {
+            const double p = P[j - 1][d[j - 1]], q = Q[j - 1][d[j - 1]];
+            const double r = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
+            const double x = wgt[j - 1] > 0.0 ? wgt[j - 1] * r : 0.0;
+            wgt[j] = x < 1.0 ? x : 1.0;
+        }
+        for (int j = 1; j <= v; ++j) {
+            cut_upto |= cut_t[j - 1] || cut_q[j - 1];
+            double h = wgt[j];
+            if (j < v) {
+                double H = 0.0;
+                for (int64_t x = 0; x < vocab; ++x) {
+                    const double m = wgt[j] * P[j][x] - Q[j][x];
+                    H += m > 0.0 ? m : 0.0;
+                }
+                const double den = H + 1.0 - wgt[j];
+                h = den > 0.0 ? H / den : 1.0;
+            }
+            const double eta = orc_uniform(seed, req, (uint32_t)(j - 1), 0u);
+            const int near = fabs(eta - h) < RATIO_MARGIN;
+            const int amb = near || cut_upto || cut_t[j] || (j < v && cut_q[j]);
+            dec[j] = (eta < h ? ORC_ALT_ACCEPT : 0) | (amb ? ORC_ALT_AMBIG : 0);
+            nf += near;
+        }
+        nd += v;
+    }
+    /* the token emitted if the chain stops at j */
+    double* w = (double*)malloc((size_t)vocab * sizeof(double));
+    int cut_upto = 0;
+    for (int j = 0; j <= v; ++j) {
+        draw_alt[2 * j] = draw_alt[2 * j + 1] = -1;
+        if (greedy) {
+            draw[j] = tr[j].argmax;
+            continue;
+        }
+        if (j > 0) cut_upto |= cut_t[j - 1] || cut_q[j - 1];
+        int bits = 0;
+        if (cut_t[j] || (j < v && cut_q[j]) || (block && cut_upto)) bits |= ORC_ALT_DRAW_ROW;
+        if (j < v) {
+            const double wj = block ? wgt[j] : 1.0;
+            double W = 0.0;
+            for (int64_t x = 0; x < vocab; ++x) {
+                const double m = wj * P[j][x] - Q[j][x];
+                w[x] = m > 0.0 ? m : 0.0;
+                W += w[x];
+            }
+            if (W < RESID_MIN) bits |= ORC_ALT_DRAW_ROW;
+            if (!(W > 0.0))
+                for (int64_t x = 0; x < vocab; ++x) w[x] = P[j][x];
+        } else {
+            for (int64_t x = 0; x < vocab; ++x) w[x] = P[j][x];
+        }
+        int64_t t;
+        if (inv_cdf_near(w, vocab, orc_uniform(seed, req, (uint32_t)j, 1u), &t, draw_alt + 2 * j))
+            bits |= ORC_ALT_DRAW_NEAR;
+        draw[j] = (int32_t)t;
+        dec[j] |= bits;
+        if (j == a_orc) nf += (bits & (ORC_ALT_DRAW_NEAR | ORC_ALT_DRAW_ROW)) != 0;
+    }
+    nd += 1;   /* the emitted token */
+    *n_flag = nf;
+    *n_dec = nd;
+    free(w);
+    free(wgt);
+    free(cut_t);
+    free(cut_q);
+}
+
+/*
  * One request's chain (C5, C6).  tgt_rows[j] (j <= v) and drf_rows[j]
  * (j < v) point at the logits rows of the window; d[j] are the drafts.
  * Outputs follow the library's layout: out_tokens has K+1 slots, -1 filled.
@@ -404,7 +589,8 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
                            int v, int K, const int32_t* d, float T, int32_t top_k, float top_p,
                            uint64_t seed, uint32_t req, int32_t layout_bad, int block,
                            int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
-                           int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+                           int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok, const orc_alt_t* alt,
+                           size_t alt_off)
 {
     *flags = 0;
     for (int j = 0; j <= K; ++j) {
@@ -412,6 +598,15 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
         pos_status[j] = 0;
         p_tok[j] = NAN;
         q_tok[j] = NAN;
+        if (alt) {
+            alt->dec[alt_off + j] = 0;
+            alt->draw[alt_off + j] = -1;
+            alt->draw_alt[2 * (alt_off + j)] = alt->draw_alt[2 * (alt_off + j) + 1] = -1;
+        }
+    }
+    if (alt) {
+        alt->n_flag[alt_off / (size_t)(K + 1)] = 0;
+        alt->n_dec[alt_off / (size_t)(K + 1)] = 0;
     }
     *accept_len = 0;
     *num_emitted = 0;
@@ -429,7 +624,9 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
     double** Q = (double**)calloc((size_t)(v + 1), sizeof(double*));
     orc_row_t* tr = (orc_row_t*)calloc((size_t)(v + 1), sizeof(orc_row_t));
     orc_row_t qr;
+    double* qcm = (double*)malloc((size_t)(v + 1) * sizeof(double));
     for (int j = 0; j <= v; ++j) {
+        qcm[j] = INFINITY;
         P[j] = (double*)malloc((size_t)vocab * sizeof(double));
         pos_status[j] |= orc_row_transform(tgt_rows[j], dtype, vocab, T, top_k, top_p, &tr[j], P[j]);
         if (!greedy && tr[j].cut_margin < CUTOFF_MARGIN) *flags |= ORC_FLAG_CUTOFF;
@@ -439,6 +636,7 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
                 Q[j] = (double*)malloc((size_t)vocab * sizeof(double));
                 pos_status[j] |= orc_row_transform(drf_rows[j], dtype, vocab, T, top_k, top_p, &qr, Q[j]);
                 if (qr.cut_margin < CUTOFF_MARGIN) *flags |= ORC_FLAG_CUTOFF;
+                qcm[j] = qr.cut_margin;
             }
         }
         if (pos_status[j] & ORC_ERROR_MASK) err = 1;
@@ -497,6 +695,11 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
         out_tokens[a] = (int32_t)t;
         *accept_len = a;
         *num_emitted = a + 1;
+        if (alt) {
+            const size_t r = alt_off / (size_t)(K + 1);
+            alternatives(P, Q, tr, qcm, d, v, vocab, greedy, block, top_p < 1.0f, seed, req, a, alt->dec + alt_off,
+                         alt->draw + alt_off, alt->draw_alt + 2 * alt_off, alt->n_flag + r, alt->n_dec + r);
+        }
     }
     for (int j = 0; j <= v; ++j) {
         free(P[j]);
@@ -505,6 +708,7 @@ static void verify_request(const void* const* tgt_rows, const void* const* drf_r
     free(P);
     free(Q);
     free(tr);
+    free(qcm);
 }
 
 static const void* row_ptr(const void* base, int dtype, int64_t row, int64_t stride)
@@ -524,7 +728,7 @@ static void verify_uniform(const void* target, const void* draft, int dtype, int
                            const int32_t* draft_tokens, const int32_t* verify_len, const float* T,
                            const int32_t* top_k, const float* top_p, uint64_t seed, int first_req, int block,
                            int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted, int32_t* pos_status,
-                           int32_t* flags, double* p_tok, double* q_tok)
+                           int32_t* flags, double* p_tok, double* q_tok, const orc_alt_t* alt)
 {
     const void** tr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
     const void** dr = (const void**)malloc((size_t)(K + 1) * sizeof(void*));
@@ -540,7 +744,7 @@ static void verify_uniform(const void* target, const void* draft, int dtype, int
                        top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad, block,
                        accept_len + r, out_tokens + (size_t)r * (K + 1), num_emitted + r,
                        pos_status + (size_t)r * (K + 1), flags + r,
-                       p_tok + (size_t)r * (K + 1), q_tok + (size_t)r * (K + 1));
+                       p_tok + (size_t)r * (K + 1), q_tok + (size_t)r * (K + 1), alt, (size_t)r * (K + 1));
     }
     free(tr);
     free(dr);
@@ -550,10 +754,10 @@ void orc_verify_chain(const void* target, const void* draft, int dtype, int n, i
                       const int32_t* draft_tokens, const int32_t* verify_len,
                       const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
                       int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
-                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok, const orc_alt_t* alt)
 {
     verify_uniform(target, draft, dtype, n, K, vocab, draft_tokens, verify_len, T, top_k, top_p, seed, first_req, 0,
-                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok);
+                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok, alt);
 }
 
 /* Block verification over the uniform layout (see block_accept); arguments
@@ -562,10 +766,10 @@ void orc_verify_block(const void* target, const void* draft, int dtype, int n, i
                       const int32_t* draft_tokens, const int32_t* verify_len,
                       const float* T, const int32_t* top_k, const float* top_p, uint64_t seed, int first_req,
                       int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
-                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+                      int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok, const orc_alt_t* alt)
 {
     verify_uniform(target, draft, dtype, n, K, vocab, draft_tokens, verify_len, T, top_k, top_p, seed, first_req, 1,
-                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok);
+                   accept_len, out_tokens, num_emitted, pos_status, flags, p_tok, q_tok, alt);
 }
 
 /*
@@ -581,7 +785,7 @@ void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, 
                        int64_t bucket, const int32_t* qo_indptr, const int32_t* verify_lens,
                        const int32_t* draft_tokens, const float* T, const int32_t* top_k, const float* top_p,
                        uint64_t seed, int first_req, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
-                       int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok)
+                       int32_t* pos_status, int32_t* flags, double* p_tok, double* q_tok, const orc_alt_t* alt)
 {
     const void** tr = (const void**)malloc((size_t)(K_max + 1) * sizeof(void*));
     const void** dr = (const void**)malloc((size_t)(K_max + 1) * sizeof(void*));
@@ -598,7 +802,8 @@ void orc_verify_ragged(const void* target, const void* draft, int dtype, int n, 
                        top_k ? top_k[r] : 0, top_p ? top_p[r] : 1.0f, seed, (uint32_t)(first_req + r), bad, 0,
                        accept_len + r, out_tokens + (size_t)r * (K_max + 1), num_emitted + r,
                        pos_status + (size_t)r * (K_max + 1), flags + r,
-                       p_tok + (size_t)r * (K_max + 1), q_tok + (size_t)r * (K_max + 1));
+                       p_tok + (size_t)r * (K_max + 1), q_tok + (size_t)r * (K_max + 1), alt,
+                       (size_t)r * (K_max + 1));
     }
     free(tr);
     free(dr);

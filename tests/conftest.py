@@ -29,3 +29,16 @@ def np_logits(t: torch.Tensor) -> np.ndarray:
 def bf16_bits(values) -> np.ndarray:
     """bf16 bit patterns of exactly representable values."""
     return np_logits(torch.tensor(values, dtype=torch.float32).to(torch.bfloat16))
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The flag rate of every GPU-oracle comparison of the session."""
+    try:
+        from tests.compare import TALLY
+    except ImportError:
+        return
+    if TALLY["decisions"]:
+        terminalreporter.write_line(
+            "oracle flags: {flagged} of {decisions} decisions ({rate:.2e}) inside their margins; "
+            "{flagged_requests} of {requests} requests flagged".format(
+                rate=TALLY["flagged"] / TALLY["decisions"], **TALLY))

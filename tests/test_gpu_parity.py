@@ -19,6 +19,9 @@ from tests.conftest import np_logits
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
+# Full-size comparisons: flagged decisions (inside the oracle's margins) must
+# stay below this fraction of all decisions compared.
+FULL_SIZE_FLAG_RATE = 1e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -73,18 +76,18 @@ def test_configs_full_vocab_few_requests(name, scale):
 def test_large_full_batch_sampled_requests():
     w = workloads.make("large", device=DEV)          # 128 x 8 rows x 248,320 bf16, the benchmark workload
     for rs in (slice(0, 3), slice(61, 63), slice(125, 128)):
-        check(w, rs)
+        check(w, rs, max_flag_rate=FULL_SIZE_FLAG_RATE)
 
 
 def test_greedy_wide_full_batch():
     w = workloads.make("greedy_wide", device=DEV)    # 512 x 8 rows x 129,280: greedy is cheap for the oracle
-    check(w)
+    check(w, max_flag_rate=FULL_SIZE_FLAG_RATE)
 
 
 def test_medium_full_batch_sampled_requests():
     w = workloads.make("medium", device=DEV)
-    check(w, slice(0, 3))
-    check(w, slice(29, 32))
+    check(w, slice(0, 3), max_flag_rate=FULL_SIZE_FLAG_RATE)
+    check(w, slice(29, 32), max_flag_rate=FULL_SIZE_FLAG_RATE)
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -219,7 +222,8 @@ def test_ragged_full_size_sampled():
         o = oracle.verify_ragged(np_logits(rows), np_logits(w.draft[r0:r1]), qo_local, ovl[r0:r1],
                                  w.draft_tokens[r0:r1].cpu().numpy(), w.temperature[r0:r1].cpu().numpy(),
                                  w.top_k[r0:r1].cpu().numpy(), w.top_p[r0:r1].cpu().numpy(), first_req=r0)
-        compare_verify(o, _Slice(g, slice(r0, r1)), w.draft_tokens[r0:r1].cpu().numpy(), ovl[r0:r1], w.V)
+        compare_verify(o, _Slice(g, slice(r0, r1)), w.draft_tokens[r0:r1].cpu().numpy(), ovl[r0:r1], w.V,
+                       max_flag_rate=FULL_SIZE_FLAG_RATE)
     acc = g.accept_len.cpu().numpy()
     assert (acc <= vl.cpu().numpy()).all()
 

@@ -151,4 +151,5 @@ def test_benchmark_step_at_full_size(name, slices):
         o = oracle.verify_chain(np_logits(w.target[a:b]), None if w.draft is None else np_logits(w.draft[a:b]),
                                 w.draft_tokens[a:b].cpu().numpy(), w.temperature[a:b].cpu().numpy(),
                                 w.top_k[a:b].cpu().numpy(), w.top_p[a:b].cpu().numpy(), seed=w.seed, first_req=a)
-        compare_verify(o, _Rows(out, a, b), w.draft_tokens[a:b].cpu().numpy(), np.full(b - a, w.K), w.V)
+        compare_verify(o, _Rows(out, a, b), w.draft_tokens[a:b].cpu().numpy(), np.full(b - a, w.K), w.V,
+                       max_flag_rate=1e-4)
