@@ -15,6 +15,8 @@
 // counters), so leftovers of an earlier call do no harm -- but all calls
 // share the one array, so calls whose work overlaps on the GPU (two streams,
 // or two host threads) race and must be serialised by the caller.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "sv.h"
@@ -25,7 +27,10 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 128;
-void* g_scratch_addr[kMaxDevices] = {nullptr};   // device address of the array, per device
+// Device address of the array, per device.  Host threads making their first
+// calls at the same time may both look it up; they store the same address,
+// and the atomic makes the store and the loads well defined.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 }  // namespace
 
@@ -39,14 +44,14 @@ extern "C" sv_status_t sv_verify_chain_noalloc(const void* target_logits, const 
     if (need > kNoAllocScratchBytes) return SV_ERR_UNSUPPORTED;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
-    if (g_scratch_addr[dev] == nullptr) {
+    void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (scratch == nullptr) {
         // The array's name is a host-side stand-in; the device address comes
         // from the runtime, once per device, with that device current.
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SV_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+            return SV_ERR_CUDA;
+        g_scratch_addr[dev].store(scratch, std::memory_order_release);
     }
     return sv_verify_chain(target_logits, draft_logits, dt, n_req, K, vocab, draft_tokens, verify_len, sp, seed,
-                           accept_len, out_tokens, num_emitted, row_status, g_scratch_addr[dev], kNoAllocScratchBytes,
-                           stream);
+                           accept_len, out_tokens, num_emitted, row_status, scratch, kNoAllocScratchBytes, stream);
 }
