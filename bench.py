@@ -291,9 +291,31 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
 
     def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
         vl_, qo_, _, _ = plan()
+        extra["verify_lens"], extra["qo"] = vl_, qo_
         return sv.verify_ragged(tgt, drf, qo_, vl_, toks, T, tk, tp, seed=w.seed, ws=ws, out=out,
                                 small_topk=small)
     return step, out, extra
+
+
+def acceptance_stats(w, sv, out, extra):
+    """What one step accepted (taken after the timed region from the outputs
+    of a plain step): mean accepted drafts and emitted tokens per request,
+    the fraction of requests whose accepted length passes each position, and
+    for trimmed windows the trim regret of sv_verify_stats (trimmed requests
+    that accepted their whole window, over trimmed requests)."""
+    vl = None if extra is None else extra.get("verify_lens")
+    st = sv.verify_stats(out.accept_len, out.num_emitted, vl, w.K).cpu().tolist()
+    acc = out.accept_len.cpu()
+    ok = out.num_emitted.cpu() > 0
+    a = acc[ok].float()
+    per_pos = [round(float((a > j).float().mean()), 4) if len(a) else None for j in range(w.K)]
+    return {"mean_accept_len": round(float(a.mean()), 4) if len(a) else None,
+            "tokens_emitted_per_step": int(st[0]), "tokens_submitted_per_step": int(st[1]),
+            "accept_rate_by_position": per_pos, "requests_with_errors": int((~ok).sum()),
+            "requests_trimmed": int(st[2]),
+            "trim_regret_rate": round(st[3] / st[2], 4) if st[2] else None,
+            "drafter": "drafts drawn from the draft distribution q (greedy requests: softmax at T = 1)"
+                       if w.name != "greedy_wide" else "per-position match probabilities of the workload"}
 
 
 def run_ours(args, rank, world, local):
@@ -390,6 +412,9 @@ def run_ours(args, rank, world, local):
     set_events(None, None)
     torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    step()
+    torch.cuda.synchronize()
+    accept = acceptance_stats(w, sv, out, extra)
     ms_per_step = sum(step_ms) / len(step_ms)
     ms_worst = max_over_ranks(ms_per_step, world)
 
@@ -429,12 +454,13 @@ def run_ours(args, rank, world, local):
                      "traffic": recorded_traffic(args.workload, roof_path), "kernel_ms_mean": statistics.mean(kern_ms),
                      "algorithmic_bytes_per_launch": roof_bytes,
                      "other_path_bytes_per_step": fast_bytes if roof_path == "hist" else hist_bytes},
+        "acceptance": accept,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, extra)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -526,31 +552,103 @@ def _host_logits(t):
     return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
 
-def oracle_sample(w, r0, r1):
-    """Run the oracle on requests r0..r1-1 of a chain workload; returns (target rows, seconds)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class pinned_core:
+    """Run the calling thread on one core (the last one it may use), as
+    taskset would, and restore its affinity afterwards."""
+
+    def __enter__(self):
+        self.saved = None
+        try:
+            self.saved = os.sched_getaffinity(0)
+            self.core = max(self.saved)
+            os.sched_setaffinity(0, {self.core})
+        except (AttributeError, OSError):
+            self.core = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
+def ragged_slice(w, extra, r0, r1):
+    """Host inputs of requests r0..r1-1 of a ragged workload as the plan laid
+    them out: their packed target rows (re-based qo_indptr) and block drafts."""
+    vl = extra["verify_lens_host"]
+    qo = extra["qo_host"]
+    rows = extra["packed"][int(qo[r0]):int(qo[r1])]
+    return (_host_logits(rows), None if w.draft is None else _host_logits(w.draft[r0:r1]), qo[r0:r1 + 1] - qo[r0],
+            vl[r0:r1])
+
+
+def oracle_sample(w, r0, r1, extra=None):
+    """Run the oracle on requests r0..r1-1 (uniform or ragged layout, keys
+    of the full batch); returns (target rows, seconds)."""
     import oracle
-    tgt = _host_logits(w.target[r0:r1])
-    drf = None if w.draft is None else _host_logits(w.draft[r0:r1])
     args = (w.draft_tokens[r0:r1].cpu().numpy(), w.temperature[r0:r1].cpu().numpy(), w.top_k[r0:r1].cpu().numpy(),
             w.top_p[r0:r1].cpu().numpy())
+    if w.layout == "ragged":
+        tgt, drf, qo, vl = ragged_slice(w, extra, r0, r1)
+        t0 = time.perf_counter()
+        oracle.verify_ragged(tgt, drf, qo, vl, *args, seed=w.seed, first_req=r0)
+        return int(qo[-1]), time.perf_counter() - t0
+    tgt = _host_logits(w.target[r0:r1])
+    drf = None if w.draft is None else _host_logits(w.draft[r0:r1])
     t0 = time.perf_counter()
     oracle.verify_chain(tgt, drf, *args, seed=w.seed, first_req=r0)
     dt = time.perf_counter() - t0
     return (r1 - r0) * (w.K + 1), dt
 
 
-def cpu_baseline(w, seconds):
+def ragged_host_plan(w, extra):
+    """The plan of a ragged workload on the host (the oracle's planner) and its
+    packed rows, for the oracle legs."""
+    import oracle
+    from speculative_decoding_verification_rows_gb300 import workloads
+    if extra is None:
+        extra = {}
+    if "verify_lens" in extra:   # the plan the timed steps used (cost table or not)
+        vl, qo = extra["verify_lens"].cpu().numpy(), extra["qo"].cpu().numpy()
+    else:
+        vl, qo, _, _ = oracle.plan_budget(w.conf.cpu().numpy(), w.budget, w.bucket)
+    extra["verify_lens_host"], extra["qo_host"] = vl, qo
+    if "packed" not in extra:
+        extra["packed"] = workloads.pack_rows(w.target, qo, vl, w.bucket)
+    return extra
+
+
+def cpu_baseline(w, seconds, extra=None):
     import oracle
     oracle.build()
-    if w.layout != "chain":
-        return None
-    rows, dt = oracle_sample(w, 0, 1)
-    per_req = max(dt, 1e-6)
-    n = int(max(1, min(w.n, seconds / per_req)))
-    rows, dt = oracle_sample(w, 0, n)
+    if w.layout == "ragged":
+        extra = ragged_host_plan(w, dict(extra or {}))
+    with pinned_core() as pin:
+        rows, dt = oracle_sample(w, 0, 1, extra)
+        per_req = max(dt, 1e-6)
+        n = int(max(1, min(w.n, seconds / per_req)))
+        rows, dt = oracle_sample(w, 0, n, extra)
+    what = "packed target rows of the plan" if w.layout == "ragged" else "target rows"
     return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"requests 0..{n - 1} of the same workload ({rows} target rows), single thread, fp64",
-            "seconds": dt, "host_cores": os.cpu_count()}
+            "sample": f"requests 0..{n - 1} of the same workload ({rows} {what}), single thread, fp64",
+            "seconds": dt, "host_cores": os.cpu_count(), "pinned_core": pin.core, "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world, local):
@@ -561,26 +659,28 @@ def run_reference(args, rank, world, local):
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = workloads.make(args.workload, device=dev)
-    if w.layout != "chain":
-        print(json.dumps({"impl": "reference", "unavailable": "reference arm times chain workloads only"}))
-        return
-    for i in range(max(args.warmup, 3)):
-        oracle_sample(w, i % w.n, i % w.n + 1)
+    extra = ragged_host_plan(w, None) if w.layout == "ragged" else None
     times, rows = [], 0
-    for i in range(args.steps):
-        r = (i * 7) % w.n
-        n_rows, dt = oracle_sample(w, r, r + 1)
-        times.append(dt)
-        rows = n_rows
+    with pinned_core() as pin:
+        for i in range(max(args.warmup, 3)):
+            oracle_sample(w, i % w.n, i % w.n + 1, extra)
+        for i in range(args.steps):
+            r = (i * 7) % w.n
+            n_rows, dt = oracle_sample(w, r, r + 1, extra)
+            times.append(dt)
+            rows += n_rows
     ms = 1e3 * sum(times) / len(times)
-    value = rows / (ms / 1e3)
-    sample = f"one request ({rows} target rows + its draft rows) of the workload per step, single thread, fp64"
+    value = rows / (sum(times))
+    sample = (f"one request of the workload per step ({rows / len(times):.1f} target rows + its draft rows on "
+              f"average), single thread pinned to core {pin.core}, fp64")
     print(json.dumps({
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "rows_per_step": rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "rows_per_step": rows / len(times)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model(), "host_cores": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

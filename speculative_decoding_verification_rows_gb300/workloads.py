@@ -1,10 +1,11 @@
 """Seeded synthetic workloads shaped like the verify steps the pages describe.
 
 This module only builds inputs: logits, drafts, sampling parameters and
-confidences.  It holds none of the verify arithmetic (no temperature, top-k,
-top-p, normalisation, acceptance, resampling or planning), so the CUDA path
-and the CPU oracle can both consume what it makes without sharing any step of
-the method.
+confidences.  It holds none of the verify arithmetic (no target distribution,
+acceptance, resampling or planning), so the CUDA path and the CPU oracle can
+both consume what it makes without sharing any step of the method; the
+drafter below samples its own tokens with torch primitives, and neither side
+runs it.
 
 Workloads (sizes as the benchmark configurations state them):
 
@@ -27,10 +28,17 @@ Workloads (sizes as the benchmark configurations state them):
                   248,320 bf16 N(0, 3^2); even requests greedy, odd ones
                   T ~ U[0.3, 1.2], top-p 0.9.
 
-The simulated drafter proposes, for each drafted position, the token at rank
-rho of its own draft row (rho in {0, 1, 2, 3} with probabilities 0.55, 0.25,
-0.13, 0.07; ``torch.topk`` ordering).  It stands in for a real draft model's
-sampler; the verify step is defined for any proposal.
+The simulated drafter draws each drafted token from its own draft row, as the
+configurations state ("draft tokens sampled from the draft softmax"; drafts
+distributed as q): softmax(l / T) over the request's top-k, cut to its top-p
+(the crossing token kept), in fp32 with torch primitives and the workload's
+seeded generator; a greedy request's drafter samples the plain softmax at
+T = 1.  Neither side of the comparison runs this code: the CUDA path and the
+oracle both read only the tokens it drew.  ``drafter="rank"`` keeps the older
+stand-in, the token at rank rho of the draft row (rho in {0, 1, 2, 3} with
+probabilities 0.55, 0.25, 0.13, 0.07; ``torch.topk`` ordering); the verify
+step is defined for any proposal.  ``greedy_wide`` states its own drafter
+(per-position match probabilities) and keeps it.
 """
 from __future__ import annotations
 
@@ -98,11 +106,48 @@ def _rank_drafts(draft32, g, n, K):
     return top4.gather(1, rho).reshape(n, K).to(torch.int32)
 
 
-def make(name: str, device="cpu", scale: Optional[dict] = None) -> Workload:
+def _sampled_drafts(draft32, T, top_k, top_p, g, chunk_rows=128):
+    """Drafter: every drafted token drawn from its draft row's distribution at
+    the request's settings (see the module docstring).  T, top_k, top_p: [n]."""
+    n, K, V = draft32.shape
+    dev = draft32.device
+    out = torch.empty((n * K,), dtype=torch.int64, device=dev)
+    x = draft32.reshape(n * K, V)
+    t_row = torch.where(T > 0, T, torch.ones_like(T)).repeat_interleave(K).float()
+    k_row = torch.where((T > 0) & (top_k > 0) & (top_k < V), top_k, torch.full_like(top_k, V)).repeat_interleave(K)
+    p_row = torch.where(T > 0, top_p, torch.ones_like(top_p)).repeat_interleave(K).float()
+    rank = torch.arange(V, device=dev)
+    for r0 in range(0, n * K, chunk_rows):
+        r1 = min(n * K, r0 + chunk_rows)
+        vals, idx = torch.sort(x[r0:r1], dim=-1, descending=True, stable=True)
+        e = torch.exp((vals - vals[:, :1]) / t_row[r0:r1, None])
+        e = torch.where(rank[None, :] < k_row[r0:r1, None], e, torch.zeros_like(e))
+        cum = torch.cumsum(e, dim=-1)
+        before = cum - e                       # mass ahead of each token in sorted order
+        keep = before < p_row[r0:r1, None] * cum[:, -1:]
+        w = torch.where(keep, e, torch.zeros_like(e))
+        pick = torch.multinomial(w, 1, generator=g)
+        out[r0:r1] = idx.gather(1, pick).squeeze(1)
+    return out.reshape(n, K).to(torch.int32)
+
+
+def _drafts(drafter, draft32, T, top_k, top_p, g, n, K):
+    if drafter == "rank":
+        return _rank_drafts(draft32, g, n, K)
+    if drafter != "q":
+        raise ValueError(f"unknown drafter {drafter!r}: 'q' or 'rank'")
+    if n * K == 0:
+        return torch.zeros((n, K), dtype=torch.int32, device=draft32.device)
+    return _sampled_drafts(draft32, T, top_k, top_p, g)
+
+
+def make(name: str, device="cpu", scale: Optional[dict] = None, drafter: str = "q") -> Workload:
     """Build workload ``name`` on ``device``.
 
     ``scale`` overrides sizes (keys n, K, V) to make a smaller case with the
     same value distributions, for tests that the oracle must finish quickly.
+    ``drafter``: "q" (drafts drawn from the draft distribution, the default)
+    or "rank" (the rank-rho stand-in); greedy_wide keeps its own drafter.
     """
     if name not in NAMES:
         raise ValueError(f"unknown workload {name!r}; choose from {NAMES}")
@@ -112,10 +157,10 @@ def make(name: str, device="cpu", scale: Optional[dict] = None) -> Workload:
         n, K, V = scale.get("n", 4), scale.get("K", 4), scale.get("V", 1024)
         tgt = torch.randn((n, K + 1, V), generator=g, device=device) * 2.0
         drf = tgt[:, :K, :] + torch.randn((n, K, V), generator=g, device=device)
-        toks = _rank_drafts(drf, g, n, K)
         T = torch.tensor([0.0, 0.0, 0.7, 0.7] * ((n + 3) // 4), device=device)[:n]
         tk = torch.tensor([0, 0, 20, 20] * ((n + 3) // 4), device=device, dtype=torch.int32)[:n]
         tp = torch.tensor([1.0, 1.0, 0.9, 0.9] * ((n + 3) // 4), device=device)[:n]
+        toks = _drafts(drafter, drf, T, tk, tp, g, n, K)
         return Workload(name, "chain", n, K, V, torch.float32, tgt.contiguous(), drf.contiguous(), toks,
                         T.float(), tk, tp.float())
     if name == "medium":
@@ -129,10 +174,11 @@ def make(name: str, device="cpu", scale: Optional[dict] = None) -> Workload:
         tgt.scatter_(2, star, lse + torch.log(torch.tensor(0.3 / 0.7, device=device)))
         drf = _correlated(tgt[:, :K, :], g)
         tgt16, drf16 = tgt.to(torch.bfloat16), drf.to(torch.bfloat16)
-        toks = _rank_drafts(drf16.float(), g, n, K)
+        T, tk, tp = (torch.full((n,), 1.0, device=device), torch.zeros(n, dtype=torch.int32, device=device),
+                     torch.full((n,), 0.95, device=device))
+        toks = _drafts(drafter, drf16.float(), T, tk, tp, g, n, K)
         return Workload(name, "chain", n, K, V, torch.bfloat16, tgt16.contiguous(), drf16.contiguous(), toks,
-                        torch.full((n,), 1.0, device=device), torch.zeros(n, dtype=torch.int32, device=device),
-                        torch.full((n,), 0.95, device=device))
+                        T, tk, tp)
     if name == "large":
         n, K, V = scale.get("n", 128), scale.get("K", 7), scale.get("V", 248_320)
         tgt = torch.randn((n, K + 1, V), generator=g, device=device) * 3.0
@@ -144,10 +190,11 @@ def make(name: str, device="cpu", scale: Optional[dict] = None) -> Workload:
         tgt.scatter_add_(2, top, 3.0 * t3.abs())
         drf = _correlated(tgt[:, :K, :], g)
         tgt16, drf16 = tgt.to(torch.bfloat16), drf.to(torch.bfloat16)
-        toks = _rank_drafts(drf16.float(), g, n, K)
+        T, tk, tp = (torch.full((n,), 0.6, device=device), torch.full((n,), 20, dtype=torch.int32, device=device),
+                     torch.full((n,), 0.95, device=device))
+        toks = _drafts(drafter, drf16.float(), T, tk, tp, g, n, K)
         return Workload(name, "chain", n, K, V, torch.bfloat16, tgt16.contiguous(), drf16.contiguous(), toks,
-                        torch.full((n,), 0.6, device=device), torch.full((n,), 20, dtype=torch.int32, device=device),
-                        torch.full((n,), 0.95, device=device))
+                        T, tk, tp)
     if name == "greedy_wide":
         n, K, V = scale.get("n", 512), scale.get("K", 7), scale.get("V", 129_280)
         tgt = torch.randn((n, K + 1, V), generator=g, device=device) * 2.0
@@ -199,14 +246,14 @@ def make(name: str, device="cpu", scale: Optional[dict] = None) -> Workload:
     tgt = torch.randn((n, K + 1, V), generator=g, device=device) * 3.0
     drf = _correlated(tgt[:, :K, :], g)
     tgt16, drf16 = tgt.to(torch.bfloat16), drf.to(torch.bfloat16)
-    toks = _rank_drafts(drf16.float(), g, n, K)
     odd = (torch.arange(n, device=device) % 2) == 1
     Tr = 0.3 + 0.9 * torch.rand(n, generator=g, device=device)
-    T = torch.where(odd, Tr, torch.zeros_like(Tr))
+    T = torch.where(odd, Tr, torch.zeros_like(Tr)).float()
+    tk = torch.zeros(n, dtype=torch.int32, device=device)
+    tp = torch.where(odd, torch.full_like(Tr, 0.9), torch.ones_like(Tr)).float()
+    toks = _drafts(drafter, drf16.float(), T, tk, tp, g, n, K)
     return Workload(name, "ragged", n, K, V, torch.bfloat16, tgt16.contiguous(), drf16.contiguous(), toks,
-                    T.float(), torch.zeros(n, dtype=torch.int32, device=device),
-                    torch.where(odd, torch.full_like(Tr, 0.9), torch.ones_like(Tr)).float(),
-                    conf=conf, budget=budget, bucket=bucket)
+                    T, tk, tp, conf=conf, budget=budget, bucket=bucket)
 
 
 def pack_rows(block: torch.Tensor, qo_indptr, verify_lens, bucket: int) -> torch.Tensor:

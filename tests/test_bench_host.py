@@ -28,3 +28,30 @@ def test_promise_is_broken_by_one_request():
     w.temperature[1] = 0.0          # greedy requests keep it whatever their top-k
     w.top_k[1] = 0
     assert bench.small_topk(w)
+
+
+@pytest.mark.parametrize("name", ["large", "ragged"])
+def test_cpu_baseline_times_the_oracle_on_one_pinned_core(name):
+    w = workloads.make(name, device="cpu", scale=SMALL[name])
+    b = bench.cpu_baseline(w, seconds=0.2)
+    assert b["kind"] == "oracle" and b["cores"] == 1 and b["value"] > 0
+    assert b["cpu_model"] and b["host_cores"] >= 1
+    if name == "ragged":
+        # the sample is the plan's packed rows: windows of the planner's lengths
+        assert "packed target rows" in b["sample"]
+
+
+def test_ragged_oracle_sample_follows_the_plan():
+    import oracle
+    w = workloads.make("ragged", device="cpu", scale=SMALL["ragged"])
+    extra = bench.ragged_host_plan(w, None)
+    rows, dt = bench.oracle_sample(w, 2, 5, extra)
+    vl = extra["verify_lens_host"]
+    assert rows == int(sum(vl[2:5]) + 3) and dt >= 0
+    # the slice gives what the whole batch gives for those requests
+    tgt, drf, qo, v = bench.ragged_slice(w, extra, 0, w.n)
+    args = (w.draft_tokens.numpy(), w.temperature.numpy(), w.top_k.numpy(), w.top_p.numpy())
+    full = oracle.verify_ragged(tgt, drf, qo, v, *args, seed=w.seed)
+    tgt, drf, qo, v = bench.ragged_slice(w, extra, 2, 5)
+    part = oracle.verify_ragged(tgt, drf, qo, v, *(a[2:5] for a in args), seed=w.seed, first_req=2)
+    assert (part["out_tokens"] == full["out_tokens"][2:5]).all()
