@@ -67,6 +67,8 @@ def parse():
                    help="ragged workload: choose the budget from a synthetic step-cost table on the device")
     p.add_argument("--no-graph", action="store_true",
                    help="launch each timed step on the stream instead of replaying it as one captured CUDA graph")
+    p.add_argument("--no-promise", action="store_true",
+                   help="never pass the small-top-k sampling promise (the full launch sequence of every call)")
     return p.parse_args()
 
 
@@ -249,7 +251,7 @@ def synthetic_cost_table(w, dev):
             0.8)
 
 
-def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
+def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False, promise=True):
     """A closure running one verify step with preallocated outputs/workspace."""
     ws = sv.Workspace(dev)
     n, K = w.n, w.K
@@ -257,7 +259,7 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False):
                                                                                  device=dev),
                        torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
                                                                                  device=dev))
-    small = small_topk(w) and method == "chain"
+    small = promise and small_topk(w) and method == "chain"
     if w.layout == "chain":
         block = method == "block"
         est = sv.Estimator(w.K, dev) if estimator else None
@@ -326,7 +328,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
-    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator)
+    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator, not args.no_promise)
     alg_bytes, rows_t = algorithmic_bytes(w)
     fast_bytes, hist_bytes = path_bytes(w)
     if extra is not None:
@@ -336,14 +338,14 @@ def run_ours(args, rank, world, local):
     # the roofline is taken on the path that reads more of the logits
     roof_path = "hist" if hist_bytes > fast_bytes else "fast"
     roof_bytes = hist_bytes if roof_path == "hist" else fast_bytes
-    # prep, row select (with finalisation), one-CTA histogram, cluster
-    # histogram (rows handed on), chain, resample (+ block decision and draw
-    # for block verification; + the planner for ragged batches, + the budget
-    # choice with a cost table).  Under the small-top-k promise: prep, row
-    # select, chain.
-    small = small_topk(w) and args.method == "chain"
+    # prep, row select (with finalisation and the chains of its requests),
+    # one-CTA histogram, cluster histogram (rows handed on), chain (the other
+    # requests), resample (+ block decision and draw for block verification;
+    # + the planner for ragged batches, + the budget choice with a cost
+    # table).  Under the small-top-k promise: prep and row select.
+    small = small_topk(w) and args.method == "chain" and not args.no_promise
     if small:
-        launches_per_step = 3
+        launches_per_step = 2
     elif w.dtype != torch.bfloat16:
         launches_per_step = 3
     else:
@@ -419,7 +421,8 @@ def run_ours(args, rank, world, local):
     ms_worst = max_over_ranks(ms_per_step, world)
 
     # end to end through the public API: pinned host inputs in, results out, every step
-    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)), args.method)
+    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)), args.method,
+                                          not args.no_promise)
     torch.cuda.synchronize()
     clk = clocks.stop()
 
@@ -465,7 +468,7 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(w, sv, dev, extra, steps, method="chain"):
+def run_e2e(w, sv, dev, extra, steps, method="chain", promise=True):
     """Same metric through the public API from pinned host buffers: H2D of every
     step's inputs and D2H of its results inside the timed region.  Two device
     input buffers and a copy stream let step i+1's inputs cross the host link
@@ -484,7 +487,7 @@ def run_e2e(w, sv, dev, extra, steps, method="chain"):
     ws_p = sv.Workspace(dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in res_host)
-    small = small_topk(w) and method == "chain"
+    small = promise and small_topk(w) and method == "chain"
     comp = torch.cuda.current_stream(dev)
     copy_s = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]

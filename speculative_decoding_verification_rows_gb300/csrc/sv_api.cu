@@ -114,6 +114,7 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.row_sync = ra.row_sync;
     ca.info = ra.info;
     ca.req = at<ReqState>(ws, L.req);
+    ca.req_done = at<int32_t>(ws, L.req_done);
     ca.jobs = at<ResampleJob>(ws, L.jobs);
     ca.tiles = at<TileSums>(ws, L.tiles);
     ca.blk_w = block ? at<double>(ws, L.blk) : nullptr;
@@ -152,12 +153,18 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     ca.out_tokens = out_tokens;
     ca.num_emitted = num_emitted;
     ca.row_status = row_status;
-    // Under the small-top-k promise every kept set is listed (at most 32
-    // tokens), so no request leaves work for the full-row resample.
+    // The one-pass row kernel runs the chain of every request whose rows it
+    // takes (greedy and top-k <= 32); the chain kernel takes the others
+    // (block verification: every request).  Under the small-top-k promise
+    // every request is of the first kind and every kept set is listed, so
+    // neither the chain kernel nor the full-row resample has work.
     const bool small_topk = (sp.flags & SV_SAMPLING_SMALL_TOPK) != 0;
+    ca.fuse = block ? 0 : 1;
+    c.ra.chain = ca;
     if (launch_prep(ca, s) != cudaSuccess) return SV_ERR_CUDA;
     sv_status_t st = run_rows(c.ra, s, small_topk);
     if (st != SV_OK) return st;
+    if (small_topk && !block) return SV_OK;
     if (launch_chain(ca, s) != cudaSuccess) return SV_ERR_CUDA;
     if (small_topk) return SV_OK;
     if (dt == SV_DTYPE_BF16 && launch_resample(ca, 0, s) != cudaSuccess) return SV_ERR_CUDA;
@@ -276,6 +283,7 @@ sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_
     ca.n_params = n_req;
     ca.sp = sp;
     ca.sp.flags = 0;   // greedy requests' features are taken at T = 1 over the whole row
+    c.ra.chain = ca;
     if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
     sv_status_t st = run_rows(c.ra, stream, false);
     if (st != SV_OK) return st;
@@ -317,6 +325,7 @@ sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row
     ca.row_to_req = row_to_req;
     ca.token_per_row = token_per_row;
     ca.sp = sp;
+    c.ra.chain = ca;
     if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
     sv_status_t st = run_rows(c.ra, stream, (sp.flags & SV_SAMPLING_SMALL_TOPK) != 0);
     if (st != SV_OK) return st;

@@ -40,9 +40,13 @@
 //    temperature, top-p over the top-k mass, normaliser, the probability of
 //    the row's token, and the kept list in index order for the resample.
 //    Greedy rows are the k = 1 case (argmax, lowest index wins ties).
+//  * In a verify call the warp that finalises a request's last row then runs
+//    the request's chain walk (acceptance, residual or bonus draw; see
+//    sv_walk.cuh), so no separate chain launch waits for the whole grid.
 #include <math.h>
 
 #include "sv_internal.cuh"
+#include "sv_walk.cuh"
 
 namespace sv {
 namespace {
@@ -335,7 +339,7 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
+__global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(const __grid_constant__ RowsArgs a)
 {
     constexpr int EPV = DT == 0 ? 8 : 4;
     constexpr int ESZ = DT == 0 ? 2 : 4;
@@ -345,6 +349,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
     extern __shared__ __align__(128) unsigned char ring[];   // warps x kStages x 4 KB
     __shared__ __align__(8) unsigned long long s_bar[kCtaWarps][kStages];
     __shared__ unsigned long long s_buf[kCtaWarps][kBufCap]; // candidate buffer of each warp
+    __shared__ double s_qp[kCtaWarps][kFastK];               // chain walk: the draft row's kept list
+    __shared__ int s_qi[kCtaWarps][kFastK];
 
     pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -434,7 +440,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
             const uint32_t bytes = chunk_bytes<DT>(row, c0, a.vocab);
             if (!__all_sync(FULL, mbar_wait(&bar[c_slot], c_phase))) {
                 // A bulk copy never arrived: flag it, let this warp's copies in
-                // flight land (bounded), and leave.
+                // flight land (bounded), fail the requests of the rows this
+                // warp has not finished (those rows will never be complete),
+                // and leave.
                 if (lane == 0) {
                     atomicOr(&a.counters->timeout, 1);
                     int s = c_slot;
@@ -448,6 +456,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
                     }
                 }
                 __syncwarp();
+                if (a.chain.fuse)
+                    for (int ii = i; ii < np; ++ii)
+                        chain_fail(a.chain, a.fast_tasks.get(t_lo + (rev ? np - 1 - ii : ii)).req);
                 return;
             }
             const unsigned char* stg = wring + c_slot * kWarpChunkBytes;
@@ -608,6 +619,16 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(RowsArgs a)
         if (__shfl_sync(FULL, last, 0)) {
             __threadfence();
             finalize_row(a.fast_tasks, a.info, a.partials, t, sp);
+            if (a.chain.fuse) {   // the request's last row: its chain walk
+                __threadfence();
+                __syncwarp();
+                int chain = 0;
+                if (lane == 0) chain = atomicAdd(&a.chain.req_done[task.req], 1) == task.req_rows - 1;
+                if (__shfl_sync(FULL, chain, 0)) {
+                    __threadfence();
+                    chain_walk(a.chain, task.req, s_qp[warp], s_qi[warp], false);
+                }
+            }
         }
     }
 }

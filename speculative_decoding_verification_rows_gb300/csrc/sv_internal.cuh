@@ -44,6 +44,7 @@ struct RowTask {
     float temp;       // 0 = greedy
     float top_p;      // >= 1 = top-p off
     int32_t is_draft; // 1: row of the draft logits
+    int32_t req_rows; // rows the request listed (its chain runs once they are all done)
 };
 
 // A list of row tasks, stored as three arrays (row index; slot, request,
@@ -67,13 +68,14 @@ struct TaskList {
         r.temp = f.x;
         r.top_p = f.y;
         r.is_draft = __float_as_int(f.z);
+        r.req_rows = __float_as_int(f.w);
         return r;
     }
     __device__ __forceinline__ void put(int64_t t, const RowTask& r) const
     {
         row[t] = r.row;
         meta[t] = make_int4(r.slot, r.req, r.token, r.k_eff);
-        samp[t] = make_float4(r.temp, r.top_p, __int_as_float(r.is_draft), 0.0f);
+        samp[t] = make_float4(r.temp, r.top_p, __int_as_float(r.is_draft), __int_as_float(r.req_rows));
     }
 };
 constexpr size_t kTaskBytes = sizeof(int64_t) + sizeof(int4) + sizeof(float4);
@@ -110,7 +112,7 @@ struct ReqState {
     int32_t v;        // verified drafts (window = v + 1 target rows)
     int32_t greedy;   // temperature == 0
     int32_t err;      // request-level error bits (params, layout)
-    int32_t pad;
+    int32_t fast;     // 1: its rows took the one-pass kernel, which also ran its chain
     uint64_t tok_bad; // bit j: draft token j out of range
 };
 
@@ -180,7 +182,7 @@ struct Counters {
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, jobs, tiles, blk, total;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, req_done, jobs, tiles, blk, total;
     int slots, max_tasks, max_jobs;
     size_t n_partials;
 };
@@ -207,6 +209,7 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab, int block = 0)
     L.partials = off;   off = align256(off + sizeof(Partial) * L.n_partials);
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
+    L.req_done = off;   off = align256(off + sizeof(int32_t) * (size_t)n_req);
     L.max_jobs = block ? n_req * (k_max + 1) : n_req;
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)L.max_jobs);
     L.tiles = off;      off = align256(off + sizeof(TileSums) * (size_t)L.max_jobs * (size_t)resample_tiles(vocab));
@@ -489,26 +492,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // ----------------------------------------------------------------------------
 // Launchers (host), one per kernel family.
 // ----------------------------------------------------------------------------
-struct RowsArgs {
-    const void* tgt;
-    const void* drf;
-    int64_t stride_t, stride_d;
-    int vocab;
-    int dtype;
-    TaskList fast_tasks;
-    TaskList slow_tasks;
-    Counters* counters;
-    RowInfo* info;
-    Partial* partials;
-    RowSync* row_sync;   // per fast task (zeroed by the prep kernel)
-    int32_t* ovf_idx;    // slow tasks the one-CTA histogram kernel could not hold (counted in n_ovf)
-    int max_tasks;
-    int num_sms;
-};
-
-cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
-cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
-
 struct ChainArgs {
     int n_req, K;          // K = k_max: slots per request = 2K + 1 (layout 2: n_req = rows)
     int n_params;          // length of the sampling-parameter arrays
@@ -516,6 +499,7 @@ struct ChainArgs {
     int layout;            // 0 uniform, 1 ragged, 2 plain rows (build_target_probs)
     int block;             // 1: block verification instead of the token-by-token chain
     int est;               // 1: estimator features (layout 2, greedy requests at T = 1)
+    int fuse;              // 1: the one-pass kernel runs the chain of each request whose rows it took
     int rows_per_req;      // layout 2 without row_to_req: request = row / rows_per_req
     const void* tgt;
     const void* drf;
@@ -538,12 +522,36 @@ struct ChainArgs {
     RowSync* row_sync;
     RowInfo* info;
     ReqState* req;
+    int32_t* req_done;   // rows of each request finished by the one-pass kernel (zeroed by prep)
     ResampleJob* jobs;
     TileSums* tiles;   // [max_jobs][resample_tiles(vocab)]
     double* blk_w;     // block verification: [n_req][K + 1] weights w_j
     unsigned long long* blk_h;   // block verification: [n_req][K + 1] residual sums H_j (2^-62 units)
     int num_sms;
 };
+
+struct RowsArgs {
+    const void* tgt;
+    const void* drf;
+    int64_t stride_t, stride_d;
+    int vocab;
+    int dtype;
+    TaskList fast_tasks;
+    TaskList slow_tasks;
+    Counters* counters;
+    RowInfo* info;
+    Partial* partials;
+    RowSync* row_sync;   // per fast task (zeroed by the prep kernel)
+    int32_t* ovf_idx;    // slow tasks the one-CTA histogram kernel could not hold (counted in n_ovf)
+    int max_tasks;
+    int num_sms;
+    ChainArgs chain;     // the chain walk the one-pass kernel runs when chain.fuse is set
+};
+
+cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
+
+
 
 cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
