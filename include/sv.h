@@ -391,6 +391,57 @@ sv_status_t sv_verify_chain_noalloc(const void* target_logits, const void* draft
                                     int32_t* num_emitted, int32_t* row_status, sv_stream_t stream);
 
 /*
+ * Vocabulary-sharded verify (jianc99/sglang PR #8, DFLASH adaptive-
+ * verification commit: the compact scatter works on a vocabulary shard and
+ * the target-verify gather is deferred).  The logits of a step may live split
+ * along the vocabulary, each shard [v0, v1) on its own device (tensor-parallel
+ * lm heads).  Each shard reduces its slice of every row of the window to one
+ * fixed-width record; the records of all shards are exchanged once (any
+ * collective that gathers equal-sized buffers, e.g. an all-gather: the size
+ * depends only on n_req and K, never on the data); every rank then merges
+ * them and finishes the step exactly as sv_verify_chain would on the whole
+ * rows -- the same accepted lengths, tokens and statuses.  Served: greedy
+ * requests and requests whose kept set is listed (top-k <= 32, with or
+ * without top-p); a request with a larger kept set gets SV_ROW_UNSUPPORTED
+ * (nothing accepted or emitted), as an fp32 one does in sv_verify_chain.
+ *
+ * sv_shard_record_bytes: bytes of one record (264): its row's top-32
+ * composite keys (logit order key above, whole-vocabulary index inverted
+ * below, descending) with their count and status bits.
+ */
+size_t sv_shard_record_bytes(void);
+
+/*
+ * One shard's records.  target_shard (device) [n_req, K + 1, v1 - v0] and
+ * draft_shard (device) [n_req, K, v1 - v0] (NULL if every request is greedy):
+ * columns v0 .. v1 - 1 of the rows sv_verify_chain takes, row stride v1 - v0;
+ * 0 <= v0 < v1 <= vocab.  draft_tokens, verify_len and sp as sv_verify_chain
+ * (tokens and top_k refer to the whole vocabulary).  records (device,
+ * 16-byte aligned) [n_req * (2K + 1)] records of sv_shard_record_bytes(), one
+ * per target position 0..K and draft position 0..K-1 of each request (slot
+ * r (2K + 1) + j, then r (2K + 1) + K + 1 + j); slots outside a request's
+ * window are left as they are and never read.  Workspace:
+ * sv_workspace_size(n_req, K, v1 - v0).  Errors: SV_ERR_INVALID_ARG for NULL
+ * pointers, sizes, a slice outside [0, vocab), a misaligned records buffer.
+ */
+sv_status_t sv_verify_chain_shard_rows(const void* target_shard, const void* draft_shard, sv_dtype_t dt, int n_req,
+                                       int K, int vocab, int v0, int v1, const int32_t* draft_tokens,
+                                       const int32_t* verify_len, sv_sampling_t sp, void* records, void* ws,
+                                       size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * The merge: records (device, 16-byte aligned) [n_shards][n_req * (2K + 1)]
+ * records, the shards' sv_verify_chain_shard_rows outputs in any shard order
+ * (shards must cover [0, vocab) without overlap).  The other arguments and
+ * the outputs are those of sv_verify_chain.  Workspace: sv_workspace_size(
+ * n_req, K, 1).
+ */
+sv_status_t sv_verify_chain_shard_merge(const void* records, int n_shards, int n_req, int K, int vocab,
+                                        const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                                        uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                                        int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream);
+
+/*
  * Measurement aid (not part of the method): when both are non-NULL, every
  * later sv_verify_chain / sv_verify_ragged / sv_build_target_probs call
  * records start_event (a cudaEvent_t) on its stream immediately before the

@@ -361,6 +361,72 @@ sv_status_t sv_verify_ragged(const void* target_logits, const void* draft_logits
                       draft_tokens, sp, seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream);
 }
 
+size_t sv_shard_record_bytes(void) { return sizeof(Partial); }
+
+sv_status_t sv_verify_chain_shard_rows(const void* target_shard, const void* draft_shard, sv_dtype_t dt, int n_req,
+                                       int K, int vocab, int v0, int v1, const int32_t* draft_tokens,
+                                       const int32_t* verify_len, sv_sampling_t sp, void* records, void* ws,
+                                       size_t ws_bytes, sv_stream_t stream)
+{
+    if (!target_shard || !records || n_req < 1 || K < 0 || vocab < 1 || v0 < 0 || v1 <= v0 || v1 > vocab ||
+        !sp.temperature)
+        return SV_ERR_INVALID_ARG;
+    if (K > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(records) & 15u) != 0u) return SV_ERR_INVALID_ARG;
+    if (K > kMaxK || vocab > kMaxVocab || n_req > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const int vs = v1 - v0;
+    const size_t need = sv_workspace_size(n_req, K, vs);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, n_req, K, vs, (int)dt, target_shard, draft_shard, vs, vs);
+    ChainArgs& ca = c.ca;
+    ca.vocab = vocab;   // parameters and tokens refer to the whole vocabulary; the rows hold [v0, v1)
+    ca.layout = 0;
+    ca.shard = 1;
+    ca.verify_len = verify_len;
+    ca.draft_tokens = draft_tokens;
+    ca.sp = sp;
+    c.ra.chain = ca;
+    c.ra.shard_out = static_cast<Partial*>(records);
+    c.ra.shard_v0 = (uint32_t)v0;
+    if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
+    return to_status(launch_fast_rows(c.ra, stream));
+}
+
+sv_status_t sv_verify_chain_shard_merge(const void* records, int n_shards, int n_req, int K, int vocab,
+                                        const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                                        uint64_t seed, int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted,
+                                        int32_t* row_status, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    if (!records || n_shards < 1 || n_req < 1 || K < 0 || vocab < 1 || !sp.temperature || !accept_len ||
+        !out_tokens || !num_emitted)
+        return SV_ERR_INVALID_ARG;
+    if (K > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(records) & 15u) != 0u) return SV_ERR_INVALID_ARG;
+    if (K > kMaxK || vocab > kMaxVocab || n_req > (1 << 22) || n_shards > 1024) return SV_ERR_UNSUPPORTED;
+    const size_t need = sv_workspace_size(n_req, K, 1);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, n_req, K, 1, (int)SV_DTYPE_BF16, nullptr, nullptr, 1, 1);
+    ChainArgs& ca = c.ca;
+    ca.vocab = vocab;
+    ca.layout = 0;
+    ca.shard = 2;
+    ca.verify_len = verify_len;
+    ca.draft_tokens = draft_tokens;
+    ca.sp = sp;
+    ca.seed = seed;
+    ca.accept_len = accept_len;
+    ca.out_tokens = out_tokens;
+    ca.num_emitted = num_emitted;
+    ca.row_status = row_status;
+    c.ra.chain = ca;
+    if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
+    if (launch_shard_merge(c.ra, records, n_shards, n_req * (2 * K + 1), stream) != cudaSuccess) return SV_ERR_CUDA;
+    return to_status(launch_chain(ca, stream));
+}
+
 sv_status_t sv_set_timing_events(void* start_event, void* stop_event)
 {
     g_ev_start = static_cast<cudaEvent_t>(start_event);

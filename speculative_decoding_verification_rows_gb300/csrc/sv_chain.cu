@@ -115,8 +115,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
             fast = greedy || k_eff <= kFastK;
             // full-vocabulary kept sets: not for fp32 rows, nor under the
-            // caller's promise that the batch has none
-            if (!err && !fast && (a.dtype != 0 || (a.sp.flags & SV_SAMPLING_SMALL_TOPK))) err |= kUnsupported;
+            // caller's promise that the batch has none, nor in a
+            // vocabulary-sharded call
+            if (!err && !fast && (a.dtype != 0 || (a.sp.flags & SV_SAMPLING_SMALL_TOPK) || a.shard)) err |= kUnsupported;
             if (a.layout == 0) {
                 v = a.verify_len ? a.verify_len[u] : K;
                 if (v < 0 || v > K) {
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 }
                 start = (int)s0;
             }
-            if (a.layout != 2 && !greedy && v > 0 && !a.drf) err |= kBadParam;   // q needs draft logits
+            if (a.layout != 2 && a.shard != 2 && !greedy && v > 0 && !a.drf) err |= kBadParam;   // q needs draft logits
             if (a.layout != 2) {
                 // one request-level error: a bad window first, then bad parameters
                 if (err & kBadLayout) err = kBadLayout;
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 st.tok_bad = tok_bad;
                 a.req[u] = st;
                 a.req_done[u] = 0;
-                if (err) {   // no rows were listed: the outputs of a failed request
+                if (err && a.accept_len) {   // no rows were listed: the outputs of a failed request
                     const int width = K + 1;
                     for (int j = 0; j < width; ++j) {
                         a.out_tokens[(size_t)u * width + j] = -1;

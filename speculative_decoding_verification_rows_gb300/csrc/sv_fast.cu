@@ -220,9 +220,14 @@ __device__ __noinline__ unsigned long long merge_buffer(unsigned long long list,
     return merge_desc(list, sort_desc(b, n));
 }
 
-// The distribution of fast task t from its parts' lists (one warp).  Out of
-// line: it runs once per row.
-__device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const Partial* parts, int t, Split sp)
+__device__ __forceinline__ void finalize_list(const RowTask& task, RowInfo* info, unsigned long long acc, uint32_t st);
+
+// Fast task t's parts' lists merged (one warp).  Out of line: it runs once
+// per row.  Its distribution goes to the task's RowInfo, or, for a vocabulary
+// shard (shard_out set), the merged list goes to the task's record with the
+// indices of the whole vocabulary (the shard starts at element v0).
+__device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const Partial* parts, int t, Split sp,
+                                         Partial* shard_out, uint32_t v0)
 {
     const int lane = threadIdx.x & 31;
     const RowTask task = tasks.get(t);
@@ -248,7 +253,27 @@ __device__ __noinline__ void finalize_row(TaskList tasks, RowInfo* infos, const 
         for (int j = 0; j < 4; ++j)
             if (wb + j <= w1) acc = merge_desc(acc, lane < (int)cnt[j] ? key[j] : 0ull);
     }
-    RowInfo* info = infos + task.slot;
+    if (shard_out) {   // a shard's record: its top k with whole-vocabulary indices
+        const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
+        const unsigned long long ck = lane < k ? acc : 0ull;
+        const int n = __popc(__ballot_sync(0xFFFFFFFFu, ck != 0ull));
+        Partial* R = shard_out + task.slot;
+        if (lane < n) R->keys[lane] = ck - (unsigned long long)v0;   // the inverted index drops by v0
+        if (lane == 0) {
+            R->status = st & (uint32_t)kNonfinite;
+            R->count = (uint32_t)n;
+        }
+        return;
+    }
+    finalize_list(task, infos + task.slot, acc, st);
+}
+
+// The distribution of a fast row from its top-k composite keys (acc, lane i
+// the i-th best) and status bits (one warp): argmax, temperature, top-p over
+// the top-k mass, normaliser, p of the row's token, the kept list.
+__device__ __forceinline__ void finalize_list(const RowTask& task, RowInfo* info, unsigned long long acc, uint32_t st)
+{
+    const int lane = threadIdx.x & 31;
     const int k = task.k_eff < kFastK ? task.k_eff : kFastK;
     const unsigned long long ck = lane < k ? acc : 0ull;
     const int n_top = __popc(__ballot_sync(0xFFFFFFFFu, ck != 0ull));
@@ -618,7 +643,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(const __grid
         }
         if (__shfl_sync(FULL, last, 0)) {
             __threadfence();
-            finalize_row(a.fast_tasks, a.info, a.partials, t, sp);
+            finalize_row(a.fast_tasks, a.info, a.partials, t, sp, a.shard_out, a.shard_v0);
             if (a.chain.fuse) {   // the request's last row: its chain walk
                 __threadfence();
                 __syncwarp();
@@ -630,6 +655,40 @@ __global__ void __launch_bounds__(kFastThreads, 1) fast_rows_kernel(const __grid
                 }
             }
         }
+    }
+}
+
+// Vocabulary-sharded verify, the merge: the records of the row's slot from
+// every shard (each the shard's top k with whole-vocabulary indices) merged
+// into the row's top k, then the same finalisation as an unsharded row.  One
+// warp per fast task, records of shard s at records + s * slots.
+__global__ void __launch_bounds__(256) shard_merge_kernel(const __grid_constant__ RowsArgs a, const Partial* records,
+                                                          int n_shards, int slots)
+{
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int n_tasks = a.counters->n_fast;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += (gridDim.x * blockDim.x) >> 5) {
+        const RowTask task = a.fast_tasks.get(t);
+        unsigned long long acc = 0ull;
+        uint32_t st = 0u;
+        for (int s0 = 0; s0 < n_shards; s0 += 4) {   // four records' loads in flight at once
+            unsigned long long key[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                key[j] = 0ull;
+                if (s0 + j < n_shards) {
+                    const Partial* R = records + (size_t)(s0 + j) * (size_t)slots + (size_t)task.slot;
+                    const uint32_t cnt = R->count;
+                    st |= R->status;
+                    key[j] = lane < (int)cnt ? R->keys[lane] : 0ull;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (s0 + j < n_shards) acc = merge_desc(acc, key[j]);
+        }
+        finalize_list(task, a.info + task.slot, acc, st);
     }
 }
 
@@ -662,4 +721,15 @@ cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s)
     return a.dtype == 0 ? launch_fast_rows_t<0>(a, s) : launch_fast_rows_t<1>(a, s);
 }
 
+}  // namespace sv
+
+namespace sv {
+cudaError_t launch_shard_merge(const RowsArgs& a, const void* records, int n_shards, int slots, cudaStream_t s)
+{
+    int grid = (a.max_tasks + 7) / 8;
+    if (grid > 4 * a.num_sms) grid = 4 * a.num_sms;
+    if (grid < 1) grid = 1;
+    return launch_pdl(shard_merge_kernel, dim3(grid), dim3(256), 0, s, a, static_cast<const Partial*>(records),
+                      n_shards, slots);
+}
 }  // namespace sv

@@ -500,6 +500,8 @@ struct ChainArgs {
     int block;             // 1: block verification instead of the token-by-token chain
     int est;               // 1: estimator features (layout 2, greedy requests at T = 1)
     int fuse;              // 1: the one-pass kernel runs the chain of each request whose rows it took
+    int shard;             // vocabulary-sharded verify (listed kept sets only): 1 a shard's rows
+                           // (no outputs), 2 the merge of the shards' records (no logits)
     int rows_per_req;      // layout 2 without row_to_req: request = row / rows_per_req
     const void* tgt;
     const void* drf;
@@ -546,9 +548,12 @@ struct RowsArgs {
     int max_tasks;
     int num_sms;
     ChainArgs chain;     // the chain walk the one-pass kernel runs when chain.fuse is set
+    Partial* shard_out;  // vocabulary shard: per-slot records instead of row results (NULL otherwise)
+    uint32_t shard_v0;   // the shard's first vocabulary element
 };
 
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_shard_merge(const RowsArgs& a, const void* records, int n_shards, int slots, cudaStream_t s);
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
 
 

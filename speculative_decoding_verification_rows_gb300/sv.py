@@ -17,6 +17,9 @@ import torch
 from . import build as _build
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+# per-position status bits (SV_ROW_* in sv.h)
+SV_ROW_NONFINITE, SV_ROW_EMPTY, SV_ROW_BAD_TOKEN, SV_ROW_BAD_PARAM, SV_ROW_BAD_LAYOUT = 1, 2, 4, 8, 16
+SV_ROW_Q_ZERO, SV_ROW_RESID_ZERO, SV_ROW_UNSUPPORTED, SV_ROW_TIMEOUT = 32, 64, 128, 256
 DTYPE_BF16, DTYPE_F32 = 0, 1
 ROW_NONFINITE, ROW_EMPTY, ROW_BAD_TOKEN, ROW_BAD_PARAM, ROW_BAD_LAYOUT = 1, 2, 4, 8, 16
 ROW_Q_ZERO, ROW_RESID_ZERO, ROW_UNSUPPORTED, ROW_TIMEOUT = 32, 64, 128, 256
@@ -27,7 +30,8 @@ EXPORTED = ("sv_workspace_size", "sv_workspace_size_block", "sv_status_string", 
             "sv_build_target_probs", "sv_verify_chain", "sv_verify_ragged", "sv_set_timing_events",
             "sv_set_hist_timing_events", "sv_verify_chain_noalloc", "sv_plan_budget_cost", "sv_verify_stats",
             "sv_verify_block", "sv_estimator_state_bytes", "sv_estimator_init", "sv_estimator_predict",
-            "sv_estimator_observe")
+            "sv_estimator_observe", "sv_shard_record_bytes", "sv_verify_chain_shard_rows",
+            "sv_verify_chain_shard_merge")
 
 
 class SVError(RuntimeError):
@@ -99,6 +103,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_estimator_predict.restype = I
     L.sv_estimator_observe.argtypes = [P, P, P, P, P, I, I, I, P]
     L.sv_estimator_observe.restype = I
+    L.sv_shard_record_bytes.argtypes = []
+    L.sv_shard_record_bytes.restype = SZ
+    L.sv_verify_chain_shard_rows.argtypes = [P, P, I, I, I, I, I, I, P, P, Sampling, P, P, SZ, P]
+    L.sv_verify_chain_shard_rows.restype = I
+    L.sv_verify_chain_shard_merge.argtypes = [P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P, SZ, P]
+    L.sv_verify_chain_shard_merge.restype = I
     L.sv_set_timing_events.argtypes = [P, P]
     L.sv_set_timing_events.restype = I
     L.sv_set_hist_timing_events.argtypes = [P, P]
@@ -409,4 +419,53 @@ def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], qo_indptr
                                    _sampling(temperature, top_k, top_p, small_topk), seed, _ptr(o.accept_len),
                                    _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status), _ptr(w),
                                    w.numel(), _stream(dev)))
+    return o
+
+
+def shard_record_bytes() -> int:
+    return int(load().sv_shard_record_bytes())
+
+
+def verify_chain_shard_rows(target_shard: torch.Tensor, draft_shard: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                            temperature: torch.Tensor, top_k: Optional[torch.Tensor], top_p: Optional[torch.Tensor],
+                            v0: int, vocab: int, verify_len: Optional[torch.Tensor] = None,
+                            ws: Optional[Workspace] = None, records: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """sv_verify_chain_shard_rows: one vocabulary shard's records (uint8 [n * (2K+1) * record bytes]).
+    target_shard [n, K+1, Vs] holds columns v0 .. v0 + Vs - 1 of the target rows, draft_shard [n, K, Vs]
+    the same of the draft rows (None if all greedy)."""
+    target_shard = _dev(target_shard)
+    n, k1, Vs = target_shard.shape
+    K = k1 - 1
+    dev = target_shard.device
+    if draft_shard is not None:
+        _dev(draft_shard, target_shard.dtype)
+        assert draft_shard.shape == (n, K, Vs)
+    nbytes = n * (2 * K + 1) * shard_record_bytes()
+    if records is None:
+        records = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    assert records.numel() >= nbytes and records.is_cuda
+    w = _ws(ws, dev, workspace_size(n, K, Vs))
+    _check(load().sv_verify_chain_shard_rows(_ptr(target_shard), _ptr(draft_shard), _dtype_code(target_shard), n, K,
+                                             vocab, v0, v0 + Vs, _ptr(draft_tokens), _ptr(verify_len),
+                                             _sampling(temperature, top_k, top_p), _ptr(records), _ptr(w), w.numel(),
+                                             _stream(dev)))
+    return records
+
+
+def verify_chain_shard_merge(records: torch.Tensor, n_shards: int, draft_tokens: torch.Tensor,
+                             temperature: torch.Tensor, top_k: Optional[torch.Tensor], top_p: Optional[torch.Tensor],
+                             vocab: int, verify_len: Optional[torch.Tensor] = None, seed: int = 0,
+                             ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None) -> VerifyOut:
+    """sv_verify_chain_shard_merge: the step's outputs from every shard's records (device
+    [n_shards, n * (2K+1) * record bytes], any shard order)."""
+    records = _dev(records)
+    n, K = draft_tokens.shape
+    dev = records.device
+    assert records.numel() >= n_shards * n * (2 * K + 1) * shard_record_bytes()
+    o = out or _outs(n, K, dev)
+    w = _ws(ws, dev, workspace_size(n, K, 1))
+    _check(load().sv_verify_chain_shard_merge(_ptr(records), n_shards, n, K, vocab, _ptr(draft_tokens),
+                                              _ptr(verify_len), _sampling(temperature, top_k, top_p), seed,
+                                              _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted),
+                                              _ptr(o.row_status), _ptr(w), w.numel(), _stream(dev)))
     return o
