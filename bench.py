@@ -67,6 +67,9 @@ def parse():
                    help="ragged workload: choose the budget from a synthetic step-cost table on the device")
     p.add_argument("--no-graph", action="store_true",
                    help="launch each timed step on the stream instead of replaying it as one captured CUDA graph")
+    p.add_argument("--shards", type=int, default=0,
+                   help="uniform layout: verify over N vocabulary shards (N record passes on this GPU, one merge; "
+                        "no exchange, one GPU holds every shard)")
     p.add_argument("--no-promise", action="store_true",
                    help="never pass the small-top-k sampling promise (the full launch sequence of every call)")
     return p.parse_args()
@@ -251,9 +254,31 @@ def synthetic_cost_table(w, dev):
             0.8)
 
 
-def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False, promise=True):
+def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False, promise=True, shards=0):
     """A closure running one verify step with preallocated outputs/workspace."""
     ws = sv.Workspace(dev)
+    if shards:
+        if w.layout != "chain" or method != "chain":
+            raise SystemExit("--shards: the uniform layout and the chain method only")
+        from speculative_decoding_verification_rows_gb300 import shard
+        n, K = w.n, w.K
+        bounds = [shard.shard_bounds(w.V, shards, r) for r in range(shards)]
+        tgt = [w.target[..., a:b].contiguous() for a, b in bounds]
+        drf = [None if w.draft is None else w.draft[..., a:b].contiguous() for a, b in bounds]
+        rec = torch.empty((shards, n * (2 * K + 1) * sv.shard_record_bytes()), dtype=torch.uint8, device=dev)
+        ws_s = [sv.Workspace(dev) for _ in range(shards)]
+        out = sv.VerifyOut(torch.empty(n, dtype=torch.int32, device=dev),
+                           torch.empty((n, K + 1), dtype=torch.int32, device=dev),
+                           torch.empty(n, dtype=torch.int32, device=dev),
+                           torch.empty((n, K + 1), dtype=torch.int32, device=dev))
+
+        def step():
+            for r, (a, _) in enumerate(bounds):
+                sv.verify_chain_shard_rows(tgt[r], drf[r], w.draft_tokens, w.temperature, w.top_k, w.top_p, a, w.V,
+                                           ws=ws_s[r], records=rec[r])
+            return sv.verify_chain_shard_merge(rec, shards, w.draft_tokens, w.temperature, w.top_k, w.top_p, w.V,
+                                               seed=w.seed, ws=ws, out=out)
+        return step, out, None
     n, K = w.n, w.K
     out = sv.VerifyOut(torch.empty(n, dtype=torch.int32, device=dev), torch.empty((n, K + 1), dtype=torch.int32,
                                                                                  device=dev),
@@ -328,16 +353,19 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
-    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator, not args.no_promise)
+    step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator, not args.no_promise,
+                                 args.shards)
     alg_bytes, rows_t = algorithmic_bytes(w)
     fast_bytes, hist_bytes = path_bytes(w)
     if extra is not None:
         rows_t = extra["rows"]
         alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2
         fast_bytes, hist_bytes = extra["path_bytes"]
-    # the roofline is taken on the path that reads more of the logits
+    # the roofline is taken on the path that reads more of the logits (with
+    # vocabulary shards: over the whole step)
     roof_path = "hist" if hist_bytes > fast_bytes else "fast"
     roof_bytes = hist_bytes if roof_path == "hist" else fast_bytes
+
     # prep, row select (with finalisation and the chains of its requests),
     # one-CTA histogram, cluster histogram (rows handed on), chain (the other
     # requests), resample (+ block decision and draw for block verification;
@@ -353,6 +381,8 @@ def run_ours(args, rank, world, local):
     launches_per_step += (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
     if args.estimator:   # prep, row select, two histogram kernels, features for the draft rows; observe
         launches_per_step += 6
+    if args.shards:      # per shard: prep, row select; then prep, merge, chain
+        launches_per_step = 2 * args.shards + 3
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     if not args.quick:
@@ -421,13 +451,15 @@ def run_ours(args, rank, world, local):
     ms_worst = max_over_ranks(ms_per_step, world)
 
     # end to end through the public API: pinned host inputs in, results out, every step
-    e2e = None if args.quick else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)), args.method,
-                                          not args.no_promise)
+    e2e = None if (args.quick or args.shards) else run_e2e(w, sv, dev, extra, max(3, min(args.steps, 10)),
+                                                            args.method, not args.no_promise)
     torch.cuda.synchronize()
     clk = clocks.stop()
 
     value = world * rows_t / (ms_worst / 1e3)
     kern_avg_s = statistics.mean(kern_ms) / 1e3
+    if args.shards:   # the records of N shards and the merge on one GPU: the rate over the whole step
+        kern_avg_s, roof_bytes = ms_worst / 1e3, fast_bytes
     peak, peak_kind = measured_peak()
     achieved = roof_bytes / kern_avg_s / 1e9
     logits_gbs_step = alg_bytes / (ms_per_step / 1e3) / 1e9
@@ -440,7 +472,8 @@ def run_ours(args, rank, world, local):
                    + (f" (scaled to {w.n} requests)" if args.requests else "")
                    + (" -- block verification" if args.method == "block" else "")
                    + (" -- with the online acceptance estimator (predict + observe)" if args.estimator else "")
-                   + (" -- budget from a synthetic step-cost table" if args.cost_table else ""),
+                   + (" -- budget from a synthetic step-cost table" if args.cost_table else "")
+                   + (f" -- over {args.shards} vocabulary shards on this GPU (records, merge)" if args.shards else ""),
                    "rows_per_step": rows_t,
                    "sampling_promise": "small_topk (every request greedy or top-k <= 32: the full-vocabulary "
                                        "kernels are not launched)" if small else None,
@@ -451,7 +484,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                    "launch": graph_note},
-        "roofline": {"bound": "hbm", "kernel": ROW_PATHS[roof_path]["kernel"],
+        "roofline": {"bound": "hbm", "kernel": ROW_PATHS[roof_path]["kernel"] if not args.shards else
+                     f"whole step over {args.shards} vocabulary shards (records + merge)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
                      "traffic": recorded_traffic(args.workload, roof_path), "kernel_ms_mean": statistics.mean(kern_ms),
@@ -644,10 +678,11 @@ def cpu_baseline(w, seconds, extra=None):
     if w.layout == "ragged":
         extra = ragged_host_plan(w, dict(extra or {}))
     with pinned_core() as pin:
-        rows, dt = oracle_sample(w, 0, 1, extra)
-        per_req = max(dt, 1e-6)
-        n = int(max(1, min(w.n, seconds / per_req)))
-        rows, dt = oracle_sample(w, 0, n, extra)
+        # requests in order, one at a time, until about `seconds` of CPU work
+        rows, dt, n = 0, 0.0, 0
+        while n < w.n and dt < seconds:
+            r_rows, r_dt = oracle_sample(w, n, n + 1, extra)
+            rows, dt, n = rows + r_rows, dt + r_dt, n + 1
     what = "packed target rows of the plan" if w.layout == "ragged" else "target rows"
     return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"requests 0..{n - 1} of the same workload ({rows} {what}), single thread, fp64",
