@@ -289,7 +289,16 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False, pro
         block = method == "block"
         est = sv.Estimator(w.K, dev) if estimator else None
 
+        q_buf = (torch.empty(int(sv.load().sv_q_rows_bytes(w.n, w.K)), dtype=torch.uint8, device=dev)
+                 if estimator and not block else None)
+
         def step(tgt=w.target, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
+            if est is not None and not block:
+                # the estimator's pass over the draft rows also serves the verify's q
+                x, _, q = est.predict_q(drf, toks, T, tk, tp, q_rows=q_buf)
+                o = sv.verify_chain_q(tgt, drf, toks, T, tk, tp, q, seed=w.seed, ws=ws, out=out, small_topk=small)
+                est.observe(x, o.accept_len, o.num_emitted)
+                return o
             if est is not None:
                 x, _ = est.predict(drf, T, tk, tp)
             o = sv.verify_chain(tgt, drf, toks, T, tk, tp, seed=w.seed, ws=ws, out=out, block=block,
@@ -380,7 +389,7 @@ def run_ours(args, rank, world, local):
         launches_per_step = 6 + (2 if args.method == "block" else 0)
     launches_per_step += (1 if w.layout == "ragged" else 0) + (1 if args.cost_table else 0)
     if args.estimator:   # prep, row select, two histogram kernels, features for the draft rows; observe
-        launches_per_step += 6
+        launches_per_step += 6 if args.method == "block" else 6 - (1 if small else 0)
     if args.shards:      # per shard: prep, row select; then prep, merge, chain
         launches_per_step = 2 * args.shards + 3
 
@@ -460,6 +469,10 @@ def run_ours(args, rank, world, local):
     kern_avg_s = statistics.mean(kern_ms) / 1e3
     if args.shards:   # the records of N shards and the merge on one GPU: the rate over the whole step
         kern_avg_s, roof_bytes = ms_worst / 1e3, fast_bytes
+    elif args.estimator and args.method == "chain" and roof_path == "fast":
+        # the timed launch is the verify's row kernel, which streams the target rows only (the
+        # estimator's pass over the draft rows made their distributions)
+        roof_bytes = w.n * (w.K + 1) * w.V * (2 if w.dtype == torch.bfloat16 else 4)
     peak, peak_kind = measured_peak()
     achieved = roof_bytes / kern_avg_s / 1e9
     logits_gbs_step = alg_bytes / (ms_per_step / 1e3) / 1e9

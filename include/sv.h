@@ -353,6 +353,42 @@ sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_
                                  size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * Bytes of the draft-row results sv_estimator_predict_q leaves for
+ * sv_verify_chain_q: n_req * K records of the library's row result (0 for
+ * sizes outside 1 <= K <= 63, n_req * K <= 2^22).
+ */
+size_t sv_q_rows_bytes(int n_req, int K);
+
+/*
+ * sv_estimator_predict that also keeps what it computed for the verify that
+ * follows (jianc99/sglang PR #8, DFLASH adaptive-verification commits: the
+ * feature logit(q_max) is a by-product of the draft distribution).  Besides
+ * x_out and p_out it writes, for every draft row (r, j), the row's
+ * distribution under request r's parameters (greedy requests at T = 1) and
+ * q of draft token draft_tokens[r, j] into q_rows (device, 16-byte aligned,
+ * sv_q_rows_bytes(n_req, K) bytes).  draft_tokens (device) [n_req, K].
+ * Workspace as sv_estimator_predict.
+ */
+sv_status_t sv_estimator_predict_q(const void* draft_logits, sv_dtype_t dt, int n_req, int K, int vocab,
+                                   sv_sampling_t sp, const double* state, const int32_t* draft_tokens, float* x_out,
+                                   float* p_out, void* q_rows, void* ws, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * sv_verify_chain with the draft rows' distributions taken from q_rows, made
+ * by sv_estimator_predict_q from the same draft logits, draft tokens and
+ * sampling parameters (for sampling requests the two transforms are the
+ * same): only the target rows are streamed.  draft_logits is still required
+ * for sampling requests -- the full-row resample of a request whose kept set
+ * is not listed reads its draft row at the emitted position.  Everything
+ * else, outputs included, as sv_verify_chain (K >= 1).
+ */
+sv_status_t sv_verify_chain_q(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                              int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                              uint64_t seed, const void* q_rows, int32_t* accept_len, int32_t* out_tokens,
+                              int32_t* num_emitted, int32_t* row_status, void* ws, size_t ws_bytes,
+                              sv_stream_t stream);
+
+/*
  * After a verify call: request r's positions 0 .. min(accept_len[r],
  * v_r - 1) are observed (label 1 below accept_len, 0 for the first rejected
  * one; v_r = verify_lens[r], or K when NULL); requests with num_emitted == 0

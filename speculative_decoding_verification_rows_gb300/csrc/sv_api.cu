@@ -128,7 +128,7 @@ bool dtype_ok(sv_dtype_t dt) { return dt == SV_DTYPE_BF16 || dt == SV_DTYPE_F32;
 sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t dt, int n, int K, int V, int bucket,
                        const int32_t* qo, const int32_t* vl, const int32_t* toks, sv_sampling_t sp, uint64_t seed,
                        int32_t* accept_len, int32_t* out_tokens, int32_t* num_emitted, int32_t* row_status, void* ws,
-                       size_t ws_bytes, cudaStream_t s, int block = 0)
+                       size_t ws_bytes, cudaStream_t s, int block = 0, const RowInfo* q_rows = nullptr)
 {
     if (!tgt || n < 1 || K < 0 || V < 1 || !sp.temperature || !accept_len || !out_tokens || !num_emitted)
         return SV_ERR_INVALID_ARG;
@@ -153,6 +153,7 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     ca.out_tokens = out_tokens;
     ca.num_emitted = num_emitted;
     ca.row_status = row_status;
+    ca.q_rows = q_rows;
     // The one-pass row kernel runs the chain of every request whose rows it
     // takes (greedy and top-k <= 32); the chain kernel takes the others
     // (block verification: every request).  Under the small-top-k promise
@@ -288,6 +289,56 @@ sv_status_t sv_estimator_predict(const void* draft_logits, sv_dtype_t dt, int n_
     sv_status_t st = run_rows(c.ra, stream, false);
     if (st != SV_OK) return st;
     return to_status(launch_est_predict(c.ra.info, state, n_req, K, x_out, p_out, c.ra.counters, stream));
+}
+
+size_t sv_q_rows_bytes(int n_req, int K)
+{
+    if (n_req < 1 || K < 1 || K > kMaxK || (long long)n_req * K > (1 << 22)) return 0;
+    return sizeof(RowInfo) * (size_t)n_req * (size_t)K;
+}
+
+sv_status_t sv_estimator_predict_q(const void* draft_logits, sv_dtype_t dt, int n_req, int K, int vocab,
+                                   sv_sampling_t sp, const double* state, const int32_t* draft_tokens, float* x_out,
+                                   float* p_out, void* q_rows, void* ws, size_t ws_bytes, sv_stream_t stream)
+{
+    if (!draft_logits || n_req < 1 || K < 1 || K > kMaxK || vocab < 1 || !sp.temperature || !state || !x_out ||
+        !p_out || !draft_tokens || !q_rows)
+        return SV_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_rows) & 15u) != 0u) return SV_ERR_INVALID_ARG;
+    if (vocab > kMaxVocab || (long long)n_req * K > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const int rows = n_req * K;
+    const size_t need = sv_workspace_size(rows, 0, vocab);
+    if (need == 0) return SV_ERR_UNSUPPORTED;
+    if (!ws_ok(ws, ws_bytes, need)) return SV_ERR_WORKSPACE;
+    Carved c = carve(ws, rows, 0, vocab, (int)dt, draft_logits, nullptr, vocab, vocab);
+    ChainArgs& ca = c.ca;
+    ca.layout = 2;
+    ca.est = 1;
+    ca.rows_per_req = K;
+    ca.n_params = n_req;
+    ca.token_per_row = draft_tokens;   // row r K + j carries draft token j of request r
+    ca.sp = sp;
+    ca.sp.flags = 0;
+    ca.info = c.ra.info = static_cast<RowInfo*>(q_rows);   // the rows' results go to the caller's buffer
+    c.ra.chain = ca;
+    if (launch_prep(ca, stream) != cudaSuccess) return SV_ERR_CUDA;
+    sv_status_t st = run_rows(c.ra, stream, false);
+    if (st != SV_OK) return st;
+    return to_status(launch_est_predict(c.ra.info, state, n_req, K, x_out, p_out, c.ra.counters, stream));
+}
+
+sv_status_t sv_verify_chain_q(const void* target_logits, const void* draft_logits, sv_dtype_t dt, int n_req, int K,
+                              int vocab, const int32_t* draft_tokens, const int32_t* verify_len, sv_sampling_t sp,
+                              uint64_t seed, const void* q_rows, int32_t* accept_len, int32_t* out_tokens,
+                              int32_t* num_emitted, int32_t* row_status, void* ws, size_t ws_bytes,
+                              sv_stream_t stream)
+{
+    if (!q_rows || K < 1) return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_rows) & 15u) != 0u) return SV_ERR_INVALID_ARG;
+    return run_verify(0, target_logits, draft_logits, dt, n_req, K, vocab, 0, nullptr, verify_len, draft_tokens, sp,
+                      seed, accept_len, out_tokens, num_emitted, row_status, ws, ws_bytes, stream, 0,
+                      static_cast<const RowInfo*>(q_rows));
 }
 
 sv_status_t sv_estimator_observe(double* state, const float* x, const int32_t* accept_len, const int32_t* num_emitted,

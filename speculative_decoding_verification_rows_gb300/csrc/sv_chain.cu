@@ -141,7 +141,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 else if (err & kBadParam) err = kBadParam;
             }
             if (!err) {
-                const int n_rows = a.layout == 2 ? 1 : (v + 1) + (greedy ? 0 : v);
+                // target rows 0..v, and draft rows 0..v-1 of a sampling request
+                // unless their results were made beforehand (q_rows)
+                const int n_rows = a.layout == 2 ? 1 : (v + 1) + ((greedy || a.q_rows) ? 0 : v);
                 if (fast) nf = n_rows; else ns = n_rows;
             }
         }
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
         int q_status = 0, q_list = 0;
         double q = 0.0;
         if (j < K) {
-            const RowInfo& Q = a.info[slot_draft(r, K, j)];
+            const RowInfo& Q = draft_info(a, r, j);
             q_status = Q.desc.status;
             q = Q.p_token;
             q_list = Q.n_list;
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
             a.blk_w[(size_t)r * width] = 1.0;
             for (int j = 1; j <= v; ++j) {
                 const double p = a.info[slot_target(r, K, j - 1)].p_token;
-                const double q = a.info[slot_draft(r, K, j - 1)].p_token;
+                const double q = draft_info(a, r, j - 1).p_token;
                 const double ratio = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
                 const double x = w > 0.0 ? w * ratio : 0.0;
                 w = x < 1.0 ? x : 1.0;
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
             s_wgt[warp][0] = 1.0;
             for (int j = 1; j <= v; ++j) {
                 const double p = a.info[slot_target(r, K, j - 1)].p_token;
-                const double q = a.info[slot_draft(r, K, j - 1)].p_token;
+                const double q = draft_info(a, r, j - 1).p_token;
                 const double ratio = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
                 const double x = w > 0.0 ? w * ratio : 0.0;
                 w = x < 1.0 ? x : 1.0;
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
             double h = wj;
             if (j < v) {
                 const RowInfo& Pj = a.info[slot_target(r, K, j)];
-                const RowInfo& Qj = a.info[slot_draft(r, K, j)];
+                const RowInfo& Qj = draft_info(a, r, j);
                 const int np = Pj.n_list, nq = Qj.n_list;
                 const bool in = lane < np;
                 const int x = in ? Pj.list_idx[lane] : 0;
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
         const double px = in ? P.list_p[lane] : 0.0;
         double w = px;
         if (residual) {
-            const RowInfo& Q = a.info[slot_draft(r, K, acc_len)];
+            const RowInfo& Q = draft_info(a, r, acc_len);
             const int nq = Q.n_list;
             if (lane < nq) {
                 s_qi[warp][lane] = Q.list_idx[lane];

@@ -525,12 +525,20 @@ struct ChainArgs {
     RowInfo* info;
     ReqState* req;
     int32_t* req_done;   // rows of each request finished by the one-pass kernel (zeroed by prep)
+    const RowInfo* q_rows;   // draft rows' results made beforehand ([n_req][K], sv_estimator_predict_q), or NULL
     ResampleJob* jobs;
     TileSums* tiles;   // [max_jobs][resample_tiles(vocab)]
     double* blk_w;     // block verification: [n_req][K + 1] weights w_j
     unsigned long long* blk_h;   // block verification: [n_req][K + 1] residual sums H_j (2^-62 units)
     int num_sms;
 };
+
+// The result of draft row j of request r: the verify's own (a row slot), or
+// one made beforehand for the same rows and parameters.
+__device__ __forceinline__ const RowInfo& draft_info(const ChainArgs& a, int r, int j)
+{
+    return a.q_rows ? a.q_rows[(size_t)r * a.K + j] : a.info[slot_draft(r, a.K, j)];
+}
 
 struct RowsArgs {
     const void* tgt;

@@ -11,7 +11,10 @@
 // One CTA: survivals in fp32 left to right per request, a 64-bit rank key
 // (survival bits, then position ascending, then request ascending -- every
 // key distinct), a byte-wise radix select of the N_sel-th largest key, and a
-// count per request.  Survival never grows along a request and the tie-break
+// count per request.  The keys live in shared memory when they fit (12,288 of
+// them), else in the workspace; the select stops at the first digit whose
+// keys are all selected (every key of the chosen prefix is then >= the
+// prefix with zeros below).  Survival never grows along a request and the tie-break
 // prefers earlier positions, so each request's selection is a prefix and its
 // count is its verify length.  No device-to-host readback anywhere.
 #include "sv_internal.cuh"
@@ -20,6 +23,7 @@ namespace sv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemKeys = 12288;   // rank keys held in shared memory (96 KB)
 
 __device__ __forceinline__ unsigned long long rank_key(float s, int i, int r)
 {
@@ -27,15 +31,18 @@ __device__ __forceinline__ unsigned long long rank_key(float s, int i, int r)
            (unsigned long long)(0xFFFFFu - (uint32_t)r);
 }
 
+template <bool SMEM>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, int ld, const int32_t* draft_len, int n,
                                                              int K, int budget_arg, const int32_t* budget_dev,
                                                              int32_t* verify_lens, int32_t* qo, int32_t* total,
-                                                             int32_t* status, unsigned long long* keys)
+                                                             int32_t* status, unsigned long long* keys_ws)
 {
+    extern __shared__ unsigned long long s_keys[];
+    unsigned long long* keys = SMEM ? s_keys : keys_ws;
     pdl_enter();
     const int budget = budget_dev ? *budget_dev : budget_arg;   // chosen on the device, or given
     __shared__ uint32_t hist[256];
-    __shared__ int s_digit, s_kk, s_any_bad;
+    __shared__ int s_digit, s_kk, s_any_bad, s_done;
     __shared__ long long s_ncand;
     __shared__ int s_warp[33];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -78,6 +85,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
         unsigned long long prefix = 0ull, mask = 0ull;
         int kk = (int)nsel;
         for (int digit = 0; digit < 8; ++digit) {   // 8-bit digits, most significant first
+            if (tid == 0) s_done = 0;
             const int shift = 56 - 8 * digit;
             for (int b = tid; b < 256; b += kPlanThreads) hist[b] = 0u;
             __syncthreads();
@@ -105,6 +113,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
                         if (excl + cnt[i] >= (uint32_t)kk) {
                             s_digit = 255 - 8 * lane - i;
                             s_kk = kk - (int)excl;
+                            s_done = excl + cnt[i] == (uint32_t)kk;   // every key of this digit is selected
                             break;
                         }
                         excl += cnt[i];
@@ -115,7 +124,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
             prefix |= (unsigned long long)s_digit << shift;
             mask |= 255ull << shift;
             kk = s_kk;
+            const int done = s_done;
             __syncthreads();
+            if (done) break;
         }
         kth = prefix;
     }
@@ -384,8 +395,23 @@ cudaError_t launch_plan(const float* conf, int ld, const int32_t* draft_len, int
                         const int32_t* budget_dev, int32_t* verify_lens, int32_t* qo_indptr, int32_t* total,
                         int32_t* status, unsigned long long* keys, cudaStream_t s)
 {
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, conf, ld, draft_len, n, K, budget, budget_dev,
-                      verify_lens, qo_indptr, total, status, keys);
+    if ((long long)n * K <= kPlanSmemKeys) {
+        static int attr_set[128] = {0};   // once per device, before any graph capture
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int& done = attr_set[(dev >= 0 && dev < 128) ? dev : 0];
+        if (!done) {
+            const cudaError_t e = cudaFuncSetAttribute(plan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)(kPlanSmemKeys * sizeof(unsigned long long)));
+            if (e != cudaSuccess) return e;
+            done = 1;
+        }
+        const size_t smem = sizeof(unsigned long long) * (size_t)(n * K > 0 ? n * K : 1);
+        return launch_pdl(plan_kernel<true>, dim3(1), dim3(kPlanThreads), smem, s, conf, ld, draft_len, n, K, budget,
+                          budget_dev, verify_lens, qo_indptr, total, status, keys);
+    }
+    return launch_pdl(plan_kernel<false>, dim3(1), dim3(kPlanThreads), 0, s, conf, ld, draft_len, n, K, budget,
+                      budget_dev, verify_lens, qo_indptr, total, status, keys);
 }
 
 cudaError_t launch_budget(const float* conf, int ld, const int32_t* draft_len, int n, int K, const int32_t* cost_tokens,

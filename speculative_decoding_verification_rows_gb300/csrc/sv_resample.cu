@@ -131,7 +131,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
 {
     const int r = job.req, pa = job.a, K = a.K;
     const RowInfo& IP = a.info[slot_target(r, K, pa)];
-    const RowInfo& IQ = a.info[slot_draft(r, K, pa)];
+    const RowInfo& IQ = draft_info(a, r, pa);
     const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (K + 1) + pa;
     P.row = (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
     P.m = IP.desc.max_logit;

@@ -57,7 +57,7 @@ __device__ __noinline__ void chain_walk(const ChainArgs& a, int r, double* q_p, 
         int q_status = 0;
         double q = 0.0;
         if (j < K) {
-            const RowInfo& Q = a.info[slot_draft(r, K, j)];
+            const RowInfo& Q = draft_info(a, r, j);
             q_status = __ldcg(&Q.desc.status);
             q = __ldcg(&Q.p_token);
         }
@@ -114,7 +114,7 @@ __device__ __noinline__ void chain_walk(const ChainArgs& a, int r, double* q_p, 
     } else {
         const bool residual = acc_len < v;
         const int np = __ldcg(&P.n_list);
-        const RowInfo* Qp = residual ? &a.info[slot_draft(r, K, acc_len)] : nullptr;
+        const RowInfo* Qp = residual ? &draft_info(a, r, acc_len) : nullptr;
         const int nq = residual ? __ldcg(&Qp->n_list) : 0;
         if (np >= 0 && nq >= 0) {
             const bool in = lane < np;

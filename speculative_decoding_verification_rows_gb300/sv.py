@@ -31,7 +31,7 @@ EXPORTED = ("sv_workspace_size", "sv_workspace_size_block", "sv_status_string", 
             "sv_set_hist_timing_events", "sv_verify_chain_noalloc", "sv_plan_budget_cost", "sv_verify_stats",
             "sv_verify_block", "sv_estimator_state_bytes", "sv_estimator_init", "sv_estimator_predict",
             "sv_estimator_observe", "sv_shard_record_bytes", "sv_verify_chain_shard_rows",
-            "sv_verify_chain_shard_merge")
+            "sv_verify_chain_shard_merge", "sv_q_rows_bytes", "sv_estimator_predict_q", "sv_verify_chain_q")
 
 
 class SVError(RuntimeError):
@@ -103,6 +103,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.sv_estimator_predict.restype = I
     L.sv_estimator_observe.argtypes = [P, P, P, P, P, I, I, I, P]
     L.sv_estimator_observe.restype = I
+    L.sv_q_rows_bytes.argtypes = [I, I]
+    L.sv_q_rows_bytes.restype = SZ
+    L.sv_estimator_predict_q.argtypes = [P, I, I, I, I, Sampling, P, P, P, P, P, P, SZ, P]
+    L.sv_estimator_predict_q.restype = I
+    L.sv_verify_chain_q.argtypes = [P, P, I, I, I, I, P, P, Sampling, U64, P, P, P, P, P, P, SZ, P]
+    L.sv_verify_chain_q.restype = I
     L.sv_shard_record_bytes.argtypes = []
     L.sv_shard_record_bytes.restype = SZ
     L.sv_verify_chain_shard_rows.argtypes = [P, P, I, I, I, I, I, I, P, P, Sampling, P, P, SZ, P]
@@ -305,6 +311,28 @@ class Estimator:
                                            _ptr(w), w.numel(), _stream(dev)))
         return x, p
 
+    def predict_q(self, draft: torch.Tensor, draft_tokens: torch.Tensor, temperature: torch.Tensor,
+                  top_k: Optional[torch.Tensor] = None, top_p: Optional[torch.Tensor] = None,
+                  q_rows: Optional[torch.Tensor] = None):
+        """sv_estimator_predict_q: (x, p, q_rows) -- q_rows (uint8 on the device) carries every draft
+        row's distribution for verify_chain_q over the same batch."""
+        draft = _dev(draft)
+        n, K, V = draft.shape
+        assert K == self.K
+        dev = draft.device
+        x = torch.empty((n, K), dtype=torch.float32, device=dev)
+        p = torch.empty((n, K), dtype=torch.float32, device=dev)
+        nbytes = int(load().sv_q_rows_bytes(n, K))
+        if q_rows is None:
+            q_rows = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        assert q_rows.numel() >= nbytes and q_rows.is_cuda
+        w = _ws(self.ws, dev, workspace_size(n * K, 0, V))
+        _check(load().sv_estimator_predict_q(_ptr(draft), _dtype_code(draft), n, K, V,
+                                             _sampling(temperature, top_k, top_p), _ptr(self.state),
+                                             _ptr(_dev(draft_tokens, torch.int32)), _ptr(x), _ptr(p), _ptr(q_rows),
+                                             _ptr(w), w.numel(), _stream(dev)))
+        return x, p, q_rows
+
     def observe(self, x: torch.Tensor, accept_len: torch.Tensor, num_emitted: torch.Tensor,
                 verify_lens: Optional[torch.Tensor] = None, refit_every: int = 100):
         x = _dev(x, torch.float32)
@@ -468,4 +496,27 @@ def verify_chain_shard_merge(records: torch.Tensor, n_shards: int, draft_tokens:
                                               _ptr(verify_len), _sampling(temperature, top_k, top_p), seed,
                                               _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted),
                                               _ptr(o.row_status), _ptr(w), w.numel(), _stream(dev)))
+    return o
+
+
+def verify_chain_q(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                   temperature: torch.Tensor, top_k: Optional[torch.Tensor], top_p: Optional[torch.Tensor],
+                   q_rows: torch.Tensor, verify_len: Optional[torch.Tensor] = None, seed: int = 0,
+                   ws: Optional[Workspace] = None, out: Optional[VerifyOut] = None,
+                   small_topk: bool = False) -> VerifyOut:
+    """sv_verify_chain_q: sv_verify_chain with the draft rows' distributions from Estimator.predict_q."""
+    target = _dev(target)
+    n, k1, V = target.shape
+    K = k1 - 1
+    dev = target.device
+    if draft is not None:
+        _dev(draft, target.dtype)
+        assert draft.shape == (n, K, V)
+    o = out or _outs(n, K, dev)
+    w = _ws(ws, dev, workspace_size(n, K, V))
+    _check(load().sv_verify_chain_q(_ptr(target), _ptr(draft), _dtype_code(target), n, K, V, _ptr(draft_tokens),
+                                    _ptr(verify_len), _sampling(temperature, top_k, top_p, small_topk), seed,
+                                    _ptr(_dev(q_rows)),
+                                    _ptr(o.accept_len), _ptr(o.out_tokens), _ptr(o.num_emitted), _ptr(o.row_status),
+                                    _ptr(w), w.numel(), _stream(dev)))
     return o

@@ -11,6 +11,7 @@ import torch
 import oracle
 from speculative_decoding_verification_rows_gb300 import build as sv_build
 from speculative_decoding_verification_rows_gb300 import sv, workloads
+from tests.compare import compare_verify
 from tests.conftest import np_logits
 
 pytestmark = pytest.mark.gpu
@@ -109,3 +110,36 @@ def test_refit_on_gpu_reaches_the_generating_slope():
         g.observe(torch.from_numpy(x).to(DEV), torch.from_numpy(acc).to(DEV), torch.from_numpy(acc + 1).to(DEV))
     slope = g.state[0].item()
     assert 0.85 < slope < 1.15, slope
+
+
+@pytest.mark.parametrize("name,scale", [("tiny", None), ("large", dict(n=6)), ("medium", dict(n=4, V=30000))])
+def test_predict_q_then_verify_q_equals_predict_then_verify(name, scale):
+    # the draft rows' results made by predict_q serve the verify that follows: the same features
+    # and predictions as predict, the same outputs as sv_verify_chain on the whole batch
+    w = workloads.make(name, device=DEV, scale=scale)
+    est_a, est_b = sv.Estimator(w.K, DEV), sv.Estimator(w.K, DEV)
+    x0, p0 = est_a.predict(w.draft, w.temperature, w.top_k, w.top_p)
+    x1, p1, q_rows = est_b.predict_q(w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p)
+    ref = sv.verify_chain(w.target, w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p, seed=3)
+    got = sv.verify_chain_q(w.target, w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p, q_rows, seed=3)
+    torch.cuda.synchronize()
+    # bit for bit (NaN where a feature has no value, e.g. fp32 rows a greedy request reads at T = 1
+    # over the whole vocabulary)
+    torch.testing.assert_close(x1, x0, rtol=0, atol=0, equal_nan=True)
+    torch.testing.assert_close(p1, p0, rtol=0, atol=0, equal_nan=True)
+    for f in ("accept_len", "out_tokens", "num_emitted", "row_status"):
+        assert torch.equal(getattr(got, f), getattr(ref, f)), f
+
+
+def test_verify_q_with_windows_matches_the_oracle():
+    w = workloads.random_case(5, 7, 4, 4099, device=DEV, mode="mixed")
+    vl = torch.tensor([4, 0, 2, 3, 1, 4, 4], dtype=torch.int32, device=DEV)
+    est = sv.Estimator(w.K, DEV)
+    _, _, q_rows = est.predict_q(w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p)
+    g = sv.verify_chain_q(w.target, w.draft, w.draft_tokens, w.temperature, w.top_k, w.top_p, q_rows,
+                          verify_len=vl, seed=9)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain(np_logits(w.target), np_logits(w.draft), w.draft_tokens.cpu().numpy(),
+                            w.temperature.cpu().numpy(), w.top_k.cpu().numpy(), w.top_p.cpu().numpy(),
+                            verify_len=vl.cpu().numpy(), seed=9)
+    compare_verify(o, g, w.draft_tokens.cpu().numpy(), vl.cpu().numpy(), w.V)
