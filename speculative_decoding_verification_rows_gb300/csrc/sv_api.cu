@@ -115,6 +115,9 @@ Carved carve(void* ws, int n_req, int k_max, int vocab, int dtype, const void* t
     ca.info = ra.info;
     ca.req = at<ReqState>(ws, L.req);
     ca.req_done = at<int32_t>(ws, L.req_done);
+    ca.pair_done = at<int32_t>(ws, L.pair_done);
+    ca.slow_req = at<int2>(ws, L.slow_req);
+    ca.slow_units = at<int2>(ws, L.slow_units);
     ca.jobs = at<ResampleJob>(ws, L.jobs);
     ca.tiles = at<TileSums>(ws, L.tiles);
     ca.blk_w = block ? at<double>(ws, L.blk) : nullptr;
@@ -161,6 +164,9 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     // neither the chain kernel nor the full-row resample has work.
     const bool small_topk = (sp.flags & SV_SAMPLING_SMALL_TOPK) != 0;
     ca.fuse = block ? 0 : 1;
+    ca.lazy = block ? 0 : 1;   // chain verify: rows past a known rejection need only their status
+    ca.lazy_grid = ca.lazy ? hist_wide_grid(ca.num_sms) : 0;
+    if (ca.lazy && ca.lazy_grid < 1) return SV_ERR_CUDA;
     c.ra.chain = ca;
     if (launch_prep(ca, s) != cudaSuccess) return SV_ERR_CUDA;
     sv_status_t st = run_rows(c.ra, s, small_topk);

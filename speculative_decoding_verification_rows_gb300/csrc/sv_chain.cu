@@ -93,6 +93,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
     __shared__ unsigned long long s_tokbad[kPrepThreads];
     int base_fast = 0, base_slow = 0;
     const int n_units = a.n_req;   // requests, or rows for the plain row layout
+    // histogram rows of chain verification: their requests, and the rows of
+    // each position over all of them (counted here, listed after the loop)
+    __shared__ int s_nsr;
+    __shared__ int s_pos[kMaxK + 1];
+    const int kinds = a.q_rows ? 1 : 2;   // histogram rows per verified position
+    if (threadIdx.x == 0) s_nsr = 0;
+    for (int j = threadIdx.x; j <= kMaxK; j += kPrepThreads) s_pos[j] = 0;
+    __syncthreads();
     const int K = a.K;
     const int W2 = a.layout == 2 ? 1 : 2 * K + 1;   // row slots per unit
     for (int u0 = 0; u0 < n_units; u0 += kPrepThreads) {
@@ -238,7 +246,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 st.err = err;
                 st.fast = (a.fuse && fast && !err) ? 1 : 0;
                 st.tok_bad = tok_bad;
+                st.first_reject = v;
+                const bool slow = !err && !fast;
+                st.slow_base = slow ? s_u[threadIdx.x].pos : -1;
                 a.req[u] = st;
+                if (slow && a.lazy) {   // the histogram path takes its rows position by position
+                    a.slow_req[atomicAdd(&s_nsr, 1)] = make_int2((u << 6) | v, st.slow_base);
+                    for (int j = 0; j <= v; ++j) {
+                        a.pair_done[(size_t)u * (K + 1) + j] = 0;
+                        atomicAdd(&s_pos[j], j < v ? kinds : 1);
+                    }
+                }
                 a.req_done[u] = 0;
                 if (err && a.accept_len) {   // no rows were listed: the outputs of a failed request
                     const int width = K + 1;
@@ -255,13 +273,45 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         base_slow += s_tot_b;
         __syncthreads();
     }
+    if (a.lazy) {
+        // The histogram rows of chain verification in position order (all
+        // requests' rows of position 0, then of position 1, ...), target row
+        // before draft row; the order among requests is immaterial.
+        const int K1 = K + 1, nsr = s_nsr;
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int j = 0; j < K1; ++j) {
+                const int c = s_pos[j];
+                s_pos[j] = run;
+                run += c;
+            }
+            a.counters->n_units = run;
+            a.counters->n_slow_req = nsr;
+        }
+        __syncthreads();
+        // rows that fit in one wave of the histogram kernel are taken one per
+        // CTA in task order: no list
+        const int n_list = a.counters->n_units > a.lazy_grid ? nsr : 0;
+        for (int i = threadIdx.x; i < n_list; i += kPrepThreads) {
+            const int2 e = a.slow_req[i];
+            const int r = e.x >> 6, v = e.x & 63;
+            for (int j = 0; j <= v; ++j) {
+                const int nk = j < v ? kinds : 1;
+                const int at = atomicAdd(&s_pos[j], nk);
+                a.slow_units[at] = make_int2((r << 7) | (j << 1), e.y + j);
+                if (nk == 2) a.slow_units[at + 1] = make_int2((r << 7) | (j << 1) | 1, e.y + v + 1 + j);
+            }
+        }
+    }
     if (threadIdx.x == 0) {
+        if (!a.lazy) a.counters->n_units = 0;
         a.counters->n_fast = base_fast;
         a.counters->n_slow = base_slow;
         a.counters->n_jobs = 0;
         a.counters->timeout = 0;
         a.counters->n_ovf = 0;
         a.counters->n_jobs2 = 0;
+        a.counters->next_slow = 0;
     }
 }
 

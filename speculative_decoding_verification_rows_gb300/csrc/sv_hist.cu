@@ -909,7 +909,8 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t x, uint32_t y)
     return r;
 }
 
-__device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, int t)
+// Returns true when the row went to the cluster kernel (no record written here).
+__device__ bool wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, int t)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
@@ -1182,6 +1183,90 @@ __device__ void wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
         }
     }
     __syncthreads();
+    return ovf;
+}
+
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t x, uint32_t y)
+{
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+
+// A row whose acceptance test can no longer matter (it lies past a position
+// its request is known to reject): one streaming pass for what the row's
+// status needs (largest and smallest order key: NaN, +inf, every element
+// -inf), and a record with that status and no distribution (p_token NaN).
+__device__ __noinline__ void scan_row(WideSmem& sm, const RowsArgs& a, const RowTask& task)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t stride = task.is_draft ? a.stride_d : a.stride_t;
+    const uint16_t* row = (const uint16_t*)(task.is_draft ? a.drf : a.tgt) + (size_t)task.row * (size_t)stride;
+    const int V = a.vocab;
+    // both keys of a word side by side: hi = max, lo = min (each u16x2)
+    uint32_t hi = 0u, lo = 0xFFFFFFFFu;
+    const int head = min(V, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 1));
+    const int nvec = (V - head) >> 3;
+    const int tail0 = head + 8 * nvec;
+    if (tid < head) {
+        const uint32_t k = key_raw16(row[tid]);
+        hi = max_u16x2(hi, k);
+        lo = min_u16x2(lo, k | 0xFFFF0000u);
+    }
+    if (tail0 + tid < V) {
+        const uint32_t k = key_raw16(row[tail0 + tid]);
+        hi = max_u16x2(hi, k);
+        lo = min_u16x2(lo, k | 0xFFFF0000u);
+    }
+    const uint4* vp = reinterpret_cast<const uint4*>(row + head);
+    for (int v0 = tid; v0 < nvec; v0 += kWideThreads * kWideUnroll) {
+        uint4 x[kWideUnroll];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            const int vi = v0 + u * kWideThreads;
+            x[u] = vi < nvec ? __ldcs(vp + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            if (v0 + u * kWideThreads < nvec) {
+                const uint32_t k0 = keys2_raw(x[u].x), k1 = keys2_raw(x[u].y), k2 = keys2_raw(x[u].z),
+                               k3 = keys2_raw(x[u].w);
+                hi = max_u16x2(hi, max_u16x2(max_u16x2(k0, k1), max_u16x2(k2, k3)));
+                lo = min_u16x2(lo, min_u16x2(min_u16x2(k0, k1), min_u16x2(k2, k3)));
+            }
+        }
+    }
+    uint32_t kmax = max(hi & 0xFFFFu, hi >> 16), kmin = min(lo & 0xFFFFu, lo >> 16);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    if (lane == 0) {
+        sm.redi[warp] = (int)kmax;
+        sm.red64[warp] = kmin;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 0; w < kWideThreads / 32; ++w) {
+            kmax = max(kmax, (uint32_t)sm.redi[w]);
+            kmin = min(kmin, (uint32_t)sm.red64[w]);
+        }
+        // -0 and +0 order as one value; only the thresholds below matter
+        const int status = (kmax >= 0xFF80u || kmin < 0x007Fu) ? kNonfinite : (kmax == 0x007Fu ? kEmpty : 0);
+        write_error_row(a.info + task.slot, key_value(kmax == 0x7FFFu ? 0x8000u : kmax), -1, status, task.temp);
+    }
+    __syncthreads();
+}
+
+// Both rows of position j of request r are done (lazy chain verify): the
+// acceptance test the chain walk will make at j, made now; a rejection
+// lowers the request's known first rejection.  Thread 0 only.
+__device__ __noinline__ void decide_position(const RowsArgs& a, int r, int j)
+{
+    const ChainArgs& c = a.chain;
+    const double p = __ldcg(&a.info[slot_target(r, c.K, j)].p_token);
+    const double q = __ldcg(&draft_info(c, r, j).p_token);
+    const double u = uniform_f64(c.seed, (uint32_t)r, (uint32_t)j, 0u);
+    const bool accept = q > 0.0 ? u * q < p : p > 0.0;
+    if (!accept) atomicMin(&c.req[r].first_reject, j);
 }
 
 __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(RowsArgs a)
@@ -1201,8 +1286,62 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
         sm.ovf = 0;
     }
     __syncthreads();
-    const int n_tasks = a.counters->n_slow;
-    for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) wide_row(sm, a, a.slow_tasks.get(t), t);
+    if (!a.chain.lazy) {
+        const int n_tasks = a.counters->n_slow;
+        for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) wide_row(sm, a, a.slow_tasks.get(t), t);
+        return;
+    }
+    // Chain verify.  When the rows all fit in one wave, each CTA takes one (in
+    // task order).  Otherwise they are listed position by position across the
+    // requests (slow_units: every request's rows of position 0, then of
+    // position 1, ...) and the CTAs take them in that order, so the tests of the early positions are
+    // decided while the later rows still wait; a row past its request's known
+    // first rejection cannot change the outcome (the walk stops at the first
+    // rejection, which is never above the known one) and gets the status scan
+    // only.
+    __shared__ int s_unit[4];
+    const ChainArgs& c = a.chain;
+    const int U = a.counters->n_units, K1 = c.K + 1;
+    const int kinds = c.q_rows ? 1 : 2;   // rows per position (the draft's results may exist already)
+    enum { kNone = 0, kFull = 1, kScan = 2 };
+    if (U <= (int)gridDim.x) {   // no test is decided early then: no CTA would wait for one
+        if ((int)blockIdx.x < U) wide_row(sm, a, a.slow_tasks.get(blockIdx.x), blockIdx.x);
+        return;
+    }
+    for (;;) {
+        if (tid == 0) {
+            int mode = kNone, t = -1, r = 0, j = 0;
+            const int u = atomicAdd(&a.counters->next_slow, 1);
+            if (u < U) {
+                const int2 e = __ldcg(&c.slow_units[u]);
+                r = e.x >> 7;
+                j = (e.x >> 1) & 63;
+                t = e.y;
+                mode = j > __ldcg(&c.req[r].first_reject) ? kScan : kFull;
+            }
+            s_unit[0] = mode;
+            s_unit[1] = t;
+            s_unit[2] = r;
+            s_unit[3] = j;
+        }
+        __syncthreads();
+        const int mode = s_unit[0], t = s_unit[1], r = s_unit[2], j = s_unit[3];
+        __syncthreads();   // s_unit is rewritten only after every thread has read it
+        if (mode == kNone) break;
+        const RowTask task = a.slow_tasks.get(t);
+        if (mode == kScan) {
+            scan_row(sm, a, task);
+            continue;
+        }
+        const bool ovf = wide_row(sm, a, task, t);
+        if (tid == 0 && !ovf && j < c.req[r].v) {   // a handed-on row decides nothing
+            __threadfence();
+            if (atomicAdd(&c.pair_done[(size_t)r * K1 + j], 1) == kinds - 1) {
+                __threadfence();
+                decide_position(a, r, j);
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -1210,6 +1349,25 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
 // Every histogram row goes to the one-CTA kernel; the rows it hands on (more
 // occupied binades than it has counters for) go to the cluster kernel, which
 // finds their number on the device.
+int hist_wide_grid(int num_sms)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static int wide_blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
+    int& nb = wide_blocks[(dev >= 0 && dev < 128) ? dev : 0];
+    if (nb == 0) {
+        const size_t smem = sizeof(WideSmem);
+        if (cudaFuncSetAttribute(wide_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return 0;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_rows_kernel, kWideThreads, smem) != cudaSuccess)
+            return 0;
+        nb = n < 1 ? 1 : n;
+    }
+    return num_sms * nb;
+}
+
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s)
 {
     int dev = 0;
@@ -1217,17 +1375,9 @@ cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s)
     const int di = (dev >= 0 && dev < 128) ? dev : 0;
     cudaError_t err = cudaSuccess;
     {
-        static int wide_blocks[128] = {0};   // CTAs per SM, once per device (before any graph capture)
-        const size_t smem = sizeof(WideSmem);
-        int& nb = wide_blocks[di];
-        if (nb == 0) {
-            err = cudaFuncSetAttribute(wide_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err != cudaSuccess) return err;
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, wide_rows_kernel, kWideThreads, smem);
-            if (err != cudaSuccess) return err;
-            if (nb < 1) nb = 1;
-        }
-        err = launch_pdl(wide_rows_kernel, dim3(a.num_sms * nb), dim3(kWideThreads), smem, s, a);
+        const int grid = hist_wide_grid(a.num_sms);
+        if (grid < 1) return cudaErrorUnknown;
+        err = launch_pdl(wide_rows_kernel, dim3(grid), dim3(kWideThreads), sizeof(WideSmem), s, a);
         if (err != cudaSuccess) return err;
     }
     int C = (a.vocab + kHistMaxSlice - 1) / kHistMaxSlice;

@@ -114,6 +114,8 @@ struct ReqState {
     int32_t err;      // request-level error bits (params, layout)
     int32_t fast;     // 1: its rows took the one-pass kernel, which also ran its chain
     uint64_t tok_bad; // bit j: draft token j out of range
+    int32_t first_reject;   // histogram path, chain verify: lowest position whose test is known to reject (v: none yet)
+    int32_t slow_base;      // index of its first row in the histogram-path task list (-1: none)
 };
 
 constexpr int kMaxK = 63;           // drafted positions per request (bit masks above)
@@ -177,12 +179,16 @@ struct Counters {
     int32_t timeout;   // set by a row kernel whose bounded wait gave up
     int32_t n_ovf;     // histogram rows handed from the one-CTA kernel to the cluster kernel
     int32_t n_jobs2;   // block verification: jobs listed after the residual sums (from index n_jobs)
-    int32_t pad[10];
+    int32_t next_slow; // histogram path, chain verify: next row of slow_units to hand out
+    int32_t n_slow_req;// requests whose rows take the histogram path (listed in slow_req)
+    int32_t n_units;   // histogram path, chain verify: rows listed in slow_units
+    int32_t pad[7];
 };
 
 // Carving of the caller's workspace.
 struct WsLayout {
-    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, req_done, jobs, tiles, blk, total;
+    size_t counters, fast_tasks, slow_tasks, ovf, info, partials, row_sync, req, req_done, pair_done, slow_req,
+        slow_units, jobs, tiles, blk, total;
     int slots, max_tasks, max_jobs;
     size_t n_partials;
 };
@@ -210,6 +216,9 @@ inline WsLayout ws_layout(int n_req, int k_max, int vocab, int block = 0)
     L.row_sync = off;   off = align256(off + sizeof(RowSync) * (size_t)L.max_tasks);
     L.req = off;        off = align256(off + sizeof(ReqState) * (size_t)n_req);
     L.req_done = off;   off = align256(off + sizeof(int32_t) * (size_t)n_req);
+    L.pair_done = off;  off = align256(off + sizeof(int32_t) * (size_t)n_req * (size_t)(k_max + 1));
+    L.slow_req = off;   off = align256(off + sizeof(int2) * (size_t)n_req);
+    L.slow_units = off; off = align256(off + sizeof(int2) * (size_t)L.max_tasks);
     L.max_jobs = block ? n_req * (k_max + 1) : n_req;
     L.jobs = off;       off = align256(off + sizeof(ResampleJob) * (size_t)L.max_jobs);
     L.tiles = off;      off = align256(off + sizeof(TileSums) * (size_t)L.max_jobs * (size_t)resample_tiles(vocab));
@@ -500,6 +509,8 @@ struct ChainArgs {
     int block;             // 1: block verification instead of the token-by-token chain
     int est;               // 1: estimator features (layout 2, greedy requests at T = 1)
     int fuse;              // 1: the one-pass kernel runs the chain of each request whose rows it took
+    int lazy;              // 1: histogram rows past a request's known first rejection get a validity scan only
+    int lazy_grid;         // CTAs of the histogram kernel: rows that fit in one wave are not listed by position
     int shard;             // vocabulary-sharded verify (listed kept sets only): 1 a shard's rows
                            // (no outputs), 2 the merge of the shards' records (no logits)
     int rows_per_req;      // layout 2 without row_to_req: request = row / rows_per_req
@@ -526,6 +537,10 @@ struct ChainArgs {
     ReqState* req;
     int32_t* req_done;   // rows of each request finished by the one-pass kernel (zeroed by prep)
     const RowInfo* q_rows;   // draft rows' results made beforehand ([n_req][K], sv_estimator_predict_q), or NULL
+    int32_t* pair_done;  // [n_req][K + 1]: rows of position j finished on the histogram path (lazy)
+    int2* slow_req;      // requests whose rows take the histogram path (lazy), n_slow_req of them:
+                         // {request << 6 | v, index of its first task}
+    int2* slow_units;    // their rows in position order (lazy): {request << 7 | position << 1 | draft, task}
     ResampleJob* jobs;
     TileSums* tiles;   // [max_jobs][resample_tiles(vocab)]
     double* blk_w;     // block verification: [n_req][K + 1] weights w_j
@@ -563,6 +578,8 @@ struct RowsArgs {
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_shard_merge(const RowsArgs& a, const void* records, int n_shards, int slots, cudaStream_t s);
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
+// CTAs of the one-CTA histogram kernel's grid on the current device (0 on error).
+int hist_wide_grid(int num_sms);
 
 
 

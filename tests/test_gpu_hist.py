@@ -191,3 +191,77 @@ def test_verify_with_handed_on_rows_in_the_batch():
     o = oracle.verify_chain(np_logits(w2.target), np_logits(w2.draft), w2.draft_tokens.cpu().numpy(),
                             w2.temperature.cpu().numpy(), w2.top_k.cpu().numpy(), w2.top_p.cpu().numpy(), seed=4)
     compare_verify(o, g, w2.draft_tokens.cpu().numpy(), np.full(w2.n, w2.K), w2.V)
+
+
+def test_rows_past_a_known_rejection_keep_their_status():
+    # Every request rejects at position 0 (its first draft token has target
+    # logit -inf, so p = 0), and the rows outnumber one wave of CTAs: rows of
+    # later positions taken after that test is decided get the status scan
+    # only.  Non-finite and all -inf rows planted there must still fail
+    # their requests exactly as the oracle says, and the others must draw
+    # their token from the residual of the full rows at position 0.
+    rng = np.random.default_rng(7)
+    n, K, V = 384, 6, 4_096
+    x = rng.normal(0, 3, (n, K + 1, V)).astype(np.float32)
+    y = (0.8 * x[:, :K] + 0.6 * rng.normal(0, 3, (n, K, V))).astype(np.float32)
+    toks = rng.integers(0, V, (n, K)).astype(np.int32)
+    x[np.arange(n), 0, toks[:, 0]] = -np.inf
+    tbits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    dbits = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    planted = {}
+    for r in range(0, n, 7):
+        j = int(rng.integers(2, K + 1))
+        kind = r // 7 % 5
+        bits = tbits if kind < 4 or j == K else dbits
+        if kind == 0:
+            bits[r, j, 5] = 0x7FC0        # NaN
+        elif kind == 1:
+            bits[r, j, 6] = 0xFFC1        # NaN with the sign bit set
+        elif kind == 2:
+            bits[r, j, V - 1] = 0x7F80    # +inf
+        elif kind == 3:
+            bits[r, j, :] = 0xFF80        # all -inf
+        else:
+            bits[r, j, 9] = 0x7FC0        # NaN in the draft row (the target row where j = K)
+        planted[r] = j
+    tgt = _bits_to_bf16(tbits).reshape(n, K + 1, V)
+    drf = _bits_to_bf16(dbits).reshape(n, K, V)
+    T = np.where(np.arange(n) % 3 == 0, 0.7, 1.0).astype(np.float32)
+    tp = np.where(np.arange(n) % 2 == 0, 0.9, 1.0).astype(np.float32)
+    tk = np.zeros(n, np.int32)
+    g = sv.verify_chain(tgt.to(DEV), drf.to(DEV), torch.from_numpy(toks).to(DEV), torch.from_numpy(T).to(DEV),
+                        torch.from_numpy(tk).to(DEV), torch.from_numpy(tp).to(DEV), seed=11)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain(np_logits(tgt), np_logits(drf), toks, T, tk, tp, seed=11)
+    assert (o["accept_len"] == 0).all()
+    failed = o["num_emitted"] == 0
+    assert failed[list(planted)].all() and failed.sum() == len(planted)
+    compare_verify(o, g, toks, np.full(n, K), V)
+
+
+def test_every_row_in_full_when_every_test_accepts():
+    # Draft rows equal to the target rows (q = p: every test accepts), more
+    # rows than one wave of CTAs: the rows are taken position by position
+    # while the early tests are decided, none is ever past a known rejection,
+    # and every one needs its full pass.
+    rng = np.random.default_rng(8)
+    n, K, V = 320, 6, 4_096
+    x = rng.normal(0, 3, (n, K + 1, V)).astype(np.float32)
+    tgt = torch.from_numpy(x).to(torch.bfloat16)
+    drf = tgt[:, :K].contiguous()
+    T = np.where(np.arange(n) % 2 == 0, 0.8, 1.0).astype(np.float32)
+    tp = np.where(np.arange(n) % 3 == 0, 0.95, 1.0).astype(np.float32)
+    tk = np.zeros(n, np.int32)
+    # each draft token drawn from its own row's kept set (so q > 0 there)
+    toks = np.empty((n, K), np.int32)
+    host = np_logits(tgt)
+    for r in range(n):
+        for j in range(K):
+            _, op = oracle.row_transform(host[r, j], float(T[r]), 0, float(tp[r]))
+            toks[r, j] = rng.choice(V, p=op / op.sum())
+    g = sv.verify_chain(tgt.to(DEV), drf.to(DEV), torch.from_numpy(toks).to(DEV), torch.from_numpy(T).to(DEV),
+                        torch.from_numpy(tk).to(DEV), torch.from_numpy(tp).to(DEV), seed=12)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain(host, np_logits(drf), toks, T, tk, tp, seed=12)
+    assert (o["accept_len"] == K).all()
+    compare_verify(o, g, toks, np.full(n, K), V)
