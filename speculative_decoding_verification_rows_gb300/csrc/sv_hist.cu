@@ -894,20 +894,6 @@ __device__ __forceinline__ uint32_t key_raw16(uint32_t h)
 {
     return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
 }
-// The same for both halves of a word: a byte permute replicates each half's
-// sign bit over the half, which selects the flip mask.
-__device__ __forceinline__ uint32_t keys2_raw(uint32_t w)
-{
-    uint32_t sgn;
-    asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(sgn) : "r"(w), "r"(0u));
-    return w ^ (sgn | 0x80008000u);
-}
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t x, uint32_t y)
-{
-    uint32_t r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
-    return r;
-}
 
 // Returns true when the row went to the cluster kernel (no record written here).
 __device__ bool wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, int t)
@@ -1184,13 +1170,6 @@ __device__ bool wide_row(WideSmem& sm, const RowsArgs& a, const RowTask& task, i
     }
     __syncthreads();
     return ovf;
-}
-
-__device__ __forceinline__ uint32_t min_u16x2(uint32_t x, uint32_t y)
-{
-    uint32_t r;
-    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
-    return r;
 }
 
 // A row whose acceptance test can no longer matter (it lies past a position

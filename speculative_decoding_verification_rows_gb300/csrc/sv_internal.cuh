@@ -143,15 +143,15 @@ __device__ __forceinline__ unsigned long long weight_fix(double w)
     return __double2ull_rz(w * 0x1p64);
 }
 
-// Chunks and tiles of the full-row resample.  A chunk (kResampleUnit
-// elements) is what one CTA of the resample kernel streams at a time; each
-// tile of it (kResampleTile elements, eight per thread) leaves a record for
-// the job's last chunk: exact fixed-point sums of the residual and of p over
-// the tile, with the elements tied at a partially kept cutoff summed apart in
-// both of their possible states (kept or not, for p and for q), and the tie
-// counts.
-constexpr int kResampleUnit = 8192;
-constexpr int kResampleTile = 2048;
+// Chunks and tiles of the full-row resample.  A chunk (eight tiles) is what
+// one CTA of the resample kernel streams at a time, one tile per warp; each
+// tile (1,024 elements, or 2,048 when the row would otherwise have more than
+// 256 tiles) leaves a record for the job's last chunk: exact fixed-point sums
+// of the residual and of p over the tile, with the elements tied at a
+// partially kept cutoff summed apart in both of their possible states (kept
+// or not, for p and for q), and the tie counts.
+constexpr int kResampleTile = 2048;    // the longest tile
+constexpr int kResampleMaxTiles = 256;
 enum TileField {
     kTsBaseRes = 0,   // residual over elements not tied at a partial cutoff
     kTsBaseP = 1,     // p over the same
@@ -164,7 +164,15 @@ enum TileField {
 struct TileSums {
     unsigned long long v[kTsFields];
 };
-__host__ __device__ __forceinline__ int resample_tiles(int vocab) { return (vocab + kResampleTile - 1) / kResampleTile; }
+__host__ __device__ __forceinline__ int resample_tile_len(int vocab)
+{
+    return vocab <= kResampleMaxTiles * (kResampleTile / 2) ? kResampleTile / 2 : kResampleTile;
+}
+__host__ __device__ __forceinline__ int resample_tiles(int vocab)
+{
+    const int t = resample_tile_len(vocab);
+    return (vocab + t - 1) / t;
+}
 
 // Request slots of the RowInfo array: target positions 0..K, then draft
 // positions 0..K-1.
@@ -247,6 +255,34 @@ __device__ __forceinline__ uint32_t key16_of_bf16(uint32_t h)
     if ((h & 0x7FFFu) == 0u) h = 0u;
     return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
 }
+// Order keys of both bf16 halves of a word, -0 kept apart from +0 (key
+// 0x7FFF, just below +0's 0x8000): a byte permute replicates each half's sign
+// bit over the half, which selects the flip mask.
+__device__ __forceinline__ uint32_t keys2_raw(uint32_t w)
+{
+    uint32_t sgn;
+    asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(sgn) : "r"(w), "r"(0u));
+    return w ^ (sgn | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t x, uint32_t y)
+{
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t x, uint32_t y)
+{
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+// Number of 16-bit halves of t that are zero (no carry crosses the halves).
+__device__ __forceinline__ int zero_halves(uint32_t t)
+{
+    const uint32_t y = (t & 0x7FFF7FFFu) + 0x7FFF7FFFu;   // bit 15 of a half: its low 15 bits are not all 0
+    return __popc(~(y | t) & 0x80008000u);
+}
+
 __device__ __forceinline__ float f32_of_key16(uint32_t k)
 {
     uint32_t h = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
@@ -389,6 +425,18 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
 #pragma unroll
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
     return x;
+}
+
+// The same for values below 2^63 whose warp total is below 2^63 (fixed-point
+// probabilities), where most warps hold zeros: a vote, then three 21-bit
+// limbs summed by the warp-reduce unit (each limb total stays below 2^26).
+__device__ __forceinline__ unsigned long long warp_sum_u63(unsigned long long x)
+{
+    if (!__any_sync(0xFFFFFFFFu, x != 0ull)) return 0ull;
+    const uint32_t l0 = (uint32_t)x & 0x1FFFFFu, l1 = (uint32_t)(x >> 21) & 0x1FFFFFu, l2 = (uint32_t)(x >> 42);
+    return (unsigned long long)__reduce_add_sync(0xFFFFFFFFu, l0) +
+           ((unsigned long long)__reduce_add_sync(0xFFFFFFFFu, l1) << 21) +
+           ((unsigned long long)__reduce_add_sync(0xFFFFFFFFu, l2) << 42);
 }
 
 // Value of a row element, by dtype (0 = bf16, 1 = fp32).

@@ -52,8 +52,15 @@ __device__ __forceinline__ unsigned long long pweight(const Dist& P, unsigned lo
 
 __device__ __forceinline__ unsigned long long fix_of(double p)
 {
-    const double x = floor(p * kFix);
-    return x <= 0.0 ? 0ull : (x >= kFix ? (unsigned long long)kFix : (unsigned long long)x);
+    const unsigned long long x = __double2ull_rd(p * kFix);   // floor; 0 for p <= 0
+    return x < (1ull << 62) ? x : (1ull << 62);
+}
+
+// A key outside the tables: its own fp64 exp (out of line: rare, and it keeps
+// the streaming loops small).
+__device__ __noinline__ unsigned long long fixp_exp(double m, double T, double z, uint32_t key)
+{
+    return fix_of(exp((key_value(key) - m) / T) / z);
 }
 
 // 62-bit fixed-point probability of a key under a distribution (kept test
@@ -63,7 +70,7 @@ __device__ __forceinline__ unsigned long long fixp(const Dist& D, uint32_t key)
     if (key < D.zero_key) return 0ull;
     const int s = D.map[key >> 7];
     if (s >= 0) return D.tab[s * 128 + (key & 127u)];
-    return fix_of(exp((key_value(key) - D.m) / D.T) / D.z);
+    return fixp_exp(D.m, D.T, D.z, key);
 }
 
 __device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_rank)
@@ -83,16 +90,16 @@ __device__ __forceinline__ uint32_t zero_key_of(double m, double T, double z)
 }
 
 constexpr int kResThreads = 256;
+constexpr int kResWarps = kResThreads / 32;
 constexpr int kResBinades = 48;    // table slots, p's and q's binades together
 constexpr int kResTile = kResampleTile;
-static_assert(kResampleTile == kResThreads * 8, "a tile is eight elements per thread");
-static_assert(kResampleUnit % kResampleTile == 0, "a chunk is whole tiles");
+constexpr int kResStep = 512;      // elements a warp loads at a time (two 16-byte vectors per lane and row)
+constexpr int kResWarpBuf = kResStep + 64;   // candidates a warp gathers before weighing them
+static_assert(kResampleTile == kResThreads * 8, "a rescanned tile is at most eight elements per thread");
+static_assert((kResTile / 2) % kResStep == 0, "a tile is whole steps");
 
 struct ResSmem {
-    alignas(16) uint16_t stage[2][kResampleUnit];   // the chunk of p's row and of q's row
-    unsigned long long bar;                         // completion of the chunk's bulk copies
-    int stage_ok;                                   // 0 after a copy did not arrive in time: plain loads from then on
-    unsigned long long buf[kResThreads * 8];        // per warp: its tile's candidates, then (rescan) their weights
+    unsigned long long buf[kResWarps * kResWarpBuf];   // per warp: its candidates, then (rescan) their weights
     unsigned long long tab[kResBinades * 128];
     double ratio[kResBinades];                      // per slot: exp(step / T) along the binade (0: one exp per key)
     uint32_t zkey[2];                               // the loaded job's zero keys of p and q
@@ -103,8 +110,8 @@ struct ResSmem {
     int last;         // this CTA finished the job's last chunk
     int found;        // token found by the target search (-1: not yet)
     int halt;         // the target search is over
-    unsigned long long red[2][kResThreads / 32][kTsFields];   // per-warp tile sums (two tiles in flight)
     unsigned long long scan[kResThreads / 32];
+    unsigned long long tacc[kResWarps][kTsTiesP - kTsTieRes];   // per warp: its tile's tied-element sums
     // the combine
     unsigned long long ex_res[2], ex_p[2];   // exact sums of the tiles where a tie group's kept part ends
     int ex_tile[2], ex_off_p[2], ex_off_q[2];
@@ -211,14 +218,16 @@ __device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
         sm.ratio[sl] = x <= 1.0 ? exp(x) : 0.0;
     }
     __syncthreads();
+    const double inv_tp = 1.0 / P.T, inv_tq = 1.0 / Q.T, inv_zp = 1.0 / P.z, inv_zq = 1.0 / Q.z;
     for (int item = tid; item < (capP + capQ) * 16; item += kResThreads) {
         const int sl = item >> 4, g = item & 15;
-        const Dist& D = sm.slot_dist[sl] ? Q : P;
+        const bool isq = sm.slot_dist[sl] != 0;
+        const Dist& D = isq ? Q : P;
         const uint32_t k0 = (uint32_t)sm.slot_bin[sl] * 128u + 8u * (uint32_t)g;
-        const double R = sm.ratio[sl], inv_z = 1.0 / D.z;
+        const double R = sm.ratio[sl], inv_z = isq ? inv_zq : inv_zp;
         unsigned long long* out = sm.tab + sl * 128 + 8 * g;
         if (R > 0.0) {
-            double cur = exp((key_value(k0) - D.m) / D.T);
+            double cur = exp((key_value(k0) - D.m) * (isq ? inv_tq : inv_tp));
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 out[j] = fix_of(cur * inv_z);
@@ -250,44 +259,40 @@ __device__ __forceinline__ void load_keys8(const uint16_t* row, int x0, int x_en
     }
 }
 
-// Canonical keys of eight consecutive staged elements.
-__device__ __forceinline__ void stage_keys8(const uint16_t* st, uint32_t k[8])
+// Eight consecutive elements as raw bf16 pairs (x0 .. x0 + 7, those at or
+// past x_end read as -inf).
+__device__ __forceinline__ uint4 load_raw8(const uint16_t* row, int x0, int x_end, bool vec_ok)
 {
-    const uint4 v = ld_shared_v4(st);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (vec_ok && x0 + 8 <= x_end) return __ldg(reinterpret_cast<const uint4*>(row + x0));
+    uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        k[2 * i] = key16_of_bf16(w[i] & 0xFFFFu);
-        k[2 * i + 1] = key16_of_bf16(w[i] >> 16);
+        const uint32_t lo = x0 + 2 * i < x_end ? row[x0 + 2 * i] : 0xFF80u;
+        const uint32_t hi = x0 + 2 * i + 1 < x_end ? row[x0 + 2 * i + 1] : 0xFF80u;
+        w[i] = lo | (hi << 16);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Bulk-copies elements [x_begin, x_end) of p's row (and q's) into the stage,
-// when the rows allow it (16-byte aligned, a whole number of 8-element
-// vectors).  Returns whether the chunk is staged.  Every thread calls it;
-// `phase` is the barrier's parity, tracked alike by every thread.
-__device__ bool stage_unit(ResSmem& sm, const Dist& P, const Dist& Q, bool residual, int x_begin, int x_end,
-                           bool vec_ok, uint32_t& phase)
+// Element i's key (canonical: -0 as +0) from four words of raw key pairs.
+__device__ __forceinline__ uint32_t canon_key(const uint32_t r[4], int i)
 {
-    const int n = x_end - x_begin;
-    if (!sm.stage_ok || !vec_ok || (n & 7)) return false;
-    const uint32_t bytes = (uint32_t)n * 2u;
-    __syncthreads();   // nobody reads the previous chunk any more
-    if (threadIdx.x == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(&sm.bar, residual ? 2u * bytes : bytes);
-        bulk_g2s(sm.stage[0], P.row + x_begin, bytes, &sm.bar);
-        if (residual) bulk_g2s(sm.stage[1], Q.row + x_begin, bytes, &sm.bar);
-    }
-    const bool ok = __syncthreads_and(mbar_wait(&sm.bar, phase)) != 0;
-    if (!ok) {   // stop staging; the copies in flight are waited for before the CTA leaves
-        __syncthreads();
-        if (threadIdx.x == 0) sm.stage_ok = 0;
-        __syncthreads();
-        return false;
-    }
-    phase ^= 1u;
-    return true;
+    const uint32_t k = (r[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    return k == 0x7FFFu ? 0x8000u : k;
+}
+
+// Elements among eight (four words of raw key pairs) whose canonical key is
+// `cut` (a canonical key: at +0 the raw keys of -0 count too).
+__device__ __forceinline__ int ties8(const uint32_t r[4], uint32_t cut)
+{
+    const uint32_t c2 = cut * 0x10001u;
+    int n = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) n += zero_halves(r[i] ^ c2);
+    if (cut == 0x8000u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) n += zero_halves(r[i] ^ 0x7FFF7FFFu);
+    return n;
 }
 
 __device__ __forceinline__ unsigned long long sat_sub(unsigned long long x, unsigned long long y)
@@ -369,7 +374,7 @@ __device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool resid
                            unsigned long long& sum_res, unsigned long long& sum_p)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    unsigned long long* wb = sm.buf + warp * 256;
+    unsigned long long* wb = sm.buf + warp * kResWarpBuf;
     const int x0 = t0 + 8 * tid;
     uint32_t kp[8], kq[8];
     load_keys8(P.row, x0, x_end, vec_ok, kp);
@@ -470,20 +475,14 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     ResSmem& sm = *reinterpret_cast<ResSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int V = a.vocab, K = a.K;
-    const int n_tiles = resample_tiles(V);
+    const int n_tiles = resample_tiles(V), tile_len = resample_tile_len(V);
     // wave 0: the jobs the chain or block kernel listed; wave 1: those the
     // block finish kernel listed after them
     const int j0 = wave ? a.counters->n_jobs : 0;
     const long long total = (long long)(wave ? a.counters->n_jobs2 : a.counters->n_jobs) * n_units;
     const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
-    if (tid == 0) {
-        sm.cur_job = -1;
-        sm.stage_ok = 1;
-        mbar_init(&sm.bar, 1);
-        mbar_fence_init();
-    }
+    if (tid == 0) sm.cur_job = -1;
     __syncthreads();
-    uint32_t phase = 0u;
     for (long long u = u_lo; u < u_hi; ++u) {
         const int j = j0 + (int)(u / n_units), c = (int)(u % n_units);
         const ResampleJob job = a.jobs[j];
@@ -495,78 +494,120 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
             if (tid == 0) sm.cur_job = j;
         }
         const bool vec_ok = ((uintptr_t)P.row & 15u) == 0u && (!residual || ((uintptr_t)Q.row & 15u) == 0u);
-        const int x_begin = c * kResampleUnit, x_end = min(V, x_begin + kResampleUnit);
         TileSums* recs = a.tiles + (size_t)j * n_tiles;
 
-        // 1. per tile of the chunk: tie counts over every element, weights
-        //    over the elements at or above p's cutoff (the others have p = 0
-        //    in every state), packed densely per warp; then the tile's record
-        const bool staged = stage_unit(sm, P, Q, residual, x_begin, x_end, vec_ok, phase);
-        unsigned long long* wb = sm.buf + warp * 256;
-        for (int t0 = x_begin; t0 < x_end; t0 += kResTile) {
-            const int x0 = t0 + 8 * tid;
-            unsigned long long acc[kTsFields] = {};
-            uint32_t kp[8], kq[8];
-            if (staged && x0 < x_end) {
-                stage_keys8(sm.stage[0] + (x0 - x_begin), kp);
-                if (residual) stage_keys8(sm.stage[1] + (x0 - x_begin), kq);
-            } else {
-                load_keys8(P.row, x0, x_end, vec_ok, kp);
-                if (residual) load_keys8(Q.row, x0, x_end, vec_ok, kq);
-            }
-            if (!residual)
+        // 1. one tile of the chunk per warp: tie counts over every element,
+        //    weights over the elements at or above p's cutoff (the others have
+        //    p = 0 in every state), gathered densely in the warp's buffer and
+        //    weighed a batch at a time; the warp writes the tile's record.
+        //    Each lane loads 16-byte vectors straight from the rows, the next
+        //    step's while it works on this one.
+        const int tile = c * kResWarps + warp;
+        const int t0 = tile * tile_len;
+        if (t0 < V) {
+            unsigned long long* wb = sm.buf + warp * kResWarpBuf;
+            unsigned long long* tacc = sm.tacc[warp];   // elements tied at a partial cutoff: rare, summed here
+            const int t_end = min(V, t0 + tile_len);
+            unsigned long long base_res = 0ull, base_p = 0ull;
+            int ties_p = 0, ties_q = 0;
+            if (lane < kTsTiesP - kTsTieRes) tacc[lane] = 0ull;
+            int nbuf = 0;
+            // the weights of the gathered candidates, into acc
+            auto weigh = [&]() {
+                __syncwarp();
+                for (int e = lane; e < nbuf; e += 32) {
+                    const uint32_t en = (uint32_t)wb[e];
+                    const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
+                    const bool tP = P.partial && ekp == P.cut_key;
+                    const bool tQ = residual && Q.partial && ekq == Q.cut_key;
+                    const unsigned long long wp = fixp(P, ekp);
+                    const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
+                    const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
+                    const unsigned long long wpw = pweight(P, wp);   // p's weighted value in the residual
+                    if (!tP && !tQ) {
+                        base_p += wp;
+                        base_res += residual ? sat_sub(wpw, wq) : wp;
+                    } else {
+                        const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) kq[i] = 0u;
-            uint32_t cm = 0u;
+                        for (int sp_ = 0; sp_ < 2; ++sp_) {
+                            const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
+                            const unsigned long long pw_ = (tP && !sp_) ? 0ull : wpw;
+                            atomicAdd(&tacc[kTsTieP - kTsTieRes + sp_], p_);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                acc[kTsTiesP] += (P.partial && kp[i] == P.cut_key) ? 1u : 0u;
-                acc[kTsTiesQ] += (residual && Q.partial && kq[i] == Q.cut_key) ? 1u : 0u;
-                if (kp[i] >= P.cut_key) cm |= 1u << i;
-            }
-            const int cnt =
-                compact8(wb, cm, [&](int i) { return (unsigned long long)kp[i] | ((unsigned long long)kq[i] << 16); });
-            for (int e = lane; e < cnt; e += 32) {
-                const uint32_t en = (uint32_t)wb[e];
-                const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
-                const bool tP = P.partial && ekp == P.cut_key;
-                const bool tQ = residual && Q.partial && ekq == Q.cut_key;
-                const unsigned long long wp = fixp(P, ekp);
-                const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
-                const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
-                const unsigned long long wpw = pweight(P, wp);   // p's weighted value in the residual
-                if (!tP && !tQ) {
-                    acc[kTsBaseP] += wp;
-                    acc[kTsBaseRes] += residual ? sat_sub(wpw, wq) : wp;
-                } else {
-                    const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
-#pragma unroll
-                    for (int sp_ = 0; sp_ < 2; ++sp_) {
-                        const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
-                        const unsigned long long pw_ = (tP && !sp_) ? 0ull : wpw;
-                        acc[kTsTieP + sp_] += p_;
-#pragma unroll
-                        for (int sq = 0; sq < 2; ++sq) {
-                            const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
-                            acc[kTsTieRes + 2 * sp_ + sq] += residual ? sat_sub(pw_, q_) : p_;
+                            for (int sq = 0; sq < 2; ++sq) {
+                                const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
+                                atomicAdd(&tacc[2 * sp_ + sq], residual ? sat_sub(pw_, q_) : p_);
+                            }
                         }
                     }
                 }
-            }
-            __syncwarp();
-            const int buf = (t0 / kResTile) & 1;
+                __syncwarp();
+                nbuf = 0;
+            };
+            uint4 np[2], nq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            const int t_stop = t0 + tile_len;
 #pragma unroll
-            for (int f = 0; f < kTsFields; ++f) {
-                const unsigned long long v = warp_sum_u64(acc[f]);
-                if (lane == 0) sm.red[buf][warp][f] = v;
+            for (int h = 0; h < 2; ++h) {
+                const int x0 = t0 + h * 256 + 8 * lane;
+                np[h] = load_raw8(P.row, x0, t_end, vec_ok);
+                if (residual) nq[h] = load_raw8(Q.row, x0, t_end, vec_ok);
             }
-            __syncthreads();
-            if (tid < kTsFields) {
-                unsigned long long v = 0ull;
+            for (int s0 = t0;; s0 += kResStep) {   // one weighing site: the loop body stays small
+                const bool more = s0 < t_stop;
+                if (more) {
+                    const uint4 cp[2] = {np[0], np[1]}, cq[2] = {nq[0], nq[1]};
+                    if (s0 + kResStep < t_stop)
 #pragma unroll
-                for (int w = 0; w < kResThreads / 32; ++w) v += sm.red[buf][w][tid];
-                recs[t0 / kResTile].v[tid] = v;
-                __threadfence();
+                        for (int h = 0; h < 2; ++h) {
+                            const int x0 = s0 + kResStep + h * 256 + 8 * lane;
+                            np[h] = load_raw8(P.row, x0, t_end, vec_ok);
+                            if (residual) nq[h] = load_raw8(Q.row, x0, t_end, vec_ok);
+                        }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // raw key pairs (two elements per word); most elements are
+                        // below p's cutoff and need no more than the pair-wise tie
+                        // counts and one packed maximum for the lane's eight
+                        const uint32_t rp[4] = {keys2_raw(cp[h].x), keys2_raw(cp[h].y), keys2_raw(cp[h].z),
+                                                keys2_raw(cp[h].w)};
+                        uint32_t rq[4] = {0u, 0u, 0u, 0u};   // canonical key 0 stands for q in p's own draw
+                        if (residual) {
+                            rq[0] = keys2_raw(cq[h].x);
+                            rq[1] = keys2_raw(cq[h].y);
+                            rq[2] = keys2_raw(cq[h].z);
+                            rq[3] = keys2_raw(cq[h].w);
+                        }
+                        if (P.partial) ties_p += ties8(rp, P.cut_key);
+                        if (residual && Q.partial) ties_q += ties8(rq, Q.cut_key);
+                        uint32_t cm = 0u;
+                        const uint32_t mx = max_u16x2(max_u16x2(rp[0], rp[1]), max_u16x2(rp[2], rp[3]));
+                        if (max(mx & 0xFFFFu, mx >> 16) + 1u >= P.cut_key)   // -0's raw key sits one below +0's
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (canon_key(rp, i) >= P.cut_key) cm |= 1u << i;
+                        if (__any_sync(0xFFFFFFFFu, cm != 0u))
+                            nbuf += compact8(wb + nbuf, cm, [&](int i) {
+                                return (unsigned long long)canon_key(rp, i) | ((unsigned long long)canon_key(rq, i) << 16);
+                            });
+                    }
+                }
+                if (!more || nbuf > kResWarpBuf - kResStep) weigh();   // room for the next step's candidates
+                if (!more) break;
+            }
+            base_res = warp_sum_u63(base_res);
+            base_p = warp_sum_u63(base_p);
+            ties_p = __reduce_add_sync(0xFFFFFFFFu, ties_p);
+            ties_q = __reduce_add_sync(0xFFFFFFFFu, ties_q);
+            if (lane == 0) {
+                TileSums& rec = recs[tile];
+                rec.v[kTsBaseRes] = base_res;
+                rec.v[kTsBaseP] = base_p;
+#pragma unroll
+                for (int f = kTsTieRes; f < kTsTiesP; ++f) rec.v[f] = tacc[f - kTsTieRes];
+                rec.v[kTsTiesP] = (unsigned long long)ties_p;
+                rec.v[kTsTiesQ] = (unsigned long long)ties_q;
+                __threadfence();   // the tile's record, before the chunk is counted done
             }
         }
         __syncthreads();
@@ -604,7 +645,8 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
         const int n_ex = min(sm.n_ex, 2);
         for (int e = 0; e < n_ex; ++e) {
             unsigned long long sr, sp_;
-            rescan_tile(sm, P, Q, residual, sm.ex_tile[e] * kResTile, V, sm.ex_off_p[e], sm.ex_off_q[e], vec_ok, 0,
+            rescan_tile(sm, P, Q, residual, sm.ex_tile[e] * tile_len, min(V, (sm.ex_tile[e] + 1) * tile_len),
+                        sm.ex_off_p[e], sm.ex_off_q[e], vec_ok, 0,
                         false, 0ull, sr, sp_);
             if (tid == 0) {
                 sm.ex_res[e] = sr;
@@ -653,7 +695,8 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
         int x = -1;
         if (sm.found_tile >= 0) {
             unsigned long long d0, d1;
-            x = rescan_tile(sm, P, Q, residual, sm.found_tile * kResTile, V, sm.tile_off_p, sm.tile_off_q, vec_ok, 1,
+            x = rescan_tile(sm, P, Q, residual, sm.found_tile * tile_len, min(V, (sm.found_tile + 1) * tile_len),
+                            sm.tile_off_p, sm.tile_off_q, vec_ok, 1,
                             use_p, sm.tile_target, d0, d1);
         }
         if (tid == 0) {
@@ -663,7 +706,6 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
         }
         __syncthreads();
     }
-    if (!sm.stage_ok && tid == 0) mbar_wait(&sm.bar, phase);   // let a late copy land before the CTA leaves
 }
 
 }  // namespace
@@ -682,7 +724,8 @@ cudaError_t launch_resample(const ChainArgs& a, int wave, cudaStream_t s)
         if (err != cudaSuccess) return err;
         if (nb < 1) nb = 1;
     }
-    const int n_units = (a.vocab + kResampleUnit - 1) / kResampleUnit;
+    const int unit = kResWarps * resample_tile_len(a.vocab);   // a chunk: one tile per warp
+    const int n_units = (a.vocab + unit - 1) / unit;
     return launch_pdl(resample_kernel, dim3(a.num_sms * nb), dim3(kResThreads), smem, s, a, n_units, wave);
 }
 
