@@ -93,7 +93,9 @@ constexpr int kResThreads = 256;
 constexpr int kResWarps = kResThreads / 32;
 constexpr int kResBinades = 48;    // table slots, p's and q's binades together
 constexpr int kResTile = kResampleTile;
-constexpr int kResStep = 512;      // elements a warp loads at a time (two 16-byte vectors per lane and row)
+constexpr int kResStep = 512;
+constexpr int kResCostJobs = 2048;   // jobs up to which the chunks are split by estimated cost
+constexpr int kResCostBase = 120;    // a chunk's fixed part, in units of one candidate's weighing      // elements a warp loads at a time (two 16-byte vectors per lane and row)
 constexpr int kResWarpBuf = kResStep + 64;   // candidates a warp gathers before weighing them
 static_assert(kResampleTile == kResThreads * 8, "a rescanned tile is at most eight elements per thread");
 static_assert((kResTile / 2) % kResStep == 0, "a tile is whole steps");
@@ -468,6 +470,44 @@ __device__ int rescan_tile(ResSmem& sm, const Dist& P, const Dist& Q, bool resid
     return found;
 }
 
+// This CTA's chunks [u_lo, u_hi) when the ranges are cut at equal estimated
+// cost rather than equal length: a chunk costs a fixed part plus its expected
+// candidates (p's kept count over the row), which the weighing loop pays for.
+// Out of line: it runs once per launch.  Every thread calls it.
+__device__ __noinline__ void cost_split(ResSmem& sm, const ChainArgs& a, int j0, int n_jobs, int n_units,
+                                        long long& u_lo, long long& u_hi)
+{
+    const int tid = threadIdx.x, K = a.K, V = a.vocab, tile_len = resample_tile_len(V);
+    long long C = 0, lo = 0, hi = 0;
+    for (int pass = 0; pass < 2; ++pass) {   // pass 0: the total; pass 1: this CTA's bounds
+        const long long x0 = C * blockIdx.x / gridDim.x, x1 = C * (blockIdx.x + 1) / gridDim.x;
+        long long before = 0;
+        for (int b0 = 0; b0 < n_jobs; b0 += kResThreads) {
+            const int jj = b0 + tid;
+            long long cost = 0;   // per chunk of job jj
+            if (jj < n_jobs) {
+                const ResampleJob job = a.jobs[j0 + jj];
+                const int kept = __ldcg(&a.info[slot_target(job.req, K, job.a)].desc.kept);
+                cost = (job.residual ? kResCostBase : kResCostBase / 2) +
+                       (long long)max(kept, 0) * tile_len / max(V, 1);
+            }
+            unsigned long long all;
+            const long long s0 = before + (long long)block_excl_u64(sm, (unsigned long long)(cost * n_units), all);
+            if (pass == 1 && jj < n_jobs) {   // this job's chunks that start below each bound
+                lo += min((long long)n_units, max(0ll, (x0 - s0 + cost - 1) / cost));
+                hi += min((long long)n_units, max(0ll, (x1 - s0 + cost - 1) / cost));
+            }
+            before += (long long)all;
+        }
+        C = before;
+    }
+    unsigned long long n_lo, n_hi;
+    block_excl_u64(sm, (unsigned long long)lo, n_lo);
+    block_excl_u64(sm, (unsigned long long)hi, n_hi);
+    u_lo = (long long)n_lo;
+    u_hi = (long long)n_hi;
+}
+
 __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units, int wave)
 {
     pdl_enter();
@@ -479,8 +519,10 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, i
     // wave 0: the jobs the chain or block kernel listed; wave 1: those the
     // block finish kernel listed after them
     const int j0 = wave ? a.counters->n_jobs : 0;
-    const long long total = (long long)(wave ? a.counters->n_jobs2 : a.counters->n_jobs) * n_units;
-    const long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
+    const int n_jobs = wave ? a.counters->n_jobs2 : a.counters->n_jobs;
+    const long long total = (long long)n_jobs * n_units;
+    long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
+    if (n_jobs <= kResCostJobs && total >= 4ll * gridDim.x) cost_split(sm, a, j0, n_jobs, n_units, u_lo, u_hi);
     if (tid == 0) sm.cur_job = -1;
     __syncthreads();
     for (long long u = u_lo; u < u_hi; ++u) {
