@@ -103,11 +103,10 @@ enum {
  *       launch only their prep, the one-pass row kernel and the chain (or row
  *       output) kernels: the full-vocabulary histogram kernels and the
  *       full-row resample, which such a batch never needs, are not launched.
- *       A request that breaks the promise is refused like an fp32 request
- *       with a full-vocabulary kept set: SV_ROW_UNSUPPORTED (at position 0 of
- *       a verify request, accept_len = num_emitted = 0; in the row's
- *       descriptor for sv_build_target_probs); the other requests are not
- *       affected.  sv_estimator_predict ignores the flag (its features take
+ *       A request that breaks the promise is refused: SV_ROW_UNSUPPORTED (at
+ *       position 0 of a verify request, accept_len = num_emitted = 0; in the
+ *       row's descriptor for sv_build_target_probs); the other requests are
+ *       not affected.  sv_estimator_predict ignores the flag (its features take
  *       greedy requests at T = 1 over the whole row), and so does
  *       sv_verify_block (it keeps its full launch sequence). */
 enum { SV_SAMPLING_SMALL_TOPK = 1 };
@@ -206,8 +205,11 @@ sv_status_t sv_build_target_probs(const void* logits, sv_dtype_t dt, int64_t row
  *   d_0 .. d_{a-1}, t, then -1; num_emitted [n_req] = a + 1; row_status
  *   [n_req, K + 1] or NULL: OR of the position's target row, draft row and
  *   token bits.
- *   fp32 logits support greedy requests and top-k <= 32; other fp32 requests
- *   get SV_ROW_UNSUPPORTED.  sp.flags = SV_SAMPLING_SMALL_TOPK skips the
+ *   bf16 and fp32 logits take every sampling combination: kept sets of up to
+ *   32 tokens are listed by the one-pass row kernel, larger ones (bf16) by
+ *   exact per-value histograms or (fp32) by a radix descent on the 32-bit
+ *   order keys with exact fixed-point masses, and their tokens are drawn by
+ *   a full-row resample.  sp.flags = SV_SAMPLING_SMALL_TOPK skips the
  *   full-vocabulary kernels (see sv_sampling_t); sv_verify_ragged takes it
  *   the same way, sv_verify_block ignores it.
  */
@@ -343,7 +345,7 @@ sv_status_t sv_estimator_init(double* state, int K, sv_stream_t stream);
 
 /*
  * Features and predictions for draft logits (device, [n_req, K, vocab], bf16
- * or fp32; fp32 needs top-k <= 32): x_out, p_out (device) fp32 [n_req, K].
+ * or fp32): x_out, p_out (device) fp32 [n_req, K].
  * p_out is the planner's conf input (sv_plan_budget / sv_plan_budget_cost).
  * A row with an error gives x = p = NaN (the planner reads NaN as 0).
  * Workspace: sv_workspace_size(n_req * K, 0, vocab).
@@ -439,7 +441,7 @@ sv_status_t sv_verify_chain_noalloc(const void* target_logits, const void* draft
  * rows -- the same accepted lengths, tokens and statuses.  Served: greedy
  * requests and requests whose kept set is listed (top-k <= 32, with or
  * without top-p); a request with a larger kept set gets SV_ROW_UNSUPPORTED
- * (nothing accepted or emitted), as an fp32 one does in sv_verify_chain.
+ * (nothing accepted or emitted).
  *
  * sv_shard_record_bytes: bytes of one record (264): its row's top-32
  * composite keys (logit order key above, whole-vocabulary index inverted

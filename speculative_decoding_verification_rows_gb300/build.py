@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsv.so")
-SOURCES = ["sv_fast.cu", "sv_hist.cu", "sv_chain.cu", "sv_resample.cu", "sv_plan.cu", "sv_est.cu", "sv_api.cu", "sv_noalloc.cu"]
+SOURCES = ["sv_fast.cu", "sv_hist.cu", "sv_chain.cu", "sv_resample.cu", "sv_plan.cu", "sv_est.cu", "sv_api.cu", "sv_noalloc.cu", "sv_rows32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

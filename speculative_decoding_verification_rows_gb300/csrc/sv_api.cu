@@ -61,10 +61,10 @@ sv_status_t run_rows(const RowsArgs& ra, cudaStream_t s, bool small_topk)
     cudaError_t e = launch_fast_rows(ra, s);
     if (e != cudaSuccess) return SV_ERR_CUDA;
     if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SV_ERR_CUDA;
-    if (ra.dtype == 0 && !small_topk) {   // fp32 rows never take the histogram path (refused in prep)
+    if (!small_topk) {   // rows whose kept sets are not listed: bf16 by exact histograms, fp32 by radix descent
         const cudaEvent_t hv0 = g_hv_start, hv1 = g_hv_stop;
         if (hv0 && hv1 && cudaEventRecord(hv0, s) != cudaSuccess) return SV_ERR_CUDA;
-        e = launch_hist_rows(ra, s);
+        e = ra.dtype == 0 ? launch_hist_rows(ra, s) : launch_rows32(ra, s);
         if (e != cudaSuccess) return SV_ERR_CUDA;
         if (hv0 && hv1 && cudaEventRecord(hv1, s) != cudaSuccess) return SV_ERR_CUDA;
     }
@@ -174,10 +174,13 @@ sv_status_t run_verify(int layout, const void* tgt, const void* drf, sv_dtype_t 
     if (small_topk && !block) return SV_OK;
     if (launch_chain(ca, s) != cudaSuccess) return SV_ERR_CUDA;
     if (small_topk) return SV_OK;
-    if (dt == SV_DTYPE_BF16 && launch_resample(ca, 0, s) != cudaSuccess) return SV_ERR_CUDA;
-    if (block && dt == SV_DTYPE_BF16) {   // requests with unlisted kept sets: decide, then draw
+    auto resample = [&](int wave) {
+        return dt == SV_DTYPE_BF16 ? launch_resample(ca, wave, s) : launch_resample32(ca, wave, s);
+    };
+    if (resample(0) != cudaSuccess) return SV_ERR_CUDA;
+    if (block) {   // requests with unlisted kept sets: decide, then draw
         if (launch_block_finish(ca, s) != cudaSuccess) return SV_ERR_CUDA;
-        if (launch_resample(ca, 1, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (resample(1) != cudaSuccess) return SV_ERR_CUDA;
     }
     return SV_OK;
 }

@@ -122,10 +122,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             greedy = T == 0.0f;
             k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
             fast = greedy || k_eff <= kFastK;
-            // full-vocabulary kept sets: not for fp32 rows, nor under the
-            // caller's promise that the batch has none, nor in a
-            // vocabulary-sharded call
-            if (!err && !fast && (a.dtype != 0 || (a.sp.flags & SV_SAMPLING_SMALL_TOPK) || a.shard)) err |= kUnsupported;
+            // full-vocabulary kept sets: not under the caller's promise that
+            // the batch has none, nor in a vocabulary-sharded call
+            if (!err && !fast && ((a.sp.flags & SV_SAMPLING_SMALL_TOPK) || a.shard)) err |= kUnsupported;
             if (a.layout == 0) {
                 v = a.verify_len ? a.verify_len[u] : K;
                 if (v < 0 || v > K) {

@@ -626,6 +626,7 @@ struct RowsArgs {
 cudaError_t launch_fast_rows(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_shard_merge(const RowsArgs& a, const void* records, int n_shards, int slots, cudaStream_t s);
 cudaError_t launch_hist_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_rows32(const RowsArgs& a, cudaStream_t s);   // fp32 rows with unlisted kept sets
 // CTAs of the one-CTA histogram kernel's grid on the current device (0 on error).
 int hist_wide_grid(int num_sms);
 
@@ -634,6 +635,7 @@ int hist_wide_grid(int num_sms);
 cudaError_t launch_prep(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_resample(const ChainArgs& a, int wave, cudaStream_t s);
+cudaError_t launch_resample32(const ChainArgs& a, int wave, cudaStream_t s);   // the same for fp32 rows
 cudaError_t launch_block_finish(const ChainArgs& a, cudaStream_t s);
 cudaError_t launch_rows_out(const ChainArgs& a, float* prob_of_token, sv_row_desc_t* desc, float* dense,
                             cudaStream_t s);
