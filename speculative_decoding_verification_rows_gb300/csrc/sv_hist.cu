@@ -829,6 +829,7 @@ constexpr int kUnclaimed = INT_MIN;      // base[] of a binade not seen yet in t
 constexpr int kClaiming = INT_MIN + 1;   // base[] while a thread assigns the binade its counters
 constexpr int kBaseMin = -65536;         // a claimed base is 128 * (slot - b) >= -65,408
 constexpr int kClaimSpins = 1 << 14;     // polls before a thread stops waiting for a claim
+constexpr int kDecideSpins = 40;         // polls (about 256 ns apart) for the previous position's test
 static_assert(kWideThreads >= 4 * kWideSlots, "the mass pass takes four threads per slot");
 static_assert(kWideThreads == kWalkThreads && kHistThreads == kWalkThreads, "walk_row takes one binade per thread");
 static_assert(2 * kWideSlots < kWideThreads, "the last thread is idle in the exps of the mass pass");
@@ -1296,7 +1297,22 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
                 r = e.x >> 7;
                 j = (e.x >> 1) & 63;
                 t = e.y;
-                mode = j > __ldcg(&c.req[r].first_reject) ? kScan : kFull;
+                int fr = __ldcg(&c.req[r].first_reject);
+                // Wait a little while the lowest undecided test before this
+                // row is being decided (one of its rows is finished): far
+                // cheaper than a full pass that a rejection there would make
+                // useless.  Bounded; after it the row gets its full pass as if
+                // nothing were decided.
+                const int32_t* done = &c.pair_done[(size_t)r * K1];
+                for (int spin = 0; spin < kDecideSpins && j <= fr; ++spin) {
+                    int i = 0;
+                    while (i < j && __ldcg(done + i) > kinds) ++i;   // decided positions
+                    if (i == j || __ldcg(done + i) == 0) break;      // all decided, or not started
+                    __nanosleep(256);
+                    fr = __ldcg(&c.req[r].first_reject);
+                }
+                fr = __ldcg(&c.req[r].first_reject);
+                mode = j > fr ? kScan : kFull;
             }
             s_unit[0] = mode;
             s_unit[1] = t;
@@ -1318,6 +1334,8 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
             if (atomicAdd(&c.pair_done[(size_t)r * K1 + j], 1) == kinds - 1) {
                 __threadfence();
                 decide_position(a, r, j);
+                __threadfence();
+                atomicAdd(&c.pair_done[(size_t)r * K1 + j], 1);   // kinds + 1: decided
             }
         }
     }
