@@ -219,16 +219,21 @@ def algorithmic_bytes(w) -> tuple[int, int]:
     return (rows_t + rows_d) * w.V * esz, rows_t
 
 
-def path_bytes(w, verify_len=None) -> tuple[int, int]:
+def path_bytes(w, verify_len=None, method="chain", promise=False) -> tuple[int, int]:
     """Bytes of the rows read by the one-pass kernel (greedy, top-k <= 32) and
     by the histogram kernels (the other sampling rows) in one step: a request
-    with window v reads v + 1 target rows, and v draft rows if it samples."""
+    with window v reads v + 1 target rows, and v draft rows if it samples.
+    In chain verification of bf16 rows without the small-top-k promise, the
+    library sends greedy rows to the histogram kernel too (as argmax scans)
+    whenever some request's kept set takes that path."""
     esz = 2 if w.dtype == torch.bfloat16 else 4
     T = w.temperature.detach().cpu()
     tk = w.top_k.detach().cpu() if w.top_k is not None else torch.zeros_like(T, dtype=torch.int32)
     greedy = T == 0
     k_eff = torch.where(greedy, torch.ones_like(tk), torch.where((tk > 0) & (tk < w.V), tk, torch.full_like(tk, w.V)))
     fast = greedy | (k_eff <= 32)
+    if method == "chain" and not promise and w.dtype == torch.bfloat16 and bool((~fast).any()):
+        fast = (~greedy) & (k_eff <= 32)
     v = torch.full_like(tk, w.K) if verify_len is None else verify_len.detach().cpu().to(tk.dtype)
     rows = (v + 1) + torch.where(greedy, torch.zeros_like(v), v)
     return int(rows[fast].sum()) * w.V * esz, int(rows[~fast].sum()) * w.V * esz
@@ -323,7 +328,7 @@ def make_step(w, sv, dev, method="chain", cost_table=False, estimator=False, pro
     vl, qo, tot, _ = plan()
     packed = workloads.pack_rows(w.target, qo.cpu(), vl.cpu(), w.bucket)
     extra = dict(packed=packed, draft_rows=int(vl[w.temperature > 0].sum()), rows=int(tot), plan=plan, table=table,
-                 path_bytes=path_bytes(w, vl))
+                 path_bytes=path_bytes(w, vl, method))
 
     def step(tgt=packed, drf=w.draft, toks=w.draft_tokens, T=w.temperature, tk=w.top_k, tp=w.top_p):
         vl_, qo_, _, _ = plan()
@@ -365,7 +370,7 @@ def run_ours(args, rank, world, local):
     step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator, not args.no_promise,
                                  args.shards)
     alg_bytes, rows_t = algorithmic_bytes(w)
-    fast_bytes, hist_bytes = path_bytes(w)
+    fast_bytes, hist_bytes = path_bytes(w, None, args.method, not args.no_promise and small_topk(w))
     if extra is not None:
         rows_t = extra["rows"]
         alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2

@@ -84,7 +84,7 @@ struct PrepUnit {
     float T, tp;
 };
 
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ ChainArgs a)
 {
     pdl_enter();
     __shared__ int s_wa[32], s_wb[32];
@@ -97,10 +97,29 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
     // each position over all of them (counted here, listed after the loop)
     __shared__ int s_nsr;
     __shared__ int s_pos[kMaxK + 1];
-    const int kinds = a.q_rows ? 1 : 2;   // histogram rows per verified position
+    const int kinds = a.q_rows ? 1 : 2;   // histogram rows per verified position (1 for greedy requests)
     if (threadIdx.x == 0) s_nsr = 0;
     for (int j = threadIdx.x; j <= kMaxK; j += kPrepThreads) s_pos[j] = 0;
+    // Chain verification with bf16 rows: when any request's kept set takes
+    // the histogram path, greedy requests go there too (their rows as argmax
+    // scans), so that their bytes stream while the histogram passes, bound by
+    // shared-memory atomics, leave the memory idle, instead of in a launch of
+    // their own before them.
+    __shared__ int s_hist_greedy;
+    if (threadIdx.x == 0) s_hist_greedy = 0;
     __syncthreads();
+    if (a.lazy && a.dtype == 0 && a.layout != 2 && !a.shard && !(a.sp.flags & SV_SAMPLING_SMALL_TOPK)) {
+        int any = 0;
+        for (int u = threadIdx.x; u < a.n_req && !any; u += kPrepThreads) {
+            const float T = a.sp.temperature[u];
+            const int tk = a.sp.top_k ? a.sp.top_k[u] : 0;
+            const int ke = (tk > 0 && tk < a.vocab) ? tk : a.vocab;
+            any = T > 0.0f && ke > kFastK;
+        }
+        if (__syncthreads_or(any) && threadIdx.x == 0) s_hist_greedy = 1;
+    }
+    __syncthreads();
+    const bool hist_greedy = s_hist_greedy != 0;
     const int K = a.K;
     const int W2 = a.layout == 2 ? 1 : 2 * K + 1;   // row slots per unit
     for (int u0 = 0; u0 < n_units; u0 += kPrepThreads) {
@@ -121,7 +140,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
             if (!req_ok || bad_params(T, tp)) err |= kBadParam;
             greedy = T == 0.0f;
             k_eff = greedy ? 1 : ((tk > 0 && tk < a.vocab) ? tk : a.vocab);
-            fast = greedy || k_eff <= kFastK;
+            fast = (greedy && !hist_greedy) || (!greedy && k_eff <= kFastK);
             // full-vocabulary kept sets: not under the caller's promise that
             // the batch has none, nor in a vocabulary-sharded call
             if (!err && !fast && ((a.sp.flags & SV_SAMPLING_SMALL_TOPK) || a.shard)) err |= kUnsupported;
@@ -250,10 +269,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
                 st.slow_base = slow ? s_u[threadIdx.x].pos : -1;
                 a.req[u] = st;
                 if (slow && a.lazy) {   // the histogram path takes its rows position by position
-                    a.slow_req[atomicAdd(&s_nsr, 1)] = make_int2((u << 6) | v, st.slow_base);
+                    a.slow_req[atomicAdd(&s_nsr, 1)] = make_int2((u << 7) | (greedy << 6) | v, st.slow_base);
+                    const int kr = greedy ? 1 : kinds;
                     for (int j = 0; j <= v; ++j) {
                         a.pair_done[(size_t)u * (K + 1) + j] = 0;
-                        atomicAdd(&s_pos[j], j < v ? kinds : 1);
+                        atomicAdd(&s_pos[j], j < v ? kr : 1);
                     }
                 }
                 a.req_done[u] = 0;
@@ -293,9 +313,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChainArgs a)
         const int n_list = a.counters->n_units > a.lazy_grid ? nsr : 0;
         for (int i = threadIdx.x; i < n_list; i += kPrepThreads) {
             const int2 e = a.slow_req[i];
-            const int r = e.x >> 6, v = e.x & 63;
+            const int r = e.x >> 7, v = e.x & 63;
+            const int kr = ((e.x >> 6) & 1) ? 1 : kinds;
             for (int j = 0; j <= v; ++j) {
-                const int nk = j < v ? kinds : 1;
+                const int nk = j < v ? kr : 1;
                 const int at = atomicAdd(&s_pos[j], nk);
                 a.slow_units[at] = make_int2((r << 7) | (j << 1), e.y + j);
                 if (nk == 2) a.slow_units[at + 1] = make_int2((r << 7) | (j << 1) | 1, e.y + v + 1 + j);
@@ -342,7 +363,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_kernel(const __grid_co
 //   accept length a = the largest j in 1..v with u(r, j-1, 0) < h_j, else 0
 //   next token: inverse CDF of max(w_a p_a - q_a, 0) (a < v) or p_v, u(r, a, 1).
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
+__global__ void __launch_bounds__(kChainWarps * 32) block_kernel(const __grid_constant__ ChainArgs a)
 {
     pdl_enter();
     __shared__ double s_qp[kChainWarps][kFastK];
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(kChainWarps * 32) block_kernel(ChainArgs a)
 // draws the emitted token (max(w_a p_a - q_a, 0), or p_v after full
 // acceptance).  One warp per request.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kChainWarps * 32) block_finish_kernel(ChainArgs a)
+__global__ void __launch_bounds__(kChainWarps * 32) block_finish_kernel(const __grid_constant__ ChainArgs a)
 {
     pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -801,7 +801,7 @@ __device__ void hist_row(cg::cluster_group& cluster, HistSmem& sm, const RowsArg
     cluster.sync();   // the histograms may be cleared for the next row
 }
 
-__global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(RowsArgs a, int slice)
+__global__ void __launch_bounds__(kHistThreads, 1) hist_rows_kernel(const __grid_constant__ RowsArgs a, int slice)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1236,6 +1236,120 @@ __device__ __noinline__ void scan_row(WideSmem& sm, const RowsArgs& a, const Row
     __syncthreads();
 }
 
+// Canonical order keys of both bf16 halves of a word (-0 as +0: the raw key
+// 0x7FFF becomes 0x8000, no carry across the halves).
+__device__ __forceinline__ uint32_t keys2_canon(uint32_t w)
+{
+    const uint32_t k = keys2_raw(w);
+    const uint32_t t = k ^ 0x7FFF7FFFu;   // zero halves where the key is -0's
+    const uint32_t z = ~(((t & 0x7FFF7FFFu) + 0x7FFF7FFFu) | t) & 0x80008000u;
+    return k + (z >> 15);
+}
+
+// A greedy row of chain verification on the histogram path: one streaming
+// pass for the first largest value (-0 as +0, lowest index among equals) and
+// the status (NaN or +inf; a row of nothing but -inf is fine for greedy), and
+// the record the one-pass kernel writes for a greedy row.  Returns the argmax
+// in thread 0.
+__device__ __noinline__ int argmax_row(WideSmem& sm, const RowsArgs& a, const RowTask& task)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint16_t* row = (const uint16_t*)a.tgt + (size_t)task.row * (size_t)a.stride_t;
+    const int V = a.vocab;
+    unsigned long long best = 0ull;   // composite: key << 32 | ~index
+    uint32_t lo = 0xFFFFFFFFu;        // smallest key (both halves)
+    auto one = [&](int i) {
+        const uint32_t k = keys2_canon(row[i]) & 0xFFFFu;
+        const unsigned long long c = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)i);
+        best = c > best ? c : best;
+        lo = min_u16x2(lo, k | 0xFFFF0000u);
+    };
+    const int head = min(V, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 1));
+    const int nvec = (V - head) >> 3;
+    const int tail0 = head + 8 * nvec;
+    if (tid < head) one(tid);
+    if (tail0 + tid < V) one(tail0 + tid);
+    const uint4* vp = reinterpret_cast<const uint4*>(row + head);
+    uint32_t best_key = 0u;   // this thread's largest key so far (its vectors come in index order)
+    for (int v0 = tid; v0 < nvec; v0 += kWideThreads * kWideUnroll) {
+        uint4 x[kWideUnroll];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            const int vi = v0 + u * kWideThreads;
+            x[u] = vi < nvec ? __ldcs(vp + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            const int vi = v0 + u * kWideThreads;
+            if (vi < nvec) {
+                const uint32_t k0 = keys2_canon(x[u].x), k1 = keys2_canon(x[u].y), k2 = keys2_canon(x[u].z),
+                               k3 = keys2_canon(x[u].w);
+                lo = min_u16x2(lo, min_u16x2(min_u16x2(k0, k1), min_u16x2(k2, k3)));
+                const uint32_t mx = max_u16x2(max_u16x2(k0, k1), max_u16x2(k2, k3));
+                const uint32_t vmax = max(mx & 0xFFFFu, mx >> 16);
+                if (vmax > best_key) {   // the vector's first element holding it
+                    best_key = vmax;
+                    const int jj = (k0 & 0xFFFFu) == vmax ? 0
+                                   : (k0 >> 16) == vmax   ? 1
+                                   : (k1 & 0xFFFFu) == vmax ? 2
+                                   : (k1 >> 16) == vmax   ? 3
+                                   : (k2 & 0xFFFFu) == vmax ? 4
+                                   : (k2 >> 16) == vmax   ? 5
+                                   : (k3 & 0xFFFFu) == vmax ? 6
+                                                            : 7;
+                    const int idx = head + 8 * vi + jj;
+                    const unsigned long long c = ((unsigned long long)vmax << 32) | (0xFFFFFFFFu - (uint32_t)idx);
+                    best = c > best ? c : best;
+                }
+            }
+        }
+    }
+    best = warp_max_u64(best);
+    uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, min(lo & 0xFFFFu, lo >> 16));
+    if (lane == 0) {
+        sm.red64[warp] = best;
+        sm.redi[warp] = (int)kmin;
+    }
+    __syncthreads();
+    int amax = 0;
+    if (tid == 0) {
+        for (int w = 0; w < kWideThreads / 32; ++w) {
+            best = sm.red64[w] > best ? sm.red64[w] : best;
+            kmin = min(kmin, (uint32_t)sm.redi[w]);
+        }
+        const uint32_t kmax = (uint32_t)(best >> 32);
+        amax = (int)(0xFFFFFFFFu - (uint32_t)best);
+        const float m = (float)key_value(kmax);
+        const int status = (kmax >= 0xFF80u || kmin < 0x007Fu) ? kNonfinite : 0;
+        RowInfo* info = a.info + task.slot;
+        info->desc.max_logit = m;
+        info->desc.argmax = amax;
+        info->desc.status = status;
+        info->desc.temperature = task.temp;
+        info->desc.log_norm = 0.0f;
+        info->desc.cutoff_logit = m;
+        info->cut_count = -1;
+        if (status) {
+            info->desc.cutoff_ties = 0;
+            info->desc.kept = 0;
+            info->p_token = nan("");
+            info->z = 0.0;
+            info->n_list = -1;
+        } else {
+            info->desc.cutoff_ties = 1;
+            info->desc.kept = 1;
+            info->p_token = task.token >= 0 ? (task.token == amax ? 1.0 : 0.0) : nan("");
+            info->z = 1.0;
+            info->z_rest = 0.0;
+            info->n_list = 1;
+            info->list_idx[0] = amax;
+            info->list_p[0] = 1.0;
+        }
+    }
+    __syncthreads();
+    return amax;
+}
+
 // Both rows of position j of request r are done (lazy chain verify): the
 // acceptance test the chain walk will make at j, made now; a rejection
 // lowers the request's known first rejection.  Thread 0 only.
@@ -1249,7 +1363,7 @@ __device__ __noinline__ void decide_position(const RowsArgs& a, int r, int j)
     if (!accept) atomicMin(&c.req[r].first_reject, j);
 }
 
-__global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(RowsArgs a)
+__global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(const __grid_constant__ RowsArgs a)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1285,7 +1399,13 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
     const int kinds = c.q_rows ? 1 : 2;   // rows per position (the draft's results may exist already)
     enum { kNone = 0, kFull = 1, kScan = 2 };
     if (U <= (int)gridDim.x) {   // no test is decided early then: no CTA would wait for one
-        if ((int)blockIdx.x < U) wide_row(sm, a, a.slow_tasks.get(blockIdx.x), blockIdx.x);
+        if ((int)blockIdx.x < U) {
+            const RowTask task = a.slow_tasks.get(blockIdx.x);
+            if (task.temp == 0.0f)
+                argmax_row(sm, a, task);
+            else
+                wide_row(sm, a, task, blockIdx.x);
+        }
         return;
     }
     for (;;) {
@@ -1304,9 +1424,10 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
                 // useless.  Bounded; after it the row gets its full pass as if
                 // nothing were decided.
                 const int32_t* done = &c.pair_done[(size_t)r * K1];
+                const int kr = c.req[r].greedy ? 1 : kinds;   // rows per position of this request
                 for (int spin = 0; spin < kDecideSpins && j <= fr; ++spin) {
                     int i = 0;
-                    while (i < j && __ldcg(done + i) > kinds) ++i;   // decided positions
+                    while (i < j && __ldcg(done + i) > kr) ++i;   // decided positions
                     if (i == j || __ldcg(done + i) == 0) break;      // all decided, or not started
                     __nanosleep(256);
                     fr = __ldcg(&c.req[r].first_reject);
@@ -1324,6 +1445,15 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(Ro
         __syncthreads();   // s_unit is rewritten only after every thread has read it
         if (mode == kNone) break;
         const RowTask task = a.slow_tasks.get(t);
+        if (task.temp == 0.0f) {   // a greedy row: the argmax scan, then its test (draft token == argmax)
+            const int amax = argmax_row(sm, a, task);
+            if (tid == 0 && j < c.req[r].v) {
+                if (c.draft_tokens[(size_t)r * c.K + j] != amax) atomicMin(&c.req[r].first_reject, j);
+                __threadfence();
+                atomicAdd(&c.pair_done[(size_t)r * K1 + j], 2);   // above one row: decided
+            }
+            continue;
+        }
         if (mode == kScan) {
             scan_row(sm, a, task);
             continue;

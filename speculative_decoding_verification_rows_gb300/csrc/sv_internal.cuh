@@ -587,7 +587,7 @@ struct ChainArgs {
     const RowInfo* q_rows;   // draft rows' results made beforehand ([n_req][K], sv_estimator_predict_q), or NULL
     int32_t* pair_done;  // [n_req][K + 1]: rows of position j finished on the histogram path (lazy)
     int2* slow_req;      // requests whose rows take the histogram path (lazy), n_slow_req of them:
-                         // {request << 6 | v, index of its first task}
+                         // {request << 7 | greedy << 6 | v, index of its first task}
     int2* slow_units;    // their rows in position order (lazy): {request << 7 | position << 1 | draft, task}
     ResampleJob* jobs;
     TileSums* tiles;   // [max_jobs][resample_tiles(vocab)]

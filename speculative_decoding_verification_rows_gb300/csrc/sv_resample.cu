@@ -508,7 +508,7 @@ __device__ __noinline__ void cost_split(ResSmem& sm, const ChainArgs& a, int j0,
     u_hi = (long long)n_hi;
 }
 
-__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(ChainArgs a, int n_units, int wave)
+__global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_constant__ ChainArgs a, int n_units, int wave)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];

@@ -532,7 +532,7 @@ __device__ void row32(R32Smem& sm, const RowsArgs& a, const RowTask& task)
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kR32Threads, 1) rows32_kernel(RowsArgs a)
+__global__ void __launch_bounds__(kR32Threads, 1) rows32_kernel(const __grid_constant__ RowsArgs a)
 {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -671,7 +671,7 @@ __device__ __forceinline__ void element_weights(const Dist32& P, const Dist32& Q
     }
 }
 
-__global__ void __launch_bounds__(kRs32Threads, 1) resample32_kernel(ChainArgs a, int wave)
+__global__ void __launch_bounds__(kRs32Threads, 1) resample32_kernel(const __grid_constant__ ChainArgs a, int wave)
 {
     pdl_enter();
     __shared__ Rs32Smem sm;

@@ -20,6 +20,21 @@ def test_promise_matches_the_row_paths(name, promise):
     assert fast + hist > 0
 
 
+def test_greedy_rows_follow_the_histogram_path_in_mixed_chain_batches():
+    # ragged mixes greedy and full-vocabulary requests: chain verification
+    # sends the greedy rows to the histogram kernel as argmax scans, block
+    # verification keeps them on the one-pass kernel
+    w = workloads.make("ragged", device="cpu", scale=SMALL["ragged"])
+    fast_c, hist_c = bench.path_bytes(w, None, "chain")
+    fast_b, hist_b = bench.path_bytes(w, None, "block")
+    assert fast_c == 0 and hist_c == fast_b + hist_b
+    assert fast_b > 0 and hist_b > 0
+    # a batch with no full-vocabulary request keeps its greedy rows on the one-pass kernel
+    w2 = workloads.make("large", device="cpu", scale=SMALL["large"])
+    w2.temperature[0] = 0.0
+    assert bench.path_bytes(w2, None, "chain")[1] == 0
+
+
 def test_promise_is_broken_by_one_request():
     w = workloads.make("large", device="cpu", scale=SMALL["large"])
     w.top_k[1] = 33
