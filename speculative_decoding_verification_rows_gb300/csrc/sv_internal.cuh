@@ -378,6 +378,84 @@ __device__ __forceinline__ dfloat df_mul(dfloat a, dfloat b)
     return dfloat{hi, e - (hi - p)};
 }
 
+// More double-float pieces, and exp in double-float arithmetic (on GB300 the
+// fp64 pipe runs at a 64th of the fp32 rate, so an fp64 exp per element, or
+// per table entry, would dominate the kernels that need them).
+constexpr double kLn2 = 0.69314718055994530942;   // ln 2
+__device__ __forceinline__ dfloat df_two_sum(float a, float b)   // a + b exactly
+{
+    const float s = a + b;
+    const float bb = s - a;
+    return dfloat{s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ dfloat df_add(dfloat a, dfloat b)
+{
+    const dfloat s = df_two_sum(a.hi, b.hi);
+    const float e = s.lo + a.lo + b.lo;
+    const float hi = s.hi + e;
+    return dfloat{hi, e - (hi - s.hi)};
+}
+
+// (x - m) / T as a double-float: the difference exactly, the quotient's
+// remainder recovered by an FMA (inv_t = 1 / T rounded; the remainder
+// corrects the first quotient to about 2^-46).
+__device__ __forceinline__ dfloat scaled_logit(float x, float m, float T, float inv_t)
+{
+    const dfloat d = df_two_sum(x, -m);
+    const float q1 = d.hi * inv_t;
+    const float q2 = (fmaf(-q1, T, d.hi) + d.lo) * inv_t;
+    const float hi = q1 + q2;
+    return dfloat{hi, q2 - (hi - q1)};
+}
+
+// exp(a) for -87 <= a <= 88, about 2^-46 relative (0 below -87, where fp32
+// ends).
+// Reduction a = k ln2 / 64 + r (Tang, "Table-driven implementation of the
+// exponential function in IEEE floating-point arithmetic", 1989), with
+// |r| <= ln2 / 128; exp(r) = 1 + r + r^2/2 + r^3 (1/6 + r/24 + r^2/120 +
+// r^3/720), the last factor in fp32 (it is below 2^-22 of the sum); then
+// times 2^(j/64) from the table and 2^n.
+constexpr float kExpK = (float)(64.0 / kLn2);
+constexpr float kCHi = 1420.0f / 131072.0f;   // ln2 / 64 to 11 bits: k * kCHi is exact for |k| < 2^13
+constexpr double kCRest = kLn2 / 64.0 - (double)kCHi;
+constexpr float kCRestHi = (float)kCRest, kCRestLo = (float)(kCRest - (double)kCRestHi);
+
+__device__ __forceinline__ dfloat exp_df(dfloat a, const dfloat* tab)
+{
+    if (!(a.hi >= -87.0f)) return dfloat{0.0f, 0.0f};
+    const float kf = rintf(a.hi * kExpK);
+    dfloat r = df_two_sum(a.hi, -kf * kCHi);
+    r = df_add(r, dfloat{a.lo, 0.0f});
+    r = df_add(r, df_mul(dfloat{kCRestHi, kCRestLo}, dfloat{-kf, 0.0f}));
+    const float rh = r.hi;
+    const float q = fmaf(fmaf(fmaf(rh, 1.0f / 720.0f, 1.0f / 120.0f), rh, 1.0f / 24.0f), rh, 1.0f / 6.0f);
+    const dfloat r2 = df_mul(r, r);
+    dfloat s = df_add(r, dfloat{0.5f * r2.hi, 0.5f * r2.lo});
+    s = df_add_f(s, rh * rh * rh * q);
+    dfloat e = df_add_f(s, 1.0f);
+    const int k = (int)kf;
+    e = df_mul(e, tab[k & 63]);
+    const int n = k >> 6;   // floor(k / 64), in [-126, 127] for -87 <= a <= 88: 2^n is a normal float
+    const float p2 = __int_as_float((n + 127) << 23);
+    return dfloat{e.hi * p2, e.lo * p2};
+}
+
+// 2^(j / 64), j = 0..63, as double-floats (every thread calls it).
+__device__ __forceinline__ void fill_exp_table(dfloat* tab)
+{
+    for (int j = threadIdx.x; j < 64; j += blockDim.x) tab[j] = df_of(exp2((double)j / 64.0));
+    __syncthreads();
+}
+
+// floor(e * 2^s) for 0 <= e <= 1 held as a double-float (s = 58 or 62).
+__device__ __forceinline__ unsigned long long fix_df(dfloat e, float scale)
+{
+    const unsigned long long h = __float2ull_rz(e.hi * scale);   // up to 2^62
+    const long long l = __float2ll_rd(e.lo * scale);              // |l| below 2^40
+    if (l < 0 && (unsigned long long)(-l) > h) return 0ull;
+    return h + (unsigned long long)l;                             // two's complement: h - |l| for l < 0
+}
+
 // ----------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): counter (req, pos, draw, 0),
 // key (seed low, seed high); u = (word0 >> 8) * 2^-24.

@@ -30,6 +30,7 @@ namespace sv {
 namespace {
 
 constexpr double kFix = 4611686018427387904.0;   // 2^62
+constexpr float kFix62f = 4611686018427387904.0f;  // the same as a float
 constexpr int kSmallLo = 135, kSmallHi = 377;      // binades of |v| < 2^-6 (both signs, and the zeros)
 
 struct Dist {                 // one row's distribution, as the weight passes need it
@@ -103,7 +104,8 @@ static_assert((kResTile / 2) % kResStep == 0, "a tile is whole steps");
 struct ResSmem {
     unsigned long long buf[kResWarps * kResWarpBuf];   // per warp: its candidates, then (rescan) their weights
     unsigned long long tab[kResBinades * 128];
-    double ratio[kResBinades];                      // per slot: exp(step / T) along the binade (0: one exp per key)
+    dfloat ratio[kResBinades];                      // per slot: exp(step / T) along the binade (0: one exp per key)
+    dfloat exp_tab[64];                             // 2^(j / 64) for the double-float exp
     uint32_t zkey[2];                               // the loaded job's zero keys of p and q
     int16_t map[2][512];
     int slot_bin[kResBinades];
@@ -212,32 +214,38 @@ __device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
     }
     __syncthreads();
     // the step ratio of each slot's binade, then 8 keys per thread: one exp,
-    // a geometric recurrence along the mantissa, a product with 1 / Z
+    // a geometric recurrence along the mantissa, a product with 1 / Z -- in
+    // double-float arithmetic (about 2^-46; the fp64 pipe would make these
+    // tables a large part of a job's time)
     for (int sl = tid; sl < capP + capQ; sl += kResThreads) {
         const Dist& D = sm.slot_dist[sl] ? Q : P;
         const uint32_t kb = (uint32_t)sm.slot_bin[sl] * 128u;
-        const double x = (key_value(kb + 1u) - key_value(kb)) / D.T;
-        sm.ratio[sl] = x <= 1.0 ? exp(x) : 0.0;
+        const float T = (float)D.T;
+        const dfloat x = scaled_logit(f32_of_key16(kb + 1u), f32_of_key16(kb), T, 1.0f / T);   // step / T >= 0
+        sm.ratio[sl] = x.hi <= 1.0f ? exp_df(x, sm.exp_tab) : dfloat{0.0f, 0.0f};
     }
     __syncthreads();
-    const double inv_tp = 1.0 / P.T, inv_tq = 1.0 / Q.T, inv_zp = 1.0 / P.z, inv_zq = 1.0 / Q.z;
+    const dfloat inv_zp = df_of(1.0 / P.z), inv_zq = df_of(1.0 / Q.z);
     for (int item = tid; item < (capP + capQ) * 16; item += kResThreads) {
         const int sl = item >> 4, g = item & 15;
         const bool isq = sm.slot_dist[sl] != 0;
         const Dist& D = isq ? Q : P;
         const uint32_t k0 = (uint32_t)sm.slot_bin[sl] * 128u + 8u * (uint32_t)g;
-        const double R = sm.ratio[sl], inv_z = isq ? inv_zq : inv_zp;
+        const dfloat R = sm.ratio[sl], inv_z = isq ? inv_zq : inv_zp;
+        const float m = (float)D.m, T = (float)D.T, inv_t = 1.0f / T;
         unsigned long long* out = sm.tab + sl * 128 + 8 * g;
-        if (R > 0.0) {
-            double cur = exp((key_value(k0) - D.m) * (isq ? inv_tq : inv_tp));
+        if (R.hi > 0.0f) {
+            dfloat cur = exp_df(scaled_logit(f32_of_key16(k0), m, T, inv_t), sm.exp_tab);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                out[j] = fix_of(cur * inv_z);
-                cur *= R;
+                out[j] = fix_df(df_mul(cur, inv_z), kFix62f);
+                cur = df_mul(cur, R);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) out[j] = fix_of(exp((key_value(k0 + j) - D.m) / D.T) * inv_z);
+            for (int j = 0; j < 8; ++j)
+                out[j] = fix_df(df_mul(exp_df(scaled_logit(f32_of_key16(k0 + j), m, T, inv_t), sm.exp_tab), inv_z),
+                                kFix62f);
         }
     }
     __syncthreads();
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
     long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
     if (n_jobs <= kResCostJobs && total >= 4ll * gridDim.x) cost_split(sm, a, j0, n_jobs, n_units, u_lo, u_hi);
     if (tid == 0) sm.cur_job = -1;
-    __syncthreads();
+    fill_exp_table(sm.exp_tab);
     for (long long u = u_lo; u < u_hi; ++u) {
         const int j = j0 + (int)(u / n_units), c = (int)(u % n_units);
         const ResampleJob job = a.jobs[j];
