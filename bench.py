@@ -19,6 +19,7 @@ slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -72,7 +73,19 @@ def parse():
                         "no exchange, one GPU holds every shard)")
     p.add_argument("--no-promise", action="store_true",
                    help="never pass the small-top-k sampling promise (the full launch sequence of every call)")
+    p.add_argument("--fp32", action="store_true",
+                   help="the workload's logits in fp32 instead of bf16 (the same values, twice the bytes)")
     return p.parse_args()
+
+
+def make_workload(args, dev, scale=None):
+    """The named workload, its logits in fp32 when --fp32 asks for it."""
+    from speculative_decoding_verification_rows_gb300 import workloads
+    w = workloads.make(args.workload, device=dev, scale=scale)
+    if getattr(args, "fp32", False) and w.dtype != torch.float32:
+        w = dataclasses.replace(w, dtype=torch.float32, target=w.target.float().contiguous(),
+                                draft=None if w.draft is None else w.draft.float().contiguous())
+    return w
 
 
 # ----------------------------------------------------------------------------
@@ -366,14 +379,14 @@ def run_ours(args, rank, world, local):
     sv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workloads.make(args.workload, device=dev, scale=dict(n=args.requests) if args.requests else None)
+    w = make_workload(args, dev, scale=dict(n=args.requests) if args.requests else None)
     step, out, extra = make_step(w, sv, dev, args.method, args.cost_table, args.estimator, not args.no_promise,
                                  args.shards)
     alg_bytes, rows_t = algorithmic_bytes(w)
     fast_bytes, hist_bytes = path_bytes(w, None, args.method, not args.no_promise and small_topk(w))
     if extra is not None:
         rows_t = extra["rows"]
-        alg_bytes = (rows_t + extra["draft_rows"]) * w.V * 2
+        alg_bytes = (rows_t + extra["draft_rows"]) * w.V * (2 if w.dtype == torch.bfloat16 else 4)
         fast_bytes, hist_bytes = extra["path_bytes"]
     # the roofline is taken on the path that reads more of the logits (with
     # vocabulary shards: over the whole step)
@@ -742,7 +755,7 @@ def run_reference(args, rank, world, local):
     from speculative_decoding_verification_rows_gb300 import workloads
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = workloads.make(args.workload, device=dev)
+    w = make_workload(args, dev)
     extra = ragged_host_plan(w, None) if w.layout == "ragged" else None
     times, rows = [], 0
     with pinned_core() as pin:

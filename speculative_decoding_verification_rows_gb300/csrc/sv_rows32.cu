@@ -32,8 +32,8 @@ constexpr int kR32Threads = 512;
 constexpr int kR32Warps = kR32Threads / 32;
 constexpr int kR32Bins = 2048;                      // bins of a level (11 key bits; the last level has 10)
 constexpr int kR32Copies = 4;                       // copies of each bin's counters (lane & 3): fewer lanes per address
-constexpr float kTwo58 = 288230376151711744.0f;     // 2^58: an element's mass in 2^-58 units, so 32 of them fit 64 bits
-constexpr float kTwo62 = 4611686018427387904.0f;    // 2^62
+// An element's mass is summed in 2^-58 units (fix_split(e, 29)); the
+// resample's weights are 2^-62 units (fix_split(p, 31)), as in the bf16 one.
 
 // Canonical order key of an fp32 pattern (-0 as +0): larger value, larger key.
 __device__ __forceinline__ uint32_t key32(uint32_t u)
@@ -46,6 +46,20 @@ __device__ __forceinline__ float value32(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 constexpr uint32_t kKeyNegInf = 0x007FFFFFu;   // key of -inf
+
+// floor(e 2^(2 hb)) for 0 <= e <= 1 held as a double-float, hb <= 31, with
+// 32-bit conversions only: e 2^hb = a + f (a its integer part), then
+// floor((f + lo 2^hb) 2^hb); about 2^-24 of a unit of 2^hb is lost in f's
+// rounding, far below the margins the sums serve.
+__device__ __forceinline__ unsigned long long fix_split(dfloat e, int hb)
+{
+    const float s = __int_as_float((127 + hb) << 23);   // 2^hb
+    const float h = e.hi * s;
+    const float a = truncf(h);
+    const int b = __float2int_rd(((h - a) + e.lo * s) * s);   // may be slightly negative
+    const long long v = ((long long)(unsigned)a << hb) + b;
+    return v > 0 ? (unsigned long long)v : 0ull;
+}
 
 __device__ __forceinline__ double u128_to_double(u128 x)
 {
@@ -138,7 +152,7 @@ __device__ void level_pass(R32Smem& sm, const float* row, int V, float m, float 
         const int b = (int)((k >> shift) & (uint32_t)(nbins - 1));
         const dfloat sl = scaled_logit(x, m, T, inv_t);
         // below -41 the mass is under 2^-59: it floors to 0 in 2^-58 units
-        const unsigned long long v = sl.hi < -41.0f ? 0ull : fix_df(exp_df(sl, sm.tab), kTwo58);
+        const unsigned long long v = sl.hi < -41.0f ? 0ull : fix_split(exp_df(sl, sm.tab), 29);
         atomicAdd(&sm.cnt[cp][b], 1u);
         if (v) {
             const unsigned long long old = atomicAdd(&sm.mlo[cp][b], v);
@@ -370,7 +384,7 @@ __device__ void row32(R32Smem& sm, const RowsArgs& a, const RowTask& task)
         cut_key = c.key;
         ties = (uint32_t)kk - c.above;
         cut_count = c.count;
-        e_cut = (u128)fix_df(exp_df(scaled_logit(value32(c.key), m, T, inv_t), sm.tab), kTwo58);
+        e_cut = (u128)fix_split(exp_df(scaled_logit(value32(c.key), m, T, inv_t), sm.tab), 29);
         kept = (uint32_t)kk;
         z_fix = c.above_mass + (u128)ties * e_cut;
         min_key = c.key;
@@ -400,7 +414,7 @@ __device__ void row32(R32Smem& sm, const RowsArgs& a, const RowTask& task)
             const u128 prod = z_fix * (u128)M;
             const u128 target = sh >= 127 ? (u128)1 : (prod + ((((u128)1) << sh) - 1)) >> sh;
             const Cut c = descend(sm, row, V, m, T, true, 0u, target, min_key, excess, excess_mass, !topk_on);
-            const u128 e_c = (u128)fix_df(exp_df(scaled_logit(value32(c.key), m, T, inv_t), sm.tab), kTwo58);
+            const u128 e_c = (u128)fix_split(exp_df(scaled_logit(value32(c.key), m, T, inv_t), sm.tab), 29);
             // ties of the value needed to reach the target (at least one)
             const u128 need = target > c.above_mass ? target - c.above_mass : (u128)0;
             uint32_t t = e_c ? (uint32_t)((need + e_c - 1) / e_c) : c.count;
@@ -562,7 +576,7 @@ __device__ __forceinline__ unsigned long long sat_sub64(unsigned long long x, un
 __device__ __forceinline__ unsigned long long weight32(const Dist32& D, float x, const dfloat* tab)
 {
     const dfloat e = exp_df(scaled_logit(x, D.m, D.T, D.inv_t), tab);
-    return fix_df(df_mul(e, df_of(D.inv_z)), kTwo62);
+    return fix_split(df_mul(e, df_of(D.inv_z)), 31);
 }
 
 // Element x's residual weight and p weight, given the ranks of x among the
