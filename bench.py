@@ -543,8 +543,11 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                    "launch": graph_note},
-        "roofline": {"bound": "hbm", "kernel": ROW_PATHS[roof_path]["kernel"] if not args.shards else
-                     f"whole step over {args.shards} vocabulary shards (records + merge)",
+        "roofline": {"bound": "hbm", "kernel": (f"whole step over {args.shards} vocabulary shards (records + merge)"
+                                                if args.shards else
+                                                "rows32_kernel (fp32 radix descent, top-p over the vocabulary)"
+                                                if roof_path == "hist" and w.dtype == torch.float32 else
+                                                ROW_PATHS[roof_path]["kernel"]),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
                      "traffic": recorded_traffic(args.workload, roof_path), "kernel_ms_mean": statistics.mean(kern_ms),
