@@ -1424,8 +1424,9 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(co
                 // useless.  Bounded; after it the row gets its full pass as if
                 // nothing were decided.
                 const int32_t* done = &c.pair_done[(size_t)r * K1];
-                const int kr = c.req[r].greedy ? 1 : kinds;   // rows per position of this request
-                for (int spin = 0; spin < kDecideSpins && j <= fr; ++spin) {
+                const bool greedy = c.req[r].greedy != 0;     // its rows get the argmax scan whatever is decided
+                const int kr = greedy ? 1 : kinds;           // rows per position of this request
+                for (int spin = 0; spin < kDecideSpins && j <= fr && !greedy; ++spin) {
                     int i = 0;
                     while (i < j && __ldcg(done + i) > kr) ++i;   // decided positions
                     if (i == j || __ldcg(done + i) == 0) break;      // all decided, or not started
