@@ -15,13 +15,13 @@
 // below the one whose weight floors to 0 weigh 0; any other kept key (small
 // magnitudes, or binades beyond the table) gets its own fp64 exp.
 //
-// Every row is cut into chunks of kResampleUnit elements spread over a
-// persistent grid.  A chunk's CTA bulk-copies the chunk of p's and q's rows
-// into shared memory, streams it once and leaves the chunk's sums, with the
-// tied elements summed in each of their possible states.  The CTA that
-// finishes a job's last chunk combines the sums, rescans in index order the
-// (at most two) chunks where a tie group's kept part ends, and then the one
-// chunk that holds the target, to find the token.
+// Every row is cut into tiles, eight tiles (one per warp) to a chunk, and the
+// chunks of all jobs are spread over a persistent grid.  A warp streams its
+// tiles of p's and q's rows once, straight from global memory, and leaves
+// each tile's sums, with the tied elements summed in each of their possible
+// states.  The CTA that finishes a job's last chunk combines the sums,
+// rescans in index order the (at most two) tiles where a tie group's kept
+// part ends, and then the one tile that holds the target, to find the token.
 #include <math.h>
 
 #include "sv_internal.cuh"
@@ -136,6 +136,17 @@ __device__ __forceinline__ int tabled_in(int x, int y)
     return n;
 }
 
+// The job's p row (target logits at its position) and q row (draft logits).
+__device__ __forceinline__ const uint16_t* job_p_row(const ChainArgs& a, int r, int pa)
+{
+    const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (a.K + 1) + pa;
+    return (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
+}
+__device__ __forceinline__ const uint16_t* job_q_row(const ChainArgs& a, int r, int pa)
+{
+    return (const uint16_t*)a.drf + ((size_t)r * a.K + pa) * (size_t)a.stride_d;
+}
+
 // The job's p and q as the weight passes need them (tables in shared memory;
 // the zero keys are those load_tables found for the loaded job).
 __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob& job, ResSmem& sm, Dist& P, Dist& Q)
@@ -143,8 +154,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
     const int r = job.req, pa = job.a, K = a.K;
     const RowInfo& IP = a.info[slot_target(r, K, pa)];
     const RowInfo& IQ = draft_info(a, r, pa);
-    const int64_t trow = a.layout == 1 ? (int64_t)a.qo_indptr[r] + pa : (int64_t)r * (K + 1) + pa;
-    P.row = (const uint16_t*)a.tgt + (size_t)trow * (size_t)a.stride_t;
+    P.row = job_p_row(a, r, pa);
     P.m = IP.desc.max_logit;
     P.T = IP.desc.temperature;
     P.z = IP.z;
@@ -157,7 +167,7 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
     P.wfix = job.wfix;
     Q = P;
     if (job.residual) {
-        Q.row = (const uint16_t*)a.drf + ((size_t)r * K + pa) * (size_t)a.stride_d;
+        Q.row = job_q_row(a, r, pa);
         Q.m = IQ.desc.max_logit;
         Q.T = IQ.desc.temperature;
         Q.z = IQ.z;
@@ -533,8 +543,11 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
     if (n_jobs <= kResCostJobs && total >= 4ll * gridDim.x) cost_split(sm, a, j0, n_jobs, n_units, u_lo, u_hi);
     if (tid == 0) sm.cur_job = -1;
     fill_exp_table(sm.exp_tab);
-    for (long long u = u_lo; u < u_hi; ++u) {
-        const int j = j0 + (int)(u / n_units), c = (int)(u % n_units);
+    // this CTA's chunks, one job at a time: [u, u_end) are those of job j
+    for (long long u = u_lo, u_end; u < u_hi; u = u_end) {
+        const int j = j0 + (int)(u / n_units);
+        u_end = min(u_hi, (long long)(j - j0 + 1) * n_units);
+        const int c_lo = (int)(u - (long long)(j - j0) * n_units), c_hi = c_lo + (int)(u_end - u);
         const ResampleJob job = a.jobs[j];
         const bool residual = job.residual != 0;
         Dist P, Q;
@@ -546,122 +559,129 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
         const bool vec_ok = ((uintptr_t)P.row & 15u) == 0u && (!residual || ((uintptr_t)Q.row & 15u) == 0u);
         TileSums* recs = a.tiles + (size_t)j * n_tiles;
 
-        // 1. one tile of the chunk per warp: tie counts over every element,
-        //    weights over the elements at or above p's cutoff (the others have
-        //    p = 0 in every state), gathered densely in the warp's buffer and
-        //    weighed a batch at a time; the warp writes the tile's record.
-        //    Each lane loads 16-byte vectors straight from the rows, the next
-        //    step's while it works on this one.
-        const int tile = c * kResWarps + warp;
-        const int t0 = tile * tile_len;
-        if (t0 < V) {
+        // 1. each warp streams its tiles of the chunks (tile c * warps + warp
+        //    of chunk c), with no barrier between them: tie counts over every
+        //    element, weights over the elements at or above p's cutoff (the
+        //    others have p = 0 in every state), gathered densely in the warp's
+        //    buffer and weighed a batch at a time; the warp writes each tile's
+        //    record.  Each lane loads 16-byte vectors straight from the rows,
+        //    the next step's (of this tile or the next) while it works on this
+        //    one.
+        {
             unsigned long long* wb = sm.buf + warp * kResWarpBuf;
             unsigned long long* tacc = sm.tacc[warp];   // elements tied at a partial cutoff: rare, summed here
-            const int t_end = min(V, t0 + tile_len);
-            unsigned long long base_res = 0ull, base_p = 0ull;
-            int ties_p = 0, ties_q = 0;
-            if (lane < kTsTiesP - kTsTieRes) tacc[lane] = 0ull;
-            int nbuf = 0;
-            // the weights of the gathered candidates, into acc
-            auto weigh = [&]() {
-                __syncwarp();
-                for (int e = lane; e < nbuf; e += 32) {
-                    const uint32_t en = (uint32_t)wb[e];
-                    const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
-                    const bool tP = P.partial && ekp == P.cut_key;
-                    const bool tQ = residual && Q.partial && ekq == Q.cut_key;
-                    const unsigned long long wp = fixp(P, ekp);
-                    const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
-                    const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
-                    const unsigned long long wpw = pweight(P, wp);   // p's weighted value in the residual
-                    if (!tP && !tQ) {
-                        base_p += wp;
-                        base_res += residual ? sat_sub(wpw, wq) : wp;
-                    } else {
-                        const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
+            const int tile_hi = min(n_tiles, c_hi * kResWarps);
+            int tile = c_lo * kResWarps + warp;
+            uint4 np[2], nq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            auto load_step = [&](int x_step, int x_end) {
 #pragma unroll
-                        for (int sp_ = 0; sp_ < 2; ++sp_) {
-                            const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
-                            const unsigned long long pw_ = (tP && !sp_) ? 0ull : wpw;
-                            atomicAdd(&tacc[kTsTieP - kTsTieRes + sp_], p_);
+                for (int h = 0; h < 2; ++h) {
+                    const int x0 = x_step + h * 256 + 8 * lane;
+                    np[h] = load_raw8(P.row, x0, x_end, vec_ok);
+                    if (residual) nq[h] = load_raw8(Q.row, x0, x_end, vec_ok);
+                }
+            };
+            if (tile < tile_hi) load_step(tile * tile_len, min(V, (tile + 1) * tile_len));
+            for (; tile < tile_hi; tile += kResWarps) {
+                const int t0 = tile * tile_len;
+                const int t_end = min(V, t0 + tile_len);
+                unsigned long long base_res = 0ull, base_p = 0ull;
+                int ties_p = 0, ties_q = 0;
+                if (lane < kTsTiesP - kTsTieRes) tacc[lane] = 0ull;
+                int nbuf = 0;
+                // the weights of the gathered candidates, into acc
+                auto weigh = [&]() {
+                    __syncwarp();
+                    for (int e = lane; e < nbuf; e += 32) {
+                        const uint32_t en = (uint32_t)wb[e];
+                        const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
+                        const bool tP = P.partial && ekp == P.cut_key;
+                        const bool tQ = residual && Q.partial && ekq == Q.cut_key;
+                        const unsigned long long wp = fixp(P, ekp);
+                        const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
+                        const unsigned long long wq = qk ? fixp(Q, ekq) : 0ull;
+                        const unsigned long long wpw = pweight(P, wp);   // p's weighted value in the residual
+                        if (!tP && !tQ) {
+                            base_p += wp;
+                            base_res += residual ? sat_sub(wpw, wq) : wp;
+                        } else {
+                            const unsigned long long wqt = tQ ? fixp(Q, ekq) : wq;
 #pragma unroll
-                            for (int sq = 0; sq < 2; ++sq) {
-                                const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
-                                atomicAdd(&tacc[2 * sp_ + sq], residual ? sat_sub(pw_, q_) : p_);
+                            for (int sp_ = 0; sp_ < 2; ++sp_) {
+                                const unsigned long long p_ = (tP && !sp_) ? 0ull : wp;
+                                const unsigned long long pw_ = (tP && !sp_) ? 0ull : wpw;
+                                atomicAdd(&tacc[kTsTieP - kTsTieRes + sp_], p_);
+#pragma unroll
+                                for (int sq = 0; sq < 2; ++sq) {
+                                    const unsigned long long q_ = tQ ? (sq ? wqt : 0ull) : wq;
+                                    atomicAdd(&tacc[2 * sp_ + sq], residual ? sat_sub(pw_, q_) : p_);
+                                }
                             }
                         }
                     }
-                }
-                __syncwarp();
-                nbuf = 0;
-            };
-            uint4 np[2], nq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-            const int t_stop = t0 + tile_len;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int x0 = t0 + h * 256 + 8 * lane;
-                np[h] = load_raw8(P.row, x0, t_end, vec_ok);
-                if (residual) nq[h] = load_raw8(Q.row, x0, t_end, vec_ok);
-            }
-            for (int s0 = t0;; s0 += kResStep) {   // one weighing site: the loop body stays small
-                const bool more = s0 < t_stop;
-                if (more) {
-                    const uint4 cp[2] = {np[0], np[1]}, cq[2] = {nq[0], nq[1]};
-                    if (s0 + kResStep < t_stop)
+                    __syncwarp();
+                    nbuf = 0;
+                };
+                const int t_stop = t0 + tile_len;
+                for (int s0 = t0;; s0 += kResStep) {   // one weighing site: the loop body stays small
+                    const bool more = s0 < t_stop;
+                    if (more) {
+                        const uint4 cp[2] = {np[0], np[1]}, cq[2] = {nq[0], nq[1]};
+                        if (s0 + kResStep < t_stop)
+                            load_step(s0 + kResStep, t_end);
+                        else if (tile + kResWarps < tile_hi)   // the first step of the warp's next tile
+                            load_step(t0 + kResWarps * tile_len, min(V, t0 + (kResWarps + 1) * tile_len));
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const int x0 = s0 + kResStep + h * 256 + 8 * lane;
-                            np[h] = load_raw8(P.row, x0, t_end, vec_ok);
-                            if (residual) nq[h] = load_raw8(Q.row, x0, t_end, vec_ok);
-                        }
+                            // raw key pairs (two elements per word); most elements are
+                            // below p's cutoff and need no more than the pair-wise tie
+                            // counts and one packed maximum for the lane's eight
+                            const uint32_t rp[4] = {keys2_raw(cp[h].x), keys2_raw(cp[h].y), keys2_raw(cp[h].z),
+                                                    keys2_raw(cp[h].w)};
+                            uint32_t rq[4] = {0u, 0u, 0u, 0u};   // canonical key 0 stands for q in p's own draw
+                            if (residual) {
+                                rq[0] = keys2_raw(cq[h].x);
+                                rq[1] = keys2_raw(cq[h].y);
+                                rq[2] = keys2_raw(cq[h].z);
+                                rq[3] = keys2_raw(cq[h].w);
+                            }
+                            if (P.partial) ties_p += ties8(rp, P.cut_key);
+                            if (residual && Q.partial) ties_q += ties8(rq, Q.cut_key);
+                            uint32_t cm = 0u;
+                            const uint32_t mx = max_u16x2(max_u16x2(rp[0], rp[1]), max_u16x2(rp[2], rp[3]));
+                            if (max(mx & 0xFFFFu, mx >> 16) + 1u >= P.cut_key)   // -0's raw key sits one below +0's
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        // raw key pairs (two elements per word); most elements are
-                        // below p's cutoff and need no more than the pair-wise tie
-                        // counts and one packed maximum for the lane's eight
-                        const uint32_t rp[4] = {keys2_raw(cp[h].x), keys2_raw(cp[h].y), keys2_raw(cp[h].z),
-                                                keys2_raw(cp[h].w)};
-                        uint32_t rq[4] = {0u, 0u, 0u, 0u};   // canonical key 0 stands for q in p's own draw
-                        if (residual) {
-                            rq[0] = keys2_raw(cq[h].x);
-                            rq[1] = keys2_raw(cq[h].y);
-                            rq[2] = keys2_raw(cq[h].z);
-                            rq[3] = keys2_raw(cq[h].w);
+                                for (int i = 0; i < 8; ++i)
+                                    if (canon_key(rp, i) >= P.cut_key) cm |= 1u << i;
+                            if (__any_sync(0xFFFFFFFFu, cm != 0u))
+                                nbuf += compact8(wb + nbuf, cm, [&](int i) {
+                                    return (unsigned long long)canon_key(rp, i) |
+                                           ((unsigned long long)canon_key(rq, i) << 16);
+                                });
                         }
-                        if (P.partial) ties_p += ties8(rp, P.cut_key);
-                        if (residual && Q.partial) ties_q += ties8(rq, Q.cut_key);
-                        uint32_t cm = 0u;
-                        const uint32_t mx = max_u16x2(max_u16x2(rp[0], rp[1]), max_u16x2(rp[2], rp[3]));
-                        if (max(mx & 0xFFFFu, mx >> 16) + 1u >= P.cut_key)   // -0's raw key sits one below +0's
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                if (canon_key(rp, i) >= P.cut_key) cm |= 1u << i;
-                        if (__any_sync(0xFFFFFFFFu, cm != 0u))
-                            nbuf += compact8(wb + nbuf, cm, [&](int i) {
-                                return (unsigned long long)canon_key(rp, i) | ((unsigned long long)canon_key(rq, i) << 16);
-                            });
                     }
+                    if (!more || nbuf > kResWarpBuf - kResStep) weigh();   // room for the next step's candidates
+                    if (!more) break;
                 }
-                if (!more || nbuf > kResWarpBuf - kResStep) weigh();   // room for the next step's candidates
-                if (!more) break;
-            }
-            base_res = warp_sum_u63(base_res);
-            base_p = warp_sum_u63(base_p);
-            ties_p = __reduce_add_sync(0xFFFFFFFFu, ties_p);
-            ties_q = __reduce_add_sync(0xFFFFFFFFu, ties_q);
-            if (lane == 0) {
-                TileSums& rec = recs[tile];
-                rec.v[kTsBaseRes] = base_res;
-                rec.v[kTsBaseP] = base_p;
+                base_res = warp_sum_u63(base_res);
+                base_p = warp_sum_u63(base_p);
+                ties_p = __reduce_add_sync(0xFFFFFFFFu, ties_p);
+                ties_q = __reduce_add_sync(0xFFFFFFFFu, ties_q);
+                if (lane == 0) {
+                    TileSums& rec = recs[tile];
+                    rec.v[kTsBaseRes] = base_res;
+                    rec.v[kTsBaseP] = base_p;
 #pragma unroll
-                for (int f = kTsTieRes; f < kTsTiesP; ++f) rec.v[f] = tacc[f - kTsTieRes];
-                rec.v[kTsTiesP] = (unsigned long long)ties_p;
-                rec.v[kTsTiesQ] = (unsigned long long)ties_q;
-                __threadfence();   // the tile's record, before the chunk is counted done
+                    for (int f = kTsTieRes; f < kTsTiesP; ++f) rec.v[f] = tacc[f - kTsTieRes];
+                    rec.v[kTsTiesP] = (unsigned long long)ties_p;
+                    rec.v[kTsTiesQ] = (unsigned long long)ties_q;
+                }
+                __syncwarp();   // tacc is reset for the next tile only after lane 0 read it
             }
+            if (lane == 0) __threadfence();   // the warp's records, before its chunks are counted done
         }
         __syncthreads();
-        if (tid == 0) sm.last = atomicAdd(&a.jobs[j].done, 1) == n_units - 1;
+        if (tid == 0) sm.last = atomicAdd(&a.jobs[j].done, c_hi - c_lo) + (c_hi - c_lo) == n_units;
         __syncthreads();
         if (!sm.last) continue;
         __threadfence();
