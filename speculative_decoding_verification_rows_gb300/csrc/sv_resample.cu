@@ -294,13 +294,6 @@ __device__ __forceinline__ uint4 load_raw8(const uint16_t* row, int x0, int x_en
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Element i's key (canonical: -0 as +0) from four words of raw key pairs.
-__device__ __forceinline__ uint32_t canon_key(const uint32_t r[4], int i)
-{
-    const uint32_t k = (r[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-    return k == 0x7FFFu ? 0x8000u : k;
-}
-
 // Elements among eight (four words of raw key pairs) whose canonical key is
 // `cut` (a canonical key: at +0 the raw keys of -0 count too).
 __device__ __forceinline__ int ties8(const uint32_t r[4], uint32_t cut)
@@ -314,6 +307,35 @@ __device__ __forceinline__ int ties8(const uint32_t r[4], uint32_t cut)
         for (int i = 0; i < 4; ++i) n += zero_halves(r[i] ^ 0x7FFF7FFFu);
     return n;
 }
+
+// Bit i set for element i among eight (four words of raw key pairs) whose
+// canonical key is at least `cut` (a canonical key).  Raw keys order as the
+// canonical ones do except -0, one below +0: at a cut of +0 the raw test
+// starts one lower.
+__device__ __forceinline__ uint32_t at_least8(const uint32_t r[4], uint32_t cut)
+{
+    const uint32_t c2 = (cut == 0x8000u ? 0x7FFFu : cut) * 0x10001u;
+    uint32_t below = 0u;   // bits 15 + 2w and 31 + 2w: the half of word w is below the cut
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t d = max_u16x2(r[w], c2) ^ r[w];   // a half is 0 where it is at least the cut
+        const uint32_t nz = (((d & 0x7FFF7FFFu) + 0x7FFF7FFFu) | d) & 0x80008000u;
+        below |= nz >> (15 - 2 * w);
+    }
+    below |= below >> 15;   // word w's high half from bit 16 + 2w to bit 1 + 2w
+    return ~below & 0xFFu;
+}
+
+// Element i's raw p key (low half) and raw q key (high half) from a word of
+// each.
+__device__ __forceinline__ uint32_t pair_raw(const uint32_t rp[4], const uint32_t rq[4], int i)
+{
+    uint32_t x;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(x) : "r"(rp[i >> 1]), "r"(rq[i >> 1]), "r"((i & 1) ? 0x7632u : 0x5410u));
+    return x;
+}
+
+__device__ __forceinline__ uint32_t canon16(uint32_t k) { return k == 0x7FFFu ? 0x8000u : k; }
 
 __device__ __forceinline__ unsigned long long sat_sub(unsigned long long x, unsigned long long y)
 {
@@ -366,15 +388,14 @@ template <typename Pack>
 __device__ __forceinline__ int compact8(unsigned long long* wb, uint32_t cm, Pack pack)
 {
     const int lane = threadIdx.x & 31;
-    const int nm = __popc(cm);
-    int incl = nm;
+    const uint32_t nm = (uint32_t)__popc(cm), below = (1u << lane) - 1u;
+    int pos = 0, total = 0;   // the lanes' counts (0 .. 8) summed bit by bit: four independent ballots
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (nm >> k) & 1u);
+        pos += __popc(b & below) << k;
+        total += __popc(b) << k;
     }
-    const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    int pos = incl - nm;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         if ((cm >> i) & 1u) wb[pos++] = pack(i);
@@ -594,8 +615,9 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
                     __syncwarp();
                     for (int e = lane; e < nbuf; e += 32) {
                         const uint32_t en = (uint32_t)wb[e];
-                        const uint32_t ekp = en & 0xFFFFu, ekq = en >> 16;
+                        const uint32_t ekp = canon16(en & 0xFFFFu), ekq = canon16(en >> 16);
                         const bool tP = P.partial && ekp == P.cut_key;
+                        ties_p += tP ? 1 : 0;   // p's tied elements are all candidates
                         const bool tQ = residual && Q.partial && ekq == Q.cut_key;
                         const unsigned long long wp = fixp(P, ekp);
                         const bool qk = residual && (ekq > Q.cut_key || (ekq == Q.cut_key && !Q.partial));
@@ -645,19 +667,10 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
                                 rq[2] = keys2_raw(cq[h].z);
                                 rq[3] = keys2_raw(cq[h].w);
                             }
-                            if (P.partial) ties_p += ties8(rp, P.cut_key);
                             if (residual && Q.partial) ties_q += ties8(rq, Q.cut_key);
-                            uint32_t cm = 0u;
-                            const uint32_t mx = max_u16x2(max_u16x2(rp[0], rp[1]), max_u16x2(rp[2], rp[3]));
-                            if (max(mx & 0xFFFFu, mx >> 16) + 1u >= P.cut_key)   // -0's raw key sits one below +0's
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    if (canon_key(rp, i) >= P.cut_key) cm |= 1u << i;
-                            if (__any_sync(0xFFFFFFFFu, cm != 0u))
-                                nbuf += compact8(wb + nbuf, cm, [&](int i) {
-                                    return (unsigned long long)canon_key(rp, i) |
-                                           ((unsigned long long)canon_key(rq, i) << 16);
-                                });
+                            const uint32_t cm = at_least8(rp, P.cut_key);
+                            if (__any_sync(0xFFFFFFFFu, cm != 0u))   // raw pairs: the weighing makes them canonical
+                                nbuf += compact8(wb + nbuf, cm, [&](int i) { return (unsigned long long)pair_raw(rp, rq, i); });
                         }
                     }
                     if (!more || nbuf > kResWarpBuf - kResStep) weigh();   // room for the next step's candidates
