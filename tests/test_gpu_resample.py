@@ -3,9 +3,10 @@ sv_verify_chain (needs a GB300).
 
 Rows here span several 8,192-element chunks of the resample kernel, so
 the cases reach its combine step: tie groups at a partially kept cutoff that
-run across chunks (for p and for q), residuals that vanish, bonus tokens,
-rows too unaligned to be staged by bulk copies, and whole-row kept sets
-(top-p 1, no top-k) whose small-magnitude keys get per-key weights.
+run across chunks (for p and for q), cutoffs at zero (-0 and +0 tied) and
+below it, residuals that vanish, bonus tokens, rows too unaligned for
+16-byte vector loads, and whole-row kept sets (top-p 1, no top-k) whose
+small-magnitude keys get per-key weights.
 """
 import numpy as np
 import pytest
@@ -57,6 +58,23 @@ def test_tie_groups_across_chunks(seed):
     tp = torch.from_numpy(rng.choice([0.2, 0.45, 0.7, 0.9], n).astype(np.float32))
     o, g = _check(tgt, drf, toks, T, tk, tp, seed)
     assert (o["accept_len"] < K).sum() > n // 4          # residual resamples happened
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_tie_groups_at_zero_and_below(seed):
+    # few distinct logits around zero, -0 and +0 among them: the cutoffs fall
+    # at zero (both zeros in one tie group) or at a negative value
+    rng = np.random.default_rng(90 + seed)
+    n, K, V = 24, 3, 40_000
+    vals = [-1.5, -1.0, -0.5, -0.0, 0.0, 0.5]
+    tgt = _few_values(rng, (n, K + 1, V), vals, [0.1, 0.15, 0.2, 0.2, 0.2, 0.15])
+    drf = _few_values(rng, (n, K, V), vals, [0.15, 0.15, 0.15, 0.2, 0.2, 0.15])
+    toks = torch.from_numpy(rng.integers(0, V, (n, K)).astype(np.int32))
+    T = torch.from_numpy(rng.choice([0.7, 1.0, 1.3], n).astype(np.float32))
+    tk = torch.zeros(n, dtype=torch.int32)
+    tp = torch.from_numpy(rng.choice([0.3, 0.5, 0.75, 0.95], n).astype(np.float32))
+    o, g = _check(tgt, drf, toks, T, tk, tp, seed)
+    assert (o["accept_len"] < K).sum() > n // 4
 
 
 @pytest.mark.parametrize("seed", range(2))
