@@ -107,6 +107,7 @@ struct ResSmem {
     dfloat ratio[kResBinades];                      // per slot: exp(step / T) along the binade (0: one exp per key)
     dfloat exp_tab[64];                             // 2^(j / 64) for the double-float exp
     uint32_t zkey[2];                               // the loaded job's zero keys of p and q
+    dfloat inv_z[2];                                // and 1 / Z of each
     int16_t map[2][512];
     int slot_bin[kResBinades];
     int slot_dist[kResBinades];
@@ -185,9 +186,10 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
 __device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
 {
     const int tid = threadIdx.x;
-    if (tid == 0) {   // one fp64 log per distribution for the whole CTA
-        sm.zkey[0] = zero_key_of(P.m, P.T, P.z);
-        sm.zkey[1] = residual ? zero_key_of(Q.m, Q.T, Q.z) : sm.zkey[0];
+    if (tid < 2) {   // the fp64 work, once per distribution for the whole CTA (lane 0: p, lane 1: q)
+        const Dist& D = tid ? Q : P;   // q is p in p's own draw
+        sm.zkey[tid] = zero_key_of(D.m, D.T, D.z);
+        sm.inv_z[tid] = df_of(1.0 / D.z);
     }
     __syncthreads();
     P.zero_key = sm.zkey[0];
@@ -235,7 +237,7 @@ __device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
         sm.ratio[sl] = x.hi <= 1.0f ? exp_df(x, sm.exp_tab) : dfloat{0.0f, 0.0f};
     }
     __syncthreads();
-    const dfloat inv_zp = df_of(1.0 / P.z), inv_zq = df_of(1.0 / Q.z);
+    const dfloat inv_zp = sm.inv_z[0], inv_zq = sm.inv_z[1];
     for (int item = tid; item < (capP + capQ) * 16; item += kResThreads) {
         const int sl = item >> 4, g = item & 15;
         const bool isq = sm.slot_dist[sl] != 0;
