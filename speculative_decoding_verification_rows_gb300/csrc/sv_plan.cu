@@ -25,6 +25,13 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemKeys = 12288;   // rank keys held in shared memory (96 KB)
 
+__device__ __forceinline__ long long warp_sum_ll(long long x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
 __device__ __forceinline__ unsigned long long rank_key(float s, int i, int r)
 {
     return ((unsigned long long)__float_as_uint(s) << 32) | ((unsigned long long)(0xFFFu - (uint32_t)i) << 20) |
@@ -51,7 +58,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
         s_ncand = 0;
     }
     __syncthreads();
-    // survivals and rank keys: keys[r * K + i], 0 for positions past K_r
+    // survivals and rank keys: keys[i * n + r] (consecutive requests side by
+    // side: no bank conflicts), 0 for positions past K_r
     long long local = 0;
     for (int r = tid; r < n; r += kPlanThreads) {
         int kr = draft_len ? draft_len[r] : K;
@@ -59,20 +67,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
             atomicOr(&s_any_bad, 1);
             kr = kr < 0 ? 0 : K;
         }
+        // eight confidences loaded at a time (independent loads), then
+        // multiplied in order
         float s = 1.0f;
-        for (int i = 0; i < K; ++i) {
-            unsigned long long key = 0ull;
-            if (i < kr) {
-                float c = conf[(size_t)r * ld + i];
-                c = (c > 0.0f) ? fminf(c, 1.0f) : 0.0f;   // NaN and -0 -> +0
-                s = __fmul_rn(s, c);
-                key = rank_key(s, i, r);
+        for (int i0 = 0; i0 < K; i0 += 8) {
+            float cv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) cv[u] = i0 + u < kr ? conf[(size_t)r * ld + i0 + u] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u;
+                if (i >= K) break;
+                unsigned long long key = 0ull;
+                if (i < kr) {
+                    const float c = (cv[u] > 0.0f) ? fminf(cv[u], 1.0f) : 0.0f;   // NaN and -0 -> +0
+                    s = __fmul_rn(s, c);
+                    key = rank_key(s, i, r);
+                }
+                keys[(size_t)i * n + r] = key;
             }
-            keys[(size_t)r * K + i] = key;
         }
         local += kr;
     }
-    atomicAdd((unsigned long long*)&s_ncand, (unsigned long long)local);
+    local = warp_sum_ll(local);
+    if (lane == 0 && local) atomicAdd((unsigned long long*)&s_ncand, (unsigned long long)local);
     __syncthreads();
     const long long ncand = s_ncand;
     long long nsel = (long long)budget - n;
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* conf, i
         int vr = 0;
         if (r < n && nsel > 0) {
             for (int i = 0; i < K; ++i) {
-                const unsigned long long key = keys[(size_t)r * K + i];
+                const unsigned long long key = keys[(size_t)i * n + r];
                 if (key == 0ull || key < kth) break;
                 ++vr;
             }
@@ -224,11 +242,17 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* con
             kr = kr < 0 ? 0 : K;
         }
         float s = 1.0f;
-        for (int i = 0; i < kr; ++i) {
-            float c = conf[(size_t)r * ld + i];
-            c = (c > 0.0f) ? fminf(c, 1.0f) : 0.0f;   // NaN and -0 -> +0
-            s = __fmul_rn(s, c);
-            sv[r * K + i] = __float_as_uint(s);
+        for (int i0 = 0; i0 < kr; i0 += 8) {   // eight loads at a time, then the products in order
+            float cv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) cv[u] = i0 + u < kr ? conf[(size_t)r * ld + i0 + u] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (i0 + u >= kr) break;
+                const float c = (cv[u] > 0.0f) ? fminf(cv[u], 1.0f) : 0.0f;   // NaN and -0 -> +0
+                s = __fmul_rn(s, c);
+                sv[r * K + i0 + u] = __float_as_uint(s);
+            }
         }
         local += kr;
     }
@@ -242,7 +266,8 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* con
         if (!(isfinite(bj) && bj >= 0.0f)) atomicOr(&s_table_bad, 1);
     }
     if (tid == 0 && !(isfinite(fixed_ms) && fixed_ms >= 0.0f)) atomicOr(&s_table_bad, 1);
-    atomicAdd((unsigned long long*)&s_ncand, (unsigned long long)local);
+    local = warp_sum_ll(local);
+    if (lane == 0 && local) atomicAdd((unsigned long long*)&s_ncand, (unsigned long long)local);
     __syncthreads();
     // descending bitonic sort
     for (int k = 2; k <= P; k <<= 1) {
