@@ -13,20 +13,21 @@
 // The features come from the row transform the verify step uses (the draft
 // rows are processed as plain rows by the prep and row kernels); q_max = 1 / z
 // because the top token's mass is exp(0), so x = -ln(z - 1) with z - 1 the
-// kept mass after the top token.  observe() runs in one CTA and reduces in a
-// fixed order, so identical inputs give identical coefficients.
+// kept mass after the top token.  observe() runs as one cluster of CTAs and
+// reduces in a fixed order, so identical inputs give identical coefficients.
 //
 // State (doubles): [0] slope, [1..K] bias, [K+1] g_a, [K+2] H_aa, [K+3 ..]
 // g_k (K), H_ak (K), H_kk (K), [4K+3] observations, [4K+4] calls.
 #include <math.h>
 
+#include <cooperative_groups.h>
+
 #include "sv_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 namespace {
-
-constexpr int kEstThreads = 512;
-constexpr int kEstWarps = kEstThreads / 32;
 
 __global__ void est_init_kernel(double* st, int K)
 {
@@ -56,88 +57,117 @@ __global__ void est_predict_kernel(const RowInfo* info, const double* st, int n,
     }
 }
 
-// Statistics of one call, then (every refit_every calls) the refit.  Warp w
-// takes requests w, w + kEstWarps, ...; lane l positions l and l + 32.
-__global__ void __launch_bounds__(kEstThreads) est_observe_kernel(double* st, const float* x, const int32_t* acc,
-                                                                    const int32_t* emitted, const int32_t* vlens, int n,
-                                                                    int K, int refit_every)
+// Statistics of one call, then (every refit_every calls) the refit.  A
+// cluster of kObsCTAs CTAs, one (request, position) item per thread, item
+// i = r * K + k: the fp64 terms of the items spread over the cluster's SMs
+// (GB300's fp64 pipe is narrow).  Each CTA sums its items per position and
+// over all positions in item order; CTA 0 then adds the CTAs' sums in CTA
+// order through distributed shared memory.  The order is fixed, so identical
+// inputs give identical coefficients.
+constexpr int kObsCTAs = 8;
+constexpr int kObsThreads = 128;
+
+struct ObsSums {
+    double pos[3][kMaxK + 1];   // per position: sum (y - p), sum w x, sum w
+    double all[3];              // over all items: sum (y - p) x, sum w x^2, count
+};
+
+__global__ void __cluster_dims__(kObsCTAs, 1, 1) __launch_bounds__(kObsThreads)
+    est_observe_kernel(double* st, const float* x, const int32_t* acc, const int32_t* emitted, const int32_t* vlens,
+                       int n, int K, int refit_every)
 {
     pdl_enter();
-    __shared__ double s_gb[kEstWarps][kMaxK + 1], s_hab[kEstWarps][kMaxK + 1], s_hbb[kEstWarps][kMaxK + 1];
-    __shared__ double s_ga[kEstWarps], s_haa[kEstWarps], s_n[kEstWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ double s_t[kObsThreads][5];   // this round's items: (y - p) x, w x^2, y - p, w x, w
+    __shared__ int s_ok[kObsThreads];
+    __shared__ ObsSums sums;
+    const int tid = threadIdx.x, rank = (int)cluster.block_rank();
     const double slope = st[0];
-    double gb[2] = {0.0, 0.0}, hab[2] = {0.0, 0.0}, hbb[2] = {0.0, 0.0};
-    double ga = 0.0, haa = 0.0, cnt = 0.0;
-    for (int r = warp; r < n; r += kEstWarps) {
-        if (emitted[r] == 0 || acc[r] < 0) continue;
-        int v = vlens ? vlens[r] : K;
-        v = v < 0 ? 0 : (v > K ? K : v);
-        const int a = acc[r];
-        const int last = a < v - 1 ? a : v - 1;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int k = lane + 32 * h;
-            if (k > last) continue;
-            const double xv = (double)x[(size_t)r * K + k];
-            if (!isfinite(xv)) continue;
-            const double y = k < a ? 1.0 : 0.0;
-            const double p = 1.0 / (1.0 + exp(-(slope * xv + st[1 + k])));
-            const double w = p * (1.0 - p);
-            ga += (y - p) * xv;
-            haa += w * xv * xv;
-            gb[h] += y - p;
-            hab[h] += w * xv;
-            hbb[h] += w;
-            cnt += 1.0;
+    const int items = n * K;
+    // thread k < K keeps position k's sums of this CTA; thread K the totals
+    double q0 = 0.0, q1 = 0.0, q2 = 0.0;
+    for (int base = 0; base < items; base += kObsCTAs * kObsThreads) {
+        const int i0 = base + rank * kObsThreads, i = i0 + tid;
+        bool ok = false;
+        double t[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+        if (i < items) {
+            const int r = i / K, k = i - r * K;
+            if (emitted[r] != 0 && acc[r] >= 0) {
+                int v = vlens ? vlens[r] : K;
+                v = v < 0 ? 0 : (v > K ? K : v);
+                const int a = acc[r];
+                const int last = a < v - 1 ? a : v - 1;
+                const double xv = (double)x[i];
+                if (k <= last && isfinite(xv)) {
+                    const double y = k < a ? 1.0 : 0.0;
+                    const double p = 1.0 / (1.0 + exp(-(slope * xv + st[1 + k])));
+                    const double w = p * (1.0 - p);
+                    t[0] = (y - p) * xv;
+                    t[1] = w * xv * xv;
+                    t[2] = y - p;
+                    t[3] = w * xv;
+                    t[4] = w;
+                    ok = true;
+                }
+            }
         }
-    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int k = lane + 32 * h;
-        if (k < K) {
-            s_gb[warp][k] = gb[h];
-            s_hab[warp][k] = hab[h];
-            s_hbb[warp][k] = hbb[h];
+        for (int f = 0; f < 5; ++f) s_t[tid][f] = t[f];
+        s_ok[tid] = ok;
+        __syncthreads();
+        const int n_here = min(kObsThreads, items - i0);
+        if (tid < K) {   // position tid: the round's items of that position, in item order
+            for (int j = (tid - i0 % K + K) % K; j < n_here; j += K)
+                if (s_ok[j]) {
+                    q0 += s_t[j][2];
+                    q1 += s_t[j][3];
+                    q2 += s_t[j][4];
+                }
+        } else if (tid == K) {
+            for (int j = 0; j < n_here; ++j)
+                if (s_ok[j]) {
+                    q0 += s_t[j][0];
+                    q1 += s_t[j][1];
+                    q2 += 1.0;
+                }
         }
+        __syncthreads();
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        ga += __shfl_xor_sync(0xFFFFFFFFu, ga, o);
-        haa += __shfl_xor_sync(0xFFFFFFFFu, haa, o);
-        cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    if (tid < K) {
+        sums.pos[0][tid] = q0;
+        sums.pos[1][tid] = q1;
+        sums.pos[2][tid] = q2;
+    } else if (tid == K) {
+        sums.all[0] = q0;
+        sums.all[1] = q1;
+        sums.all[2] = q2;
     }
-    if (lane == 0) {
-        s_ga[warp] = ga;
-        s_haa[warp] = haa;
-        s_n[warp] = cnt;
-    }
-    __syncthreads();
+    cluster.sync();
     double* g_b = st + K + 3;
     double* h_ab = g_b + K;
     double* h_bb = h_ab + K;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        double a0 = 0.0, a1 = 0.0, a2 = 0.0;
-        for (int w = 0; w < kEstWarps; ++w) {
-            a0 += s_gb[w][k];
-            a1 += s_hab[w][k];
-            a2 += s_hbb[w][k];
+    double tot[3] = {0.0, 0.0, 0.0};
+    if (rank == 0 && tid <= K) {
+        for (int c = 0; c < kObsCTAs; ++c) {
+            const ObsSums* o = cluster.map_shared_rank(&sums, c);
+#pragma unroll
+            for (int f = 0; f < 3; ++f) tot[f] += tid < K ? o->pos[f][tid] : o->all[f];
         }
-        g_b[k] += a0;
-        h_ab[k] += a1;
-        h_bb[k] += a2;
+    }
+    cluster.sync();   // the other CTAs' sums stay in place until CTA 0 has read them
+    if (rank != 0) return;
+    if (tid < K) {
+        g_b[tid] += tot[0];
+        h_ab[tid] += tot[1];
+        h_bb[tid] += tot[2];
+    }
+    if (tid == K) {
+        st[K + 1] += tot[0];
+        st[K + 2] += tot[1];
+        st[4 * K + 3] += tot[2];
     }
     __syncthreads();
-    if (threadIdx.x != 0) return;
-    double a0 = 0.0, a1 = 0.0, a2 = 0.0;
-    for (int w = 0; w < kEstWarps; ++w) {
-        a0 += s_ga[w];
-        a1 += s_haa[w];
-        a2 += s_n[w];
-    }
-    st[K + 1] += a0;
-    st[K + 2] += a1;
-    st[4 * K + 3] += a2;
+    if (tid != 0) return;
     st[4 * K + 4] += 1.0;
     if (refit_every <= 0 || fmod(st[4 * K + 4], (double)refit_every) != 0.0) return;
     // refit: damped ridge Newton step on the arrowhead system
@@ -172,16 +202,17 @@ cudaError_t launch_est_init(double* state, int K, cudaStream_t s)
 cudaError_t launch_est_predict(const RowInfo* info, const double* state, int n, int K, float* x, float* p,
                                const Counters* counters, cudaStream_t s)
 {
-    int grid = (n * K + 255) / 256;
+    // one warp per CTA: the fp64 log and exp of the rows spread over the SMs
+    int grid = (n * K + 31) / 32;
     if (grid < 1) grid = 1;
-    if (grid > 1024) grid = 1024;
-    return launch_pdl(est_predict_kernel, dim3(grid), dim3(256), 0, s, info, state, n, K, x, p, counters);
+    if (grid > 4096) grid = 4096;
+    return launch_pdl(est_predict_kernel, dim3(grid), dim3(32), 0, s, info, state, n, K, x, p, counters);
 }
 
 cudaError_t launch_est_observe(double* state, const float* x, const int32_t* accept_len, const int32_t* num_emitted,
                                const int32_t* verify_lens, int n, int K, int refit_every, cudaStream_t s)
 {
-    return launch_pdl(est_observe_kernel, dim3(1), dim3(kEstThreads), 0, s, state, x, accept_len, num_emitted,
+    return launch_pdl(est_observe_kernel, dim3(kObsCTAs), dim3(kObsThreads), 0, s, state, x, accept_len, num_emitted,
                       verify_lens, n, K, refit_every);
 }
 
