@@ -94,9 +94,9 @@ constexpr int kResThreads = 256;
 constexpr int kResWarps = kResThreads / 32;
 constexpr int kResBinades = 48;    // table slots, p's and q's binades together
 constexpr int kResTile = kResampleTile;
-constexpr int kResStep = 512;
+constexpr int kResStep = 512;        // elements a warp loads at a time (two 16-byte vectors per lane and row)
 constexpr int kResCostJobs = 2048;   // jobs up to which the chunks are split by estimated cost
-constexpr int kResCostBase = 120;    // a chunk's fixed part, in units of one candidate's weighing      // elements a warp loads at a time (two 16-byte vectors per lane and row)
+constexpr int kResCostBase = 120;    // a chunk's fixed part, in units of one candidate's gathering and weighing
 constexpr int kResWarpBuf = kResStep + 64;   // candidates a warp gathers before weighing them
 static_assert(kResampleTile == kResThreads * 8, "a rescanned tile is at most eight elements per thread");
 static_assert((kResTile / 2) % kResStep == 0, "a tile is whole steps");
