@@ -1366,6 +1366,7 @@ __device__ __noinline__ void decide_position(const RowsArgs& a, int r, int j)
 __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(const __grid_constant__ RowsArgs a)
 {
     pdl_enter();
+    if (a.counters->n_slow == 0) return;   // no histogram rows in this batch
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw);
     const int tid = threadIdx.x;
