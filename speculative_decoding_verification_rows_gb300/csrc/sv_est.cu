@@ -60,10 +60,11 @@ __global__ void est_predict_kernel(const RowInfo* info, const double* st, int n,
 // Statistics of one call, then (every refit_every calls) the refit.  A
 // cluster of kObsCTAs CTAs, one (request, position) item per thread, item
 // i = r * K + k: the fp64 terms of the items spread over the cluster's SMs
-// (GB300's fp64 pipe is narrow).  Each CTA sums its items per position and
-// over all positions in item order; CTA 0 then adds the CTAs' sums in CTA
-// order through distributed shared memory.  The order is fixed, so identical
-// inputs give identical coefficients.
+// (GB300's fp64 pipe is narrow).  Each warp sums its items over all
+// positions by a butterfly and per position in item order, the CTA adds its
+// warps' sums in warp order, and CTA 0 adds the CTAs' sums in CTA order
+// through distributed shared memory: short dependent chains, in an order
+// fixed in advance, so identical inputs give identical coefficients.
 constexpr int kObsCTAs = 8;
 constexpr int kObsThreads = 128;
 
@@ -78,10 +79,12 @@ __global__ void __cluster_dims__(kObsCTAs, 1, 1) __launch_bounds__(kObsThreads)
 {
     pdl_enter();
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ double s_t[kObsThreads][5];   // this round's items: (y - p) x, w x^2, y - p, w x, w
+    __shared__ double s_t[kObsThreads][3];                    // this round's items: y - p, w x, w
     __shared__ int s_ok[kObsThreads];
+    __shared__ double s_w[kObsThreads / 32][3];                 // per warp: sum (y - p) x, sum w x^2, count
+    __shared__ double s_pw[kObsThreads / 32][3][kMaxK + 1];     // per warp and position: the three sums
     __shared__ ObsSums sums;
-    const int tid = threadIdx.x, rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, rank = (int)cluster.block_rank();
     const double slope = st[0];
     const int items = n * K;
     // thread k < K keeps position k's sums of this CTA; thread K the totals
@@ -89,47 +92,75 @@ __global__ void __cluster_dims__(kObsCTAs, 1, 1) __launch_bounds__(kObsThreads)
     for (int base = 0; base < items; base += kObsCTAs * kObsThreads) {
         const int i0 = base + rank * kObsThreads, i = i0 + tid;
         bool ok = false;
-        double t[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+        double t0 = 0.0, t1 = 0.0, t2 = 0.0, t3 = 0.0, t4 = 0.0;
         if (i < items) {
             const int r = i / K, k = i - r * K;
-            if (emitted[r] != 0 && acc[r] >= 0) {
-                int v = vlens ? vlens[r] : K;
-                v = v < 0 ? 0 : (v > K ? K : v);
-                const int a = acc[r];
-                const int last = a < v - 1 ? a : v - 1;
-                const double xv = (double)x[i];
-                if (k <= last && isfinite(xv)) {
-                    const double y = k < a ? 1.0 : 0.0;
-                    const double p = 1.0 / (1.0 + exp(-(slope * xv + st[1 + k])));
-                    const double w = p * (1.0 - p);
-                    t[0] = (y - p) * xv;
-                    t[1] = w * xv * xv;
-                    t[2] = y - p;
-                    t[3] = w * xv;
-                    t[4] = w;
-                    ok = true;
-                }
+            const int em = emitted[r], a = acc[r], vr = vlens ? vlens[r] : K;   // independent loads
+            const double xv = (double)x[i], bk = st[1 + k];
+            const int v = vr < 0 ? 0 : (vr > K ? K : vr);
+            const int last = a < v - 1 ? a : v - 1;
+            if (em != 0 && a >= 0 && k <= last && isfinite(xv)) {
+                const double y = k < a ? 1.0 : 0.0;
+                const double p = 1.0 / (1.0 + exp(-(slope * xv + bk)));
+                const double w = p * (1.0 - p);
+                t0 = (y - p) * xv;
+                t1 = w * xv * xv;
+                t2 = y - p;
+                t3 = w * xv;
+                t4 = w;
+                ok = true;
             }
         }
+        // the totals: a butterfly over the warp, then the warps in order
+        double c0 = t0, c1 = t1, c2 = ok ? 1.0 : 0.0;
 #pragma unroll
-        for (int f = 0; f < 5; ++f) s_t[tid][f] = t[f];
+        for (int o = 16; o; o >>= 1) {
+            c0 += __shfl_xor_sync(0xFFFFFFFFu, c0, o);
+            c1 += __shfl_xor_sync(0xFFFFFFFFu, c1, o);
+            c2 += __shfl_xor_sync(0xFFFFFFFFu, c2, o);
+        }
+        if (lane == 0) {
+            s_w[warp][0] = c0;
+            s_w[warp][1] = c1;
+            s_w[warp][2] = c2;
+        }
+        s_t[tid][0] = t2;
+        s_t[tid][1] = t3;
+        s_t[tid][2] = t4;
         s_ok[tid] = ok;
         __syncthreads();
+        // per position: each warp's items of that position in item order, then the warps in order
         const int n_here = min(kObsThreads, items - i0);
-        if (tid < K) {   // position tid: the round's items of that position, in item order
-            for (int j = (tid - i0 % K + K) % K; j < n_here; j += K)
-                if (s_ok[j]) {
-                    q0 += s_t[j][2];
-                    q1 += s_t[j][3];
-                    q2 += s_t[j][4];
+        for (int j = tid; j < (kObsThreads / 32) * K; j += kObsThreads) {
+            const int k = j % K, w = j / K;
+            double b0 = 0.0, b1 = 0.0, b2 = 0.0;
+            for (int l = ((k - (i0 + 32 * w) % K) % K + K) % K; l < 32; l += K) {
+                const int jj = 32 * w + l;
+                if (jj < n_here && s_ok[jj]) {
+                    b0 += s_t[jj][0];
+                    b1 += s_t[jj][1];
+                    b2 += s_t[jj][2];
                 }
+            }
+            s_pw[w][0][k] = b0;
+            s_pw[w][1][k] = b1;
+            s_pw[w][2][k] = b2;
+        }
+        __syncthreads();
+        if (tid < K) {
+#pragma unroll
+            for (int w = 0; w < kObsThreads / 32; ++w) {
+                q0 += s_pw[w][0][tid];
+                q1 += s_pw[w][1][tid];
+                q2 += s_pw[w][2][tid];
+            }
         } else if (tid == K) {
-            for (int j = 0; j < n_here; ++j)
-                if (s_ok[j]) {
-                    q0 += s_t[j][0];
-                    q1 += s_t[j][1];
-                    q2 += 1.0;
-                }
+#pragma unroll
+            for (int w = 0; w < kObsThreads / 32; ++w) {
+                q0 += s_w[w][0];
+                q1 += s_w[w][1];
+                q2 += s_w[w][2];
+            }
         }
         __syncthreads();
     }
