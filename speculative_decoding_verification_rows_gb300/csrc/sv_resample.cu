@@ -80,13 +80,14 @@ __device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_ra
 }
 
 // Key below which every weight floors to 0: values under m + T (ln Z - 62 ln 2),
-// less two keys for the roundings of the bound (0 when the bound is too close
-// to zero for that margin to mean anything).
-__device__ __forceinline__ uint32_t zero_key_of(double m, double T, double z)
+// less two keys for the roundings of the bound.  The bound is taken in fp32
+// (an error under 1e-5 T + 1e-7 |m|, where two keys are at least |v0| / 128),
+// and is 0 when it is too close to zero for that margin to cover the error.
+__device__ __forceinline__ uint32_t zero_key_of(float m, float T, double z)
 {
-    const double v0 = m + T * (log(z) - 62.0 * 0.69314718055994530942);
-    if (!(fabs(v0) > 1e-3 * T) || !(v0 > -3.0e38)) return 0u;
-    const uint32_t k = key16_of_bf16(__float_as_uint((float)v0) >> 16);
+    const float v0 = m + T * (logf((float)z) - 62.0f * (float)kLn2);
+    if (!(fabsf(v0) > 2e-3f * T + 1e-4f * fabsf(m)) || !(v0 > -3.0e38f)) return 0u;
+    const uint32_t k = key16_of_bf16(__float_as_uint(v0) >> 16);
     return k >= 2u ? k - 2u : 0u;
 }
 
@@ -186,10 +187,10 @@ __device__ __forceinline__ void job_dists(const ChainArgs& a, const ResampleJob&
 __device__ void load_tables(ResSmem& sm, Dist& P, Dist& Q, bool residual)
 {
     const int tid = threadIdx.x;
-    if (tid < 2) {   // the fp64 work, once per distribution for the whole CTA (lane 0: p, lane 1: q)
+    if (tid < 2) {   // once per distribution for the whole CTA (lane 0: p, lane 1: q)
         const Dist& D = tid ? Q : P;   // q is p in p's own draw
-        sm.zkey[tid] = zero_key_of(D.m, D.T, D.z);
-        sm.inv_z[tid] = df_of(1.0 / D.z);
+        sm.zkey[tid] = zero_key_of((float)D.m, (float)D.T, D.z);
+        sm.inv_z[tid] = df_recip(D.z);
     }
     __syncthreads();
     P.zero_key = sm.zkey[0];
