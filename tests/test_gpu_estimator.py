@@ -51,7 +51,7 @@ def test_features_and_predictions_match_the_oracle(seed, mode, V):
 def _calls(rng, n, K, n_calls):
     for _ in range(n_calls):
         x = rng.normal(0.0, 2.0, (n, K)).astype(np.float32)
-        alive = rng.uniform(size=(n, K)) < scipy.special.expit(x + np.array([1.0, 0.5, 0.0, -0.5][:K]))
+        alive = rng.uniform(size=(n, K)) < scipy.special.expit(x + np.linspace(1.0, -0.5, K))
         acc = np.array([np.argmin(a) if not a.all() else K for a in alive], np.int32)
         vl = rng.integers(0, K + 1, n).astype(np.int32)
         acc = np.minimum(acc, vl).astype(np.int32)
@@ -60,9 +60,12 @@ def _calls(rng, n, K, n_calls):
         yield x, acc, emitted, vl
 
 
-def test_observe_and_refit_match_the_oracle():
-    rng = np.random.default_rng(7)
-    K, n = 4, 300
+@pytest.mark.parametrize("K,n", [(4, 300), (1, 2_500), (40, 37), (63, 20)])
+def test_observe_and_refit_match_the_oracle(K, n):
+    # items (request, position) spread over the CTAs of the observe cluster in
+    # one or several rounds, positions repeating inside a warp (K = 1, 4) or
+    # not (K = 40, 63)
+    rng = np.random.default_rng(7 + K)
     g = sv.Estimator(K)
     g.state[0] = 3.0
     o = oracle.Estimator(K)
