@@ -80,9 +80,11 @@ __device__ __forceinline__ bool kept_key(const Dist& D, uint32_t key, int tie_ra
 }
 
 // Key below which every weight floors to 0: values under m + T (ln Z - 62 ln 2),
-// less two keys for the roundings of the bound.  The bound is taken in fp32
-// (an error under 1e-5 T + 1e-7 |m|, where two keys are at least |v0| / 128),
-// and is 0 when it is too close to zero for that margin to cover the error.
+// less two keys for the roundings of the bound.  The bound is taken in fp32,
+// an error of about 1e-5 T + 1e-7 |m| (ln Z <= 22, 62 ln 2 and their
+// difference each within an fp32 rounding, then the product and the sum),
+// while two keys span at least |v0| / 128; the bound is 0 where that margin
+// would not cover the error with room to spare.
 __device__ __forceinline__ uint32_t zero_key_of(float m, float T, double z)
 {
     const float v0 = m + T * (logf((float)z) - 62.0f * (float)kLn2);
