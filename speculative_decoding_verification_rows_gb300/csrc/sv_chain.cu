@@ -26,6 +26,11 @@ namespace sv {
 namespace {
 
 constexpr int kPrepThreads = 1024;
+// A greedy request's histogram-path rows (argmax scans, the same cost whether
+// or not an earlier test rejects) are listed this many positions ahead of the
+// sampling rows of their position, so that the CTAs a short scan frees early
+// take them while the first sampling tests are still being decided.
+constexpr int kGreedyAhead = 2;
 
 
 __device__ __forceinline__ int bad_params(float T, float top_p)
@@ -96,10 +101,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
     // histogram rows of chain verification: their requests, and the rows of
     // each position over all of them (counted here, listed after the loop)
     __shared__ int s_nsr;
-    __shared__ int s_pos[kMaxK + 1];
+    __shared__ int s_pos[kMaxK + 1];    // per listing bucket: the sampling rows, then (s_posg) the greedy rows
+    __shared__ int s_posg[kMaxK + 1];
     const int kinds = a.q_rows ? 1 : 2;   // histogram rows per verified position (1 for greedy requests)
     if (threadIdx.x == 0) s_nsr = 0;
-    for (int j = threadIdx.x; j <= kMaxK; j += kPrepThreads) s_pos[j] = 0;
+    for (int j = threadIdx.x; j <= kMaxK; j += kPrepThreads) s_pos[j] = s_posg[j] = 0;
     // Chain verification with bf16 rows: when any request's kept set takes
     // the histogram path, greedy requests go there too (their rows as argmax
     // scans), so that their bytes stream while the histogram passes, bound by
@@ -270,10 +276,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
                 a.req[u] = st;
                 if (slow && a.lazy) {   // the histogram path takes its rows position by position
                     a.slow_req[atomicAdd(&s_nsr, 1)] = make_int2((u << 7) | (greedy << 6) | v, st.slow_base);
-                    const int kr = greedy ? 1 : kinds;
                     for (int j = 0; j <= v; ++j) {
                         a.pair_done[(size_t)u * (K + 1) + j] = 0;
-                        atomicAdd(&s_pos[j], j < v ? kr : 1);
+                        if (greedy)
+                            atomicAdd(&s_posg[max(0, j - kGreedyAhead)], 1);
+                        else
+                            atomicAdd(&s_pos[j], j < v ? kinds : 1);
                     }
                 }
                 a.req_done[u] = 0;
@@ -295,14 +303,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
     if (a.lazy) {
         // The histogram rows of chain verification in position order (all
         // requests' rows of position 0, then of position 1, ...), target row
-        // before draft row; the order among requests is immaterial.
+        // before draft row, greedy requests' rows kGreedyAhead positions
+        // early (after the sampling rows of the position they join); the
+        // order among requests is immaterial.
         const int K1 = K + 1, nsr = s_nsr;
         if (threadIdx.x == 0) {
             int run = 0;
             for (int j = 0; j < K1; ++j) {
-                const int c = s_pos[j];
+                const int cs = s_pos[j], cg = s_posg[j];
                 s_pos[j] = run;
-                run += c;
+                s_posg[j] = run + cs;
+                run += cs + cg;
             }
             a.counters->n_units = run;
             a.counters->n_slow_req = nsr;
@@ -315,9 +326,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
             const int2 e = a.slow_req[i];
             const int r = e.x >> 7, v = e.x & 63;
             const int kr = ((e.x >> 6) & 1) ? 1 : kinds;
+            const bool g = ((e.x >> 6) & 1) != 0;
             for (int j = 0; j <= v; ++j) {
                 const int nk = j < v ? kr : 1;
-                const int at = atomicAdd(&s_pos[j], nk);
+                const int at = g ? atomicAdd(&s_posg[max(0, j - kGreedyAhead)], nk) : atomicAdd(&s_pos[j], nk);
                 a.slow_units[at] = make_int2((r << 7) | (j << 1), e.y + j);
                 if (nk == 2) a.slow_units[at + 1] = make_int2((r << 7) | (j << 1) | 1, e.y + v + 1 + j);
             }
