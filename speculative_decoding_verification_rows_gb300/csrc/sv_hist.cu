@@ -829,7 +829,7 @@ constexpr int kUnclaimed = INT_MIN;      // base[] of a binade not seen yet in t
 constexpr int kClaiming = INT_MIN + 1;   // base[] while a thread assigns the binade its counters
 constexpr int kBaseMin = -65536;         // a claimed base is 128 * (slot - b) >= -65,408
 constexpr int kClaimSpins = 1 << 14;     // polls before a thread stops waiting for a claim
-constexpr int kDecideSpins = 40;         // polls (about 256 ns apart) for the previous position's test
+constexpr int kDecideSpins = 120;        // polls (about 256 ns apart) for the previous position's test
 static_assert(kWideThreads >= 4 * kWideSlots, "the mass pass takes four threads per slot");
 static_assert(kWideThreads == kWalkThreads && kHistThreads == kWalkThreads, "walk_row takes one binade per thread");
 static_assert(2 * kWideSlots < kWideThreads, "the last thread is idle in the exps of the mass pass");
@@ -1469,6 +1469,10 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(co
                 __threadfence();
                 atomicAdd(&c.pair_done[(size_t)r * K1 + j], 1);   // kinds + 1: decided
             }
+        } else if (tid == 0 && ovf && j < c.req[r].v) {
+            // a handed-on row leaves the position's test to the chain kernel:
+            // mark it so that no later row of the request waits for it here
+            atomicAdd(&c.pair_done[(size_t)r * K1 + j], kinds + 1);
         }
     }
 }
