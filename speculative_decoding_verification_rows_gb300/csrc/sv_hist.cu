@@ -1365,8 +1365,8 @@ __device__ __noinline__ void decide_position(const RowsArgs& a, int r, int j)
 
 __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(const __grid_constant__ RowsArgs a)
 {
-    pdl_enter();
-    if (a.counters->n_slow == 0) return;   // no histogram rows in this batch
+    // the counters are cleared before the wait for the kernel before this
+    // one (shared memory only: it overlaps that kernel's end)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw);
     const int tid = threadIdx.x;
@@ -1380,6 +1380,8 @@ __global__ void __launch_bounds__(kWideThreads, kWideBlocks) wide_rows_kernel(co
         sm.n_slots = 0;
         sm.ovf = 0;
     }
+    pdl_enter();
+    if (a.counters->n_slow == 0) return;   // no histogram rows in this batch
     __syncthreads();
     if (!a.chain.lazy) {
         const int n_tasks = a.counters->n_slow;

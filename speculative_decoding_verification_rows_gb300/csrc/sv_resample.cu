@@ -554,10 +554,11 @@ __device__ __noinline__ void cost_split(ResSmem& sm, const ChainArgs& a, int j0,
 
 __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_constant__ ChainArgs a, int n_units, int wave)
 {
-    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ResSmem& sm = *reinterpret_cast<ResSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    fill_exp_table(sm.exp_tab);   // constants into shared memory: before the wait for the kernel before this one
+    pdl_enter();
     const int V = a.vocab, K = a.K;
     const int n_tiles = resample_tiles(V), tile_len = resample_tile_len(V);
     // wave 0: the jobs the chain or block kernel listed; wave 1: those the
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kResThreads, 2) resample_kernel(const __grid_c
     long long u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
     if (n_jobs <= kResCostJobs && total >= 4ll * gridDim.x) cost_split(sm, a, j0, n_jobs, n_units, u_lo, u_hi);
     if (tid == 0) sm.cur_job = -1;
-    fill_exp_table(sm.exp_tab);
+    __syncthreads();
     // this CTA's chunks, one job at a time: [u, u_end) are those of job j
     for (long long u = u_lo, u_end; u < u_hi; u = u_end) {
         const int j = j0 + (int)(u / n_units);
